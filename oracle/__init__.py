@@ -1,0 +1,210 @@
+"""fp64 CPU oracle of the MoE-FFN forward layer -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  It is the checker, not the product: the product
+path (``sparse_mixture_experts_48_b300``) never imports it and shares no code
+with it.  The arithmetic lives in ``moe_oracle.c`` (plain single-threaded C,
+fp64); this file only builds it, marshals arrays and chains its steps in the
+order the pages give them:
+
+  logits -> gate probabilities -> top-k on the logits -> renormalised weights
+  -> capacity / drops / grouped order -> expert FFNs + gate-weighted sum (+
+  shared experts) -> balance statistics f, P, L_aux.
+
+Every function takes the STORED input values (fp32 arrays, or uint16 arrays
+of bf16 bits) and widens them to double itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "libmoe_oracle.so")
+
+RELU, GELU, SWIGLU = 0, 1, 2
+SOFTMAX, SIGMOID_NORM = 0, 1
+F32, BF16 = 0, 1
+
+
+def build(force: bool = False) -> str:
+    src = os.path.join(_HERE, "moe_oracle.c")
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(src):
+        # -O2, no fast-math: the C library's exp/erf in double, IEEE order of operations.
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", _SO, src, "-lm"])
+    return _SO
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def _L() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_SO)
+        i32, i64, dbl, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+        lib.oracle_router_logits.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp]
+        lib.oracle_gate_probs.argtypes = [i64, i32, i32, vp, vp]
+        lib.oracle_topk_row.argtypes = [i32, i32, vp, vp]
+        lib.oracle_topk.argtypes = [i64, i32, i32, vp, vp]
+        lib.oracle_topk_weights.argtypes = [i64, i32, i32, i32, vp, vp, vp]
+        lib.oracle_capacity.restype = i64
+        lib.oracle_capacity.argtypes = [i64, i32, dbl]
+        lib.oracle_dispatch.argtypes = [i64, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp]
+        lib.oracle_act.restype = dbl
+        lib.oracle_act.argtypes = [i32, dbl]
+        lib.oracle_expert_ffn.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        lib.oracle_layer_rows.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, i64, vp, vp, vp, vp,
+                                          vp, vp, vp, vp, vp, vp]
+        lib.oracle_balance.argtypes = [i64, i32, i32, dbl, vp, vp, vp, vp, vp]
+        _lib = lib
+    return _lib
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def _stored(a: Optional[np.ndarray], dtype: int) -> Optional[np.ndarray]:
+    if a is None:
+        return None
+    want = np.float32 if dtype == F32 else np.uint16
+    if a.dtype != want:
+        raise TypeError(f"oracle expects stored {want.__name__} values, got {a.dtype}")
+    return np.ascontiguousarray(a)
+
+
+# ---- single steps -----------------------------------------------------------
+
+def router_logits(x, W_g, b_g, dtype: int) -> np.ndarray:
+    x, W_g, b_g = _stored(x, dtype), _stored(W_g, dtype), _stored(b_g, dtype)
+    T, d = x.shape
+    E = W_g.shape[1]
+    out = np.empty((T, E), np.float64)
+    _L().oracle_router_logits(T, d, E, dtype, _p(x), _p(W_g), _p(b_g), _p(out))
+    return out
+
+
+def gate_probs(logits: np.ndarray, gating: int) -> np.ndarray:
+    logits = np.ascontiguousarray(logits, np.float64)
+    T, E = logits.shape
+    out = np.empty((T, E), np.float64)
+    _L().oracle_gate_probs(T, E, gating, _p(logits), _p(out))
+    return out
+
+
+def topk_row(values: Sequence[float], k: int) -> np.ndarray:
+    v = np.ascontiguousarray(values, np.float64)
+    idx = np.empty(k, np.int32)
+    _L().oracle_topk_row(v.size, k, _p(v), _p(idx))
+    return idx
+
+
+def topk(logits: np.ndarray, k: int) -> np.ndarray:
+    logits = np.ascontiguousarray(logits, np.float64)
+    T, E = logits.shape
+    idx = np.empty((T, k), np.int32)
+    _L().oracle_topk(T, E, k, _p(logits), _p(idx))
+    return idx
+
+
+def topk_weights(logits: np.ndarray, idx: np.ndarray, gating: int) -> np.ndarray:
+    logits = np.ascontiguousarray(logits, np.float64)
+    idx = np.ascontiguousarray(idx, np.int32)
+    T, E = logits.shape
+    k = idx.shape[1]
+    w = np.empty((T, k), np.float64)
+    _L().oracle_topk_weights(T, E, k, gating, _p(logits), _p(idx), _p(w))
+    return w
+
+
+def capacity(T: int, E: int, capacity_factor: float) -> int:
+    return int(_L().oracle_capacity(T, E, capacity_factor))
+
+
+def dispatch(idx: np.ndarray, E: int, C: int) -> Dict[str, np.ndarray]:
+    idx = np.ascontiguousarray(idx, np.int32)
+    T, k = idx.shape
+    n_pre = np.empty(E, np.int32)
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    dropped = np.empty((T, k), np.uint8)
+    slot = np.empty((T, k), np.int32)
+    perm = np.full(max(T * k, 1), -1, np.int32)
+    _L().oracle_dispatch(T, E, k, C, _p(idx), _p(n_pre), _p(counts), _p(offsets), _p(dropped), _p(slot),
+                         _p(perm))
+    return dict(n_pre=n_pre, counts=counts, offsets=offsets, dropped=dropped, slot=slot,
+                perm=perm[: int(offsets[E])])
+
+
+def act(kind: int, z: float) -> float:
+    return float(_L().oracle_act(kind, z))
+
+
+def expert_ffn(xrow: np.ndarray, g: int, cfg, W1, b1, W2, b2, W3) -> np.ndarray:
+    dt = cfg.dtype
+    xr = np.ascontiguousarray(xrow, np.float64)
+    out = np.empty(cfg.d, np.float64)
+    _L().oracle_expert_ffn(cfg.d, cfg.f, cfg.act, dt, g, _p(xr), _p(_stored(W1, dt)), _p(_stored(b1, dt)),
+                           _p(_stored(W2, dt)), _p(_stored(b2, dt)), _p(_stored(W3, dt)), _p(out))
+    return out
+
+
+def layer_rows(cfg, rows: Sequence[int], inp: Dict, idx: np.ndarray, w: np.ndarray,
+               dropped: np.ndarray) -> np.ndarray:
+    dt = cfg.dtype
+    rows = np.ascontiguousarray(rows, np.int64)
+    y = np.empty((rows.size, cfg.d), np.float64)
+    _L().oracle_layer_rows(cfg.d, cfg.f, cfg.E, idx.shape[1], cfg.S, cfg.act, dt, _p(rows), rows.size,
+                           _p(_stored(inp["x"], dt)), _p(_stored(inp["W1"], dt)), _p(_stored(inp["b1"], dt)),
+                           _p(_stored(inp["W2"], dt)), _p(_stored(inp["b2"], dt)), _p(_stored(inp["W3"], dt)),
+                           _p(np.ascontiguousarray(idx, np.int32)), _p(np.ascontiguousarray(w, np.float64)),
+                           _p(np.ascontiguousarray(dropped, np.uint8)), _p(y))
+    return y
+
+
+def balance(n_pre: np.ndarray, probs: np.ndarray, k: int, alpha: float):
+    n_pre = np.ascontiguousarray(n_pre, np.int32)
+    probs = np.ascontiguousarray(probs, np.float64)
+    T, E = probs.shape
+    f = np.empty(E, np.float64)
+    P = np.empty(E, np.float64)
+    L = np.empty(1, np.float64)
+    _L().oracle_balance(T, E, k, alpha, _p(n_pre), _p(probs), _p(f), _p(P), _p(L))
+    return f, P, float(L[0])
+
+
+# ---- the layer, chained ---------------------------------------------------------
+
+def routing(cfg, logits: np.ndarray) -> Dict[str, np.ndarray]:
+    """Steps after the logits up to the grouped order, on the given logits."""
+    probs = gate_probs(logits, cfg.gating)
+    idx = topk(logits, cfg.k)
+    w = topk_weights(logits, idx, cfg.gating)
+    C = capacity(logits.shape[0], cfg.E, cfg.capacity_factor)
+    disp = dispatch(idx, cfg.E, C)
+    f, P, L_aux = balance(disp["n_pre"], probs, cfg.k, cfg.alpha)
+    out = dict(probs=probs, topk_idx=idx, topk_w=w, capacity=C, f=f, P=P, L_aux=L_aux)
+    out.update(disp)
+    return out
+
+
+def forward(cfg, inp: Dict, rows: Optional[Sequence[int]] = None,
+            logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """The whole layer.  ``rows``: token rows whose output y is computed (all
+    when None; routing and statistics always cover every token).  ``logits``:
+    route on these logits instead of the oracle's own (used to compare the
+    integer decisions on the very fp32 logits another implementation made)."""
+    own = router_logits(inp["x"], inp["W_g"], inp["b_g"], cfg.dtype) if logits is None else None
+    lg = own if logits is None else np.ascontiguousarray(logits, np.float64)
+    out = routing(cfg, lg)
+    out["logits"] = lg
+    rows = np.arange(cfg.T) if rows is None else np.asarray(rows, np.int64)
+    out["rows"] = rows
+    out["y"] = layer_rows(cfg, rows, inp, out["topk_idx"], out["topk_w"], out["dropped"])
+    return out

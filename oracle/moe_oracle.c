@@ -1,0 +1,268 @@
+/*
+ * oracle/moe_oracle.c -- TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT PATH.
+ *
+ * A plain, slow, single-threaded fp64 CPU restatement of the forward pass of a
+ * token-choice Mixture-of-Experts feed-forward layer, written step by step
+ * from the pages' definitions so that each step can be checked against them
+ * by eye.  Only the tests, the package's smoke check and the bench's CPU
+ * baseline may load it.  It shares no code, header or constant with the CUDA
+ * path: it reads the stored input values (fp32, or bf16 bits) and widens them
+ * to double, and does every sum and product in double.
+ *
+ * Sources (page title, section):
+ *   [P1] "MoE混合专家模型：Transformer稀疏前馈网络原理与PyTorch实现"
+ *        §1.3 (sparse FFN data flow), §2.1 (router: linear + softmax, top-k,
+ *        renormalise), §2.3 (Switch load-balance loss), §3.2 (capacity factor),
+ *        §4.1 (TopKRouter / ExpertFFN / MoEFFN listing).
+ *   [P2] "MoE架构解析" §2.1 (token choice), §三 关键技术① (expert capacity,
+ *        overflow tokens skip the layer), §四 技术飞跃② (shared experts,
+ *        always active), 技术飞跃③ (normalised sigmoid gating).
+ *   [P3] "手撕一个极简 MoE-FFN" §三 (Router, top_k_routing, worked example),
+ *        §四 (Expert FFN), §五/§六 (weighted sum), §七 (load-balancing loss
+ *        with f = counts / (T*k)).
+ *   [P4] "Mixture of Experts混合专家模型架构原理与路由策略实现",
+ *        门控网络的数学原理 (Gate(x) = softmax(W_g x), W_g is [d_model, E]),
+ *        从零实现一个简化版MoE层 (GELU expert).
+ *   [P5] "术业有专攻：learn-minimind MoE混合专家模型架构入门指南" §二
+ *        (experts are SwiGLU FFNs).
+ *
+ * Readings taken where the pages are silent or disagree (each is stated at
+ * the function that uses it): selection on logits with ties to the lower
+ * index; capacity C = ceil(T * cf / E) in fp64, slots given in token order;
+ * a dropped slot contributes 0 and the kept weights are not renormalised;
+ * shared experts are added with weight 1 after the routed sum; f counts
+ * selections before the capacity cut; P under sigmoid gating is the mean of
+ * sigma_e / sum_e' sigma_e'; GELU is the exact erf form; SwiGLU is
+ * W2 (silu(x W1) * (x W3)); weights are stored [in, out].
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ODT_F32 = 0, ODT_BF16 = 1 };
+enum { OACT_RELU = 0, OACT_GELU = 1, OACT_SWIGLU = 2 };
+enum { OGATE_SOFTMAX = 0, OGATE_SIGMOID_NORM = 1 };
+
+/* Step 0: the stored value widened to double (bf16 -> fp32 bits -> double, exact). */
+static double ld(const void* p, int dtype, int64_t i) {
+  if (dtype == ODT_F32) return (double)((const float*)p)[i];
+  uint32_t u = (uint32_t)((const uint16_t*)p)[i] << 16;
+  float v;
+  memcpy(&v, &u, 4);
+  return (double)v;
+}
+
+/* Router logits l[t,e] = b_g[e] + sum_i x[t,i] W_g[i,e]   [P1 §2.1; P3 §三; P4 门控网络的数学原理].
+ * W_g is stored [d, E] (the gate formula's [d_model, num_experts]); b_g may be NULL. */
+void oracle_router_logits(int64_t T, int d, int E, int dtype, const void* x, const void* Wg,
+                          const void* bg, double* logits) {
+  for (int64_t t = 0; t < T; ++t) {
+    double* l = logits + t * E;
+    for (int e = 0; e < E; ++e) l[e] = bg ? ld(bg, dtype, e) : 0.0;
+    for (int i = 0; i < d; ++i) {
+      double xi = ld(x, dtype, t * d + i);
+      for (int e = 0; e < E; ++e) l[e] += xi * ld(Wg, dtype, (int64_t)i * E + e);
+    }
+  }
+}
+
+/* Gate probabilities per token over all E experts.
+ *  softmax        p_e = exp(l_e - max) / sum_e' exp(l_e' - max)      [P1 §2.1; P3 §三]
+ *  normalised sigmoid: s_e = 1 / (1 + exp(-l_e)),  p_e = s_e / sum_e' s_e'
+ *                 (sigmoid per expert, then a global normalisation)  [P2 技术飞跃③]
+ * These p feed the balance statistic P_i. */
+void oracle_gate_probs(int64_t T, int E, int gating, const double* logits, double* probs) {
+  for (int64_t t = 0; t < T; ++t) {
+    const double* l = logits + t * E;
+    double* p = probs + t * E;
+    double z = 0.0;
+    if (gating == OGATE_SOFTMAX) {
+      double m = l[0];
+      for (int e = 1; e < E; ++e) if (l[e] > m) m = l[e];
+      for (int e = 0; e < E; ++e) { p[e] = exp(l[e] - m); z += p[e]; }
+    } else {
+      for (int e = 0; e < E; ++e) { p[e] = 1.0 / (1.0 + exp(-l[e])); z += p[e]; }
+    }
+    for (int e = 0; e < E; ++e) p[e] /= z;
+  }
+}
+
+/* Top-k selection on one row of values: the k largest, listed in descending
+ * value, equal values ordered by ascending index.  [P1 §2.1; P3 §三 top_k_routing]
+ * Reading: torch.topk leaves the order of ties open; the lower index wins.  A
+ * stable insertion sort of the indices 0..E-1 by value realises exactly that. */
+void oracle_topk_row(int E, int k, const double* v, int32_t* idx) {
+  int order[1024];
+  for (int e = 0; e < E; ++e) order[e] = e;
+  for (int i = 1; i < E; ++i) {
+    int key = order[i], j = i - 1;
+    while (j >= 0 && v[order[j]] < v[key]) { order[j + 1] = order[j]; --j; }
+    order[j + 1] = key;
+  }
+  for (int j = 0; j < k; ++j) idx[j] = order[j];
+}
+
+/* Selection of every token on its logits.  Softmax and the sigmoid are
+ * increasing, so choosing on the logits picks the same experts as choosing on
+ * the probabilities, without ties created by rounding of exp. */
+void oracle_topk(int64_t T, int E, int k, const double* logits, int32_t* idx) {
+  for (int64_t t = 0; t < T; ++t) oracle_topk_row(E, k, logits + t * E, idx + t * k);
+}
+
+/* Renormalised top-k weights  w_j = g_j / sum_{j' < k} g_j'   [P1 §2.1; P3 §三]
+ * with g = softmax probability, or g = sigmoid(l) for normalised-sigmoid
+ * gating (the selected sigmoids divided by their sum) [P2 技术飞跃③]. */
+void oracle_topk_weights(int64_t T, int E, int k, int gating, const double* logits,
+                         const int32_t* idx, double* w) {
+  double* p = (double*)malloc(sizeof(double) * (size_t)E);
+  for (int64_t t = 0; t < T; ++t) {
+    const double* l = logits + t * E;
+    if (gating == OGATE_SOFTMAX) {
+      oracle_gate_probs(1, E, OGATE_SOFTMAX, l, p);
+    } else {
+      for (int e = 0; e < E; ++e) p[e] = 1.0 / (1.0 + exp(-l[e]));
+    }
+    double z = 0.0;
+    for (int j = 0; j < k; ++j) z += p[idx[t * k + j]];
+    for (int j = 0; j < k; ++j) w[t * k + j] = p[idx[t * k + j]] / z;
+  }
+  free(p);
+}
+
+/* Expert capacity  C = ceil((T / E) * capacity_factor), evaluated as
+ * ceil(T * cf / E) in double; cf <= 0 means no limit (returns -1).
+ * [P2 §三 关键技术①; P1 §3.2] */
+int64_t oracle_capacity(int64_t T, int E, double cf) {
+  if (cf <= 0.0) return -1;
+  return (int64_t)ceil((double)T * cf / (double)E);
+}
+
+/* Capacity, drops and the expert-grouped order of the kept assignments.
+ * Walk the tokens in order t = 0..T-1, and each token's choices j = 0..k-1;
+ * the assignment takes the next free slot of its expert while fewer than C
+ * are taken, otherwise it is dropped (it skips the layer: that slot adds
+ * nothing to y) [P2 §三 关键技术①].  Outputs:
+ *   n_pre[e]    selections of e before the cut (feeds f_i)
+ *   counts[e]   kept assignments of e = min(n_pre[e], C)
+ *   offsets[e]  exclusive prefix sum of counts (offsets[E] = total kept)
+ *   dropped     1 where the assignment (t,j) was cut
+ *   slot        offsets[e] + rank of (t,j) among e's kept assignments, or -1
+ *   perm[slot]  the token at each row of the grouped order: experts
+ *               ascending, tokens ascending within an expert [P3 §六]. */
+void oracle_dispatch(int64_t T, int E, int k, int64_t C, const int32_t* idx, int32_t* n_pre,
+                     int32_t* counts, int32_t* offsets, uint8_t* dropped, int32_t* slot, int32_t* perm) {
+  int32_t* rank = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T * k + 1));
+  for (int e = 0; e < E; ++e) { n_pre[e] = 0; counts[e] = 0; }
+  for (int64_t t = 0; t < T; ++t) {
+    for (int j = 0; j < k; ++j) {
+      int e = idx[t * k + j];
+      n_pre[e] += 1;
+      if (C < 0 || counts[e] < C) {
+        rank[t * k + j] = counts[e];
+        counts[e] += 1;
+        dropped[t * k + j] = 0;
+      } else {
+        rank[t * k + j] = -1;
+        dropped[t * k + j] = 1;
+      }
+    }
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  for (int64_t t = 0; t < T; ++t) {
+    for (int j = 0; j < k; ++j) {
+      int64_t a = t * k + j;
+      if (dropped[a]) { slot[a] = -1; continue; }
+      slot[a] = offsets[idx[a]] + rank[a];
+      perm[slot[a]] = (int32_t)t;
+    }
+  }
+  free(rank);
+}
+
+/* Activations.  ReLU [P3 §四]; GELU in its exact erf form, the default of
+ * F.gelu in the pages' experts [P1 §4.1; P4 简化版MoE层]; SiLU z * sigmoid(z)
+ * for the SwiGLU gate [P5 §二]. */
+double oracle_act(int act, double z) {
+  if (act == OACT_RELU) return z > 0.0 ? z : 0.0;
+  if (act == OACT_GELU) return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
+  return z / (1.0 + exp(-z));
+}
+
+/* One expert on one input row.  Expert g's weights are the g-th slabs of the
+ * stacked tensors W1/W3 [G, d, f], W2 [G, f, d], b1 [G, f], b2 [G, d].
+ *   ReLU / GELU:  o = W2^T act(W1^T x + b1) + b2         [P3 §四; P1 §4.1; P4]
+ *   SwiGLU:       o = W2^T (silu(W1^T x) * (W3^T x))     [P5 §二], no biases.
+ * Dropout in the pages' experts is the identity at inference. */
+void oracle_expert_ffn(int d, int f, int act, int dtype, int g, const double* xrow, const void* W1,
+                       const void* b1, const void* W2, const void* b2, const void* W3, double* out) {
+  double* h = (double*)calloc((size_t)f, sizeof(double));
+  double* u = (act == OACT_SWIGLU) ? (double*)calloc((size_t)f, sizeof(double)) : NULL;
+  const int64_t w1o = (int64_t)g * d * f, w2o = (int64_t)g * f * d;
+  if (b1 && act != OACT_SWIGLU)
+    for (int j = 0; j < f; ++j) h[j] = ld(b1, dtype, (int64_t)g * f + j);
+  for (int i = 0; i < d; ++i) {
+    double xi = xrow[i];
+    for (int j = 0; j < f; ++j) h[j] += xi * ld(W1, dtype, w1o + (int64_t)i * f + j);
+    if (u)
+      for (int j = 0; j < f; ++j) u[j] += xi * ld(W3, dtype, w1o + (int64_t)i * f + j);
+  }
+  for (int j = 0; j < f; ++j)
+    h[j] = (act == OACT_SWIGLU) ? oracle_act(OACT_SWIGLU, h[j]) * u[j] : oracle_act(act, h[j]);
+  for (int c = 0; c < d; ++c) out[c] = (b2 && act != OACT_SWIGLU) ? ld(b2, dtype, (int64_t)g * d + c) : 0.0;
+  for (int j = 0; j < f; ++j) {
+    double hj = h[j];
+    for (int c = 0; c < d; ++c) out[c] += hj * ld(W2, dtype, w2o + (int64_t)j * d + c);
+  }
+  free(h);
+  free(u);
+}
+
+/* Layer output for the listed token rows:
+ *   y[t] = sum_{j<k, kept} w_j * E_{idx_j}(x_t)  +  sum_{s<S} E_{E+s}(x_t)
+ * summed in that order [P1 §1.3; P3 §五; P2 §四 技术飞跃② for the always-on
+ * shared experts, added with weight 1].  A dropped assignment contributes 0 and
+ * the kept weights are left as they are [P2 §三 关键技术①]. */
+void oracle_layer_rows(int d, int f, int E, int k, int S, int act, int dtype, const int64_t* rows,
+                       int64_t nrows, const void* x, const void* W1, const void* b1, const void* W2,
+                       const void* b2, const void* W3, const int32_t* idx, const double* w,
+                       const uint8_t* dropped, double* y) {
+  double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+  double* o = (double*)malloc(sizeof(double) * (size_t)d);
+  for (int64_t r = 0; r < nrows; ++r) {
+    int64_t t = rows[r];
+    double* yr = y + r * d;
+    for (int i = 0; i < d; ++i) { xr[i] = ld(x, dtype, t * d + i); yr[i] = 0.0; }
+    for (int j = 0; j < k; ++j) {
+      if (dropped[t * k + j]) continue;
+      oracle_expert_ffn(d, f, act, dtype, idx[t * k + j], xr, W1, b1, W2, b2, W3, o);
+      for (int i = 0; i < d; ++i) yr[i] += w[t * k + j] * o[i];
+    }
+    for (int s = 0; s < S; ++s) {
+      oracle_expert_ffn(d, f, act, dtype, E + s, xr, W1, b1, W2, b2, W3, o);
+      for (int i = 0; i < d; ++i) yr[i] += o[i];
+    }
+  }
+  free(xr);
+  free(o);
+}
+
+/* Switch-style balance statistics   [P1 §2.3; P3 §七]
+ *   f_i = (selections of i before the capacity cut) / (T * k)
+ *   P_i = (1/T) sum_t p[t,i]
+ *   L_aux = alpha * E * sum_i f_i * P_i
+ * Reading: f divides by T*k as in the kamacoder listing, so sum_i f_i = 1 and
+ * L_aux = alpha exactly when routing is uniform.  T = 0 gives zeros. */
+void oracle_balance(int64_t T, int E, int k, double alpha, const int32_t* n_pre, const double* probs,
+                    double* f, double* P, double* L_aux) {
+  double L = 0.0;
+  for (int e = 0; e < E; ++e) {
+    double s = 0.0;
+    for (int64_t t = 0; t < T; ++t) s += probs[t * E + e];
+    f[e] = T > 0 ? (double)n_pre[e] / ((double)T * (double)k) : 0.0;
+    P[e] = T > 0 ? s / (double)T : 0.0;
+    L += f[e] * P[e];
+  }
+  *L_aux = alpha * (double)E * L;
+}
