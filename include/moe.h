@@ -1,0 +1,174 @@
+/*
+ * moe.h -- C ABI of libmoe.so: the forward pass of a token-choice
+ * Mixture-of-Experts feed-forward layer on one NVIDIA B300 (sm_103a).
+ *
+ * The layer, per token t of x [T, d]:
+ *   1. router logits    l[t,e] = b_g[e] + sum_i x[t,i] W_g[i,e]
+ *        ("MoE混合专家模型：Transformer稀疏前馈网络原理与PyTorch实现" §2.1;
+ *         "Mixture of Experts混合专家模型架构原理与路由策略实现", 门控网络的数学原理:
+ *         W_g has shape [d_model, num_experts])
+ *   2. gating           softmax over the E experts ("手撕一个极简 MoE-FFN" §三), or
+ *                       normalised sigmoid: sigmoid per expert, then normalised
+ *                       ("MoE架构解析" §四 技术飞跃③)
+ *   3. top-k            the k largest logits (descending; equal logits: lower
+ *                       expert index first), weights renormalised to sum 1
+ *                       ("手撕一个极简 MoE-FFN" §三, worked example: scores
+ *                       [0.1,0.5,0.3,0.1], k=2 -> experts [1,2], weights
+ *                       [0.625,0.375]); sigmoid gating divides the selected
+ *                       sigmoids by their sum
+ *   4. capacity         C = ceil(T * capacity_factor / E); each expert keeps its
+ *                       first C assignments in token order (token t before t+1,
+ *                       a token's choices in rank order), the rest are dropped:
+ *                       they add nothing to y (they reach the next layer through
+ *                       the residual, which is outside this layer)
+ *                       ("MoE架构解析" §三 关键技术①)
+ *   5. experts          ReLU/GELU: o = act(x W1[e] + b1[e]) W2[e] + b2[e]
+ *                       ("手撕一个极简 MoE-FFN" §四; GELU is the exact erf form);
+ *                       SwiGLU: o = (silu(x W1[e]) * (x W3[e])) W2[e]
+ *                       ("术业有专攻：learn-minimind MoE混合专家模型架构入门指南" §二)
+ *   6. combine          y[t] = sum_{j<k, kept} w_j o_{idx_j}(t) + sum_{s<S} o_{E+s}(t),
+ *                       accumulated in fp32 in exactly that order; shared experts
+ *                       are always active with weight 1 ("MoE架构解析" §四 技术飞跃②)
+ *   7. balance stats    f_i = (selections of i before the capacity cut) / (T k),
+ *                       P_i = mean_t p[t,i], L_aux = alpha * E * sum_i f_i P_i
+ *                       ("手撕一个极简 MoE-FFN" §七; "MoE混合专家模型..." §2.3)
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers (cudaMalloc'd or torch-owned),
+ *    owned by the caller.  The library never allocates, frees or keeps them.
+ *  - Layouts are dense row-major; weights are stored [in, out]:
+ *      x [T, d]; W_g [d, E]; b_g [E]; W1, W3 [E+S, d, f]; W2 [E+S, f, d];
+ *      b1 [E+S, f]; b2 [E+S, d]; y [T, d].  Experts 0..E-1 are routed,
+ *      E..E+S-1 are the shared experts.
+ *    x, W_g, b_g, W*, b*, y have the config's dtype (fp32, or bf16 bits);
+ *    topk_w, f, P, L_aux, router_logits are always fp32.
+ *  - Work is enqueued on `stream` and returns without synchronising.  Host
+ *    checks happen before anything is enqueued; on a non-OK status nothing was
+ *    launched.  Device-side failures (a bounded wait that ran out) are
+ *    recorded in the workspace and reported by moe_check_device_errors().
+ *  - Calls are deterministic: the same inputs give bitwise the same outputs.
+ *  - Calls sharing one workspace must be ordered on the GPU (same stream, or
+ *    synchronised); concurrent calls need separate workspaces.
+ */
+#ifndef MOE_B300_MOE_H
+#define MOE_B300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream; /* a cudaStream_t; NULL = the legacy default stream */
+typedef struct CUevent_st* moe_event;   /* a cudaEvent_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* NULL where a tensor is required, bad sizes, aliasing, misalignment */
+  MOE_ERR_UNSUPPORTED = 2, /* a valid layer this build does not run (e.g. k > 8, d % 64 for bf16) */
+  MOE_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch error, sticky error) */
+  MOE_ERR_TIMEOUT = 5,     /* a device-side wait exceeded its limit; outputs are not valid */
+  MOE_ERR_DEVICE = 6       /* a device-side consistency check failed; outputs are not valid */
+} moe_status;
+
+enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID_NORM = 1 };
+enum { MOE_ACT_RELU = 0, MOE_ACT_GELU = 1, MOE_ACT_SWIGLU = 2, MOE_ACT_NONE = 3 };
+enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 };
+
+/* Number of kernels moe_forward enqueues (the stages that stage events bracket):
+ * router, scan, gather, expert GEMM 1, expert GEMM 2, combine. */
+#define MOE_NUM_STAGES 6
+
+/* The layer.  64 bytes, natural alignment. */
+typedef struct {
+  int64_t T;              /* tokens, >= 0 */
+  int32_t d_model;        /* d */
+  int32_t d_ff;           /* f, hidden width of every expert */
+  int32_t E;              /* routed experts, 1..256 */
+  int32_t k;              /* experts per token, 1..min(E, 8) */
+  int32_t n_shared;       /* always-on shared experts S, 0..8 */
+  int32_t act;            /* MOE_ACT_RELU / _GELU / _SWIGLU */
+  int32_t gating;         /* MOE_GATE_SOFTMAX / _SIGMOID_NORM */
+  int32_t dtype;          /* MOE_DT_F32 / _BF16: storage of x, weights, biases and y */
+  double capacity_factor; /* <= 0: no capacity limit */
+  double alpha;           /* coefficient of L_aux (the pages use 0.01) */
+  int64_t reserved;       /* must be 0 */
+} moe_config;
+
+/* Launch options; pass NULL for defaults. */
+typedef struct {
+  /* If non-NULL: MOE_NUM_STAGES + 1 created events.  Event i is recorded on
+   * `stream` just before stage i, event MOE_NUM_STAGES after the last one. */
+  moe_event* stage_events;
+  /* Limit of every device-side wait in nanoseconds; 0 = 2 s.  A wait that
+   * runs out makes the kernel stop cleanly and records MOE_ERR_TIMEOUT. */
+  int64_t wait_timeout_ns;
+} moe_launch_opts;
+
+/* Human-readable name of a status.  Never NULL. */
+const char* moe_status_string(moe_status s);
+
+/* MOE_OK if the config describes a layer this build runs, else the reason. */
+moe_status moe_validate_config(const moe_config* cfg);
+
+/* Device workspace bytes moe_forward needs for `cfg` (0 if cfg is invalid).
+ * It holds the routing scratch, the expert-grouped copy of x [T*k, d], the
+ * hidden activations [T*k + S*T, f] and expert outputs [T*k + S*T, d]. */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* Expert capacity C = ceil(T * capacity_factor / E) computed in double, or -1
+ * when capacity_factor <= 0 (no limit) ("MoE架构解析" §三 关键技术①). */
+int64_t moe_capacity(const moe_config* cfg);
+
+/* The layer's forward pass (steps 1-7 above).
+ * Inputs (device, read only):
+ *   x, W_g, W1, W2 required; b_g, b1, b2 optional (NULL = no bias; biases are
+ *   not used with SwiGLU); W3 required iff act == MOE_ACT_SWIGLU.
+ * Outputs (device, written):
+ *   y [T, d] (must not overlap x), topk_idx int32 [T, k] (descending logit),
+ *   topk_w fp32 [T, k], expert_counts int32 [E] (kept assignments per expert),
+ *   dropped_mask uint8 [T, k] (1 = cut by capacity), f fp32 [E], P fp32 [E],
+ *   L_aux fp32 [1].
+ * Optional outputs (NULL = not written):
+ *   router_logits fp32 [T, E]; perm_token int32 [T*k]: token of each row of
+ *   the expert-grouped order (experts ascending, tokens ascending inside an
+ *   expert; entries past sum(expert_counts) are not written); slot int32 [T, k]:
+ *   row of assignment (t, j) in that order, -1 if dropped.
+ * workspace: device, 256-byte aligned, >= moe_workspace_size(cfg) bytes,
+ *   owned by the caller, contents need not be initialised.
+ * All device pointers must be 16-byte aligned.  T == 0 is valid: it writes
+ * expert_counts = f = P = 0 and L_aux = 0. */
+moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
+                       const void* W1, const void* b1, const void* W2, const void* b2, const void* W3,
+                       void* y, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                       uint8_t* dropped_mask, float* f, float* P, float* L_aux, float* router_logits,
+                       int32_t* perm_token, int32_t* slot, void* workspace, size_t workspace_bytes,
+                       moe_stream stream, const moe_launch_opts* opts);
+
+/* Waits for `stream`, then reports the device-side status of the last call
+ * that used `workspace`: MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE, or
+ * MOE_ERR_CUDA if the stream itself reports an error.  Synchronising. */
+moe_status moe_check_device_errors(const void* workspace, moe_stream stream);
+
+/* The expert grouped GEMM on its own (the layer's step 5 for one weight set):
+ *   for every group g and row r in [seg_offsets[g], seg_offsets[g+1]):
+ *     act == MOE_ACT_NONE:    C[r, :] = A[r, :] B[g] (+ bias[g])
+ *     act == MOE_ACT_RELU/GELU: C[r, :] = act(A[r, :] B[g] + bias[g])
+ *     act == MOE_ACT_SWIGLU:  C[r, :] = silu(A[r, :] B[g]) * (A[r, :] B3[g])
+ * A [M, K], B and B3 [G, K, N], bias [G, N] or NULL, C [M, N]; rows of C
+ * outside every group are not written.  seg_offsets: DEVICE int32 [G+1],
+ * non-decreasing, seg_offsets[0] >= 0, seg_offsets[G] <= M.  fp32
+ * accumulation; C is rounded to dtype.  bf16 needs K, N multiples of 64.
+ * workspace: >= moe_grouped_gemm_workspace_size(G) bytes, 256-byte aligned. */
+size_t moe_grouped_gemm_workspace_size(int32_t G);
+moe_status moe_grouped_gemm(int32_t dtype, int32_t act, int32_t G, const int32_t* seg_offsets, int64_t M,
+                            int32_t K, int32_t N, const void* A, const void* B, const void* B3,
+                            const void* bias, void* C, void* workspace, size_t workspace_bytes,
+                            moe_stream stream, const moe_launch_opts* opts);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_MOE_H */

@@ -1,0 +1,281 @@
+"""B300-native forward pass of a token-choice Mixture-of-Experts FFN layer.
+
+A thin ctypes binding over ``libmoe.so`` (C ABI in ``include/moe.h``).  Every
+step of the layer runs in the library's CUDA kernels; this module only checks
+tensor shapes, allocates outputs and workspace through PyTorch, and passes raw
+device pointers and the current CUDA stream.  There is no fallback: if the
+library is missing, or no CUDA device is present, calls raise.
+
+    import sparse_mixture_experts_48_b300 as moe
+    cfg = moe.MoEConfig(T=4096, d=768, f=3072, E=8, k=2, S=0, act=moe.GELU,
+                        gating=moe.SOFTMAX, dtype=moe.BF16)
+    out = moe.forward(cfg, x, W_g, b_g, W1, b1, W2, b2)      # torch CUDA tensors
+    out.y, out.topk_idx, out.topk_w, out.expert_counts, out.L_aux ...
+
+bf16 tensors may be passed as torch.bfloat16 or as int16/uint16 raw bits.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+RELU, GELU, SWIGLU, NONE = 0, 1, 2, 3
+SOFTMAX, SIGMOID_NORM = 0, 1
+F32, BF16 = 0, 1
+NUM_STAGES = 6
+STAGE_NAMES = ("router", "scan", "gather", "expert_gemm1", "expert_gemm2", "combine")
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+@dataclasses.dataclass(frozen=True)
+class MoEConfig:
+    T: int
+    d: int
+    f: int
+    E: int
+    k: int
+    S: int = 0
+    act: int = SWIGLU
+    gating: int = SOFTMAX
+    dtype: int = BF16
+    capacity_factor: float = 0.0
+    alpha: float = 0.01
+
+
+class _CConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("n_shared", ctypes.c_int32),
+                ("act", ctypes.c_int32), ("gating", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("capacity_factor", ctypes.c_double), ("alpha", ctypes.c_double), ("reserved", ctypes.c_int64)]
+
+
+class _COpts(ctypes.Structure):
+    _fields_ = [("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("wait_timeout_ns", ctypes.c_int64)]
+
+
+_lib_handle: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmoe.so.  Raises if it has not been built."""
+    global _lib_handle
+    if _lib_handle is not None:
+        return _lib_handle
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m sparse_mixture_experts_48_b300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64
+    cfgp = ctypes.POINTER(_CConfig)
+    optp = ctypes.POINTER(_COpts)
+    L.moe_status_string.restype = ctypes.c_char_p
+    L.moe_status_string.argtypes = [ctypes.c_int]
+    L.moe_validate_config.restype = ctypes.c_int
+    L.moe_validate_config.argtypes = [cfgp]
+    L.moe_workspace_size.restype = sz
+    L.moe_workspace_size.argtypes = [cfgp]
+    L.moe_capacity.restype = i64
+    L.moe_capacity.argtypes = [cfgp]
+    L.moe_forward.restype = ctypes.c_int
+    L.moe_forward.argtypes = [cfgp] + [vp] * 8 + [vp] * 11 + [vp, sz, vp, optp]
+    L.moe_check_device_errors.restype = ctypes.c_int
+    L.moe_check_device_errors.argtypes = [vp, vp]
+    L.moe_grouped_gemm_workspace_size.restype = sz
+    L.moe_grouped_gemm_workspace_size.argtypes = [i32]
+    L.moe_grouped_gemm.restype = ctypes.c_int
+    L.moe_grouped_gemm.argtypes = [i32, i32, i32, vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, optp]
+    _lib_handle = L
+    return L
+
+
+def exported_symbols() -> Sequence[str]:
+    return ("moe_status_string", "moe_validate_config", "moe_workspace_size", "moe_capacity", "moe_forward",
+            "moe_check_device_errors", "moe_grouped_gemm_workspace_size", "moe_grouped_gemm")
+
+
+def c_config(cfg) -> _CConfig:
+    return _CConfig(int(cfg.T), int(cfg.d), int(cfg.f), int(cfg.E), int(cfg.k), int(cfg.S), int(cfg.act),
+                    int(cfg.gating), int(cfg.dtype), float(cfg.capacity_factor), float(cfg.alpha), 0)
+
+
+def validate(cfg) -> int:
+    return int(lib().moe_validate_config(ctypes.byref(c_config(cfg))))
+
+
+def workspace_size(cfg) -> int:
+    return int(lib().moe_workspace_size(ctypes.byref(c_config(cfg))))
+
+
+def capacity(cfg) -> int:
+    return int(lib().moe_capacity(ctypes.byref(c_config(cfg))))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _opts(stage_events, timeout_ns: int):
+    if stage_events is None and not timeout_ns:
+        return None, None
+    arr = None
+    if stage_events is not None:
+        arr = (ctypes.c_void_p * len(stage_events))(*[ctypes.c_void_p(e.cuda_event) for e in stage_events])
+    o = _COpts(ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)) if arr is not None else None, int(timeout_ns))
+    return o, arr
+
+
+_STORE = {F32: (torch.float32,), BF16: (torch.bfloat16, torch.int16, torch.uint16)}
+
+
+def _check(t: Optional[torch.Tensor], name: str, shape, dtypes, required=True):
+    if t is None:
+        if required:
+            raise ValueError(f"{name} is required")
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected one of {dtypes}")
+
+
+@dataclasses.dataclass
+class MoEOutput:
+    y: torch.Tensor
+    topk_idx: torch.Tensor
+    topk_w: torch.Tensor
+    expert_counts: torch.Tensor
+    dropped_mask: torch.Tensor
+    f: torch.Tensor
+    P: torch.Tensor
+    L_aux: torch.Tensor
+    router_logits: Optional[torch.Tensor] = None
+    perm_token: Optional[torch.Tensor] = None
+    slot: Optional[torch.Tensor] = None
+    workspace: Optional[torch.Tensor] = None
+
+
+def alloc_outputs(cfg, device, debug: bool = False, y_dtype=None) -> MoEOutput:
+    T, d, E, k = cfg.T, cfg.d, cfg.E, cfg.k
+    yd = y_dtype or (torch.float32 if cfg.dtype == F32 else torch.bfloat16)
+    out = MoEOutput(
+        y=torch.empty((T, d), dtype=yd, device=device),
+        topk_idx=torch.empty((T, k), dtype=torch.int32, device=device),
+        topk_w=torch.empty((T, k), dtype=torch.float32, device=device),
+        expert_counts=torch.empty((E,), dtype=torch.int32, device=device),
+        dropped_mask=torch.empty((T, k), dtype=torch.uint8, device=device),
+        f=torch.empty((E,), dtype=torch.float32, device=device),
+        P=torch.empty((E,), dtype=torch.float32, device=device),
+        L_aux=torch.empty((1,), dtype=torch.float32, device=device))
+    if debug:
+        out.router_logits = torch.empty((T, E), dtype=torch.float32, device=device)
+        out.perm_token = torch.full((max(T * k, 1),), -1, dtype=torch.int32, device=device)
+        out.slot = torch.empty((T, k), dtype=torch.int32, device=device)
+    return out
+
+
+def alloc_workspace(cfg, device) -> torch.Tensor:
+    n = workspace_size(cfg)
+    if n == 0:
+        raise MoEError(validate(cfg), "moe_workspace_size")
+    return torch.empty((n,), dtype=torch.uint8, device=device)
+
+
+def forward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutput] = None,
+            workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+            debug: bool = False, stage_events=None, timeout_ns: int = 0) -> MoEOutput:
+    """Enqueue the layer's forward pass on ``stream`` (default: the current one).
+
+    Asynchronous: returns once the kernels are enqueued.  Host-detected errors
+    raise MoEError; device-side ones are reported by check_device_errors()."""
+    if not torch.cuda.is_available():
+        raise RuntimeError("the MoE layer runs on a CUDA device; none is available")
+    T, d, f, E, k, S = cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S
+    G = E + S
+    st = _STORE[cfg.dtype]
+    _check(x, "x", (T, d), st)
+    _check(W_g, "W_g", (d, E), st)
+    _check(b_g, "b_g", (E,), st, required=False)
+    _check(W1, "W1", (G, d, f), st)
+    _check(W3, "W3", (G, d, f), st, required=cfg.act == SWIGLU)
+    _check(W2, "W2", (G, f, d), st)
+    _check(b1, "b1", (G, f), st, required=False)
+    _check(b2, "b2", (G, d), st, required=False)
+    dev = x.device
+    if out is None:
+        out = alloc_outputs(cfg, dev, debug=debug)
+    if workspace is None:
+        workspace = out.workspace if out.workspace is not None else alloc_workspace(cfg, dev)
+    out.workspace = workspace
+    opts, keep = _opts(stage_events, timeout_ns)
+    ccfg = c_config(cfg)
+    with torch.cuda.device(dev):
+        status = lib().moe_forward(
+            ctypes.byref(ccfg), _ptr(x), _ptr(W_g), _ptr(b_g), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(W3),
+            _ptr(out.y), _ptr(out.topk_idx), _ptr(out.topk_w), _ptr(out.expert_counts), _ptr(out.dropped_mask),
+            _ptr(out.f), _ptr(out.P), _ptr(out.L_aux), _ptr(out.router_logits), _ptr(out.perm_token),
+            _ptr(out.slot), _ptr(workspace), workspace.numel(), _stream_handle(stream),
+            ctypes.byref(opts) if opts is not None else None)
+    del keep
+    if status != 0:
+        raise MoEError(status, "moe_forward")
+    return out
+
+
+def check_device_errors(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise ``stream`` and return the device status of the last call."""
+    return int(lib().moe_check_device_errors(_ptr(workspace), _stream_handle(stream)))
+
+
+def grouped_gemm(dtype: int, act: int, seg_offsets: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                 B3: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
+                 C: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None, stage_events=None, timeout_ns: int = 0):
+    """C[r] = epilogue(A[r] @ B[g]) for the rows r of each group g (see moe.h)."""
+    G, K, N = B.shape
+    M = A.shape[0]
+    if seg_offsets.dtype != torch.int32 or tuple(seg_offsets.shape) != (G + 1,) or not seg_offsets.is_cuda:
+        raise ValueError("seg_offsets must be a CUDA int32 tensor of G+1 entries")
+    if A.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    st = _STORE[dtype]
+    _check(A, "A", (M, K), st)
+    _check(B, "B", (G, K, N), st)
+    _check(B3, "B3", (G, K, N), st, required=act == SWIGLU)
+    _check(bias, "bias", (G, N), st, required=False)
+    if C is None:
+        C = torch.zeros((M, N), dtype=A.dtype, device=A.device)
+    if workspace is None:
+        workspace = torch.empty((lib().moe_grouped_gemm_workspace_size(G),), dtype=torch.uint8, device=A.device)
+    opts, keep = _opts(stage_events, timeout_ns)
+    with torch.cuda.device(A.device):
+        status = lib().moe_grouped_gemm(dtype, act, G, _ptr(seg_offsets), M, K, N, _ptr(A), _ptr(B), _ptr(B3),
+                                        _ptr(bias), _ptr(C), _ptr(workspace), workspace.numel(),
+                                        _stream_handle(stream), ctypes.byref(opts) if opts is not None else None)
+    del keep
+    if status != 0:
+        raise MoEError(status, "moe_grouped_gemm")
+    return C, workspace

@@ -1,0 +1,195 @@
+// K2 -- dispatch: capacity slots in token order, drops, the expert-grouped
+// order of the kept assignments, the balance statistics, and the gather of x
+// rows into the expert-contiguous buffer the grouped GEMM reads.
+//
+// Two launches:
+//   scan    one CTA: per expert, an exclusive prefix over the router CTAs of
+//           their selection counts (so every assignment's rank among earlier
+//           tokens choosing the same expert is known), the pre-capacity
+//           counts n_e, kept counts min(n_e, C), segment offsets, f, P, L_aux
+//           and the segment / tile table of the grouped GEMMs.
+//   gather  one warp per token: rank = CTA prefix + local rank; kept iff
+//           rank < C; slot = offset[e] + rank; then the token's row of x is
+//           read once with 16-byte loads and written to each kept slot.
+// All sums use a fixed order, so results are bitwise reproducible.
+//
+// Sources: "MoE架构解析" §三 关键技术① (capacity = tokens / experts x capacity
+// factor; overflow skips the layer); "手撕一个极简 MoE-FFN" §六 (gather the
+// tokens of one expert and run the expert once on the batch), §七 (f = counts /
+// (T k), P = mean score, L = alpha N sum f P); "MoE混合专家模型：Transformer稀疏
+// 前馈网络原理与PyTorch实现" §2.3 (Switch load-balance loss).
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kMaxE = 256;
+
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
+  __shared__ int s_npre[kMaxE];
+  __shared__ double s_psum[kMaxE];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
+  const int E = a.E;
+  for (int e = warp; e < E; e += nwarps) {
+    int run = 0;
+    double ps = 0.0;
+    for (int64_t b0 = 0; b0 < a.nblk; b0 += 32) {
+      const int64_t b = b0 + lane;
+      const int v = b < a.nblk ? a.hist[b * E + e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += n;
+      }
+      if (b < a.nblk) a.base[b * E + e] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+      if (b < a.nblk) ps += (double)a.psum[b * E + e];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    if (lane == 0) { s_npre[e] = run; s_psum[e] = ps; }
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  const double Tk = (double)a.T * (double)a.k;
+  int off = 0;
+  double L = 0.0;
+  for (int e = 0; e < E; ++e) {
+    const int n = s_npre[e];
+    const int c = (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
+    a.n_pre[e] = n;
+    a.counts[e] = c;
+    a.offsets[e] = off;
+    off += c;
+    const double fe = a.T > 0 ? (double)n / Tk : 0.0;
+    const double Pe = a.T > 0 ? s_psum[e] / (double)a.T : 0.0;
+    a.f[e] = (float)fe;
+    a.P[e] = (float)Pe;
+    L += fe * Pe;
+  }
+  a.offsets[E] = off;
+  *a.L_aux = (float)(a.alpha * (double)E * L);
+  // Segments of the grouped GEMMs: routed experts read the grouped copy of x,
+  // shared experts read x itself and write rows T*k + s*T.
+  int mt = 0;
+  const int G = E + a.S;
+  for (int g = 0; g < G; ++g) {
+    int rows, w, orow, arow, asrc;
+    if (g < E) { rows = a.counts[g]; w = g; orow = a.offsets[g]; arow = orow; asrc = 0; }
+    else { rows = (int)a.T; w = g; orow = (int)(a.rows_tk + (int64_t)(g - E) * a.T); arow = 0; asrc = 1; }
+    a.seg.rows[g] = rows;
+    a.seg.w[g] = w;
+    a.seg.out_row[g] = orow;
+    a.seg.a_row[g] = arow;
+    a.seg.a_src[g] = asrc;
+    a.seg.mtile_start[g] = mt;
+    mt += (rows + kGemmBM - 1) / kGemmBM;
+  }
+  a.seg.mtile_start[G] = mt;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(GatherArgs a) {
+  const int lane = threadIdx.x % 32;
+  const int64_t t = (int64_t)blockIdx.x * kGatherWarps + threadIdx.x / 32;
+  if (t >= a.T) return;
+  const int k = a.k, E = a.E;
+  int my_slot = -1;
+  if (lane < k) {
+    const int e = a.topk_idx[t * k + lane];
+    const int64_t b = t / kRouterBM;
+    const int r = a.base[b * E + e] + (int)a.lrank[t * k + lane];
+    const bool kept = a.capacity < 0 || r < a.capacity;
+    my_slot = kept ? a.offsets[e] + r : -1;
+    a.slot[t * k + lane] = my_slot;
+    a.dropped[t * k + lane] = kept ? 0 : 1;
+    if (kept && a.perm_token) a.perm_token[my_slot] = (int32_t)t;
+  }
+  int slots[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) slots[j] = __shfl_sync(0xffffffffu, my_slot, j);
+  const int esz = a.dtype == MOE_DT_BF16 ? 2 : 4;
+  const int64_t chunks = (int64_t)a.d * esz / 16;
+  const uint4* src = (const uint4*)((const uint8_t*)a.x + t * chunks * 16);
+  uint4* dst = (uint4*)a.xperm;
+  constexpr int U = 4;
+  for (int64_t c0 = lane; c0 < chunks; c0 += 32 * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t c = c0 + u * 32;
+      if (c < chunks) v[u] = ld_stream(src + c);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k && slots[j] >= 0) {
+        uint4* drow = dst + (int64_t)slots[j] * chunks;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t c = c0 + u * 32;
+          if (c < chunks) drow[c] = v[u];
+        }
+      }
+    }
+  }
+}
+
+// Segment table of the standalone grouped GEMM from caller row offsets.  The
+// offsets are checked on the device: if any segment is not inside [0, M] or
+// they decrease, no segment gets rows (nothing is computed or written) and the
+// error word records it.
+__global__ void segments_kernel(const int32_t* off, int G, int64_t M, SegTable seg, uint32_t* err) {
+  if (threadIdx.x != 0) return;
+  bool bad = false;
+  for (int g = 0; g < G; ++g) {
+    const int64_t lo = off[g], hi = off[g + 1];
+    if (lo < 0 || hi < lo || hi > M) bad = true;
+  }
+  int mt = 0;
+  for (int g = 0; g < G; ++g) {
+    const int rows = bad ? 0 : off[g + 1] - off[g];
+    seg.rows[g] = rows;
+    seg.w[g] = g;
+    seg.out_row[g] = bad ? 0 : off[g];
+    seg.a_row[g] = seg.out_row[g];
+    seg.a_src[g] = 0;
+    seg.mtile_start[g] = mt;
+    mt += (rows + kGemmBM - 1) / kGemmBM;
+  }
+  seg.mtile_start[G] = mt;
+  if (bad) record_error(err, kErrDevice, 0x200);
+}
+
+}  // namespace
+
+cudaError_t launch_segments_from_offsets(const int32_t* offsets, int G, int64_t M, SegTable seg, uint32_t* err,
+                                         cudaStream_t s) {
+  segments_kernel<<<1, 32, 0, s>>>(offsets, G, M, seg, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s) {
+  scan_kernel<<<1, kScanThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {
+  if (a.T == 0) return cudaSuccess;
+  const int64_t blocks = (a.T + kGatherWarps - 1) / kGatherWarps;
+  gather_kernel<<<(unsigned)blocks, kGatherWarps * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,102 @@
+// Host-side launchers of the MoE-FFN kernels (one per pipeline stage).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct RouterArgs {
+  const void* x;    // [T, d]
+  const void* Wg;   // [d, E]
+  const void* bg;   // [E] or null
+  int64_t T;
+  int d, E, k, gating, dtype;
+  float* logits_out;   // [T, E] or null
+  int32_t* topk_idx;   // [T, k]
+  float* topk_w;       // [T, k]
+  uint8_t* lrank;      // [T, k] rank among the CTA's earlier tokens choosing the same expert
+  int32_t* hist;       // [nblk, E] selections per router CTA
+  float* psum;         // [nblk, E] sum of gate probabilities per router CTA
+};
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+
+struct ScanArgs {
+  int64_t T;
+  int E, k, S;
+  int64_t capacity;    // -1: unlimited
+  double alpha;
+  int64_t nblk;
+  const int32_t* hist;
+  const float* psum;
+  int32_t* base;       // [nblk, E]
+  int32_t* n_pre;      // [E]
+  int32_t* counts;     // [E] kept
+  int32_t* offsets;    // [E+1]
+  float* f;
+  float* P;
+  float* L_aux;
+  SegTable seg;
+  int64_t rows_tk;     // T * k: first H / O row of the shared experts
+};
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
+
+struct GatherArgs {
+  const void* x;
+  int64_t T;
+  int d, E, k, dtype;
+  int64_t capacity;
+  const int32_t* topk_idx;
+  const uint8_t* lrank;
+  const int32_t* base;
+  const int32_t* offsets;
+  int32_t* slot;        // [T, k]
+  uint8_t* dropped;     // [T, k]
+  int32_t* perm_token;  // [T*k] or null
+  void* xperm;          // [T*k, d]
+};
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
+
+struct CombineArgs {
+  const void* o;        // [rows_all, d]
+  int64_t T;
+  int d, k, S, dtype;
+  int64_t rows_tk;
+  const int32_t* slot;
+  const float* topk_w;
+  void* y;              // [T, d]
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+
+// Grouped GEMM over the segment table.
+struct GemmArgs {
+  int dtype;
+  int act;              // MOE_ACT_*
+  int G;
+  int K, N;
+  bool a_from_out_rows; // A row of segment g = seg.out_row[g] (else seg.a_row / seg.a_src)
+  SegTable seg;
+  const void* A0;       // [rows_A0, K]
+  int64_t rows_A0;
+  const void* A1;       // [rows_A1, K] (second A source) or null
+  int64_t rows_A1;
+  const void* B;        // [Gw, K, N]
+  const void* B3;       // [Gw, K, N] or null (SwiGLU)
+  int Gw;               // weight slabs
+  const void* bias;     // [Gw, N] or null
+  void* C;              // [rows, N]
+  int64_t max_mtiles;   // upper bound of seg.mtile_start[G]
+  uint32_t* err;
+  int64_t timeout_ns;
+};
+cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
+
+// Builds a segment table from row offsets (standalone grouped GEMM entry point).
+cudaError_t launch_segments_from_offsets(const int32_t* offsets, int G, int64_t M, SegTable seg, uint32_t* err,
+                                         cudaStream_t s);
+
+int sm_count();
+
+}  // namespace moe

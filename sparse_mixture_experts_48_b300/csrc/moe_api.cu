@@ -1,0 +1,271 @@
+// The C ABI of libmoe.so (declared in include/moe.h): argument checks,
+// workspace layout, and the launch sequence of the layer's kernels.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 8;
+constexpr int kMaxShared = 8;
+constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+moe_status check_cfg(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d_model <= 0 || c->d_ff <= 0 || c->E <= 0 || c->k <= 0 || c->n_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->k > c->E) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_GELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (c->gating != MOE_GATE_SOFTMAX && c->gating != MOE_GATE_SIGMOID_NORM) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_DT_F32 && c->dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->reserved != 0) return MOE_ERR_INVALID_ARG;
+  if (!isfinite(c->capacity_factor) || !isfinite(c->alpha)) return MOE_ERR_INVALID_ARG;
+  if (c->E > kMaxE || c->k > kMaxK || c->n_shared > kMaxShared) return MOE_ERR_UNSUPPORTED;
+  if (c->dtype == MOE_DT_BF16 && (c->d_model % 64 != 0 || c->d_ff % 64 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (c->dtype == MOE_DT_F32 && (c->d_model % 4 != 0 || c->d_ff % 4 != 0)) return MOE_ERR_UNSUPPORTED;
+  // Row indices of the grouped buffers are int32 (and TMA coordinates).
+  const int64_t rows_all = c->T * (int64_t)c->k + (int64_t)c->n_shared * c->T;
+  if (rows_all >= ((int64_t)1 << 31) - 2 * kGemmBM) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+WsLayout layout(const moe_config* c) {
+  WsLayout L;
+  const size_t esz = c->dtype == MOE_DT_BF16 ? 2 : 4;
+  L.nblk = (c->T + kRouterBM - 1) / kRouterBM;
+  L.rows_tk = c->T * (int64_t)c->k;
+  L.rows_all = L.rows_tk + (int64_t)c->n_shared * c->T;
+  L.G = c->E + c->n_shared;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align_up(off + (bytes ? bytes : 1), 256);
+    return at;
+  };
+  L.hdr = take(sizeof(WsHeader));
+  L.hist = take((size_t)L.nblk * c->E * 4);
+  L.psum = take((size_t)L.nblk * c->E * 4);
+  L.base = take((size_t)L.nblk * c->E * 4);
+  L.lrank = take((size_t)L.rows_tk);
+  L.npre = take((size_t)c->E * 4);
+  L.offsets = take((size_t)(c->E + 1) * 4);
+  L.seg = take((size_t)(6 * L.G + 1) * 4);
+  L.slot = take((size_t)L.rows_tk * 4);
+  L.xperm = take((size_t)L.rows_tk * c->d_model * esz);
+  L.h = take((size_t)L.rows_all * c->d_ff * esz);
+  L.o = take((size_t)L.rows_all * c->d_model * esz);
+  L.total = off;
+  return L;
+}
+
+SegTable seg_table(uint8_t* ws, size_t off, int G) {
+  int* p = (int*)(ws + off);
+  SegTable s;
+  s.rows = p;
+  s.w = p + G;
+  s.out_row = p + 2 * G;
+  s.a_row = p + 3 * G;
+  s.a_src = p + 4 * G;
+  s.mtile_start = p + 5 * G;
+  return s;
+}
+
+int64_t capacity_of(const moe_config* c) {
+  if (c->capacity_factor <= 0.0) return -1;
+  // ceil(T * cf / E) in double, the expert-capacity formula.
+  return (int64_t)ceil((double)c->T * c->capacity_factor / (double)c->E);
+}
+
+struct StageClock {
+  const moe_launch_opts* o;
+  cudaStream_t s;
+  cudaError_t mark(int i) const {
+    if (o && o->stage_events) return cudaEventRecord((cudaEvent_t)o->stage_events[i], s);
+    return cudaSuccess;
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status moe_validate_config(const moe_config* cfg) { return check_cfg(cfg); }
+
+size_t moe_workspace_size(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return layout(cfg).total;
+}
+
+int64_t moe_capacity(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return -1;
+  return capacity_of(cfg);
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, const void* b_g, const void* W1,
+                       const void* b1, const void* W2, const void* b2, const void* W3, void* y, int32_t* topk_idx,
+                       float* topk_w, int32_t* expert_counts, uint8_t* dropped_mask, float* f, float* P,
+                       float* L_aux, float* router_logits, int32_t* perm_token, int32_t* slot, void* workspace,
+                       size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts) {
+  moe_status st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  // Required tensors.
+  if (!x || !W_g || !W1 || !W2 || !y || !topk_idx || !topk_w || !expert_counts || !dropped_mask || !f || !P ||
+      !L_aux)
+    return MOE_ERR_INVALID_ARG;
+  if (swiglu != (W3 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (swiglu && (b1 || b2)) return MOE_ERR_INVALID_ARG;
+  const void* all[] = {x, W_g, b_g, W1, b1, W2, b2, W3, y, topk_idx, topk_w, expert_counts, dropped_mask,
+                       f, P, L_aux, router_logits, perm_token, slot};
+  for (const void* p : all)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  // y must not overlap x.
+  const size_t esz = c.dtype == MOE_DT_BF16 ? 2 : 4;
+  const size_t xbytes = (size_t)c.T * c.d_model * esz;
+  if (xbytes && (const uint8_t*)y < (const uint8_t*)x + xbytes && (const uint8_t*)x < (const uint8_t*)y + xbytes)
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout(&c);
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  const int64_t timeout = (opts && opts->wait_timeout_ns > 0) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = (uint8_t*)workspace;
+  WsHeader* hdr = (WsHeader*)(ws + L.hdr);
+  const SegTable seg = seg_table(ws, L.seg, L.G);
+  int32_t* slot_buf = slot ? slot : (int32_t*)(ws + L.slot);
+  const int64_t C = capacity_of(&c);
+  StageClock clk{opts, s};
+
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 1. router
+  if (clk.mark(0) != cudaSuccess) return MOE_ERR_CUDA;
+  RouterArgs ra;
+  ra.x = x; ra.Wg = W_g; ra.bg = b_g; ra.T = c.T; ra.d = c.d_model; ra.E = c.E; ra.k = c.k;
+  ra.gating = c.gating; ra.dtype = c.dtype; ra.logits_out = router_logits; ra.topk_idx = topk_idx;
+  ra.topk_w = topk_w; ra.lrank = ws + L.lrank; ra.hist = (int32_t*)(ws + L.hist); ra.psum = (float*)(ws + L.psum);
+  if (launch_router(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 2. scan: ranks, capacity, offsets, statistics, segment table
+  if (clk.mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+  ScanArgs sa;
+  sa.T = c.T; sa.E = c.E; sa.k = c.k; sa.S = c.n_shared; sa.capacity = C; sa.alpha = c.alpha; sa.nblk = L.nblk;
+  sa.hist = ra.hist; sa.psum = ra.psum; sa.base = (int32_t*)(ws + L.base); sa.n_pre = (int32_t*)(ws + L.npre);
+  sa.counts = expert_counts; sa.offsets = (int32_t*)(ws + L.offsets); sa.f = f; sa.P = P; sa.L_aux = L_aux;
+  sa.seg = seg; sa.rows_tk = L.rows_tk;
+  if (launch_scan(sa, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 3. gather into the expert-grouped buffer
+  if (clk.mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+  GatherArgs ga;
+  ga.x = x; ga.T = c.T; ga.d = c.d_model; ga.E = c.E; ga.k = c.k; ga.dtype = c.dtype; ga.capacity = C;
+  ga.topk_idx = topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.offsets = sa.offsets; ga.slot = slot_buf;
+  ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm;
+  if (launch_gather(ga, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 4./5. expert GEMMs
+  const int64_t max_mtiles = (L.rows_tk + kGemmBM - 1) / kGemmBM + c.E +
+                             (int64_t)c.n_shared * ((c.T + kGemmBM - 1) / kGemmBM);
+  GemmArgs g1;
+  memset(&g1, 0, sizeof(g1));
+  g1.dtype = c.dtype; g1.act = c.act; g1.G = L.G; g1.K = c.d_model; g1.N = c.d_ff; g1.a_from_out_rows = false;
+  g1.seg = seg; g1.A0 = ws + L.xperm; g1.rows_A0 = L.rows_tk > 0 ? L.rows_tk : 1;
+  g1.A1 = c.n_shared > 0 ? x : nullptr; g1.rows_A1 = c.T;
+  g1.B = W1; g1.B3 = W3; g1.Gw = L.G; g1.bias = b1; g1.C = ws + L.h; g1.max_mtiles = c.T > 0 ? max_mtiles : 0;
+  g1.err = &hdr->err; g1.timeout_ns = timeout;
+  if (clk.mark(3) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_grouped_gemm(g1, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  GemmArgs g2 = g1;
+  g2.act = MOE_ACT_NONE; g2.K = c.d_ff; g2.N = c.d_model; g2.a_from_out_rows = true;
+  g2.A0 = ws + L.h; g2.rows_A0 = L.rows_all > 0 ? L.rows_all : 1; g2.A1 = nullptr; g2.rows_A1 = 0;
+  g2.B = W2; g2.B3 = nullptr; g2.bias = b2; g2.C = ws + L.o;
+  if (clk.mark(4) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_grouped_gemm(g2, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 6. combine
+  if (clk.mark(5) != cudaSuccess) return MOE_ERR_CUDA;
+  CombineArgs ca;
+  ca.o = ws + L.o; ca.T = c.T; ca.d = c.d_model; ca.k = c.k; ca.S = c.n_shared; ca.dtype = c.dtype;
+  ca.rows_tk = L.rows_tk; ca.slot = slot_buf; ca.topk_w = topk_w; ca.y = y;
+  if (launch_combine(ca, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (clk.mark(6) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_check_device_errors(const void* workspace, moe_stream stream) {
+  if (!workspace) return MOE_ERR_WORKSPACE;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  WsHeader h;
+  if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h.err & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (h.err & kErrDevice) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+size_t moe_grouped_gemm_workspace_size(int32_t G) {
+  if (G <= 0) return 0;
+  return align_up(sizeof(WsHeader), 256) + align_up((size_t)(6 * G + 1) * 4, 256);
+}
+
+moe_status moe_grouped_gemm(int32_t dtype, int32_t act, int32_t G, const int32_t* seg_offsets, int64_t M, int32_t K,
+                            int32_t N, const void* A, const void* B, const void* B3, const void* bias, void* C,
+                            void* workspace, size_t workspace_bytes, moe_stream stream,
+                            const moe_launch_opts* opts) {
+  if (dtype != MOE_DT_F32 && dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+  if (act != MOE_ACT_NONE && act != MOE_ACT_RELU && act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU)
+    return MOE_ERR_INVALID_ARG;
+  if (G <= 0 || M < 0 || K <= 0 || N <= 0 || !seg_offsets || !A || !B || !C) return MOE_ERR_INVALID_ARG;
+  if ((act == MOE_ACT_SWIGLU) != (B3 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (G > 264) return MOE_ERR_UNSUPPORTED;
+  if (dtype == MOE_DT_BF16 && (K % 64 != 0 || N % 64 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (M >= ((int64_t)1 << 31) - 2 * kGemmBM) return MOE_ERR_UNSUPPORTED;
+  const void* all[] = {seg_offsets, A, B, B3, bias, C};
+  for (const void* p : all)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_grouped_gemm_workspace_size(G);
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = (uint8_t*)workspace;
+  WsHeader* hdr = (WsHeader*)ws;
+  const SegTable seg = seg_table(ws, align_up(sizeof(WsHeader), 256), G);
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_segments_from_offsets(seg_offsets, G, M, seg, &hdr->err, s) != cudaSuccess) return MOE_ERR_CUDA;
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.dtype = dtype; g.act = act; g.G = G; g.K = K; g.N = N; g.a_from_out_rows = true; g.seg = seg;
+  g.A0 = A; g.rows_A0 = M > 0 ? M : 1; g.A1 = nullptr; g.B = B; g.B3 = B3; g.Gw = G; g.bias = bias; g.C = C;
+  g.max_mtiles = M > 0 ? (M + kGemmBM - 1) / kGemmBM + G : 0;
+  g.err = &hdr->err;
+  g.timeout_ns = (opts && opts->wait_timeout_ns > 0) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
+  if (opts && opts->stage_events && cudaEventRecord((cudaEvent_t)opts->stage_events[0], s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_grouped_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (opts && opts->stage_events && cudaEventRecord((cudaEvent_t)opts->stage_events[1], s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // extern "C"

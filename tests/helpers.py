@@ -1,0 +1,95 @@
+"""Shared test plumbing: host <-> device copies of stored values and the
+parity checks of the CUDA path against the fp64 oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import seeded_inputs as si
+import sparse_mixture_experts_48_b300 as moe
+
+# Bounds on y: max |y_gpu - y_ref| <= TOL * RMS(y_ref) over the compared rows.
+Y_TOL = {si.F32: 1e-4, si.BF16: 2e-2}
+# Logits: |l_gpu - l_ref| <= 1e-5 * sum_i |x_i W_g[i,e]| + 1e-6 |b_e| (the scale of
+# the dot product's rounding; a plain relative bound is undefined near zero).
+LOGIT_REL = 1e-5
+TOPK_W_RTOL = 1e-6
+LAUX_RTOL = 1e-5
+
+
+def to_dev(a, device="cuda"):
+    if a is None:
+        return None
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def to_host_f32(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.float().cpu().numpy()
+    return t.cpu().numpy()
+
+
+def device_inputs(inp):
+    return {k: to_dev(v) for k, v in inp.items()}
+
+
+def run(cfg, dinp, debug=True, **kw):
+    return moe.forward(cfg, dinp["x"], dinp["W_g"], dinp["b_g"], dinp["W1"], dinp["b1"], dinp["W2"],
+                       dinp["b2"], dinp["W3"], debug=debug, **kw)
+
+
+def logit_scale(inp):
+    x = si.as_f32(inp["x"]).astype(np.float64)
+    W = si.as_f32(inp["W_g"]).astype(np.float64)
+    s = LOGIT_REL * (np.abs(x) @ np.abs(W))
+    if inp["b_g"] is not None:
+        s += 1e-6 * np.abs(si.as_f32(inp["b_g"]).astype(np.float64))[None, :]
+    return s + 1e-30
+
+
+def check_routing(cfg, inp, out, own_logits=None):
+    """Logits within tolerance; every integer decision bitwise equal to the
+    oracle's decisions taken on the GPU's own fp32 logits; flips against the
+    oracle's own fp64 logits only where the k-th and (k+1)-th logits nearly tie."""
+    T, E, k = cfg.T, cfg.E, cfg.k
+    gl = out.router_logits.cpu().numpy().astype(np.float64)
+    if own_logits is None:
+        own_logits = oracle.router_logits(inp["x"], inp["W_g"], inp["b_g"], cfg.dtype)
+    scale = logit_scale(inp)
+    err = np.abs(gl - own_logits)
+    assert np.all(err <= scale), f"logit error {err.max():.3e}, ratio {(err / scale).max():.3f}"
+
+    ref = oracle.routing(cfg, gl)
+    assert np.array_equal(out.topk_idx.cpu().numpy(), ref["topk_idx"])
+    np.testing.assert_allclose(out.topk_w.cpu().numpy(), ref["topk_w"], rtol=TOPK_W_RTOL, atol=1e-7)
+    assert np.array_equal(out.expert_counts.cpu().numpy(), ref["counts"])
+    assert np.array_equal(out.dropped_mask.cpu().numpy(), ref["dropped"])
+    nk = int(ref["offsets"][-1])
+    assert np.array_equal(out.perm_token.cpu().numpy()[:nk], ref["perm"])
+    assert np.array_equal(out.slot.cpu().numpy(), ref["slot"])
+    np.testing.assert_allclose(out.f.cpu().numpy(), ref["f"], rtol=1e-6, atol=0)
+    np.testing.assert_allclose(out.P.cpu().numpy(), ref["P"], rtol=1e-5, atol=1e-9)
+    la = float(out.L_aux.cpu().numpy()[0])
+    assert abs(la - ref["L_aux"]) <= LAUX_RTOL * abs(ref["L_aux"]) + 1e-12, (la, ref["L_aux"])
+    assert int(out.expert_counts.sum()) == T * k - int(out.dropped_mask.sum())
+
+    own_idx = oracle.topk(own_logits, k)
+    diff = np.nonzero(np.any(own_idx != ref["topk_idx"], axis=1))[0]
+    if diff.size:
+        srt = -np.sort(-own_logits[diff], axis=1)
+        gap = srt[:, k - 1] - (srt[:, k] if k < E else -np.inf)
+        assert np.all(gap <= 2 * scale[diff].max(axis=1)), "routing differs away from a near-tie"
+    return ref, gl, diff.size
+
+
+def check_y(cfg, inp, out, gl, rows):
+    ref = oracle.forward(cfg, inp, rows=rows, logits=gl)
+    y = to_host_f32(out.y)[rows].astype(np.float64)
+    yr = ref["y"]
+    rms = float(np.sqrt(np.mean(yr ** 2)))
+    err = float(np.abs(y - yr).max()) if y.size else 0.0
+    assert err <= Y_TOL[cfg.dtype] * rms, f"max|dy| = {err:.4e} > {Y_TOL[cfg.dtype]} * RMS {rms:.4e}"
+    return err / rms if rms > 0 else 0.0

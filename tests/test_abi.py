@@ -1,0 +1,130 @@
+"""The C-ABI library: it loads, exports every entry point include/moe.h
+declares, and its host-side checks answer before anything touches a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import sparse_mixture_experts_48_b300 as moe
+import seeded_inputs as si
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from sparse_mixture_experts_48_b300 import build
+    build.build()
+    return moe.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_entry_point(L):
+    declared = _declared()
+    assert declared, "no entry points parsed from moe.h"
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (moe_\w+)", out))
+    assert set(declared) <= exported, set(declared) - exported
+    assert set(declared) == set(moe.exported_symbols())
+    for name in declared:
+        assert hasattr(L, name)
+
+
+def test_config_struct_layout():
+    assert ctypes.sizeof(moe._CConfig) == 64
+    assert moe._CConfig.capacity_factor.offset == 40 and moe._CConfig.reserved.offset == 56
+
+
+def test_status_strings(L):
+    for code, name in moe.STATUS.items():
+        assert L.moe_status_string(code).decode() == name
+
+
+def _cfg(**kw):
+    base = dict(T=4096, d=768, f=3072, E=8, k=2, S=0, act=moe.GELU, gating=moe.SOFTMAX, dtype=moe.BF16)
+    base.update(kw)
+    return moe.MoEConfig(**base)
+
+
+@pytest.mark.parametrize("name", si.CONFIG_ORDER)
+def test_the_five_workloads_are_valid(L, name):
+    c = si.CONFIGS[name]
+    assert moe.validate(c) == 0
+    assert moe.workspace_size(c) > 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=0), 1), (dict(k=9, E=16), 2), (dict(k=3, E=2), 1), (dict(E=0), 1), (dict(E=257), 2),
+    (dict(d=0), 1), (dict(T=-1), 1), (dict(act=7), 1), (dict(gating=2), 1), (dict(dtype=3), 1),
+    (dict(d=96), 2), (dict(f=100), 2), (dict(S=9), 2), (dict(S=-1), 1),
+    (dict(dtype=moe.F32, d=66), 2), (dict(capacity_factor=float("nan")), 1),
+])
+def test_invalid_configs(L, kw, status):
+    c = _cfg(**kw)
+    assert moe.validate(c) == status
+    assert moe.workspace_size(c) == 0
+
+
+def test_capacity_formula_matches_the_pages_reading(L):
+    c = si.CONFIGS["skew_capacity_gelu_bf16"]
+    assert moe.capacity(c) == 640            # ceil(8192 * 1.25 / 16)
+    assert moe.capacity(_cfg(T=10, E=3, capacity_factor=1.0)) == 4
+    assert moe.capacity(_cfg(capacity_factor=0.0)) == -1
+
+
+def test_empty_batch_is_valid(L):
+    c = _cfg(T=0)
+    assert moe.validate(c) == 0 and moe.workspace_size(c) > 0
+
+
+def _call_forward(L, cfg, **over):
+    """moe_forward with fake, aligned, never-dereferenced pointers: every case
+    here is rejected by the host checks before any CUDA call."""
+    P = ctypes.c_void_p
+    args = dict(x=P(0x10000), W_g=P(0x20000), b_g=None, W1=P(0x30000), b1=None, W2=P(0x40000), b2=None,
+                W3=None, y=P(0x50000000), topk_idx=P(0x60000), topk_w=P(0x70000), counts=P(0x80000),
+                dropped=P(0x90000), f=P(0xA0000), Pp=P(0xB0000), L_aux=P(0xC0000), logits=None, perm=None,
+                slot=None, ws=P(0x100000), ws_bytes=moe.workspace_size(cfg))
+    args.update(over)
+    c = moe.c_config(cfg)
+    return L.moe_forward(ctypes.byref(c), args["x"], args["W_g"], args["b_g"], args["W1"], args["b1"],
+                         args["W2"], args["b2"], args["W3"], args["y"], args["topk_idx"], args["topk_w"],
+                         args["counts"], args["dropped"], args["f"], args["Pp"], args["L_aux"], args["logits"],
+                         args["perm"], args["slot"], args["ws"], args["ws_bytes"], None, None)
+
+
+def test_forward_host_checks(L):
+    c = _cfg()
+    P = ctypes.c_void_p
+    assert _call_forward(L, c, x=None) == 1
+    assert _call_forward(L, c, L_aux=None) == 1
+    assert _call_forward(L, c, W3=P(0xD0000)) == 1                  # W3 without SwiGLU
+    assert _call_forward(L, _cfg(act=moe.SWIGLU)) == 1             # SwiGLU without W3
+    assert _call_forward(L, c, x=P(0x10008)) == 1                   # misaligned
+    assert _call_forward(L, c, y=P(0x10000 + 64)) == 1              # y overlaps x
+    assert _call_forward(L, c, ws_bytes=moe.workspace_size(c) - 1) == 3
+    assert _call_forward(L, c, ws=None) == 3
+    assert _call_forward(L, c, ws=P(0x100080)) == 3                 # workspace not 256-byte aligned
+    assert _call_forward(L, _cfg(k=9, E=16)) == 2
+
+
+def test_grouped_gemm_host_checks(L):
+    P = ctypes.c_void_p
+    ws = moe.lib().moe_grouped_gemm_workspace_size(4)
+    assert ws > 0
+    f = L.moe_grouped_gemm
+    assert f(moe.BF16, moe.NONE, 4, None, 256, 128, 128, P(0x1000), P(0x2000), None, None, P(0x3000),
+             P(0x100000), ws, None, None) == 1
+    assert f(moe.BF16, moe.NONE, 4, P(0x800), 256, 100, 128, P(0x1000), P(0x2000), None, None, P(0x3000),
+             P(0x100000), ws, None, None) == 2
+    assert f(moe.BF16, moe.SWIGLU, 4, P(0x800), 256, 128, 128, P(0x1000), P(0x2000), None, None, P(0x3000),
+             P(0x100000), ws, None, None) == 1
+    assert f(moe.BF16, moe.NONE, 4, P(0x800), 256, 128, 128, P(0x1000), P(0x2000), None, None, P(0x3000),
+             P(0x100000), ws - 1, None, None) == 3

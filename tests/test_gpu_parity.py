@@ -1,0 +1,137 @@
+"""GPU parity of the whole layer against the fp64 oracle, through the C ABI.
+
+Small cases run every output row: they span several router CTAs (64 tokens),
+several 128-row GEMM tiles with ragged segment tails, and the column tails of
+the N tiles.  Full-size cases use the workload shapes the bench times, with
+routing checked on every token and y on sampled rows the oracle computes one
+by one."""
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as si
+import sparse_mixture_experts_48_b300 as moe
+from helpers import check_routing, check_y, device_inputs, run, to_host_f32
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "tiny_top1_relu_f32": dict(),
+    "gpt2_top2_gelu_bf16": dict(T=300),
+    "skew_capacity_gelu_bf16": dict(T=700, f=1024),
+    "mixtral_swiglu_bf16": dict(T=300, d=512, f=1024),
+    "deepseek_shared_sigmoid_bf16": dict(T=300, d=512, f=320),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from sparse_mixture_experts_48_b300 import build
+    build.build()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_small(name):
+    cfg = si.CONFIGS[name].replace(**SMALL[name])
+    inp = si.layer_inputs(cfg, seed=1)
+    out = run(cfg, device_inputs(inp))
+    assert moe.check_device_errors(out.workspace) == 0
+    ref, gl, _ = check_routing(cfg, inp, out)
+    check_y(cfg, inp, out, gl, np.arange(cfg.T))
+    if cfg.capacity_factor > 0:
+        assert out.dropped_mask.sum() > 0
+
+
+EDGE = [
+    ("one_token", "gpt2_top2_gelu_bf16", dict(T=1)),
+    ("k_equals_E", "gpt2_top2_gelu_bf16", dict(T=130, E=4, k=4, d=256, f=512)),
+    ("E_not_multiple_of_8", "gpt2_top2_gelu_bf16", dict(T=200, E=5, k=3, d=256, f=256)),
+    ("max_E_and_k", "deepseek_shared_sigmoid_bf16", dict(T=150, E=256, k=8, S=1, d=256, f=192)),
+    ("capacity_one", "skew_capacity_gelu_bf16", dict(T=100, E=16, k=2, d=256, f=256, capacity_factor=0.1)),
+    ("sigmoid_top1_capacity", "deepseek_shared_sigmoid_bf16",
+     dict(T=333, E=8, k=1, S=1, d=256, f=128, capacity_factor=1.0, router_bias=True, router_bias_std=1.0)),
+    ("relu_bf16_no_bias", "gpt2_top2_gelu_bf16", dict(T=257, act=si.RELU, ffn_bias=False, router_bias=False,
+                                                     d=192, f=448)),
+    ("f32_swiglu_shared", "tiny_top1_relu_f32", dict(T=150, E=6, k=2, S=2, act=si.SWIGLU, ffn_bias=False,
+                                                    gating=si.SIGMOID_NORM)),
+    ("f32_gelu_capacity", "tiny_top1_relu_f32", dict(T=190, E=4, k=2, act=si.GELU, capacity_factor=0.6)),
+]
+
+
+@pytest.mark.parametrize("label,base,over", EDGE, ids=[e[0] for e in EDGE])
+def test_layer_edge_cases(label, base, over):
+    cfg = si.CONFIGS[base].replace(**over)
+    inp = si.layer_inputs(cfg, seed=2)
+    out = run(cfg, device_inputs(inp))
+    assert moe.check_device_errors(out.workspace) == 0
+    ref, gl, _ = check_routing(cfg, inp, out)
+    check_y(cfg, inp, out, gl, np.arange(cfg.T))
+
+
+def test_all_tokens_choose_one_expert_with_capacity():
+    cfg = si.CONFIGS["skew_capacity_gelu_bf16"].replace(T=260, d=128, f=128, E=8, k=1, capacity_factor=1.0)
+    inp = si.layer_inputs(cfg, seed=3)
+    inp["W_g"] = np.zeros_like(inp["W_g"])
+    b = np.zeros(cfg.E, np.float32)
+    b[5] = 4.0
+    inp["b_g"] = si.f32_to_bf16(b)
+    out = run(cfg, device_inputs(inp))
+    C = moe.capacity(cfg)
+    counts = out.expert_counts.cpu().numpy()
+    assert counts[5] == C and counts.sum() == C
+    dropped = out.dropped_mask.cpu().numpy()[:, 0]
+    assert np.all(dropped[:C] == 0) and np.all(dropped[C:] == 1)
+    y = to_host_f32(out.y)
+    assert np.all(y[C:] == 0)            # every choice dropped: the layer adds nothing
+    ref, gl, _ = check_routing(cfg, inp, out)
+    check_y(cfg, inp, out, gl, np.arange(cfg.T))
+
+
+def test_empty_batch():
+    cfg = si.CONFIGS["gpt2_top2_gelu_bf16"].replace(T=0)
+    inp = si.layer_inputs(cfg.replace(T=1), seed=0)
+    dinp = device_inputs(inp)
+    dinp["x"] = dinp["x"][:0]
+    out = run(cfg, dinp)
+    assert moe.check_device_errors(out.workspace) == 0
+    assert out.expert_counts.sum() == 0 and float(out.L_aux[0]) == 0.0
+    assert torch.all(out.f == 0) and torch.all(out.P == 0)
+
+
+@pytest.mark.parametrize("name", ["gpt2_top2_gelu_bf16", "deepseek_shared_sigmoid_bf16"])
+def test_deterministic(name):
+    cfg = si.CONFIGS[name].replace(**SMALL[name])
+    dinp = device_inputs(si.layer_inputs(cfg, seed=4))
+    a = run(cfg, dinp)
+    b = run(cfg, dinp)
+    torch.cuda.synchronize()
+    for field in ("y", "topk_idx", "topk_w", "expert_counts", "dropped_mask", "f", "P", "L_aux", "router_logits",
+                  "perm_token", "slot"):
+        ta, tb = getattr(a, field), getattr(b, field)
+        assert torch.equal(ta.view(torch.uint8) if ta.dtype == torch.bfloat16 else ta,
+                           tb.view(torch.uint8) if tb.dtype == torch.bfloat16 else tb), field
+
+
+def _sample_rows(T, out, n=12, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = {0, T - 1, T // 2}
+    dropped = np.nonzero(out.dropped_mask.cpu().numpy().any(axis=1))[0]
+    if dropped.size:
+        rows.update(rng.choice(dropped, size=min(3, dropped.size), replace=False).tolist())
+    while len(rows) < n:
+        rows.add(int(rng.integers(0, T)))
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("name", si.CONFIG_ORDER)
+def test_layer_full_size_sampled(name):
+    """The workload shapes at full size, in the bench's launch configuration."""
+    cfg = si.CONFIGS[name]
+    inp = si.layer_inputs(cfg, seed=0)
+    out = run(cfg, device_inputs(inp))
+    assert moe.check_device_errors(out.workspace) == 0
+    ref, gl, flips = check_routing(cfg, inp, out)
+    n = 8 if name == "mixtral_swiglu_bf16" else 16
+    check_y(cfg, inp, out, gl, _sample_rows(cfg.T, out, n=n))
+    # properties that hold at any size
+    assert np.isfinite(to_host_f32(out.y)).all()
