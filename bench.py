@@ -1,0 +1,389 @@
+"""Bench of the MoE-FFN forward layer on B300: tokens/s and grouped-GEMM TFLOPS.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--T TOKENS] [--no-cpu] [--no-e2e]
+
+A step is one whole forward pass of the layer (router, scan, gather, expert
+GEMM 1, expert GEMM 2, combine) over one batch of T synthetic tokens.  The
+default workload is the Mixtral-shaped layer (T=16384, d=4096, f=14336, E=8,
+k=2, SwiGLU, bf16) on which the grouped-GEMM bar is stated.  Inputs are larger
+than L2 (x is 134 MB, expert weights 2.8 GB), so no L2 flush is done.
+
+Prints one JSON line on rank 0.  Under torchrun each rank runs an independent
+replica of the layer on its own GPU (the layer has no cross-GPU step); value is
+the total tokens/s of all ranks over the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on this host's cores instead, on a
+bounded sample of the same workload (routing of all T tokens plus the expert
+FFNs of a few tokens, extrapolated to T).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "MoE-layer tokens/s on 1 B300; grouped-GEMM TFLOPS as % of bf16 peak"
+DEFAULT_WORKLOAD = "mixtral_swiglu_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(cfg):
+    act = {si.RELU: "ReLU", si.GELU: "GELU", si.SWIGLU: "SwiGLU"}[cfg.act]
+    gate = {si.SOFTMAX: "softmax", si.SIGMOID_NORM: "normalised sigmoid"}[cfg.gating]
+    dt = {si.F32: "fp32", si.BF16: "bf16"}[cfg.dtype]
+    cap = f", capacity factor {cfg.capacity_factor}" if cfg.capacity_factor > 0 else ""
+    sh = f", {cfg.S} shared experts" if cfg.S else ""
+    return (f"{cfg.name}: T={cfg.T}, d_model={cfg.d}, d_ff={cfg.f}, E={cfg.E}, k={cfg.k}{sh}, {act} experts, "
+            f"{gate} gating, {dt}{cap}")
+
+
+def algorithmic(cfg, rows_A: int):
+    """Per-forward algorithmic work.  rows_A = kept assignments + S * T."""
+    T, d, f, E, m = cfg.T, cfg.d, cfg.f, cfg.E, cfg.n_mats
+    b = 2 if cfg.dtype == si.BF16 else 4
+    g1 = 2.0 * rows_A * d * f * (m - 1)         # x W1 (and x W3)
+    g2 = 2.0 * rows_A * f * d                   # h W2
+    kept = rows_A - cfg.S * T
+    return {
+        "gemm1_flop": g1, "gemm2_flop": g2,
+        "router_bytes": T * d * b + d * E * b + T * cfg.k * 8.0,
+        "gather_bytes": T * d * b + kept * d * b,
+        "combine_bytes": rows_A * d * 4.0 + T * d * b,
+    }
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+
+
+def oracle_sample(cfg, inp, n_ffn_tokens: int, seed: int = 0):
+    """Time the oracle on all T tokens' routing plus n tokens' expert FFNs;
+    return (seconds extrapolated to the full batch, description)."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    logits = oracle.router_logits(inp["x"], inp["W_g"], inp["b_g"], cfg.dtype)
+    r = oracle.routing(cfg, logits)
+    t_route = time.perf_counter() - t0
+    rows = np.random.default_rng(seed).choice(cfg.T, size=n_ffn_tokens, replace=False)
+    t1 = time.perf_counter()
+    oracle.layer_rows(cfg, rows, inp, r["topk_idx"], r["topk_w"], r["dropped"])
+    t_ffn = time.perf_counter() - t1
+    total = t_route + t_ffn * cfg.T / n_ffn_tokens
+    desc = (f"routing, dispatch and statistics of all {cfg.T} tokens ({t_route:.2f} s) + expert FFNs and "
+            f"combine of {n_ffn_tokens} random tokens ({t_ffn:.2f} s), extrapolated linearly to {cfg.T} tokens")
+    return total, desc
+
+
+def ffn_sample_size(cfg, budget_s: float = 12.0) -> int:
+    # ~1.5 GMAC/s for the oracle's fp64 loops; per token (k + S) experts of m d f MACs
+    per_tok = (cfg.k + cfg.S) * cfg.n_mats * cfg.d * cfg.f / 1.5e9
+    return int(max(2, min(cfg.T, budget_s / max(per_tok, 1e-9))))
+
+
+def run_reference(args, cfg):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = si.layer_inputs(cfg, seed=0)
+    n = max(2, ffn_sample_size(cfg, budget_s=2.0))
+    times, descs = [], []
+    for i in range(args.warmup + args.steps):
+        s, desc = oracle_sample(cfg, inp, n, seed=i)
+        if i >= args.warmup:
+            times.append(s)
+            descs.append(desc)
+    sec = statistics.median(times)
+    value = cfg.T / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "T": cfg.T, "parallelism": "single host thread"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": descs[0] + f"; median of {args.steps} samples"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=si.CONFIG_ORDER)
+    ap.add_argument("--T", type=int, default=0, help="override the token count (profiling runs)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop")
+    args = ap.parse_args()
+    cfg = si.CONFIGS[args.workload]
+    if args.T:
+        cfg = cfg.replace(T=args.T)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+
+    import torch
+    import torch.distributed as dist
+
+    import sparse_mixture_experts_48_b300 as moe
+    from sparse_mixture_experts_48_b300 import build as mbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if rank == 0:
+        mbuild.build()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist.barrier()
+        mbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    inp = si.layer_inputs(cfg, seed=rank)
+
+    def to_dev(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    d = {k: to_dev(v) for k, v in inp.items()}
+    args_in = [d[n] for n in ("x", "W_g", "b_g", "W1", "b1", "W2", "b2", "W3")]
+    out = moe.alloc_outputs(cfg, dev)
+    ws = moe.alloc_workspace(cfg, dev)
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)] for _ in range(K)]
+
+    def step(i=None):
+        moe.forward(cfg, *args_in, out=out, workspace=ws, stage_events=ev[i] if i is not None else None)
+
+    for _ in range(W):
+        step()
+    status = moe.check_device_errors(ws)
+    if status != 0:
+        raise SystemExit(f"device error during warm-up: {moe.STATUS.get(status)}")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    torch.cuda.synchronize()
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        t_start.record()
+        for i in range(K):
+            step(i)
+        t_end.record()
+        torch.cuda.synchronize()
+    barrier()
+    status = moe.check_device_errors(ws)
+    if status != 0:
+        raise SystemExit(f"device error in the timed region: {moe.STATUS.get(status)}")
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / K
+    value = world * cfg.T / (ms_step / 1e3)
+
+    # per-kernel durations from the stage events (on the launching stream)
+    stage_ms = np.array([[ev[i][s].elapsed_time(ev[i][s + 1]) for s in range(moe.NUM_STAGES)] for i in range(K)])
+    stage_avg = stage_ms.mean(axis=0)
+    rows_A = int(out.expert_counts.sum().item()) + cfg.S * cfg.T
+    alg = algorithmic(cfg, rows_A)
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tc_burst = float(peaks["bf16_tflops"])
+    tc_sust = float(peaks.get("bf16_tflops_sustained", tc_burst))
+    kernels = {}
+    for s, name in enumerate(moe.STAGE_NAMES):
+        kernels[name] = {"ms": round(float(stage_avg[s]), 5)}
+    for name, key in (("router", "router_bytes"), ("gather", "gather_bytes"), ("combine", "combine_bytes")):
+        gbs = alg[key] / (stage_avg[moe.STAGE_NAMES.index(name)] / 1e3) / 1e9
+        kernels[name].update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4), "bytes": alg[key]})
+    for name, key in (("expert_gemm1", "gemm1_flop"), ("expert_gemm2", "gemm2_flop")):
+        tf = alg[key] / (stage_avg[moe.STAGE_NAMES.index(name)] / 1e3) / 1e12
+        kernels[name].update({"TFLOP/s": round(tf, 1), "frac_bf16_sustained": round(tf / tc_sust, 4),
+                              "frac_bf16_burst": round(tf / tc_burst, 4), "flop": alg[key]})
+    gemm_ms = stage_avg[3] + stage_avg[4]
+    gemm_tf = (alg["gemm1_flop"] + alg["gemm2_flop"]) / (gemm_ms / 1e3) / 1e12
+    dom = "expert_gemm1"
+    dom_tf = kernels[dom]["TFLOP/s"]
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        tj = json.load(open(tpath))
+        ent = tj.get(cfg.name, {}).get(dom)
+        if ent and ent.get("T") == cfg.T:
+            traffic = ent.get("bytes_per_launch")
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": tc_sust, "unit": "TFLOP/s",
+                "frac": round(dom_tf / tc_sust, 4), "traffic": traffic,
+                "peak_source": f"{peak_kind} bf16_tflops_sustained (cuBLAS bf16, back to back)",
+                "frac_of_burst_peak": round(dom_tf / tc_burst, 4)}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        x_host = torch.empty(d["x"].shape, dtype=d["x"].dtype, pin_memory=True)
+        x_host.copy_(d["x"].cpu())
+        y_host = torch.empty(out.y.shape, dtype=out.y.dtype, pin_memory=True)
+        small = [out.topk_idx, out.topk_w, out.expert_counts, out.dropped_mask, out.f, out.P, out.L_aux]
+        small_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in small]
+        x_dev = torch.empty_like(d["x"])
+        args_e2e = [x_dev] + args_in[1:]
+
+        def e2e_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.forward(cfg, *args_e2e, out=out, workspace=ws)
+            y_host.copy_(out.y, non_blocking=True)
+            for h, t in zip(small_host, small):
+                h.copy_(t, non_blocking=True)
+
+        for _ in range(W):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = e0.elapsed_time(e1) / K
+        if world > 1:
+            tt = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        bi = x_host.numel() * x_host.element_size()
+        bo = y_host.numel() * y_host.element_size() + sum(h.numel() * h.element_size() for h in small_host)
+        e2e = {"value": world * cfg.T / (e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        n = ffn_sample_size(cfg)
+        sec, desc = oracle_sample(cfg, inp, n)
+        cpu = {"value": cfg.T / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": desc + f"; single thread of {os.cpu_count()} host cores"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if cfg.dtype == si.BF16 else "f32", "data": "synthetic",
+            "config": {"workload": workload_desc(cfg), "T": cfg.T, "d_model": cfg.d, "d_ff": cfg.f, "E": cfg.E,
+                       "k": cfg.k, "n_shared": cfg.S, "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "no flush: inputs larger than L2 (x %.0f MB, expert weights %.2f GB)" % (
+                           inp["x"].nbytes / 1e6, sum(inp[n].nbytes for n in ("W1", "W2", "W3")
+                                                      if inp[n] is not None) / 1e9)},
+            "grouped_gemm": {"tflops": round(gemm_tf, 1), "frac_of_bf16_sustained": round(gemm_tf / tc_sust, 4),
+                             "frac_of_bf16_burst": round(gemm_tf / tc_burst, 4), "ms": round(float(gemm_ms), 4)},
+            "roofline": roofline,
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": moe.NUM_STAGES * K,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -94,13 +94,19 @@ typedef struct {
   int32_t dtype;          /* MOE_DT_F32 / _BF16: storage of x, weights, biases and y */
   double capacity_factor; /* <= 0: no capacity limit */
   double alpha;           /* coefficient of L_aux (the pages use 0.01) */
-  int64_t reserved;       /* must be 0 */
+  int64_t flags;          /* OR of MOE_FLAG_*; other bits must be 0 */
 } moe_config;
+
+/* y is written in fp32 whatever `dtype` is (e.g. for an fp32 residual stream).
+ * Without it y has the storage dtype and carries that dtype's final rounding. */
+#define MOE_FLAG_Y_F32 1
 
 /* Launch options; pass NULL for defaults. */
 typedef struct {
-  /* If non-NULL: MOE_NUM_STAGES + 1 created events.  Event i is recorded on
-   * `stream` just before stage i, event MOE_NUM_STAGES after the last one. */
+  /* If non-NULL: created events recorded on `stream` around the kernels.
+   * moe_forward: MOE_NUM_STAGES + 1 events; event i just before stage i,
+   * event MOE_NUM_STAGES after the last.  moe_grouped_gemm: 2 events, before
+   * and after the GEMM kernel. */
   moe_event* stage_events;
   /* Limit of every device-side wait in nanoseconds; 0 = 2 s.  A wait that
    * runs out makes the kernel stop cleanly and records MOE_ERR_TIMEOUT. */
@@ -115,7 +121,8 @@ moe_status moe_validate_config(const moe_config* cfg);
 
 /* Device workspace bytes moe_forward needs for `cfg` (0 if cfg is invalid).
  * It holds the routing scratch, the expert-grouped copy of x [T*k, d], the
- * hidden activations [T*k + S*T, f] and expert outputs [T*k + S*T, d]. */
+ * hidden activations [T*k + S*T, f] (dtype) and the expert outputs
+ * [T*k + S*T, d] (fp32, so that the gate-weighted sum rounds only once). */
 size_t moe_workspace_size(const moe_config* cfg);
 
 /* Expert capacity C = ceil(T * capacity_factor / E) computed in double, or -1
@@ -127,7 +134,8 @@ int64_t moe_capacity(const moe_config* cfg);
  *   x, W_g, W1, W2 required; b_g, b1, b2 optional (NULL = no bias; biases are
  *   not used with SwiGLU); W3 required iff act == MOE_ACT_SWIGLU.
  * Outputs (device, written):
- *   y [T, d] (must not overlap x), topk_idx int32 [T, k] (descending logit),
+ *   y [T, d] in dtype, or fp32 with MOE_FLAG_Y_F32 (must not overlap x),
+ *   topk_idx int32 [T, k] (descending logit),
  *   topk_w fp32 [T, k], expert_counts int32 [E] (kept assignments per expert),
  *   dropped_mask uint8 [T, k] (1 = cut by capacity), f fp32 [E], P fp32 [E],
  *   L_aux fp32 [1].

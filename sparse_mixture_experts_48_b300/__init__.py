@@ -27,6 +27,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 RELU, GELU, SWIGLU, NONE = 0, 1, 2, 3
+FLAG_Y_F32 = 1
 SOFTMAX, SIGMOID_NORM = 0, 1
 F32, BF16 = 0, 1
 NUM_STAGES = 6
@@ -55,13 +56,14 @@ class MoEConfig:
     dtype: int = BF16
     capacity_factor: float = 0.0
     alpha: float = 0.01
+    y_f32: bool = False        # write y in fp32 whatever dtype is
 
 
 class _CConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("act", ctypes.c_int32), ("gating", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("capacity_factor", ctypes.c_double), ("alpha", ctypes.c_double), ("reserved", ctypes.c_int64)]
+                ("capacity_factor", ctypes.c_double), ("alpha", ctypes.c_double), ("flags", ctypes.c_int64)]
 
 
 class _COpts(ctypes.Structure):
@@ -108,9 +110,11 @@ def exported_symbols() -> Sequence[str]:
             "moe_check_device_errors", "moe_grouped_gemm_workspace_size", "moe_grouped_gemm")
 
 
-def c_config(cfg) -> _CConfig:
+def c_config(cfg, y_f32: Optional[bool] = None) -> _CConfig:
+    yf = bool(getattr(cfg, "y_f32", False)) if y_f32 is None else bool(y_f32)
     return _CConfig(int(cfg.T), int(cfg.d), int(cfg.f), int(cfg.E), int(cfg.k), int(cfg.S), int(cfg.act),
-                    int(cfg.gating), int(cfg.dtype), float(cfg.capacity_factor), float(cfg.alpha), 0)
+                    int(cfg.gating), int(cfg.dtype), float(cfg.capacity_factor), float(cfg.alpha),
+                    FLAG_Y_F32 if yf else 0)
 
 
 def validate(cfg) -> int:
@@ -139,6 +143,9 @@ def _opts(stage_events, timeout_ns: int):
         return None, None
     arr = None
     if stage_events is not None:
+        for e in stage_events:
+            if not e.cuda_event:       # torch creates the CUDA event on its first record
+                e.record()
         arr = (ctypes.c_void_p * len(stage_events))(*[ctypes.c_void_p(e.cuda_event) for e in stage_events])
     o = _COpts(ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)) if arr is not None else None, int(timeout_ns))
     return o, arr
@@ -178,9 +185,9 @@ class MoEOutput:
     workspace: Optional[torch.Tensor] = None
 
 
-def alloc_outputs(cfg, device, debug: bool = False, y_dtype=None) -> MoEOutput:
+def alloc_outputs(cfg, device, debug: bool = False, y_f32: bool = False) -> MoEOutput:
     T, d, E, k = cfg.T, cfg.d, cfg.E, cfg.k
-    yd = y_dtype or (torch.float32 if cfg.dtype == F32 else torch.bfloat16)
+    yd = torch.float32 if (cfg.dtype == F32 or y_f32) else torch.bfloat16
     out = MoEOutput(
         y=torch.empty((T, d), dtype=yd, device=device),
         topk_idx=torch.empty((T, k), dtype=torch.int32, device=device),
@@ -206,8 +213,11 @@ def alloc_workspace(cfg, device) -> torch.Tensor:
 
 def forward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutput] = None,
             workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
-            debug: bool = False, stage_events=None, timeout_ns: int = 0) -> MoEOutput:
+            debug: bool = False, stage_events=None, timeout_ns: int = 0,
+            y_f32: Optional[bool] = None) -> MoEOutput:
     """Enqueue the layer's forward pass on ``stream`` (default: the current one).
+
+    ``y_f32``: write y in fp32 (default: the config's ``y_f32``, else its dtype).
 
     Asynchronous: returns once the kernels are enqueued.  Host-detected errors
     raise MoEError; device-side ones are reported by check_device_errors()."""
@@ -225,13 +235,17 @@ def forward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutpu
     _check(b1, "b1", (G, f), st, required=False)
     _check(b2, "b2", (G, d), st, required=False)
     dev = x.device
+    yf = bool(getattr(cfg, "y_f32", False)) if y_f32 is None else bool(y_f32)
     if out is None:
-        out = alloc_outputs(cfg, dev, debug=debug)
+        out = alloc_outputs(cfg, dev, debug=debug, y_f32=yf)
+    want = torch.float32 if (cfg.dtype == F32 or yf) else torch.bfloat16
+    if out.y.dtype != want or tuple(out.y.shape) != (T, d):
+        raise ValueError(f"y must be {want} of shape {(T, d)}")
     if workspace is None:
         workspace = out.workspace if out.workspace is not None else alloc_workspace(cfg, dev)
     out.workspace = workspace
     opts, keep = _opts(stage_events, timeout_ns)
-    ccfg = c_config(cfg)
+    ccfg = c_config(cfg, y_f32=yf)
     with torch.cuda.device(dev):
         status = lib().moe_forward(
             ctypes.byref(ccfg), _ptr(x), _ptr(W_g), _ptr(b_g), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(W3),

@@ -196,7 +196,7 @@ __device__ __forceinline__ void map_tile(const Ctl& c, int G, int n_tiles, int t
 __device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.f + erff(v * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu(float v) { return v / (1.f + __expf(-v)); }
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool OUT_F32>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3,
@@ -408,12 +408,18 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) f[i] = gelu_erf(f[i]);
             }
-            uint32_t p[16];
+            if (OUT_F32) {
+              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.C) + orow * a.N + col0);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-            uint4* dst = reinterpret_cast<uint4*>(C + orow * a.N + col0);
+              for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+            } else {
+              uint32_t p[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+              for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+              uint4* dst = reinterpret_cast<uint4*>(C + orow * a.N + col0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+            }
           }
         }
       }
@@ -495,6 +501,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.dtype == MOE_DT_F32) return launch_grouped_gemm_f32(a, s);
   if (a.max_mtiles <= 0) return cudaSuccess;
   if (a.G > MAX_G || a.K % BK != 0 || a.N % 64 != 0) return cudaErrorInvalidValue;
+  if (a.out_f32 && a.act == MOE_ACT_SWIGLU) return cudaErrorInvalidValue;
   CUtensorMap mA0, mA1, mB, mB3;
   const bool swiglu = a.act == MOE_ACT_SWIGLU;
   if (!map_rows(&mA0, a.A0, a.rows_A0, a.K)) return cudaErrorInvalidValue;
@@ -512,17 +519,20 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s) {
   const int bn = swiglu ? 128 : 256;
   const int64_t max_tiles = a.max_mtiles * ((a.N + bn - 1) / bn);
   const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
+  auto go = [&](auto kernel) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, THREADS, kSmemBytes, s>>>(mA0, mA1, mB, mB3, a);
+    return cudaSuccess;
+  };
   cudaError_t e;
-  if (swiglu) {
-    e = cudaFuncSetAttribute(gemm_tcgen05_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    gemm_tcgen05_kernel<true><<<grid, THREADS, kSmemBytes, s>>>(mA0, mA1, mB, mB3, a);
-  } else {
-    e = cudaFuncSetAttribute(gemm_tcgen05_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    gemm_tcgen05_kernel<false><<<grid, THREADS, kSmemBytes, s>>>(mA0, mA1, mB, mB3, a);
-  }
+  if (swiglu)
+    e = go(gemm_tcgen05_kernel<true, false>);
+  else if (a.out_f32)
+    e = go(gemm_tcgen05_kernel<false, true>);
+  else
+    e = go(gemm_tcgen05_kernel<false, false>);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

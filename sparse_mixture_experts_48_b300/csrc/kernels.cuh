@@ -60,9 +60,10 @@ struct GatherArgs {
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
 
 struct CombineArgs {
-  const void* o;        // [rows_all, d]
+  const float* o;       // [rows_all, d] expert outputs, fp32
   int64_t T;
-  int d, k, S, dtype;
+  int d, k, S;
+  bool y_f32;           // y is fp32 (else bf16)
   int64_t rows_tk;
   const int32_t* slot;
   const float* topk_w;
@@ -87,6 +88,7 @@ struct GemmArgs {
   int Gw;               // weight slabs
   const void* bias;     // [Gw, N] or null
   void* C;              // [rows, N]
+  bool out_f32;         // C is fp32 (else the dtype of A and B)
   int64_t max_mtiles;   // upper bound of seg.mtile_start[G]
   uint32_t* err;
   int64_t timeout_ns;

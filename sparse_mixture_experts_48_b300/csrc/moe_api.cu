@@ -26,7 +26,7 @@ moe_status check_cfg(const moe_config* c) {
   if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_GELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (c->gating != MOE_GATE_SOFTMAX && c->gating != MOE_GATE_SIGMOID_NORM) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_DT_F32 && c->dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
-  if (c->reserved != 0) return MOE_ERR_INVALID_ARG;
+  if (c->flags & ~(int64_t)MOE_FLAG_Y_F32) return MOE_ERR_INVALID_ARG;
   if (!isfinite(c->capacity_factor) || !isfinite(c->alpha)) return MOE_ERR_INVALID_ARG;
   if (c->E > kMaxE || c->k > kMaxK || c->n_shared > kMaxShared) return MOE_ERR_UNSUPPORTED;
   if (c->dtype == MOE_DT_BF16 && (c->d_model % 64 != 0 || c->d_ff % 64 != 0)) return MOE_ERR_UNSUPPORTED;
@@ -61,7 +61,7 @@ WsLayout layout(const moe_config* c) {
   L.slot = take((size_t)L.rows_tk * 4);
   L.xperm = take((size_t)L.rows_tk * c->d_model * esz);
   L.h = take((size_t)L.rows_all * c->d_ff * esz);
-  L.o = take((size_t)L.rows_all * c->d_model * esz);
+  L.o = take((size_t)L.rows_all * c->d_model * 4);
   L.total = off;
   return L;
 }
@@ -143,8 +143,10 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
     if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
   // y must not overlap x.
   const size_t esz = c.dtype == MOE_DT_BF16 ? 2 : 4;
+  const bool y_f32 = (c.flags & MOE_FLAG_Y_F32) != 0 || c.dtype == MOE_DT_F32;
   const size_t xbytes = (size_t)c.T * c.d_model * esz;
-  if (xbytes && (const uint8_t*)y < (const uint8_t*)x + xbytes && (const uint8_t*)x < (const uint8_t*)y + xbytes)
+  const size_t ybytes = (size_t)c.T * c.d_model * (y_f32 ? 4 : 2);
+  if (xbytes && (const uint8_t*)y < (const uint8_t*)x + xbytes && (const uint8_t*)x < (const uint8_t*)y + ybytes)
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = layout(&c);
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
@@ -201,14 +203,14 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   GemmArgs g2 = g1;
   g2.act = MOE_ACT_NONE; g2.K = c.d_ff; g2.N = c.d_model; g2.a_from_out_rows = true;
   g2.A0 = ws + L.h; g2.rows_A0 = L.rows_all > 0 ? L.rows_all : 1; g2.A1 = nullptr; g2.rows_A1 = 0;
-  g2.B = W2; g2.B3 = nullptr; g2.bias = b2; g2.C = ws + L.o;
+  g2.B = W2; g2.B3 = nullptr; g2.bias = b2; g2.C = ws + L.o; g2.out_f32 = true;
   if (clk.mark(4) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_grouped_gemm(g2, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 6. combine
   if (clk.mark(5) != cudaSuccess) return MOE_ERR_CUDA;
   CombineArgs ca;
-  ca.o = ws + L.o; ca.T = c.T; ca.d = c.d_model; ca.k = c.k; ca.S = c.n_shared; ca.dtype = c.dtype;
+  ca.o = (const float*)(ws + L.o); ca.T = c.T; ca.d = c.d_model; ca.k = c.k; ca.S = c.n_shared; ca.y_f32 = y_f32;
   ca.rows_tk = L.rows_tk; ca.slot = slot_buf; ca.topk_w = topk_w; ca.y = y;
   if (launch_combine(ca, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (clk.mark(6) != cudaSuccess) return MOE_ERR_CUDA;

@@ -85,11 +85,24 @@ def check_routing(cfg, inp, out, own_logits=None):
     return ref, gl, diff.size
 
 
+def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers at |v|: the error of storing v in bf16."""
+    _, e = np.frexp(np.abs(v))            # |v| = m 2^e, m in [0.5, 1)
+    return np.where(v == 0, 0.0, np.ldexp(1.0, e - 9))
+
+
 def check_y(cfg, inp, out, gl, rows):
+    """max |y - y_ref| <= TOL * RMS(y_ref).  When y is stored in bf16 its own
+    final rounding (half a bf16 spacing at y_ref) is added to the bound: a bf16
+    number cannot sit closer to the exact value than that.  With y in fp32 the
+    bound is applied as it stands."""
     ref = oracle.forward(cfg, inp, rows=rows, logits=gl)
     y = to_host_f32(out.y)[rows].astype(np.float64)
     yr = ref["y"]
     rms = float(np.sqrt(np.mean(yr ** 2)))
-    err = float(np.abs(y - yr).max()) if y.size else 0.0
-    assert err <= Y_TOL[cfg.dtype] * rms, f"max|dy| = {err:.4e} > {Y_TOL[cfg.dtype]} * RMS {rms:.4e}"
-    return err / rms if rms > 0 else 0.0
+    bound = Y_TOL[cfg.dtype] * rms
+    if out.y.dtype == torch.bfloat16:
+        bound = bound + half_ulp_bf16(yr)
+    dy = np.abs(y - yr)
+    assert np.all(dy <= bound), f"max|dy| = {dy.max():.4e}, TOL * RMS = {Y_TOL[cfg.dtype] * rms:.4e}"
+    return float(dy.max()) / rms if rms > 0 else 0.0

@@ -39,7 +39,7 @@ def test_exports_every_declared_entry_point(L):
 
 def test_config_struct_layout():
     assert ctypes.sizeof(moe._CConfig) == 64
-    assert moe._CConfig.capacity_factor.offset == 40 and moe._CConfig.reserved.offset == 56
+    assert moe._CConfig.capacity_factor.offset == 40 and moe._CConfig.flags.offset == 56
 
 
 def test_status_strings(L):

@@ -30,11 +30,12 @@ def _built():
     build.build()
 
 
+@pytest.mark.parametrize("y_f32", [False, True], ids=["y_dtype", "y_f32"])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_layer_small(name):
+def test_layer_small(name, y_f32):
     cfg = si.CONFIGS[name].replace(**SMALL[name])
     inp = si.layer_inputs(cfg, seed=1)
-    out = run(cfg, device_inputs(inp))
+    out = run(cfg, device_inputs(inp), y_f32=y_f32)
     assert moe.check_device_errors(out.workspace) == 0
     ref, gl, _ = check_routing(cfg, inp, out)
     check_y(cfg, inp, out, gl, np.arange(cfg.T))
