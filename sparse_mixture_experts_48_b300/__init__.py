@@ -101,13 +101,16 @@ def lib() -> ctypes.CDLL:
     L.moe_grouped_gemm_workspace_size.argtypes = [i32]
     L.moe_grouped_gemm.restype = ctypes.c_int
     L.moe_grouped_gemm.argtypes = [i32, i32, i32, vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, optp]
+    L.moe_grouped_gemm_noalloc.restype = ctypes.c_int
+    L.moe_grouped_gemm_noalloc.argtypes = [i32, i32, i32, vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, optp]
     _lib_handle = L
     return L
 
 
 def exported_symbols() -> Sequence[str]:
     return ("moe_status_string", "moe_validate_config", "moe_workspace_size", "moe_capacity", "moe_forward",
-            "moe_check_device_errors", "moe_grouped_gemm_workspace_size", "moe_grouped_gemm")
+            "moe_check_device_errors", "moe_grouped_gemm_workspace_size", "moe_grouped_gemm",
+            "moe_grouped_gemm_noalloc")
 
 
 def c_config(cfg, y_f32: Optional[bool] = None) -> _CConfig:
@@ -293,3 +296,29 @@ def grouped_gemm(dtype: int, act: int, seg_offsets: torch.Tensor, A: torch.Tenso
     if status != 0:
         raise MoEError(status, "moe_grouped_gemm")
     return C, workspace
+
+
+def grouped_gemm_noalloc(dtype: int, act: int, seg_offsets: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                         B3: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
+                         C: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """grouped_gemm without a workspace, for callers that cannot allocate at
+    call time: the library's own fixed device scratch is used instead (see
+    moe.h).  Pass C to avoid any allocation here; if it is omitted, torch (not
+    the library) allocates it."""
+    G, K, N = B.shape
+    M = A.shape[0]
+    if seg_offsets.dtype != torch.int32 or tuple(seg_offsets.shape) != (G + 1,) or not seg_offsets.is_cuda:
+        raise ValueError("seg_offsets must be a CUDA int32 tensor of G+1 entries")
+    st = _STORE[dtype]
+    _check(A, "A", (M, K), st)
+    _check(B, "B", (G, K, N), st)
+    _check(B3, "B3", (G, K, N), st, required=act == SWIGLU)
+    _check(bias, "bias", (G, N), st, required=False)
+    if C is None:
+        C = torch.zeros((M, N), dtype=A.dtype, device=A.device)
+    with torch.cuda.device(A.device):
+        status = lib().moe_grouped_gemm_noalloc(dtype, act, G, _ptr(seg_offsets), M, K, N, _ptr(A), _ptr(B),
+                                                _ptr(B3), _ptr(bias), _ptr(C), _stream_handle(stream), None)
+    if status != 0:
+        raise MoEError(status, "moe_grouped_gemm_noalloc")
+    return C
