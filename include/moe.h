@@ -147,7 +147,8 @@ int64_t moe_capacity(const moe_config* cfg);
  * workspace: device, 256-byte aligned, >= moe_workspace_size(cfg) bytes,
  *   owned by the caller, contents need not be initialised.
  * All device pointers must be 16-byte aligned.  T == 0 is valid: it writes
- * expert_counts = f = P = 0 and L_aux = 0. */
+ * expert_counts = f = P = 0 and L_aux = 0, and the per-token tensors (x, y,
+ * topk_idx, topk_w, dropped_mask and the optional ones) may then be NULL. */
 moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
                        const void* W1, const void* b1, const void* W2, const void* b2, const void* W3,
                        void* y, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,

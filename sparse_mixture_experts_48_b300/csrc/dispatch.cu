@@ -32,6 +32,9 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   __shared__ double s_psum[kMaxE];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
   const int E = a.E;
+  // An earlier stage gave up: its partials are not valid.  Publish empty
+  // segments so that nothing later reads or writes through them.
+  const bool failed = *(volatile const uint32_t*)a.err != 0u;
   for (int e = warp; e < E; e += nwarps) {
     int run = 0;
     double ps = 0.0;
@@ -58,7 +61,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   int off = 0;
   double L = 0.0;
   for (int e = 0; e < E; ++e) {
-    const int n = s_npre[e];
+    const int n = failed ? 0 : s_npre[e];
     const int c = (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
     a.n_pre[e] = n;
     a.counts[e] = c;
@@ -79,7 +82,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   for (int g = 0; g < G; ++g) {
     int rows, w, orow, arow, asrc;
     if (g < E) { rows = a.counts[g]; w = g; orow = a.offsets[g]; arow = orow; asrc = 0; }
-    else { rows = (int)a.T; w = g; orow = (int)(a.rows_tk + (int64_t)(g - E) * a.T); arow = 0; asrc = 1; }
+    else { rows = failed ? 0 : (int)a.T; w = g; orow = (int)(a.rows_tk + (int64_t)(g - E) * a.T); arow = 0; asrc = 1; }
     a.seg.rows[g] = rows;
     a.seg.w[g] = w;
     a.seg.out_row[g] = orow;
@@ -104,7 +107,7 @@ constexpr int kGatherWarps = 8;
 __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(GatherArgs a) {
   const int lane = threadIdx.x % 32;
   const int64_t t = (int64_t)blockIdx.x * kGatherWarps + threadIdx.x / 32;
-  if (t >= a.T) return;
+  if (t >= a.T || *(volatile const uint32_t*)a.err != 0u) return;
   const int k = a.k, E = a.E;
   int my_slot = -1;
   if (lane < k) {

@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 cudaError_t launch_grouped_gemm_f32(const GemmArgs& a, cudaStream_t s);
@@ -61,6 +62,7 @@ struct Ctl {
   uint64_t done;
   uint32_t tmem_base;
   uint32_t abort;
+  uint32_t skip;      // an earlier stage failed: compute nothing
   int mt[MAX_G + 1];
   int rows[MAX_G];
   int w[MAX_G];
@@ -70,69 +72,6 @@ struct Ctl {
 };
 
 constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
-
-// ---- PTX wrappers -------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0u;
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// Bounded wait.  Returns false if the CTA is aborting or the limit ran out
-// (which starts the abort).
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort, uint64_t limit_ns,
-                                       uint32_t* err, uint32_t where) {
-  if (mbar_try(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try(bar, parity)) return true;
-    if (*abort) return false;
-    if ((i & 7u) == 0u && globaltimer_ns() - t0 > limit_ns) {
-      *abort = 1u;
-      record_error(err, kErrTimeout, where);
-      return false;
-    }
-  }
-}
-// Bounded wait used while tearing down: ignores the abort flag.
-__device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
-  return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(map), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(dst),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -238,6 +177,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(smem_u32(&c.done), 1);
     c.abort = 0u;
+    c.skip = *(volatile const uint32_t*)a.err;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
@@ -256,7 +196,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
-  const int total = c.mt[G] * n_tiles;
+  const int total = c.skip ? 0 : c.mt[G] * n_tiles;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -439,49 +379,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---- host: tensor maps --------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeTiledFn)p;
-  }
-  return fn;
-}
-
 // Row-major [rows, K] bf16, box 64 (K) x 128 (rows).
-bool map_rows(CUtensorMap* m, const void* ptr, int64_t rows, int K) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc || rows <= 0) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {BK, BM};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
+bool map_rows(CUtensorMap* m, const void* ptr, int64_t rows, int K) { return tmap_bf16_2d(m, ptr, rows, K, BK, BM); }
 
 // Stacked weights [G, K, N] bf16, box 64 (N) x 64 (K) x 1.
 bool map_weights(CUtensorMap* m, const void* ptr, int G, int K, int N) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)K, (cuuint64_t)G};
-  cuuint64_t strides[2] = {(cuuint64_t)N * 2, (cuuint64_t)K * N * 2};
-  cuuint32_t box[3] = {64, BK, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return tmap_bf16_3d(m, ptr, G, K, N, 64, BK);
 }
 
 }  // namespace

@@ -20,6 +20,8 @@ struct RouterArgs {
   uint8_t* lrank;      // [T, k] rank among the CTA's earlier tokens choosing the same expert
   int32_t* hist;       // [nblk, E] selections per router CTA
   float* psum;         // [nblk, E] sum of gate probabilities per router CTA
+  uint32_t* err;       // workspace status word
+  int64_t timeout_ns;  // limit of every device-side wait
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 
@@ -40,6 +42,7 @@ struct ScanArgs {
   float* L_aux;
   SegTable seg;
   int64_t rows_tk;     // T * k: first H / O row of the shared experts
+  const uint32_t* err; // workspace status word: non-zero = an earlier stage failed
 };
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
 
@@ -56,6 +59,7 @@ struct GatherArgs {
   uint8_t* dropped;     // [T, k]
   int32_t* perm_token;  // [T*k] or null
   void* xperm;          // [T*k, d]
+  const uint32_t* err;  // non-zero: skip (the ranks are not valid)
 };
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
 
@@ -68,6 +72,7 @@ struct CombineArgs {
   const int32_t* slot;
   const float* topk_w;
   void* y;              // [T, d]
+  const uint32_t* err;  // non-zero: skip (an earlier stage failed)
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 

@@ -131,10 +131,11 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
   const bool swiglu = c.act == MOE_ACT_SWIGLU;
-  // Required tensors.
-  if (!x || !W_g || !W1 || !W2 || !y || !topk_idx || !topk_w || !expert_counts || !dropped_mask || !f || !P ||
-      !L_aux)
-    return MOE_ERR_INVALID_ARG;
+  // Required tensors.  With T == 0 the per-token tensors hold no elements and
+  // may be NULL (allocators hand out NULL for empty buffers).
+  const bool empty = c.T == 0;
+  if (!W_g || !W1 || !W2 || !expert_counts || !f || !P || !L_aux) return MOE_ERR_INVALID_ARG;
+  if (!empty && (!x || !y || !topk_idx || !topk_w || !dropped_mask)) return MOE_ERR_INVALID_ARG;
   if (swiglu != (W3 != nullptr)) return MOE_ERR_INVALID_ARG;
   if (swiglu && (b1 || b2)) return MOE_ERR_INVALID_ARG;
   const void* all[] = {x, W_g, b_g, W1, b1, W2, b2, W3, y, topk_idx, topk_w, expert_counts, dropped_mask,
@@ -168,6 +169,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   ra.x = x; ra.Wg = W_g; ra.bg = b_g; ra.T = c.T; ra.d = c.d_model; ra.E = c.E; ra.k = c.k;
   ra.gating = c.gating; ra.dtype = c.dtype; ra.logits_out = router_logits; ra.topk_idx = topk_idx;
   ra.topk_w = topk_w; ra.lrank = ws + L.lrank; ra.hist = (int32_t*)(ws + L.hist); ra.psum = (float*)(ws + L.psum);
+  ra.err = &hdr->err; ra.timeout_ns = timeout;
   if (launch_router(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 2. scan: ranks, capacity, offsets, statistics, segment table
@@ -176,7 +178,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   sa.T = c.T; sa.E = c.E; sa.k = c.k; sa.S = c.n_shared; sa.capacity = C; sa.alpha = c.alpha; sa.nblk = L.nblk;
   sa.hist = ra.hist; sa.psum = ra.psum; sa.base = (int32_t*)(ws + L.base); sa.n_pre = (int32_t*)(ws + L.npre);
   sa.counts = expert_counts; sa.offsets = (int32_t*)(ws + L.offsets); sa.f = f; sa.P = P; sa.L_aux = L_aux;
-  sa.seg = seg; sa.rows_tk = L.rows_tk;
+  sa.seg = seg; sa.rows_tk = L.rows_tk; sa.err = &hdr->err;
   if (launch_scan(sa, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 3. gather into the expert-grouped buffer
@@ -184,7 +186,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   GatherArgs ga;
   ga.x = x; ga.T = c.T; ga.d = c.d_model; ga.E = c.E; ga.k = c.k; ga.dtype = c.dtype; ga.capacity = C;
   ga.topk_idx = topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.offsets = sa.offsets; ga.slot = slot_buf;
-  ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm;
+  ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm; ga.err = &hdr->err;
   if (launch_gather(ga, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 4./5. expert GEMMs
@@ -211,7 +213,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   if (clk.mark(5) != cudaSuccess) return MOE_ERR_CUDA;
   CombineArgs ca;
   ca.o = (const float*)(ws + L.o); ca.T = c.T; ca.d = c.d_model; ca.k = c.k; ca.S = c.n_shared; ca.y_f32 = y_f32;
-  ca.rows_tk = L.rows_tk; ca.slot = slot_buf; ca.topk_w = topk_w; ca.y = y;
+  ca.rows_tk = L.rows_tk; ca.slot = slot_buf; ca.topk_w = topk_w; ca.y = y; ca.err = &hdr->err;
   if (launch_combine(ca, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (clk.mark(6) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;

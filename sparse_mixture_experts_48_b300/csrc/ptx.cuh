@@ -1,0 +1,82 @@
+// Inline-PTX wrappers shared by the kernels that stage tiles with TMA:
+// mbarriers (init, arrive, expect-tx, bounded waits) and tiled bulk-tensor
+// loads into shared memory.
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bounded wait.  Returns false if `abort` is set or the limit ran out (which
+// sets `abort` and records kErrTimeout at `where`).
+static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort, uint64_t limit_ns,
+                                       uint32_t* err, uint32_t where) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if (*abort) return false;
+    if ((i & 7u) == 0u && globaltimer_ns() - t0 > limit_ns) {
+      *abort = 1u;
+      record_error(err, kErrTimeout, where);
+      return false;
+    }
+  }
+}
+// Bounded wait used while tearing down: ignores any abort flag.
+static __device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+// ---- host: tensor maps (cuTensorMapEncodeTiled through the runtime's driver entry point) ----
+// Row-major bf16 matrix [rows, cols] (cols contiguous), box box_cols x box_rows,
+// 128-byte swizzle, zero fill outside the matrix.  False if it cannot be encoded
+// (unaligned base or stride, or no driver entry point).
+bool tmap_bf16_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows);
+// Stacked bf16 matrices [G, rows, cols], box box_cols x box_rows x 1, 128-byte swizzle.
+bool tmap_bf16_3d(CUtensorMap* m, const void* ptr, int G, int64_t rows, int64_t cols, int box_cols, int box_rows);
+
+}  // namespace moe

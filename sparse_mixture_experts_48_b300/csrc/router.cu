@@ -5,10 +5,11 @@
 // The logit contraction has N = E <= 256 and K = d: per token it does 2 d E
 // flops on d * 2 bytes of x, so for E >= 16 plain FP32 FMA would fall below the
 // HBM rate.  The bf16 path therefore runs the contraction on the tensor cores
-// with warp-level mma.sync (m16n8k16, fp32 accumulate); x and W_g tiles are
-// staged in shared memory by a 3-stage cp.async pipeline.  Nothing here is a
-// large GEMM worth a TMEM pipeline: the kernel streams x once and is bound by
-// HBM.  The gating, selection and partial sums run on one thread per token.
+// with warp-level mma.sync (m16n8k16, fp32 accumulate); x tiles are staged in
+// shared memory by TMA into a deep ring, W_g tiles (small, L2-resident) by
+// cp.async.  Nothing here is a large GEMM worth a TMEM pipeline: the kernel
+// streams x once and is bound by HBM.  The gating, selection and partial sums
+// run on one thread per token.
 //
 // Sources: "MoE混合专家模型：Transformer稀疏前馈网络原理与PyTorch实现" §2.1 (linear +
 // softmax router, top-k, renormalise); "手撕一个极简 MoE-FFN" §三 (Router,
@@ -19,17 +20,13 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kThreads = 128;
 constexpr int kBK = 64;        // bf16 k-tile (128 bytes per x row)
-constexpr int kStages = 3;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool full) {
   int n = full ? 16 : 0;   // 0 source bytes: the 16 destination bytes are zero-filled
@@ -132,51 +129,73 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
 }
 
 // ---- bf16: tensor-core logits ---------------------------------------------------
-// Shared memory: the cp.async pipeline, later reused for the fp32 logits
-// [kRouterBM][EP + 1]; the selection bit masks sit after the larger of the two.
-__host__ __device__ constexpr size_t bf16_bits_offset(int NT) {
-  return (size_t)kStages * (kRouterBM * kBK * 2 + kBK * 8 * NT * 2) > (size_t)kRouterBM * (8 * NT + 1) * 4
-             ? (size_t)kStages * (kRouterBM * kBK * 2 + kBK * 8 * NT * 2)
-             : (size_t)kRouterBM * (8 * NT + 1) * 4;
-}
-__host__ __device__ constexpr size_t bf16_smem_bytes(int NT) {
-  return bf16_bits_offset(NT) + (size_t)8 * NT * ((kRouterBM + 31) / 32) * 4;
-}
+// A CTA owns kRouterBM = 64 tokens and walks d in k-tiles of 64.  Per k-tile a
+// ring stage holds the x tile [64 tokens][64 k] (8 KB, brought by one TMA copy
+// with the 128-byte swizzle, rows past T zero-filled) and the W_g tile
+// [64 k][EP experts] (cp.async, same swizzle for EP >= 64).  The ring is deep
+// (up to 8 stages, about 64 KB of x in flight per CTA) because the kernel
+// only streams x once: its speed is the number of bytes it keeps in flight.
+// After the ring the same shared memory holds the fp32 logits [64][EP + 1].
+template <int NT>
+struct RouterBf16 {
+  static constexpr int EP = 8 * NT;
+  static constexpr int XS = kRouterBM * kBK * 2;   // 8 KB, a multiple of 1 KB (swizzle atom)
+  static constexpr int WS = kBK * EP * 2;           // 1 KB * NT
+  static constexpr int STAGE = XS + WS;
+  static constexpr int STAGES = (96 * 1024 / STAGE) > 8 ? 8 : ((96 * 1024 / STAGE) < 2 ? 2 : 96 * 1024 / STAGE);
+  static constexpr size_t RING = (size_t)STAGES * STAGE;
+  static constexpr size_t LOGITS = (size_t)kRouterBM * (EP + 1) * 4;
+  static constexpr size_t BITS_OFF = RING > LOGITS ? RING : LOGITS;
+  static constexpr size_t BITS = (size_t)EP * ((kRouterBM + 31) / 32) * 4;
+  static constexpr size_t BAR_OFF = BITS_OFF + BITS;
+  static constexpr size_t SMEM = 1024 + BAR_OFF + STAGES * 8 + 16;   // + 1 KB to align the ring
+};
+
+constexpr uint32_t kWhereRouter = 0x300;
 
 // NT n-tiles of 8 experts; EP = 8 NT >= E.  Warp w computes tokens 16w..16w+15.
 template <int NT>
-__global__ void __launch_bounds__(kThreads) router_bf16_kernel(RouterArgs a) {
-  constexpr int EP = 8 * NT;
-  constexpr int RW = EP / 8;                  // 16-byte chunks per W_g row
-  constexpr int XS = kRouterBM * kBK * 2;     // bytes of one x stage
-  constexpr int WS = kBK * EP * 2;            // bytes of one W stage
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* xs = smem;
-  uint8_t* ws = smem + kStages * XS;
-  uint32_t* bits = (uint32_t*)(smem + bf16_bits_offset(NT));
+__global__ void __launch_bounds__(kThreads) router_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                               RouterArgs a) {
+  using L = RouterBf16<NT>;
+  constexpr int EP = L::EP, RW = EP / 8, STAGES = L::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint32_t* bits = (uint32_t*)(smem + L::BITS_OFF);
+  uint64_t* full = (uint64_t*)(smem + L::BAR_OFF);
+  uint32_t* abort_flag = (uint32_t*)(full + STAGES);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int64_t blk = blockIdx.x;
   const int64_t t0 = blk * kRouterBM;
   const int d = a.d, E = a.E;
-  const uint16_t* x = (const uint16_t*)a.x;
   const uint16_t* W = (const uint16_t*)a.Wg;
   const int nk = d / kBK;
   const bool wvec = (E % 8) == 0;
+  const uint64_t limit = (uint64_t)a.timeout_ns;
 
-  auto xswz = [](int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); };
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&full[s]), 1);
+    *abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
+  }
+  __syncthreads();
+
   auto wswz = [](int r, int c) { return r * (EP * 2) + ((RW >= 8 ? (c ^ (r & 7)) : c) << 4); };
+  auto xs = [&](int st) { return smem + st * L::STAGE; };
+  auto ws = [&](int st) { return smem + st * L::STAGE + L::XS; };
 
-  auto load_stage = [&](int kt, int st) {
-    const uint32_t xb = smem_u32(xs + st * XS);
-    for (int i = tid; i < kRouterBM * 8; i += kThreads) {
-      int r = i >> 3, c = i & 7;
-      int64_t t = t0 + r;
-      bool ok = t < a.T;
-      const uint16_t* src = x + (ok ? t : 0) * d + kt * kBK + c * 8;
-      cp_async16(xb + xswz(r, c), src, ok);
+  auto issue = [&](int kt, int st) {
+    if (tid == 0) {
+      // The slot was last read (ldmatrix) before the barrier this thread passed.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      const uint32_t fb = smem_u32(&full[st]);
+      mbar_expect_tx(fb, (uint32_t)L::XS);
+      tma_load_2d(smem_u32(xs(st)), &tmX, kt * kBK, (int)t0, fb);
     }
-    const uint32_t wb = smem_u32(ws + st * WS);
+    const uint32_t wb = smem_u32(ws(st));
     if (wvec) {
       for (int i = tid; i < kBK * RW; i += kThreads) {
         int r = i / RW, c = i % RW;
@@ -188,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) router_bf16_kernel(RouterArgs a) {
       for (int i = tid; i < kBK * EP; i += kThreads) {
         int r = i / EP, e = i % EP;
         uint16_t v = e < E ? W[(int64_t)(kt * kBK + r) * E + e] : (uint16_t)0;
-        *(uint16_t*)(ws + st * WS + wswz(r, e / 8) + (e % 8) * 2) = v;
+        *(uint16_t*)(ws(st) + wswz(r, e / 8) + (e % 8) * 2) = v;
       }
     }
   };
@@ -199,31 +218,36 @@ __global__ void __launch_bounds__(kThreads) router_bf16_kernel(RouterArgs a) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[n][q] = 0.f;
 
+  int issued = 0;
 #pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < nk) load_stage(s, s);
+  for (int s = 0; s < STAGES - 1; ++s) {
+    if (s < nk) { issue(s, s); ++issued; }
     cp_async_commit();
   }
+  int stop = -1;   // k-tile at which the CTA gave up, or -1
   for (int kt = 0; kt < nk; ++kt) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
+    const int st = kt % STAGES;
+    cp_async_wait<STAGES - 2>();
+    const bool ok = mbar_wait(smem_u32(&full[st]), (uint32_t)(kt / STAGES) & 1u, abort_flag, limit, a.err,
+                              kWhereRouter + 1);
+    if (__syncthreads_or(!ok)) { stop = kt; break; }
     {
-      int nxt = kt + kStages - 1;
-      if (nxt < nk) load_stage(nxt, nxt % kStages);
+      const int nxt = kt + STAGES - 1;
+      if (nxt < nk) { issue(nxt, nxt % STAGES); ++issued; }
       cp_async_commit();
     }
-    const int st = kt % kStages;
-    const uint32_t xb = smem_u32(xs + st * XS);
-    const uint32_t wb = smem_u32(ws + st * WS);
+    const uint32_t xb = smem_u32(xs(st));
+    const uint32_t wb = smem_u32(ws(st));
 #pragma unroll
     for (int ks = 0; ks < kBK / 16; ++ks) {
       uint32_t af[4];
       {
+        // x tile row r, 16-byte chunk c sits at r * 128 + ((c ^ (r & 7)) << 4).
         int r = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
         int c = ks * 2 + (lane >> 4);
         asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                      : "=r"(af[0]), "=r"(af[1]), "=r"(af[2]), "=r"(af[3])
-                     : "r"(xb + xswz(r, c)));
+                     : "r"(xb + r * 128 + ((c ^ (r & 7)) << 4)));
       }
 #pragma unroll
       for (int np = 0; np < (NT + 1) / 2; ++np) {
@@ -255,8 +279,20 @@ __global__ void __launch_bounds__(kThreads) router_bf16_kernel(RouterArgs a) {
     }
   }
   cp_async_wait<0>();
+  if (stop >= 0) {
+    // Stop cleanly: every TMA copy this CTA started lands before it exits.
+    // Tiles before `stop` were consumed; tiles stop..issued-1 (at most
+    // STAGES - 1, one per slot) may still be in flight.  The error word is
+    // set, so the later stages of the layer skip their work.
+    if (tid == 0)
+      for (int kt = stop; kt < issued; ++kt)
+        mbar_drain(smem_u32(&full[kt % STAGES]), (uint32_t)(kt / STAGES) & 1u,
+                   limit > 2000000000ull ? limit : 2000000000ull);
+    __syncthreads();
+    return;
+  }
   __syncthreads();
-  // Logits to shared memory (reusing the pipeline buffers).
+  // Logits to shared memory (reusing the ring: every copy has been consumed).
   float* sl = (float*)smem;
   const int ldl = EP + 1;
   {
@@ -314,11 +350,13 @@ __global__ void __launch_bounds__(kThreads) router_f32_kernel(RouterArgs a) {
 
 template <int NT>
 cudaError_t launch_bf16(const RouterArgs& a, int64_t nblk, cudaStream_t s) {
-  const size_t bytes = bf16_smem_bytes(NT);
+  const size_t bytes = RouterBf16<NT>::SMEM;
+  CUtensorMap tmX;
+  if (!tmap_bf16_2d(&tmX, a.x, a.T, a.d, kBK, kRouterBM)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(router_bf16_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)bytes);
   if (e != cudaSuccess) return e;
-  router_bf16_kernel<NT><<<(unsigned)nblk, kThreads, bytes, s>>>(a);
+  router_bf16_kernel<NT><<<(unsigned)nblk, kThreads, bytes, s>>>(tmX, a);
   return cudaGetLastError();
 }
 

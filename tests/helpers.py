@@ -92,13 +92,26 @@ def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
 
 
 def check_y(cfg, inp, out, gl, rows):
-    """max |y - y_ref| <= TOL * RMS(y_ref).  When y is stored in bf16 its own
-    final rounding (half a bf16 spacing at y_ref) is added to the bound: a bf16
-    number cannot sit closer to the exact value than that.  With y in fp32 the
-    bound is applied as it stands."""
+    """max |y - y_ref| <= TOL * RMS(y_ref) over the rows the experts produce.
+
+    A row whose every routed choice was cut by the capacity limit (and that has
+    no shared expert) skips the layer: its y is exactly 0 by definition, and it
+    is checked to be exactly 0.  The magnitude scale RMS(y_ref) is taken over
+    the other rows, so that a batch in which the capacity cut removes most
+    tokens does not shrink the bound of the rows that are computed.
+
+    When y is stored in bf16 its own final rounding (half a bf16 spacing at
+    y_ref) is added to the bound: a bf16 number cannot sit closer to the exact
+    value than that.  With y in fp32 the bound is applied as it stands."""
     ref = oracle.forward(cfg, inp, rows=rows, logits=gl)
     y = to_host_f32(out.y)[rows].astype(np.float64)
     yr = ref["y"]
+    skipped = np.asarray(ref["dropped"])[rows].all(axis=1) if cfg.S == 0 else np.zeros(len(rows), bool)
+    assert np.all(y[skipped] == 0.0) and np.all(yr[skipped] == 0.0), "a row that skipped the layer is not 0"
+    live = ~skipped
+    if not live.any():
+        return 0.0
+    y, yr = y[live], yr[live]
     rms = float(np.sqrt(np.mean(yr ** 2)))
     bound = Y_TOL[cfg.dtype] * rms
     if out.y.dtype == torch.bfloat16:

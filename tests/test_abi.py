@@ -113,6 +113,11 @@ def test_forward_host_checks(L):
     assert _call_forward(L, c, ws=None) == 3
     assert _call_forward(L, c, ws=P(0x100080)) == 3                 # workspace not 256-byte aligned
     assert _call_forward(L, _cfg(k=9, E=16)) == 2
+    # T == 0: the per-token tensors are empty and may be NULL (the host checks
+    # pass; without a GPU the first CUDA call then reports MOE_ERR_CUDA).
+    e = _cfg(T=0)
+    assert _call_forward(L, e, x=None, y=None, topk_idx=None, topk_w=None, dropped=None) in (0, 4)
+    assert _call_forward(L, e, W_g=None) == 1
 
 
 def test_grouped_gemm_host_checks(L):
