@@ -26,6 +26,19 @@ namespace {
 
 constexpr int kScanThreads = 1024;
 constexpr int kMaxE = 256;
+constexpr int kScanU = 4;   // 32-block chunks loaded per round, per lane
+
+// Exclusive prefix over 32 lanes of per-lane partial sums (lane order).
+__device__ __forceinline__ int warp_excl_scan(int v, int lane, int* total) {
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += n;
+  }
+  *total = __shfl_sync(0xffffffffu, incl, 31);
+  return incl - v;
+}
 
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   __shared__ int s_npre[kMaxE];
@@ -35,63 +48,141 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   // An earlier stage gave up: its partials are not valid.  Publish empty
   // segments so that nothing later reads or writes through them.
   const bool failed = *(volatile const uint32_t*)a.err != 0u;
+
+  // Phase 1, one warp per expert: exclusive prefix over the router CTAs of
+  // their selection counts (the rank base of each CTA's tokens), the expert's
+  // total selections n_e, and the sum of its gate probabilities.  Loads of
+  // kScanU chunks are issued before their scans.
   for (int e = warp; e < E; e += nwarps) {
     int run = 0;
     double ps = 0.0;
-    for (int64_t b0 = 0; b0 < a.nblk; b0 += 32) {
-      const int64_t b = b0 + lane;
-      const int v = b < a.nblk ? a.hist[b * E + e] : 0;
-      int incl = v;
+    for (int64_t b0 = 0; b0 < a.nblk; b0 += 32 * kScanU) {
+      int v[kScanU];
+      float p[kScanU];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        int n = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += n;
+      for (int u = 0; u < kScanU; ++u) {
+        const int64_t b = b0 + 32 * u + lane;
+        v[u] = b < a.nblk ? a.hist[e * a.nblk + b] : 0;
+        p[u] = b < a.nblk ? a.psum[e * a.nblk + b] : 0.f;
       }
-      if (b < a.nblk) a.base[b * E + e] = run + incl - v;
-      run += __shfl_sync(0xffffffffu, incl, 31);
-      if (b < a.nblk) ps += (double)a.psum[b * E + e];
+#pragma unroll
+      for (int u = 0; u < kScanU; ++u) {
+        const int64_t b = b0 + 32 * u + lane;
+        int tot;
+        const int ex = warp_excl_scan(v[u], lane, &tot);
+        if (b < a.nblk) a.base[e * a.nblk + b] = run + ex;
+        run += tot;
+        ps += (double)p[u];
+      }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-    if (lane == 0) { s_npre[e] = run; s_psum[e] = ps; }
+    if (lane == 0) {
+      s_npre[e] = failed ? 0 : run;
+      s_psum[e] = ps;
+    }
   }
   __syncthreads();
-  if (threadIdx.x != 0) return;
+  if (warp != 0) return;
+
+  // Phase 2, one warp: lane l owns experts [l * PE, (l + 1) * PE).
+  const int PE = (E + 31) / 32;
+  const int e0 = lane * PE;
+  int cnt_local = 0;
+  for (int i = 0; i < PE; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      const int n = s_npre[e];
+      cnt_local += (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
+    }
+  }
+  int kept_total;
+  int off = warp_excl_scan(cnt_local, lane, &kept_total);
   const double Tk = (double)a.T * (double)a.k;
-  int off = 0;
   double L = 0.0;
-  for (int e = 0; e < E; ++e) {
-    const int n = failed ? 0 : s_npre[e];
-    const int c = (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
-    a.n_pre[e] = n;
-    a.counts[e] = c;
-    a.offsets[e] = off;
-    off += c;
-    const double fe = a.T > 0 ? (double)n / Tk : 0.0;
-    const double Pe = a.T > 0 ? s_psum[e] / (double)a.T : 0.0;
-    a.f[e] = (float)fe;
-    a.P[e] = (float)Pe;
-    L += fe * Pe;
+  for (int i = 0; i < PE; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      const int n = s_npre[e];
+      const int c = (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
+      a.n_pre[e] = n;
+      a.counts[e] = c;
+      a.offsets[e] = off;
+      off += c;
+      const double fe = a.T > 0 ? (double)n / Tk : 0.0;
+      const double Pe = a.T > 0 ? s_psum[e] / (double)a.T : 0.0;
+      a.f[e] = (float)fe;
+      a.P[e] = (float)Pe;
+      L += fe * Pe;
+    }
   }
-  a.offsets[E] = off;
-  *a.L_aux = (float)(a.alpha * (double)E * L);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);   // fixed tree order
+  if (lane == 0) {
+    a.offsets[E] = kept_total;
+    *a.L_aux = (float)(a.alpha * (double)E * L);
+  }
   // Segments of the grouped GEMMs: routed experts read the grouped copy of x,
-  // shared experts read x itself and write rows T*k + s*T.
-  int mt = 0;
+  // shared experts read x itself and write rows T*k + s*T.  The offsets of
+  // the routed segments are this warp's own (in registers / recomputed), so
+  // nothing is read back from global memory.
   const int G = E + a.S;
-  for (int g = 0; g < G; ++g) {
-    int rows, w, orow, arow, asrc;
-    if (g < E) { rows = a.counts[g]; w = g; orow = a.offsets[g]; arow = orow; asrc = 0; }
-    else { rows = failed ? 0 : (int)a.T; w = g; orow = (int)(a.rows_tk + (int64_t)(g - E) * a.T); arow = 0; asrc = 1; }
-    a.seg.rows[g] = rows;
-    a.seg.w[g] = w;
-    a.seg.out_row[g] = orow;
-    a.seg.a_row[g] = arow;
-    a.seg.a_src[g] = asrc;
-    a.seg.mtile_start[g] = mt;
-    mt += (rows + kGemmBM - 1) / kGemmBM;
+  const int PG = (G + 31) / 32;
+  const int g0 = lane * PG;
+  int mt_local = 0;
+  for (int i = 0; i < PG; ++i) {
+    const int g = g0 + i;
+    if (g < G) {
+      int rows;
+      if (g < E) {
+        const int n = s_npre[g];
+        rows = (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
+      } else {
+        rows = failed ? 0 : (int)a.T;
+      }
+      mt_local += (rows + kGemmBM - 1) / kGemmBM;
+    }
   }
-  a.seg.mtile_start[G] = mt;
+  int mt_total;
+  int mt = warp_excl_scan(mt_local, lane, &mt_total);
+  // Row offsets of routed segments: exclusive prefix of kept counts over g < E.
+  int row_local = 0;
+  for (int i = 0; i < PG; ++i) {
+    const int g = g0 + i;
+    if (g < E) {
+      const int n = s_npre[g];
+      row_local += (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
+    }
+  }
+  int row_total;
+  int orow_r = warp_excl_scan(row_local, lane, &row_total);
+  for (int i = 0; i < PG; ++i) {
+    const int g = g0 + i;
+    if (g < G) {
+      int rows, orow, arow, asrc;
+      if (g < E) {
+        const int n = s_npre[g];
+        rows = (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
+        orow = orow_r;
+        orow_r += rows;
+        arow = orow;
+        asrc = 0;
+      } else {
+        rows = failed ? 0 : (int)a.T;
+        orow = (int)(a.rows_tk + (int64_t)(g - E) * a.T);
+        arow = 0;
+        asrc = 1;
+      }
+      a.seg.rows[g] = rows;
+      a.seg.w[g] = g;
+      a.seg.out_row[g] = orow;
+      a.seg.a_row[g] = arow;
+      a.seg.a_src[g] = asrc;
+      a.seg.mtile_start[g] = mt;
+      mt += (rows + kGemmBM - 1) / kGemmBM;
+    }
+  }
+  if (lane == 0) a.seg.mtile_start[G] = mt_total;
 }
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
@@ -113,7 +204,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(GatherArgs a)
   if (lane < k) {
     const int e = a.topk_idx[t * k + lane];
     const int64_t b = t / kRouterBM;
-    const int r = a.base[b * E + e] + (int)a.lrank[t * k + lane];
+    const int r = a.base[e * a.nblk + b] + (int)a.lrank[t * k + lane];
     const bool kept = a.capacity < 0 || r < a.capacity;
     my_slot = kept ? a.offsets[e] + r : -1;
     a.slot[t * k + lane] = my_slot;

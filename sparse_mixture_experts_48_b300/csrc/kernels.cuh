@@ -18,8 +18,9 @@ struct RouterArgs {
   int32_t* topk_idx;   // [T, k]
   float* topk_w;       // [T, k]
   uint8_t* lrank;      // [T, k] rank among the CTA's earlier tokens choosing the same expert
-  int32_t* hist;       // [nblk, E] selections per router CTA
-  float* psum;         // [nblk, E] sum of gate probabilities per router CTA
+  int64_t nblk;        // router CTAs (kRouterBM tokens each)
+  int32_t* hist;       // [E, nblk] selections per router CTA (expert-major: the scan reads rows)
+  float* psum;         // [E, nblk] sum of gate probabilities per router CTA
   uint32_t* err;       // workspace status word
   int64_t timeout_ns;  // limit of every device-side wait
 };
@@ -33,7 +34,7 @@ struct ScanArgs {
   int64_t nblk;
   const int32_t* hist;
   const float* psum;
-  int32_t* base;       // [nblk, E]
+  int32_t* base;       // [E, nblk] rank of each router CTA's first selection of e
   int32_t* n_pre;      // [E]
   int32_t* counts;     // [E] kept
   int32_t* offsets;    // [E+1]
@@ -53,7 +54,8 @@ struct GatherArgs {
   int64_t capacity;
   const int32_t* topk_idx;
   const uint8_t* lrank;
-  const int32_t* base;
+  const int32_t* base;  // [E, nblk]
+  int64_t nblk;
   const int32_t* offsets;
   int32_t* slot;        // [T, k]
   uint8_t* dropped;     // [T, k]

@@ -169,7 +169,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   ra.x = x; ra.Wg = W_g; ra.bg = b_g; ra.T = c.T; ra.d = c.d_model; ra.E = c.E; ra.k = c.k;
   ra.gating = c.gating; ra.dtype = c.dtype; ra.logits_out = router_logits; ra.topk_idx = topk_idx;
   ra.topk_w = topk_w; ra.lrank = ws + L.lrank; ra.hist = (int32_t*)(ws + L.hist); ra.psum = (float*)(ws + L.psum);
-  ra.err = &hdr->err; ra.timeout_ns = timeout;
+  ra.err = &hdr->err; ra.timeout_ns = timeout; ra.nblk = L.nblk;
   if (launch_router(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 2. scan: ranks, capacity, offsets, statistics, segment table
@@ -186,7 +186,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   GatherArgs ga;
   ga.x = x; ga.T = c.T; ga.d = c.d_model; ga.E = c.E; ga.k = c.k; ga.dtype = c.dtype; ga.capacity = C;
   ga.topk_idx = topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.offsets = sa.offsets; ga.slot = slot_buf;
-  ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm; ga.err = &hdr->err;
+  ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm; ga.err = &hdr->err; ga.nblk = L.nblk;
   if (launch_gather(ga, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 4./5. expert GEMMs

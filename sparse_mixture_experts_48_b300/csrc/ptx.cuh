@@ -46,6 +46,12 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
     }
   }
 }
+// mbar_wait with its first poll inlined (the common case: already complete).
+__device__ __forceinline__ bool mbar_wait_i(uint32_t bar, uint32_t parity, volatile uint32_t* abort, uint64_t limit_ns,
+                                            uint32_t* err, uint32_t where) {
+  if (mbar_try(bar, parity)) return true;
+  return mbar_wait(bar, parity, abort, limit_ns, err, where);
+}
 // Bounded wait used while tearing down: ignores any abort flag.
 static __device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
@@ -76,6 +82,10 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 // 128-byte swizzle, zero fill outside the matrix.  False if it cannot be encoded
 // (unaligned base or stride, or no driver entry point).
 bool tmap_bf16_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows);
+// As tmap_bf16_2d with the swizzle chosen by the box row size: 16 bytes none,
+// 32 / 64 / 128 bytes the matching swizzle mode.
+bool tmap_bf16_2d_swizzle(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows,
+                          int row_bytes);
 // Stacked bf16 matrices [G, rows, cols], box box_cols x box_rows x 1, 128-byte swizzle.
 bool tmap_bf16_3d(CUtensorMap* m, const void* ptr, int G, int64_t rows, int64_t cols, int box_cols, int box_rows);
 

@@ -5,11 +5,14 @@
 // The logit contraction has N = E <= 256 and K = d: per token it does 2 d E
 // flops on d * 2 bytes of x, so for E >= 16 plain FP32 FMA would fall below the
 // HBM rate.  The bf16 path therefore runs the contraction on the tensor cores
-// with warp-level mma.sync (m16n8k16, fp32 accumulate); x tiles are staged in
-// shared memory by TMA into a deep ring, W_g tiles (small, L2-resident) by
-// cp.async.  Nothing here is a large GEMM worth a TMEM pipeline: the kernel
-// streams x once and is bound by HBM.  The gating, selection and partial sums
-// run on one thread per token.
+// with warp-level mma.sync (m16n8k16, fp32 accumulate).  One producer warp
+// streams x (and W_g when E is 8, 16, 32, 64, 128 or 256) by TMA into a deep
+// shared-memory ring; eight MMA warps (four 16-token row blocks x two k-groups
+// taking the even and odd k-tiles) consume it, each at its own pace (full /
+// empty mbarriers per stage, no block-wide barrier in the loop).  Nothing here
+// is a large GEMM worth a TMEM pipeline: the kernel streams x once, and its
+// speed is set by how many bytes and independent instructions are in flight.
+// The gating and selection tail runs on four threads per token.
 //
 // Sources: "MoE混合专家模型：Transformer稀疏前馈网络原理与PyTorch实现" §2.1 (linear +
 // softmax router, top-k, renormalise); "手撕一个极简 MoE-FFN" §三 (Router,
@@ -25,94 +28,128 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kBK = 64;        // bf16 k-tile (128 bytes per x row)
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool full) {
-  int n = full ? 16 : 0;   // 0 source bytes: the 16 destination bytes are zero-filled
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+constexpr int kRowBlocks = 4;                         // m16 row blocks of a CTA's 64 tokens
+constexpr int kMmaWarps = 2 * kRowBlocks;             // x 2 k-groups (even / odd k-tiles)
+constexpr int kThreadsBf16 = (kMmaWarps + 1) * 32;    // + the producer warp
+constexpr int kThreadsF32 = 256;
+constexpr int kTPT = 4;                               // threads per token in the tail
+constexpr int kBK = 64;                               // bf16 k-tile (128 bytes per x row)
+constexpr uint32_t kWhereRouter = 0x300;
+static_assert(kRouterBM == 16 * kRowBlocks, "one m16 row block per MMA warp of a k-group");
 
 // ---- the per-token tail shared by both dtypes ----------------------------------
 // sl: [kRouterBM][ldl] fp32 logits without bias, rows of this CTA's tokens.
-// bits: [E][1 + kRouterBM/32] scratch words.
+// bits: [E][kRouterBM / 32] scratch words.  The kTPT = 4 threads 4i..4i+3 (one
+// warp) own token i: thread q adds the bias, gates and keeps a sorted top-k of
+// the experts e = q mod 4, then the lists are merged in two butterfly rounds,
+// so all four threads end with the same k experts.  Needs blockDim >=
+// kTPT * kRouterBM.
 __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const RouterArgs& a, int64_t blk) {
-  constexpr int NW = (kRouterBM + 31) / 32;
+  constexpr int NW = kRouterBM / 32;
   const int tid = threadIdx.x;
   const int E = a.E, k = a.k;
   const int64_t t0 = blk * kRouterBM;
   for (int i = tid; i < E * NW; i += blockDim.x) bits[i] = 0u;
   __syncthreads();
 
-  const int64_t t = t0 + tid;
-  const bool valid = tid < kRouterBM && t < a.T;
+  const int tok = tid / kTPT, q = tid % kTPT;
+  const int64_t t = t0 + tok;
+  const bool valid = tid < kTPT * kRouterBM && t < a.T;
   float val[8];
   int idx[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) { val[j] = 0.f; idx[j] = -1; }
-  if (valid) {
-    float* l = sl + tid * ldl;
-    const bool bf = a.dtype == MOE_DT_BF16;
-    for (int e = 0; e < E; ++e) {
-      float b = 0.f;
-      if (a.bg) b = bf ? bf16_bits_to_f32(((const uint16_t*)a.bg)[e]) : ((const float*)a.bg)[e];
-      l[e] += b;
+  // Keeps (val, idx) sorted: larger logit first, equal logits by lower index.
+  auto insert = [&](float cv, int ci) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        const bool better = idx[j] < 0 || cv > val[j] || (cv == val[j] && ci < idx[j]);
+        if (better) {
+          const float tv = val[j]; const int ti = idx[j];
+          val[j] = cv; idx[j] = ci;
+          cv = tv; ci = ti;
+        }
+      }
     }
-    if (a.logits_out)
-      for (int e = 0; e < E; ++e) a.logits_out[t * E + e] = l[e];
-    // Top-k by insertion: larger logit first, equal logits by lower index.
-    for (int e = 0; e < E; ++e) {
-      float cv = l[e];
-      int ci = e;
+  };
+  if (tid < kTPT * kRouterBM) {     // whole warps: the shuffles see every thread of each quad
+    float* l = sl + tok * ldl;
+    const bool bf = a.dtype == MOE_DT_BF16;
+    if (valid) {
+      for (int e = q; e < E; e += kTPT) {
+        float b = 0.f;
+        if (a.bg) b = bf ? bf16_bits_to_f32(((const uint16_t*)a.bg)[e]) : ((const float*)a.bg)[e];
+        l[e] += b;
+        if (a.logits_out) a.logits_out[t * E + e] = l[e];
+        insert(l[e], e);
+      }
+    }
+    // Butterfly merge: take the partner's whole list, then insert it
+    // (inserting while exchanging would read a half-merged list).
+#pragma unroll
+    for (int m = 1; m < kTPT; m <<= 1) {
+      float pv[8];
+      int pi[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        if (j < k) {
-          bool better = idx[j] < 0 || cv > val[j] || (cv == val[j] && ci < idx[j]);
-          if (better) {
-            float tv = val[j]; int ti = idx[j];
-            val[j] = cv; idx[j] = ci;
-            cv = tv; ci = ti;
+        pv[j] = __shfl_xor_sync(0xffffffffu, val[j], m);
+        pi[j] = __shfl_xor_sync(0xffffffffu, idx[j], m);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < k && pi[j] >= 0) insert(pv[j], pi[j]);
+    }
+    // Gating over all E (these p feed P), and the renormalised top-k weights.
+    float z = 0.f;
+    if (valid) {
+      if (a.gating == MOE_GATE_SOFTMAX) {
+        const float mx = val[0];
+        for (int e = q; e < E; e += kTPT) { const float v = expf(l[e] - mx); l[e] = v; z += v; }
+      } else {
+        for (int e = q; e < E; e += kTPT) { const float v = 1.f / (1.f + expf(-l[e])); l[e] = v; z += v; }
+      }
+    }
+    // The same total on every thread of the quad: (z0 + z1) + (z2 + z3), each
+    // pair summed lower thread first.
+#pragma unroll
+    for (int m = 1; m < kTPT; m <<= 1) {
+      const float zp = __shfl_xor_sync(0xffffffffu, z, m);
+      z = (q & m) ? zp + z : z + zp;
+    }
+    if (valid) {
+      const float rz = 1.f / z;
+      for (int e = q; e < E; e += kTPT) l[e] *= rz;
+      if (q == 0) {
+        float g[8], zsel = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j < k) {
+            g[j] = a.gating == MOE_GATE_SOFTMAX ? expf(val[j] - val[0]) : 1.f / (1.f + expf(-val[j]));
+            zsel += g[j];
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j < k) {
+            a.topk_idx[t * k + j] = idx[j];
+            a.topk_w[t * k + j] = g[j] / zsel;
+            atomicOr(&bits[idx[j] * NW + tok / 32], 1u << (tok % 32));
           }
         }
       }
     }
-    // Gating over all E (these p feed P), and the renormalised top-k weights.
-    float z = 0.f, zsel = 0.f;
-    float g[8];
-    if (a.gating == MOE_GATE_SOFTMAX) {
-      const float m = val[0];
-      for (int e = 0; e < E; ++e) { float v = expf(l[e] - m); l[e] = v; z += v; }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) if (j < k) { g[j] = expf(val[j] - m); zsel += g[j]; }
-    } else {
-      for (int e = 0; e < E; ++e) { float v = 1.f / (1.f + expf(-l[e])); l[e] = v; z += v; }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) if (j < k) { g[j] = 1.f / (1.f + expf(-val[j])); zsel += g[j]; }
-    }
-    const float rz = 1.f / z;
-    for (int e = 0; e < E; ++e) l[e] *= rz;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < k) {
-        a.topk_idx[t * k + j] = idx[j];
-        a.topk_w[t * k + j] = g[j] / zsel;
-        atomicOr(&bits[idx[j] * NW + tid / 32], 1u << (tid % 32));
-      }
-    }
   }
   __syncthreads();
-  if (valid) {
-    const int w = tid / 32;
-    const uint32_t below = (1u << (tid % 32)) - 1u;
+  if (valid && q == 0) {
+    const int w = tok / 32;
+    const uint32_t below = (1u << (tok % 32)) - 1u;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j < k) {
         const uint32_t* be = bits + idx[j] * NW;
         int r = __popc(be[w] & below);
-        for (int q = 0; q < w; ++q) r += __popc(be[q]);
+        for (int qq = 0; qq < w; ++qq) r += __popc(be[qq]);
         a.lrank[t * k + j] = (uint8_t)r;
       }
     }
@@ -120,183 +157,231 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
   const int nvalid = (int)(a.T - t0 < kRouterBM ? a.T - t0 : kRouterBM);
   for (int e = tid; e < E; e += blockDim.x) {
     int h = 0;
-    for (int q = 0; q < NW; ++q) h += __popc(bits[e * NW + q]);
-    a.hist[blk * E + e] = h;
+    for (int qq = 0; qq < NW; ++qq) h += __popc(bits[e * NW + qq]);
+    a.hist[e * a.nblk + blk] = h;
     float s = 0.f;
     for (int r = 0; r < nvalid; ++r) s += sl[r * ldl + e];   // fixed order
-    a.psum[blk * E + e] = s;
+    a.psum[e * a.nblk + blk] = s;
   }
 }
 
 // ---- bf16: tensor-core logits ---------------------------------------------------
 // A CTA owns kRouterBM = 64 tokens and walks d in k-tiles of 64.  Per k-tile a
-// ring stage holds the x tile [64 tokens][64 k] (8 KB, brought by one TMA copy
-// with the 128-byte swizzle, rows past T zero-filled) and the W_g tile
-// [64 k][EP experts] (cp.async, same swizzle for EP >= 64).  The ring is deep
-// (up to 8 stages, about 64 KB of x in flight per CTA) because the kernel
-// only streams x once: its speed is the number of bytes it keeps in flight.
+// ring stage holds KSUB consecutive x tiles [64 tokens][64 k] (8 KB each, one
+// TMA copy each, 128-byte swizzle, rows past T zero-filled) and the matching
+// W_g tiles [64 k][EP experts], kept as boxes of at most 64 experts whose rows
+// are swizzled like the TMA copy writes them.  The ring holds about 100 KB:
+// the kernel's speed is the number of bytes it keeps in flight.
 // After the ring the same shared memory holds the fp32 logits [64][EP + 1].
-template <int NT>
+template <int NT, int KSUB_, int STAGES_>
 struct RouterBf16 {
   static constexpr int EP = 8 * NT;
-  static constexpr int XS = kRouterBM * kBK * 2;   // 8 KB, a multiple of 1 KB (swizzle atom)
-  static constexpr int WS = kBK * EP * 2;           // 1 KB * NT
-  static constexpr int STAGE = XS + WS;
-  static constexpr int STAGES = (96 * 1024 / STAGE) > 8 ? 8 : ((96 * 1024 / STAGE) < 2 ? 2 : 96 * 1024 / STAGE);
+  static constexpr int KSUB = KSUB_;                // k-tiles per ring stage
+  static constexpr int STAGES = STAGES_;
+  static constexpr int WCOLS = EP < 64 ? EP : 64;   // experts per W box
+  static constexpr int WRB = WCOLS * 2;             // bytes of one W box row: 16 .. 128
+  static constexpr int XS = kRouterBM * kBK * 2;    // 8 KB per x k-tile, a multiple of 1 KB (swizzle atom)
+  static constexpr int WS = kBK * EP * 2;           // 1 KB * NT per W k-tile
+  static constexpr int STAGE = KSUB * (XS + WS);    // [KSUB x tiles][KSUB W tiles]
   static constexpr size_t RING = (size_t)STAGES * STAGE;
   static constexpr size_t LOGITS = (size_t)kRouterBM * (EP + 1) * 4;
   static constexpr size_t BITS_OFF = RING > LOGITS ? RING : LOGITS;
-  static constexpr size_t BITS = (size_t)EP * ((kRouterBM + 31) / 32) * 4;
-  static constexpr size_t BAR_OFF = BITS_OFF + BITS;
-  static constexpr size_t SMEM = 1024 + BAR_OFF + STAGES * 8 + 16;   // + 1 KB to align the ring
+  static constexpr size_t BITS = (size_t)EP * (kRouterBM / 32) * 4;
+  static constexpr size_t BAR_OFF = (BITS_OFF + BITS + 7) / 8 * 8;
+  static constexpr size_t SMEM = 1024 + BAR_OFF + 2 * STAGES * 8 + 16;   // + 1 KB to align the ring
+
+  // Byte offset in a W k-tile of 16-byte chunk c (experts 8c..8c+7) of k-row r:
+  // box c / (WRB/16), and inside it the TMA swizzle of WRB-byte rows
+  // (16-byte chunk index XOR address bits 7.. of the row start).
+  __device__ static int woff(int r, int c) {
+    constexpr int CPR = WRB / 16;
+    const int box = c / CPR, cb = c % CPR;
+    return box * (kBK * WRB) + r * WRB + ((cb ^ ((r * WRB / 128) & (CPR - 1))) << 4);
+  }
 };
 
-constexpr uint32_t kWhereRouter = 0x300;
+// Ring shape per expert count: a stage spans KSUB consecutive k-tiles, so a
+// token row is fetched KSUB * 128 contiguous bytes at a time (DRAM pages are
+// opened for more than one 128-byte piece), and the ring stays near 108 KB so
+// that two CTAs share an SM.  An even KSUB gives both k-groups of MMA warps
+// the same share of every stage.
+template <int NT> struct RouterShape;
+template <> struct RouterShape<1> { static constexpr int KSUB = 4, STAGES = 3; };
+template <> struct RouterShape<2> { static constexpr int KSUB = 2, STAGES = 5; };
+template <> struct RouterShape<4> { static constexpr int KSUB = 2, STAGES = 4; };
+template <> struct RouterShape<8> { static constexpr int KSUB = 2, STAGES = 3; };
+template <> struct RouterShape<16> { static constexpr int KSUB = 2, STAGES = 2; };
+template <> struct RouterShape<32> { static constexpr int KSUB = 1, STAGES = 2; };
 
-// NT n-tiles of 8 experts; EP = 8 NT >= E.  Warp w computes tokens 16w..16w+15.
-template <int NT>
-__global__ void __launch_bounds__(kThreads) router_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
-                                                               RouterArgs a) {
-  using L = RouterBf16<NT>;
-  constexpr int EP = L::EP, RW = EP / 8, STAGES = L::STAGES;
+// NT n-tiles of 8 experts; EP = 8 NT >= E.  Warps 0-7 compute (row block w %
+// 4: tokens 16 (w % 4) .. + 15; k-tiles of parity w / 4); warp 8 is the producer.  tma_w: W_g tiles come by TMA (E == EP);
+// otherwise the producer warp copies them with plain loads.
+template <int NT, int KSUB, int STAGES_>
+__global__ void __launch_bounds__(kThreadsBf16) router_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                   const __grid_constant__ CUtensorMap tmW,
+                                                                   RouterArgs a, int tma_w) {
+  using L = RouterBf16<NT, KSUB, STAGES_>;
+  constexpr int EP = L::EP, STAGES = L::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint32_t* bits = (uint32_t*)(smem + L::BITS_OFF);
   uint64_t* full = (uint64_t*)(smem + L::BAR_OFF);
-  uint32_t* abort_flag = (uint32_t*)(full + STAGES);
+  uint64_t* empty = full + STAGES;
+  uint32_t* abort_flag = (uint32_t*)(empty + STAGES);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int64_t blk = blockIdx.x;
   const int64_t t0 = blk * kRouterBM;
-  const int d = a.d, E = a.E;
-  const uint16_t* W = (const uint16_t*)a.Wg;
-  const int nk = d / kBK;
-  const bool wvec = (E % 8) == 0;
+  const int E = a.E;
+  const int nk = a.d / kBK;                 // k-tiles
+  const int ns = (nk + KSUB - 1) / KSUB;    // ring steps
   const uint64_t limit = (uint64_t)a.timeout_ns;
+  const uint64_t drain_limit = limit > 2000000000ull ? limit : 2000000000ull;
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&full[s]), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), tma_w ? 1u : 33u);   // producer lane 0 (+ 32 lanes after plain copies)
+      mbar_init(smem_u32(&empty[s]), kMmaWarps);
+    }
     *abort_flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
   }
   __syncthreads();
 
-  auto wswz = [](int r, int c) { return r * (EP * 2) + ((RW >= 8 ? (c ^ (r & 7)) : c) << 4); };
-  auto xs = [&](int st) { return smem + st * L::STAGE; };
-  auto ws = [&](int st) { return smem + st * L::STAGE + L::XS; };
-
-  auto issue = [&](int kt, int st) {
-    if (tid == 0) {
-      // The slot was last read (ldmatrix) before the barrier this thread passed.
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      const uint32_t fb = smem_u32(&full[st]);
-      mbar_expect_tx(fb, (uint32_t)L::XS);
-      tma_load_2d(smem_u32(xs(st)), &tmX, kt * kBK, (int)t0, fb);
-    }
-    const uint32_t wb = smem_u32(ws(st));
-    if (wvec) {
-      for (int i = tid; i < kBK * RW; i += kThreads) {
-        int r = i / RW, c = i % RW;
-        bool ok = c * 8 < E;
-        const uint16_t* src = W + (int64_t)(kt * kBK + r) * E + (ok ? c * 8 : 0);
-        cp_async16(wb + wswz(r, c), src, ok);
-      }
-    } else {
-      for (int i = tid; i < kBK * EP; i += kThreads) {
-        int r = i / EP, e = i % EP;
-        uint16_t v = e < E ? W[(int64_t)(kt * kBK + r) * E + e] : (uint16_t)0;
-        *(uint16_t*)(ws(st) + wswz(r, e / 8) + (e % 8) * 2) = v;
-      }
-    }
-  };
-
+  bool stopped = false;
   float acc[NT][4];
 #pragma unroll
   for (int n = 0; n < NT; ++n)
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[n][q] = 0.f;
 
-  int issued = 0;
-#pragma unroll
-  for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < nk) { issue(s, s); ++issued; }
-    cp_async_commit();
-  }
-  int stop = -1;   // k-tile at which the CTA gave up, or -1
-  for (int kt = 0; kt < nk; ++kt) {
-    const int st = kt % STAGES;
-    cp_async_wait<STAGES - 2>();
-    const bool ok = mbar_wait(smem_u32(&full[st]), (uint32_t)(kt / STAGES) & 1u, abort_flag, limit, a.err,
-                              kWhereRouter + 1);
-    if (__syncthreads_or(!ok)) { stop = kt; break; }
-    {
-      const int nxt = kt + STAGES - 1;
-      if (nxt < nk) { issue(nxt, nxt % STAGES); ++issued; }
-      cp_async_commit();
+  if (warp == kMmaWarps) {
+    // ---------------- producer ----------------
+    const uint16_t* W = (const uint16_t*)a.Wg;
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
+      if (tma_w) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
     }
-    const uint32_t xb = smem_u32(xs(st));
-    const uint32_t wb = smem_u32(ws(st));
-#pragma unroll
-    for (int ks = 0; ks < kBK / 16; ++ks) {
-      uint32_t af[4];
-      {
-        // x tile row r, 16-byte chunk c sits at r * 128 + ((c ^ (r & 7)) << 4).
-        int r = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-        int c = ks * 2 + (lane >> 4);
-        asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(af[0]), "=r"(af[1]), "=r"(af[2]), "=r"(af[3])
-                     : "r"(xb + r * 128 + ((c ^ (r & 7)) << 4)));
+    int kt = 0;   // ring step
+    for (; kt < ns; ++kt) {
+      const int st = kt % STAGES;
+      const int k0 = kt * KSUB;
+      const int nsub = nk - k0 < KSUB ? nk - k0 : KSUB;
+      bool ok = true;
+      if (kt >= STAGES)
+        ok = mbar_wait_i(smem_u32(&empty[st]), (uint32_t)((kt / STAGES) - 1) & 1u, abort_flag, limit, a.err,
+                         kWhereRouter + 1);
+      if (!__all_sync(0xffffffffu, ok)) { stopped = true; break; }
+      uint8_t* xs = smem + st * L::STAGE;
+      uint8_t* ws = xs + KSUB * L::XS;
+      const uint32_t fb = smem_u32(&full[st]);
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(fb, (uint32_t)(nsub * (L::XS + (tma_w ? L::WS : 0))));
+        for (int i = 0; i < nsub; ++i) tma_load_2d(smem_u32(xs + i * L::XS), &tmX, (k0 + i) * kBK, (int)t0, fb);
+        if (tma_w)
+          for (int i = 0; i < nsub; ++i)
+            for (int b = 0; b < EP / L::WCOLS; ++b)
+              tma_load_2d(smem_u32(ws + i * L::WS + b * (kBK * L::WRB)), &tmW, b * L::WCOLS, (k0 + i) * kBK, fb);
       }
+      if (!tma_w) {
+        // W_g rows are E * 2 bytes: not TMA-able unless E is a multiple of 8,
+        // and E < EP leaves a zero tail.  Plain copies, then every lane arrives.
+        const bool vec = (E % 8) == 0;
+        for (int i = lane; i < nsub * kBK * (EP / 8); i += 32) {
+          const int sub = i / (kBK * (EP / 8)), rem = i % (kBK * (EP / 8));
+          const int r = rem / (EP / 8), c = rem % (EP / 8);
+          const uint16_t* src = W + (int64_t)((k0 + sub) * kBK + r) * E;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (vec) {
+            if (c * 8 < E) v = *reinterpret_cast<const uint4*>(src + c * 8);
+          } else {
+            uint32_t h[8];
 #pragma unroll
-      for (int np = 0; np < (NT + 1) / 2; ++np) {
-        uint32_t bf[4];
-        const int i = lane >> 3;
-        const int kr = ks * 16 + (lane & 7) + 8 * (i & 1);
-        if (NT == 1) {
-          asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
-                       : "=r"(bf[0]), "=r"(bf[1])
-                       : "r"(wb + wswz(kr, 0)));
-        } else {
-          const int nc = 2 * np + (i >> 1);
-          asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(bf[0]), "=r"(bf[1]), "=r"(bf[2]), "=r"(bf[3])
-                       : "r"(wb + wswz(kr, nc)));
+            for (int q = 0; q < 8; ++q) h[q] = (c * 8 + q < E) ? (uint32_t)src[c * 8 + q] : 0u;
+            v = make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
+          }
+          *reinterpret_cast<uint4*>(ws + sub * L::WS + L::woff(r, c)) = v;
+        }
+        mbar_arrive(fb);
+      }
+    }
+    if (stopped && lane == 0) {
+      // Every TMA copy this CTA started lands before it exits: the last
+      // STAGES ring steps issued, one per slot, may still be in flight.
+      for (int j = kt - STAGES > 0 ? kt - STAGES : 0; j < kt; ++j)
+        mbar_drain(smem_u32(&full[j % STAGES]), (uint32_t)(j / STAGES) & 1u, drain_limit);
+    }
+  } else {
+    // ---------------- MMA warps ----------------
+    // Warp w: row block w % 4, k-group w / 4 (k-tiles of that parity).  Every
+    // warp waits on and releases every stage, so the empty barrier's phases
+    // stay in step even when a stage holds no k-tile of the warp's parity.
+    const int rb = warp % kRowBlocks, kg = warp / kRowBlocks;
+    for (int kt = 0; kt < ns; ++kt) {
+      const int st = kt % STAGES;
+      const int nsub = nk - kt * KSUB < KSUB ? nk - kt * KSUB : KSUB;
+      bool ok = mbar_wait_i(smem_u32(&full[st]), (uint32_t)(kt / STAGES) & 1u, abort_flag, limit, a.err,
+                            kWhereRouter + 2);
+      if (!__all_sync(0xffffffffu, ok)) { stopped = true; break; }
+      for (int sub = 0; sub < nsub; ++sub) {
+      if (((kt * KSUB + sub) & 1) != kg) continue;
+      const uint32_t xb = smem_u32(smem + st * L::STAGE) + sub * L::XS;
+      const uint32_t wb = smem_u32(smem + st * L::STAGE) + KSUB * L::XS + sub * L::WS;
+#pragma unroll
+      for (int ks = 0; ks < kBK / 16; ++ks) {
+        uint32_t af[4];
+        {
+          // x tile row r, 16-byte chunk c sits at r * 128 + ((c ^ (r & 7)) << 4).
+          const int r = rb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+          const int c = ks * 2 + (lane >> 4);
+          asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(af[0]), "=r"(af[1]), "=r"(af[2]), "=r"(af[3])
+                       : "r"(xb + r * 128 + ((c ^ (r & 7)) << 4)));
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int n = 2 * np + h;
-          if (n < NT) {
-            asm volatile(
-                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                "{%0,%1,%2,%3};"
-                : "+f"(acc[n][0]), "+f"(acc[n][1]), "+f"(acc[n][2]), "+f"(acc[n][3])
-                : "r"(af[0]), "r"(af[1]), "r"(af[2]), "r"(af[3]), "r"(bf[2 * h]), "r"(bf[2 * h + 1]));
+        for (int np = 0; np < (NT + 1) / 2; ++np) {
+          uint32_t bf[4];
+          const int i = lane >> 3;
+          const int kr = ks * 16 + (lane & 7) + 8 * (i & 1);
+          if (NT == 1) {
+            asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                         : "=r"(bf[0]), "=r"(bf[1])
+                         : "r"(wb + L::woff(kr, 0)));
+          } else {
+            const int nc = 2 * np + (i >> 1);
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(bf[0]), "=r"(bf[1]), "=r"(bf[2]), "=r"(bf[3])
+                         : "r"(wb + L::woff(kr, nc)));
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int n = 2 * np + h;
+            if (n < NT) {
+              asm volatile(
+                  "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                  "{%0,%1,%2,%3};"
+                  : "+f"(acc[n][0]), "+f"(acc[n][1]), "+f"(acc[n][2]), "+f"(acc[n][3])
+                  : "r"(af[0]), "r"(af[1]), "r"(af[2]), "r"(af[3]), "r"(bf[2 * h]), "r"(bf[2 * h + 1]));
+            }
           }
         }
       }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
     }
   }
-  cp_async_wait<0>();
-  if (stop >= 0) {
-    // Stop cleanly: every TMA copy this CTA started lands before it exits.
-    // Tiles before `stop` were consumed; tiles stop..issued-1 (at most
-    // STAGES - 1, one per slot) may still be in flight.  The error word is
-    // set, so the later stages of the layer skip their work.
-    if (tid == 0)
-      for (int kt = stop; kt < issued; ++kt)
-        mbar_drain(smem_u32(&full[kt % STAGES]), (uint32_t)(kt / STAGES) & 1u,
-                   limit > 2000000000ull ? limit : 2000000000ull);
-    __syncthreads();
-    return;
-  }
-  __syncthreads();
-  // Logits to shared memory (reusing the ring: every copy has been consumed).
+  // Every warp is past its last read of the ring before the logits overwrite it.
+  if (__syncthreads_or(stopped)) return;
   float* sl = (float*)smem;
   const int ldl = EP + 1;
-  {
-    const int r0 = warp * 16 + (lane >> 2);
+  // logits = (even k-tiles) + (odd k-tiles): k-group 1 stores its partial, and
+  // the k-group 0 warp of the same row block (same lane -> same elements) adds
+  // its own in front.
+  const int r0 = (warp % kRowBlocks) * 16 + (lane >> 2);
+  if (warp >= kRowBlocks && warp < kMmaWarps) {
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
       const int c = n * 8 + 2 * (lane & 3);
@@ -307,12 +392,23 @@ __global__ void __launch_bounds__(kThreads) router_bf16_kernel(const __grid_cons
     }
   }
   __syncthreads();
+  if (warp < kRowBlocks) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int c = n * 8 + 2 * (lane & 3);
+      sl[r0 * ldl + c] = acc[n][0] + sl[r0 * ldl + c];
+      sl[r0 * ldl + c + 1] = acc[n][1] + sl[r0 * ldl + c + 1];
+      sl[(r0 + 8) * ldl + c] = acc[n][2] + sl[(r0 + 8) * ldl + c];
+      sl[(r0 + 8) * ldl + c + 1] = acc[n][3] + sl[(r0 + 8) * ldl + c + 1];
+    }
+  }
+  __syncthreads();
   router_finalize(sl, ldl, bits, a, blk);
 }
 
 // ---- fp32: CUDA-core logits ------------------------------------------------------
 constexpr int kBK32 = 32;
-__global__ void __launch_bounds__(kThreads) router_f32_kernel(RouterArgs a) {
+__global__ void __launch_bounds__(kThreadsF32) router_f32_kernel(RouterArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int E = a.E, d = a.d;
   const int ldl = E + 1;
@@ -324,20 +420,20 @@ __global__ void __launch_bounds__(kThreads) router_f32_kernel(RouterArgs a) {
   const int64_t blk = blockIdx.x, t0 = blk * kRouterBM;
   const float* x = (const float*)a.x;
   const float* W = (const float*)a.Wg;
-  for (int i = tid; i < kRouterBM * ldl; i += kThreads) sl[i] = 0.f;
+  for (int i = tid; i < kRouterBM * ldl; i += kThreadsF32) sl[i] = 0.f;
   for (int kt = 0; kt < d; kt += kBK32) {
     __syncthreads();
-    for (int i = tid; i < kRouterBM * kBK32; i += kThreads) {
+    for (int i = tid; i < kRouterBM * kBK32; i += kThreadsF32) {
       int r = i / kBK32, c = i % kBK32;
       int64_t t = t0 + r;
       xs[r * (kBK32 + 1) + c] = (t < a.T && kt + c < d) ? x[t * d + kt + c] : 0.f;
     }
-    for (int i = tid; i < kBK32 * E; i += kThreads) {
+    for (int i = tid; i < kBK32 * E; i += kThreadsF32) {
       int r = i / E, e = i % E;
       wsm[i] = (kt + r < d) ? W[(int64_t)(kt + r) * E + e] : 0.f;
     }
     __syncthreads();
-    for (int o = tid; o < kRouterBM * E; o += kThreads) {
+    for (int o = tid; o < kRouterBM * E; o += kThreadsF32) {
       int r = o / E, e = o % E;
       float s = sl[r * ldl + e];
       for (int c = 0; c < kBK32; ++c) s = fmaf(xs[r * (kBK32 + 1) + c], wsm[c * E + e], s);
@@ -350,13 +446,23 @@ __global__ void __launch_bounds__(kThreads) router_f32_kernel(RouterArgs a) {
 
 template <int NT>
 cudaError_t launch_bf16(const RouterArgs& a, int64_t nblk, cudaStream_t s) {
-  const size_t bytes = RouterBf16<NT>::SMEM;
-  CUtensorMap tmX;
+  constexpr int KSUB = RouterShape<NT>::KSUB, STAGES = RouterShape<NT>::STAGES;
+  using L = RouterBf16<NT, KSUB, STAGES>;
+  static_assert(L::SMEM <= 113 * 1024, "two router CTAs per SM");
+  const size_t bytes = L::SMEM;
+  CUtensorMap tmX, tmW;
   if (!tmap_bf16_2d(&tmX, a.x, a.T, a.d, kBK, kRouterBM)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(router_bf16_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)bytes);
+  int tma_w = 0;
+  if (a.E == L::EP) {
+    if (!tmap_bf16_2d_swizzle(&tmW, a.Wg, a.d, a.E, L::WCOLS, kBK, L::WRB)) return cudaErrorInvalidValue;
+    tma_w = 1;
+  } else {
+    tmW = tmX;   // not read
+  }
+  auto kern = router_bf16_kernel<NT, KSUB, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  router_bf16_kernel<NT><<<(unsigned)nblk, kThreads, bytes, s>>>(tmX, a);
+  kern<<<(unsigned)nblk, kThreadsBf16, bytes, s>>>(tmX, tmW, a, tma_w);
   return cudaGetLastError();
 }
 
@@ -367,11 +473,11 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
   if (nblk == 0) return cudaSuccess;
   if (a.dtype == MOE_DT_F32) {
     size_t bytes = (size_t)kRouterBM * (a.E + 1) * 4 + (size_t)kRouterBM * (kBK32 + 1) * 4 +
-                   (size_t)kBK32 * a.E * 4 + (size_t)a.E * ((kRouterBM + 31) / 32) * 4;
+                   (size_t)kBK32 * a.E * 4 + (size_t)a.E * (kRouterBM / 32) * 4;
     cudaError_t e = cudaFuncSetAttribute(router_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)bytes);
     if (e != cudaSuccess) return e;
-    router_f32_kernel<<<(unsigned)nblk, kThreads, bytes, s>>>(a);
+    router_f32_kernel<<<(unsigned)nblk, kThreadsF32, bytes, s>>>(a);
     return cudaGetLastError();
   }
   const int ep = (a.E + 7) / 8;
