@@ -199,6 +199,8 @@ def main():
     ap.add_argument("--T", type=int, default=0, help="override the token count (profiling runs)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop")
+    ap.add_argument("--gemm-one-cta", action="store_true",
+                    help="bf16 expert GEMMs on the one-CTA tile kernel instead of the CTA-pair kernel")
     args = ap.parse_args()
     cfg = si.CONFIGS[args.workload]
     if args.T:
@@ -245,7 +247,8 @@ def main():
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)] for _ in range(K)]
 
     def step(i=None):
-        moe.forward(cfg, *args_in, out=out, workspace=ws, stage_events=ev[i] if i is not None else None)
+        moe.forward(cfg, *args_in, out=out, workspace=ws, stage_events=ev[i] if i is not None else None,
+                    gemm_single_cta=args.gemm_one_cta)
 
     for _ in range(W):
         step()
@@ -327,7 +330,7 @@ def main():
 
         def e2e_step():
             x_dev.copy_(x_host, non_blocking=True)
-            moe.forward(cfg, *args_e2e, out=out, workspace=ws)
+            moe.forward(cfg, *args_e2e, out=out, workspace=ws, gemm_single_cta=args.gemm_one_cta)
             y_host.copy_(out.y, non_blocking=True)
             for h, t in zip(small_host, small):
                 h.copy_(t, non_blocking=True)
@@ -368,6 +371,7 @@ def main():
             "dtype": "bf16" if cfg.dtype == si.BF16 else "f32", "data": "synthetic",
             "config": {"workload": workload_desc(cfg), "T": cfg.T, "d_model": cfg.d, "d_ff": cfg.f, "E": cfg.E,
                        "k": cfg.k, "n_shared": cfg.S, "parallelism": "replicas" if world > 1 else "single GPU",
+                       "expert_gemm": "one-CTA 128x256 tiles" if args.gemm_one_cta else "CTA-pair 256x256 tiles",
                        "l2": "no flush: inputs larger than L2 (x %.0f MB, expert weights %.2f GB)" % (
                            inp["x"].nbytes / 1e6, sum(inp[n].nbytes for n in ("W1", "W2", "W3")
                                                       if inp[n] is not None) / 1e9)},

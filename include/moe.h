@@ -111,7 +111,14 @@ typedef struct {
   /* Limit of every device-side wait in nanoseconds; 0 = 2 s.  A wait that
    * runs out makes the kernel stop cleanly and records MOE_ERR_TIMEOUT. */
   int64_t wait_timeout_ns;
+  /* OR of MOE_OPT_*; 0 = defaults. */
+  int64_t flags;
 } moe_launch_opts;
+
+/* bf16 expert GEMMs: run the one-CTA 128 x 256 tile kernel instead of the
+ * default CTA-pair (2-SM) 256 x 256 tile kernel.  Same results up to fp32
+ * summation order inside the tensor core; kept for comparison and testing. */
+#define MOE_OPT_GEMM_SINGLE_CTA 1
 
 /* Human-readable name of a status.  Never NULL. */
 const char* moe_status_string(moe_status s);

@@ -67,7 +67,11 @@ class _CConfig(ctypes.Structure):
 
 
 class _COpts(ctypes.Structure):
-    _fields_ = [("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("wait_timeout_ns", ctypes.c_int64)]
+    _fields_ = [("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("wait_timeout_ns", ctypes.c_int64),
+                ("flags", ctypes.c_int64)]
+
+
+OPT_GEMM_SINGLE_CTA = 1
 
 
 _lib_handle: Optional[ctypes.CDLL] = None
@@ -141,8 +145,8 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _opts(stage_events, timeout_ns: int):
-    if stage_events is None and not timeout_ns:
+def _opts(stage_events, timeout_ns: int, flags: int = 0):
+    if stage_events is None and not timeout_ns and not flags:
         return None, None
     arr = None
     if stage_events is not None:
@@ -150,7 +154,8 @@ def _opts(stage_events, timeout_ns: int):
             if not e.cuda_event:       # torch creates the CUDA event on its first record
                 e.record()
         arr = (ctypes.c_void_p * len(stage_events))(*[ctypes.c_void_p(e.cuda_event) for e in stage_events])
-    o = _COpts(ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)) if arr is not None else None, int(timeout_ns))
+    o = _COpts(ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)) if arr is not None else None, int(timeout_ns),
+               int(flags))
     return o, arr
 
 
@@ -217,10 +222,12 @@ def alloc_workspace(cfg, device) -> torch.Tensor:
 def forward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutput] = None,
             workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
             debug: bool = False, stage_events=None, timeout_ns: int = 0,
-            y_f32: Optional[bool] = None) -> MoEOutput:
+            y_f32: Optional[bool] = None, gemm_single_cta: bool = False) -> MoEOutput:
     """Enqueue the layer's forward pass on ``stream`` (default: the current one).
 
     ``y_f32``: write y in fp32 (default: the config's ``y_f32``, else its dtype).
+    ``gemm_single_cta``: bf16 expert GEMMs on the one-CTA tile kernel instead
+    of the default CTA-pair kernel.
 
     Asynchronous: returns once the kernels are enqueued.  Host-detected errors
     raise MoEError; device-side ones are reported by check_device_errors()."""
@@ -247,7 +254,7 @@ def forward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutpu
     if workspace is None:
         workspace = out.workspace if out.workspace is not None else alloc_workspace(cfg, dev)
     out.workspace = workspace
-    opts, keep = _opts(stage_events, timeout_ns)
+    opts, keep = _opts(stage_events, timeout_ns, OPT_GEMM_SINGLE_CTA if gemm_single_cta else 0)
     ccfg = c_config(cfg, y_f32=yf)
     with torch.cuda.device(dev):
         status = lib().moe_forward(
@@ -270,7 +277,8 @@ def check_device_errors(workspace: torch.Tensor, stream: Optional[torch.cuda.Str
 def grouped_gemm(dtype: int, act: int, seg_offsets: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
                  B3: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
                  C: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                 stream: Optional[torch.cuda.Stream] = None, stage_events=None, timeout_ns: int = 0):
+                 stream: Optional[torch.cuda.Stream] = None, stage_events=None, timeout_ns: int = 0,
+                 single_cta: bool = False):
     """C[r] = epilogue(A[r] @ B[g]) for the rows r of each group g (see moe.h)."""
     G, K, N = B.shape
     M = A.shape[0]
@@ -287,7 +295,7 @@ def grouped_gemm(dtype: int, act: int, seg_offsets: torch.Tensor, A: torch.Tenso
         C = torch.zeros((M, N), dtype=A.dtype, device=A.device)
     if workspace is None:
         workspace = torch.empty((lib().moe_grouped_gemm_workspace_size(G),), dtype=torch.uint8, device=A.device)
-    opts, keep = _opts(stage_events, timeout_ns)
+    opts, keep = _opts(stage_events, timeout_ns, OPT_GEMM_SINGLE_CTA if single_cta else 0)
     with torch.cuda.device(A.device):
         status = lib().moe_grouped_gemm(dtype, act, G, _ptr(seg_offsets), M, K, N, _ptr(A), _ptr(B), _ptr(B3),
                                         _ptr(bias), _ptr(C), _ptr(workspace), workspace.numel(),

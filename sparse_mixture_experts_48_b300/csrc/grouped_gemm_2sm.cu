@@ -1,0 +1,433 @@
+// K3 on CTA pairs -- grouped expert GEMM with 2-CTA tcgen05 MMAs (cta_group::2).
+//
+//   C[r, :] = epilogue( A[r, :] B[w(g)] )   for each row r of each segment g
+//
+// A thread-block cluster of two CTAs on two SMs computes one 256 x 256 pair
+// tile: CTA rank 0 (the leader) and rank 1 each stage their own 128 rows of A
+// and their own half of the 256 B columns (for SwiGLU: the leader the 128 x W1
+// columns, the peer the same 128 x W3 columns), and one leader thread issues
+// M256 N256 K16 MMAs that read both CTAs' shared memory and accumulate into
+// both CTAs' TMEM (128 lanes x 256 columns each).  Against the single-CTA
+// 128 x 256 tile, every SM stages and feeds the tensor core 32 KB instead of
+// 48 KB per 64-deep k-block for the same MMA work, so a 6-stage ring fits.
+//
+// Persistent: each pair walks the pair tiles (segment-major, then 256-column
+// block, then 256-row block) with a stride of the number of pairs.  Roles:
+//   warp 0      TMA producer of its CTA.  Its copies complete on the LEADER's
+//               full barrier (.cta_group::2), which the leader's producer arms
+//               with both CTAs' byte count (64 KB per stage).
+//   warp 1      TMEM owner (both CTAs allocate collectively); in the leader one
+//               lane issues the MMAs and commits to both CTAs' empty / tfull
+//               barriers (an mbarrier signal multicast to the pair; no data is
+//               multicast).
+//   warps 2-9   epilogue of its CTA's 128 rows, as in the single-CTA kernel;
+//               drained accumulators are released on the leader's tempty
+//               barrier (16 arrivals: both CTAs' epilogue warps).
+// Rows past a segment's end are computed but never stored; B boxes past N are
+// zero-filled by TMA (their columns are never stored).  Every wait is bounded;
+// set-up and tear-down meet at cluster barriers that both CTAs always reach.
+//
+// Sources: "手撕一个极简 MoE-FFN" §四 (Expert = w2(act(w1 x))), §六 (group the
+// tokens of each expert and run it once on the batch); "MoE混合专家模型：
+// Transformer稀疏前馈网络原理与PyTorch实现" §4.1 (GELU expert); "术业有专攻：
+// learn-minimind MoE混合专家模型架构入门指南" §二 (SwiGLU experts).
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BMP = 256;                        // rows of a pair tile
+constexpr int BMC = 128;                        // rows per CTA
+constexpr int BK = 64;                          // 128 bytes of bf16: one swizzle row
+constexpr int MMA_N = 256;
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BMC * BK * 2;           // 16 KB
+constexpr int B_BOX_BYTES = 64 * BK * 2;        // 8 KB: 64 columns x 64 k
+constexpr int B_BYTES = 2 * B_BOX_BYTES;        // 16 KB: this CTA's 128 columns
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
+constexpr uint32_t kPairStageTx = 2u * STAGE_BYTES;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + EPI_WARPS * 32;
+constexpr int TMEM_COLS = 512;                  // two 256-column accumulators
+constexpr int MAX_G = 264;
+constexpr uint32_t kWhere = 0x400;
+constexpr uint32_t kIdescPair = idesc_bf16(BMP, MMA_N);
+
+struct Ctl {
+  uint64_t full[STAGES];    // leader: both CTAs' copies of the stage have landed
+  uint64_t empty[STAGES];   // each CTA: the MMAs reading the stage are done
+  uint64_t tfull[2];        // each CTA: accumulator complete
+  uint64_t tempty[2];       // leader: both CTAs' epilogues drained the accumulator
+  uint64_t done;            // each CTA: every MMA of the pair is done
+  uint32_t tmem_base;
+  uint32_t abort;
+  uint32_t skip;
+  int mt[MAX_G + 1];        // prefix of ceil(rows / 256) over the segments
+  int rows[MAX_G];
+  int w[MAX_G];
+  int orow[MAX_G];
+  int arow[MAX_G];
+  int asrc[MAX_G];
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+
+__device__ __forceinline__ void map_tile(const Ctl& c, int G, int n_tiles, int tile, int& g, int& m, int& n) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (c.mt[mid] * n_tiles <= tile) lo = mid; else hi = mid - 1;
+  }
+  g = lo;
+  const int local = tile - c.mt[g] * n_tiles;
+  const int mtg = c.mt[g + 1] - c.mt[g];
+  n = local / mtg;
+  m = local - n * mtg;
+}
+
+template <bool SWIGLU, bool OUT_F32>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3, GemmArgs a) {
+  constexpr int BN_OUT = SWIGLU ? 128 : 256;   // output columns per pair tile
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;            // 1 KB aligned ring for the 128-byte swizzle
+  uint8_t* ring = smem_raw + (base - raw);
+  Ctl& c = *reinterpret_cast<Ctl*>(ring + STAGES * STAGE_BYTES);
+  volatile uint32_t* abort = &c.abort;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();        // 0: leader, 1: peer
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int G = a.G;
+  const int n_tiles = (a.N + BN_OUT - 1) / BN_OUT;
+  const int nkb = a.K / BK;
+  const uint64_t limit = (uint64_t)a.timeout_ns;
+  const uint64_t drain_limit = limit > 2000000000ull ? limit : 2000000000ull;
+
+  // ---- set-up ----
+  for (int i = threadIdx.x; i < G; i += blockDim.x) {
+    c.rows[i] = a.seg.rows[i];
+    c.w[i] = a.seg.w[i];
+    c.orow[i] = a.seg.out_row[i];
+    c.arow[i] = a.a_from_out_rows ? a.seg.out_row[i] : a.seg.a_row[i];
+    c.asrc[i] = a.a_from_out_rows ? 0 : a.seg.a_src[i];
+  }
+  if (warp == 0) {
+    // Pair m-tiles per segment: exclusive prefix of ceil(rows / 256), lane l
+    // owning segments [l * PG, (l + 1) * PG).
+    const int PG = (G + 31) / 32;
+    int local = 0;
+    for (int i = 0; i < PG; ++i) {
+      const int g = lane * PG + i;
+      if (g < G) local += (a.seg.rows[g] + BMP - 1) / BMP;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - local;
+    for (int i = 0; i < PG; ++i) {
+      const int g = lane * PG + i;
+      if (g < G) {
+        c.mt[g] = run;
+        run += (a.seg.rows[g] + BMP - 1) / BMP;
+      }
+    }
+    if (lane == 31) c.mt[G] = incl;
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&c.full[s]), 1);
+      mbar_init(smem_u32(&c.empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&c.tfull[s]), 1);
+      mbar_init(smem_u32(&c.tempty[s]), 2 * EPI_WARPS);
+    }
+    mbar_init(smem_u32(&c.done), 1);
+    c.abort = 0u;
+    c.skip = *(volatile const uint32_t*)a.err;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA0) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA1) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+    if (SWIGLU) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB3) : "memory");
+  }
+  if (warp == 1) {
+    __syncwarp();
+    // Collective with the peer CTA's warp 1: the same columns in both TMEMs.
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&c.tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();     // both CTAs' barriers are initialised before either signals the other
+  tc_fence_after();
+  const uint32_t tmem = c.tmem_base;
+  const int total = c.skip ? 0 : c.mt[G] * n_tiles;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      const uint32_t full_leader = mapa_shared(smem_u32(&c.full[0]), 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[STAGES];
+      bool issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) { issued[s] = false; issued_phase[s] = 0; }
+      for (int tile = pair; tile < total; tile += npairs) {
+        int g, m, n;
+        map_tile(c, G, n_tiles, tile, g, m, n);
+        const int arow = c.arow[g] + m * BMP + (int)rank * BMC;
+        const CUtensorMap* amap = c.asrc[g] ? &tmA1 : &tmA0;
+        const int wslab = c.w[g];
+        // B columns of this CTA: SwiGLU -> W1 (leader) or W3 (peer) columns
+        // n0..n0+127; otherwise columns n0 + 128 rank .. + 127.
+        const CUtensorMap* bmap = (SWIGLU && rank) ? &tmB3 : &tmB;
+        const int bcol = SWIGLU ? n * BN_OUT : n * BN_OUT + (int)rank * 128;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_i(smem_u32(&c.empty[stage]), phase ^ 1u, abort, limit, a.err, kWhere + 1)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_expect_tx(smem_u32(&c.full[stage]), kPairStageTx);
+          const uint32_t fb = full_leader + (uint32_t)(stage * 8);
+          const uint32_t sa = base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          tma_load_2d_pair(sa, amap, kb * BK, arow, fb);
+          tma_load_3d_pair(sb, bmap, bcol, kb * BK, wslab, fb);
+          tma_load_3d_pair(sb + B_BOX_BYTES, bmap, bcol + 64, kb * BK, wslab, fb);
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      // Both CTAs' copies complete on the leader's barriers: the leader
+      // waits for every stage it armed before the pair may tear down.
+      if (rank == 0)
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) mbar_drain(smem_u32(&c.full[s]), issued_phase[s], drain_limit);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (leader) ----------------
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = pair; tile < total && ok; tile += npairs, ++it) {
+        const int acc = it & 1;
+        const uint32_t aphase = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait_i(smem_u32(&c.tempty[acc]), aphase ^ 1u, abort, limit, a.err, kWhere + 2)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * MMA_N);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_i(smem_u32(&c.full[stage]), phase, abort, limit, a.err, kWhere + 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // A: K-major, 8-row groups 1024 B apart; a K step of 16 is 32 bytes.
+            const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+            // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row k groups
+            // 1024 B apart (SBO); a K step of 16 rows is 2048 bytes.
+            const uint64_t bd = smem_desc(sb + kk * 2048, B_BOX_BYTES, 1024);
+            mma_bf16_cta2<kIdescPair>(d_tmem, ad, bd, (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit_cta2(smem_u32(&c.empty[stage]), 0x3);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit_cta2(smem_u32(&c.tfull[acc]), 0x3);
+      }
+      // Every MMA of the pair (it writes both TMEMs) completes before either
+      // CTA releases its TMEM.
+      mma_commit_cta2(smem_u32(&c.done), 0x3);
+    }
+    if (lane == 0) mbar_drain(smem_u32(&c.done), 0u, drain_limit);
+  } else {
+    // ---------------- epilogue (both CTAs) ----------------
+    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;       // which half of the tile's columns
+    const int row = q * 32 + lane;
+    const uint32_t tempty_leader = mapa_shared(smem_u32(&c.tempty[0]), 0);
+    int it = 0;
+    const uint16_t* bias = (const uint16_t*)a.bias;
+    uint16_t* C = (uint16_t*)a.C;
+    for (int tile = pair; tile < total; tile += npairs, ++it) {
+      int g, m, n;
+      map_tile(c, G, n_tiles, tile, g, m, n);
+      const int acc = it & 1;
+      const uint32_t aphase = (uint32_t)(it >> 1) & 1u;
+      bool ok = mbar_wait_i(smem_u32(&c.tfull[acc]), aphase, abort, limit, a.err, kWhere + 4);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int grow = m * BMP + (int)rank * BMC + row;
+      const bool valid = grow < c.rows[g];
+      const int64_t orow = (int64_t)c.orow[g] + grow;
+      const int wslab = c.w[g];
+      const int n0 = n * BN_OUT;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * MMA_N);
+      constexpr int CHUNKS = BN_OUT / 32;   // 32-column chunks per tile
+      for (int ch = half * (CHUNKS / 2); ch < (half + 1) * (CHUNKS / 2); ++ch) {
+        const int col0 = n0 + ch * 32;
+        uint32_t v[32];
+        tmem_ld32(tbase + (uint32_t)(ch * 32), v);
+        if (SWIGLU) {
+          uint32_t u[32];
+          tmem_ld32(tbase + 128u + (uint32_t)(ch * 32), u);
+          tmem_wait_ld();
+          if (valid && col0 < a.N) {
+            uint32_t p[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float h0 = silu(__uint_as_float(v[2 * i])) * __uint_as_float(u[2 * i]);
+              const float h1 = silu(__uint_as_float(v[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+              p[i] = pack_bf16x2(h0, h1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(C + orow * a.N + col0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+          }
+        } else {
+          tmem_wait_ld();
+          if (valid && col0 < a.N) {
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+            if (bias) {
+              const uint16_t* bp = bias + (int64_t)wslab * a.N + col0;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) f[i] += bf16_bits_to_f32(bp[i]);
+            }
+            if (a.act == MOE_ACT_RELU) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) f[i] = f[i] > 0.f ? f[i] : 0.f;
+            } else if (a.act == MOE_ACT_GELU) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) f[i] = gelu_erf(f[i]);
+            }
+            if (OUT_F32) {
+              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.C) + orow * a.N + col0);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+            } else {
+              uint32_t p[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+              uint4* dst = reinterpret_cast<uint4*>(C + orow * a.N + col0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader + (uint32_t)(acc * 8));
+    }
+  }
+
+  // ---- tear-down: both CTAs here, nothing in flight, then free TMEM ----
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+bool map_rows(CUtensorMap* m, const void* ptr, int64_t rows, int K) { return tmap_bf16_2d(m, ptr, rows, K, BK, BMC); }
+bool map_weights(CUtensorMap* m, const void* ptr, int G, int K, int N) {
+  return tmap_bf16_3d(m, ptr, G, K, N, 64, BK);
+}
+
+template <bool SWIGLU, bool OUT_F32>
+cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtensorMap& mA1, const CUtensorMap& mB,
+                        const CUtensorMap& mB3, int64_t max_pair_tiles, cudaStream_t s) {
+  auto kernel = gemm_pair_kernel<SWIGLU, OUT_F32>;
+  static int max_clusters = -1;   // per kernel instantiation, per process (one device type)
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters < 0) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * (sm_count() / 2), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    max_clusters = n;
+  }
+  const int64_t pairs = max_pair_tiles < max_clusters ? max_pair_tiles : max_clusters;
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kernel, mA0, mA1, mB, mB3, a);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_pair(const GemmArgs& a, cudaStream_t s) {
+  if (a.max_mtiles <= 0) return cudaSuccess;
+  if (a.G > MAX_G || a.K % BK != 0 || a.N % 64 != 0) return cudaErrorInvalidValue;
+  if (a.out_f32 && a.act == MOE_ACT_SWIGLU) return cudaErrorInvalidValue;
+  CUtensorMap mA0, mA1, mB, mB3;
+  const bool swiglu = a.act == MOE_ACT_SWIGLU;
+  if (!map_rows(&mA0, a.A0, a.rows_A0, a.K)) return cudaErrorInvalidValue;
+  if (a.A1) {
+    if (!map_rows(&mA1, a.A1, a.rows_A1, a.K)) return cudaErrorInvalidValue;
+  } else {
+    mA1 = mA0;
+  }
+  if (!map_weights(&mB, a.B, a.Gw, a.K, a.N)) return cudaErrorInvalidValue;
+  if (swiglu) {
+    if (!map_weights(&mB3, a.B3, a.Gw, a.K, a.N)) return cudaErrorInvalidValue;
+  } else {
+    mB3 = mB;
+  }
+  const int bn = swiglu ? 128 : 256;
+  // a.max_mtiles bounds the 128-row tiles, hence also the 256-row pair tiles.
+  const int64_t max_pair_tiles = a.max_mtiles * ((a.N + bn - 1) / bn);
+  cudaError_t e;
+  if (swiglu)
+    e = launch_pair<true, false>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
+  else if (a.out_f32)
+    e = launch_pair<false, true>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
+  else
+    e = launch_pair<false, false>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -33,6 +33,7 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace moe {
 cudaError_t launch_grouped_gemm_f32(const GemmArgs& a, cudaStream_t s);
@@ -73,52 +74,6 @@ struct Ctl {
 
 constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
 
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor (tcgen05 format): start address, leading and
-// stride byte offsets (all >> 4), descriptor version 1 at bits 46-47, and the
-// 128-byte swizzle mode (2) in bits 61-63.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A and
-// B bf16 (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B N-major (bit 16
-// = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
-                            ((uint32_t)(MMA_N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
 __device__ __forceinline__ void map_tile(const Ctl& c, int G, int n_tiles, int tile, int& g, int& m, int& n) {
   int lo = 0, hi = G - 1;
   while (lo < hi) {
@@ -131,9 +86,6 @@ __device__ __forceinline__ void map_tile(const Ctl& c, int G, int n_tiles, int t
   n = local / mtg;
   m = local - n * mtg;
 }
-
-__device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.f + erff(v * 0.70710678118654752f)); }
-__device__ __forceinline__ float silu(float v) { return v / (1.f + __expf(-v)); }
 
 template <bool SWIGLU, bool OUT_F32>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -274,16 +226,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row k groups 1024 B
             // apart (SBO); a K step of 16 rows is 2048 bytes.
             const uint64_t bd = smem_desc(sb + kk * 2048, B_BOX_BYTES, 1024);
-            mma_bf16(d_tmem, ad, bd, (kb | kk) != 0 ? 1u : 0u);
+            mma_bf16_cta1<idesc_bf16(BM, MMA_N)>(d_tmem, ad, bd, (kb | kk) != 0 ? 1u : 0u);
           }
-          mma_commit(smem_u32(&c.empty[stage]));
+          mma_commit_cta1(smem_u32(&c.empty[stage]));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(smem_u32(&c.tfull[acc]));
+        mma_commit_cta1(smem_u32(&c.tfull[acc]));
       }
       // All MMAs issued by this thread complete before TMEM is released.
-      mma_commit(smem_u32(&c.done));
+      mma_commit_cta1(smem_u32(&c.done));
       mbar_drain(smem_u32(&c.done), 0u, drain_limit);
     }
   } else {
@@ -402,6 +354,7 @@ int sm_count() {
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.dtype == MOE_DT_F32) return launch_grouped_gemm_f32(a, s);
+  if (!a.single_cta) return launch_grouped_gemm_pair(a, s);
   if (a.max_mtiles <= 0) return cudaSuccess;
   if (a.G > MAX_G || a.K % BK != 0 || a.N % 64 != 0) return cudaErrorInvalidValue;
   if (a.out_f32 && a.act == MOE_ACT_SWIGLU) return cudaErrorInvalidValue;

@@ -99,8 +99,10 @@ struct GemmArgs {
   int64_t max_mtiles;   // upper bound of seg.mtile_start[G]
   uint32_t* err;
   int64_t timeout_ns;
+  bool single_cta;      // bf16: the one-CTA 128 x 256 tile kernel instead of the CTA-pair kernel
 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_grouped_gemm_pair(const GemmArgs& a, cudaStream_t s);
 
 // Builds a segment table from row offsets (standalone grouped GEMM entry point).
 cudaError_t launch_segments_from_offsets(const int32_t* offsets, int G, int64_t M, SegTable seg, uint32_t* err,

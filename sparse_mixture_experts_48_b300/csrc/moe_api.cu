@@ -199,6 +199,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   g1.A1 = c.n_shared > 0 ? x : nullptr; g1.rows_A1 = c.T;
   g1.B = W1; g1.B3 = W3; g1.Gw = L.G; g1.bias = b1; g1.C = ws + L.h; g1.max_mtiles = c.T > 0 ? max_mtiles : 0;
   g1.err = &hdr->err; g1.timeout_ns = timeout;
+  g1.single_cta = opts && (opts->flags & MOE_OPT_GEMM_SINGLE_CTA);
   if (clk.mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_grouped_gemm(g1, s) != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -264,6 +265,7 @@ moe_status moe_grouped_gemm(int32_t dtype, int32_t act, int32_t G, const int32_t
   g.max_mtiles = M > 0 ? (M + kGemmBM - 1) / kGemmBM + G : 0;
   g.err = &hdr->err;
   g.timeout_ns = (opts && opts->wait_timeout_ns > 0) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
+  g.single_cta = opts && (opts->flags & MOE_OPT_GEMM_SINGLE_CTA);
   if (opts && opts->stage_events && cudaEventRecord((cudaEvent_t)opts->stage_events[0], s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_grouped_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;

@@ -33,12 +33,13 @@ def _ref(A, B, B3, bias, offsets, act):
     return out
 
 
+@pytest.mark.parametrize("single_cta", [False, True], ids=["cta_pair", "one_cta"])
 @pytest.mark.parametrize("act", [moe.NONE, moe.RELU, moe.GELU, moe.SWIGLU])
-@pytest.mark.parametrize("shape", [(5, 256, 192), (3, 64, 320), (2, 1024, 256)])
-def test_grouped_gemm_bf16(act, shape):
+@pytest.mark.parametrize("shape", [(5, 256, 192), (3, 64, 320), (2, 1024, 256), (4, 128, 640)])
+def test_grouped_gemm_bf16(act, shape, single_cta):
     G, K, N = shape
     rng = np.random.default_rng(G * 7 + K + N + act)
-    sizes = rng.integers(0, 300, size=G)
+    sizes = rng.integers(0, 600, size=G)
     sizes[rng.integers(0, G)] = 0                       # an empty group
     offsets = np.concatenate([[7], 7 + np.cumsum(sizes)]).astype(np.int32)   # rows before the first group
     M = int(offsets[-1]) + 5                            # and after the last
@@ -47,7 +48,8 @@ def test_grouped_gemm_bf16(act, shape):
     B3 = si.normal(G * K * N, 11, 3, std=1 / np.sqrt(K), dtype=si.BF16).reshape(G, K, N) if act == moe.SWIGLU else None
     bias = si.normal(G * N, 11, 4, std=0.1, dtype=si.BF16).reshape(G, N) if act in (moe.NONE, moe.GELU) else None
     C0 = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")   # sentinel outside the groups
-    C, ws = moe.grouped_gemm(moe.BF16, act, to_dev(offsets), to_dev(A), to_dev(B), to_dev(B3), to_dev(bias), C=C0)
+    C, ws = moe.grouped_gemm(moe.BF16, act, to_dev(offsets), to_dev(A), to_dev(B), to_dev(B3), to_dev(bias), C=C0,
+                             single_cta=single_cta)
     assert moe.check_device_errors(ws) == 0
     got = to_host_f32(C).astype(np.float64)
     ref = _ref(A, B, B3, bias, offsets, act)

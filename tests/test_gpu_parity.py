@@ -69,6 +69,17 @@ def test_layer_edge_cases(label, base, over):
     check_y(cfg, inp, out, gl, np.arange(cfg.T))
 
 
+@pytest.mark.parametrize("name", ["mixtral_swiglu_bf16", "deepseek_shared_sigmoid_bf16", "gpt2_top2_gelu_bf16"])
+def test_layer_small_one_cta_gemm(name):
+    """The layer with its bf16 expert GEMMs on the one-CTA tile kernel."""
+    cfg = si.CONFIGS[name].replace(**SMALL[name])
+    inp = si.layer_inputs(cfg, seed=5)
+    out = run(cfg, device_inputs(inp), gemm_single_cta=True)
+    assert moe.check_device_errors(out.workspace) == 0
+    ref, gl, _ = check_routing(cfg, inp, out)
+    check_y(cfg, inp, out, gl, np.arange(cfg.T))
+
+
 def test_all_tokens_choose_one_expert_with_capacity():
     cfg = si.CONFIGS["skew_capacity_gelu_bf16"].replace(T=260, d=128, f=128, E=8, k=1, capacity_factor=1.0)
     inp = si.layer_inputs(cfg, seed=3)
