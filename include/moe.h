@@ -163,6 +163,24 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
                        int32_t* perm_token, int32_t* slot, void* workspace, size_t workspace_bytes,
                        moe_stream stream, const moe_launch_opts* opts);
 
+/* The same forward pass with HOST buffers: x_host and the outputs are host
+ * memory (page-locked, e.g. cudaHostAlloc, for the copies to run
+ * asynchronously; pageable memory works but its copies block the host).
+ * Enqueued on `stream`: one host->device copy of x into the workspace,
+ * moe_forward on device copies of every tensor, then one device->host copy per
+ * output.  The weights (W_g .. W3) stay device pointers.  The host outputs are
+ * complete once `stream` is synchronised.
+ * workspace: >= moe_forward_host_workspace_size(cfg) bytes (moe_forward's
+ * workspace followed by the device copies of x and the outputs).
+ * Two calls on two streams with two workspaces overlap one call's copies
+ * with the other's kernels; calls sharing a workspace must be ordered. */
+size_t moe_forward_host_workspace_size(const moe_config* cfg);
+moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const void* W_g, const void* b_g,
+                            const void* W1, const void* b1, const void* W2, const void* b2, const void* W3,
+                            void* y_host, int32_t* topk_idx_host, float* topk_w_host, int32_t* expert_counts_host,
+                            uint8_t* dropped_mask_host, float* f_host, float* P_host, float* L_aux_host,
+                            void* workspace, size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts);
+
 /* Waits for `stream`, then reports the device-side status of the last call
  * that used `workspace`: MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE, or
  * MOE_ERR_CUDA if the stream itself reports an error.  Synchronising. */

@@ -99,6 +99,10 @@ def lib() -> ctypes.CDLL:
     L.moe_capacity.argtypes = [cfgp]
     L.moe_forward.restype = ctypes.c_int
     L.moe_forward.argtypes = [cfgp] + [vp] * 8 + [vp] * 11 + [vp, sz, vp, optp]
+    L.moe_forward_host_workspace_size.restype = sz
+    L.moe_forward_host_workspace_size.argtypes = [cfgp]
+    L.moe_forward_host.restype = ctypes.c_int
+    L.moe_forward_host.argtypes = [cfgp] + [vp] * 8 + [vp] * 8 + [vp, sz, vp, optp]
     L.moe_check_device_errors.restype = ctypes.c_int
     L.moe_check_device_errors.argtypes = [vp, vp]
     L.moe_grouped_gemm_workspace_size.restype = sz
@@ -113,8 +117,8 @@ def lib() -> ctypes.CDLL:
 
 def exported_symbols() -> Sequence[str]:
     return ("moe_status_string", "moe_validate_config", "moe_workspace_size", "moe_capacity", "moe_forward",
-            "moe_check_device_errors", "moe_grouped_gemm_workspace_size", "moe_grouped_gemm",
-            "moe_grouped_gemm_noalloc")
+            "moe_forward_host_workspace_size", "moe_forward_host", "moe_check_device_errors",
+            "moe_grouped_gemm_workspace_size", "moe_grouped_gemm", "moe_grouped_gemm_noalloc")
 
 
 def c_config(cfg, y_f32: Optional[bool] = None) -> _CConfig:
@@ -266,6 +270,66 @@ def forward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutpu
     del keep
     if status != 0:
         raise MoEError(status, "moe_forward")
+    return out
+
+
+def alloc_host_outputs(cfg, y_f32: bool = False) -> MoEOutput:
+    """Page-locked host tensors for the outputs of forward_host."""
+    T, d, E, k = cfg.T, cfg.d, cfg.E, cfg.k
+    yd = torch.float32 if (cfg.dtype == F32 or y_f32) else torch.bfloat16
+    pin = dict(pin_memory=True)
+    return MoEOutput(
+        y=torch.empty((T, d), dtype=yd, **pin), topk_idx=torch.empty((T, k), dtype=torch.int32, **pin),
+        topk_w=torch.empty((T, k), dtype=torch.float32, **pin),
+        expert_counts=torch.empty((E,), dtype=torch.int32, **pin),
+        dropped_mask=torch.empty((T, k), dtype=torch.uint8, **pin), f=torch.empty((E,), dtype=torch.float32, **pin),
+        P=torch.empty((E,), dtype=torch.float32, **pin), L_aux=torch.empty((1,), dtype=torch.float32, **pin))
+
+
+def host_workspace_size(cfg, y_f32: Optional[bool] = None) -> int:
+    return int(lib().moe_forward_host_workspace_size(ctypes.byref(c_config(cfg, y_f32=y_f32))))
+
+
+def forward_host(cfg, x_host: torch.Tensor, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutput] = None,
+                 workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+                 y_f32: Optional[bool] = None, gemm_single_cta: bool = False) -> MoEOutput:
+    """The layer on a host batch: x_host (page-locked CPU tensor) in, host
+    outputs back (moe_forward_host).  Weights are CUDA tensors.  Asynchronous:
+    the host outputs are valid once ``stream`` is synchronised.  Alternating
+    two workspaces on two streams overlaps one batch's copies with another's
+    kernels."""
+    if not torch.cuda.is_available():
+        raise RuntimeError("the MoE layer runs on a CUDA device; none is available")
+    T, d, f, E, k, S = cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S
+    G = E + S
+    st = _STORE[cfg.dtype]
+    if x_host.is_cuda or not x_host.is_contiguous() or tuple(x_host.shape) != (T, d) or x_host.dtype not in st:
+        raise ValueError("x_host must be a contiguous CPU tensor of shape (T, d) in the config's dtype")
+    _check(W_g, "W_g", (d, E), st)
+    _check(b_g, "b_g", (E,), st, required=False)
+    _check(W1, "W1", (G, d, f), st)
+    _check(W3, "W3", (G, d, f), st, required=cfg.act == SWIGLU)
+    _check(W2, "W2", (G, f, d), st)
+    _check(b1, "b1", (G, f), st, required=False)
+    _check(b2, "b2", (G, d), st, required=False)
+    yf = bool(getattr(cfg, "y_f32", False)) if y_f32 is None else bool(y_f32)
+    if out is None:
+        out = alloc_host_outputs(cfg, y_f32=yf)
+    dev = W1.device
+    if workspace is None:
+        workspace = torch.empty((host_workspace_size(cfg, yf),), dtype=torch.uint8, device=dev)
+    out.workspace = workspace
+    opts, keep = _opts(None, 0, OPT_GEMM_SINGLE_CTA if gemm_single_cta else 0)
+    ccfg = c_config(cfg, y_f32=yf)
+    with torch.cuda.device(dev):
+        status = lib().moe_forward_host(
+            ctypes.byref(ccfg), _ptr(x_host), _ptr(W_g), _ptr(b_g), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(W3),
+            _ptr(out.y), _ptr(out.topk_idx), _ptr(out.topk_w), _ptr(out.expert_counts), _ptr(out.dropped_mask),
+            _ptr(out.f), _ptr(out.P), _ptr(out.L_aux), _ptr(workspace), workspace.numel(), _stream_handle(stream),
+            ctypes.byref(opts) if opts is not None else None)
+    del keep
+    if status != 0:
+        raise MoEError(status, "moe_forward_host")
     return out
 
 

@@ -84,6 +84,35 @@ int64_t capacity_of(const moe_config* c) {
   return (int64_t)ceil((double)c->T * c->capacity_factor / (double)c->E);
 }
 
+// Device staging of moe_forward_host, placed after the moe_forward workspace.
+struct HostStage {
+  size_t x, y, idx, w, cnt, drop, f, P, L, total;
+};
+
+HostStage host_stage(const moe_config* c, size_t base) {
+  HostStage h;
+  const size_t esz = c->dtype == MOE_DT_BF16 ? 2 : 4;
+  const bool y_f32 = (c->flags & MOE_FLAG_Y_F32) != 0 || c->dtype == MOE_DT_F32;
+  const size_t tk = (size_t)c->T * c->k;
+  size_t off = align_up(base, 256);
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align_up(off + (bytes ? bytes : 1), 256);
+    return at;
+  };
+  h.x = take((size_t)c->T * c->d_model * esz);
+  h.y = take((size_t)c->T * c->d_model * (y_f32 ? 4 : 2));
+  h.idx = take(tk * 4);
+  h.w = take(tk * 4);
+  h.cnt = take((size_t)c->E * 4);
+  h.drop = take(tk);
+  h.f = take((size_t)c->E * 4);
+  h.P = take((size_t)c->E * 4);
+  h.L = take(4);
+  h.total = off;
+  return h;
+}
+
 struct StageClock {
   const moe_launch_opts* o;
   cudaStream_t s;
@@ -217,6 +246,48 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   ca.rows_tk = L.rows_tk; ca.slot = slot_buf; ca.topk_w = topk_w; ca.y = y; ca.err = &hdr->err;
   if (launch_combine(ca, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (clk.mark(6) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+size_t moe_forward_host_workspace_size(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return host_stage(cfg, layout(cfg).total).total;
+}
+
+moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const void* W_g, const void* b_g,
+                            const void* W1, const void* b1, const void* W2, const void* b2, const void* W3,
+                            void* y_host, int32_t* topk_idx_host, float* topk_w_host, int32_t* expert_counts_host,
+                            uint8_t* dropped_mask_host, float* f_host, float* P_host, float* L_aux_host,
+                            void* workspace, size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts) {
+  moe_status st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  const bool empty = c.T == 0;
+  if (!expert_counts_host || !f_host || !P_host || !L_aux_host) return MOE_ERR_INVALID_ARG;
+  if (!empty && (!x_host || !y_host || !topk_idx_host || !topk_w_host || !dropped_mask_host))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout(&c);
+  const HostStage h = host_stage(&c, L.total);
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < h.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = (uint8_t*)workspace;
+  const size_t esz = c.dtype == MOE_DT_BF16 ? 2 : 4;
+  const bool y_f32 = (c.flags & MOE_FLAG_Y_F32) != 0 || c.dtype == MOE_DT_F32;
+  const size_t tk = (size_t)c.T * c.k;
+  const size_t xbytes = (size_t)c.T * c.d_model * esz, ybytes = (size_t)c.T * c.d_model * (y_f32 ? 4 : 2);
+  if (xbytes && cudaMemcpyAsync(ws + h.x, x_host, xbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = moe_forward(cfg, ws + h.x, W_g, b_g, W1, b1, W2, b2, W3, ws + h.y, (int32_t*)(ws + h.idx),
+                   (float*)(ws + h.w), (int32_t*)(ws + h.cnt), ws + h.drop, (float*)(ws + h.f), (float*)(ws + h.P),
+                   (float*)(ws + h.L), nullptr, nullptr, nullptr, workspace, L.total, stream, opts);
+  if (st != MOE_OK) return st;
+  struct Copy { void* dst; size_t off, bytes; } copies[] = {
+      {y_host, h.y, ybytes},          {topk_idx_host, h.idx, tk * 4}, {topk_w_host, h.w, tk * 4},
+      {expert_counts_host, h.cnt, (size_t)c.E * 4}, {dropped_mask_host, h.drop, tk},
+      {f_host, h.f, (size_t)c.E * 4}, {P_host, h.P, (size_t)c.E * 4}, {L_aux_host, h.L, 4}};
+  for (const Copy& cp : copies)
+    if (cp.bytes && cudaMemcpyAsync(cp.dst, ws + cp.off, cp.bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

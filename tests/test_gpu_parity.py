@@ -147,3 +147,27 @@ def test_layer_full_size_sampled(name):
     check_y(cfg, inp, out, gl, _sample_rows(cfg.T, out, n=n))
     # properties that hold at any size
     assert np.isfinite(to_host_f32(out.y)).all()
+
+
+@pytest.mark.parametrize("name", ["gpt2_top2_gelu_bf16", "skew_capacity_gelu_bf16", "tiny_top1_relu_f32"])
+def test_forward_host_matches_device_forward(name):
+    """moe_forward_host (host x in, host outputs back) gives bitwise the
+    outputs of moe_forward on the same inputs, on two streams with two
+    workspaces in flight at once."""
+    cfg = si.CONFIGS[name].replace(**SMALL[name])
+    inp = si.layer_inputs(cfg, seed=6)
+    dinp = device_inputs(inp)
+    ref = run(cfg, dinp, debug=False)
+    torch.cuda.synchronize()
+    x_host = dinp["x"].cpu().pin_memory()
+    w = [dinp[n] for n in ("W_g", "b_g", "W1", "b1", "W2", "b2", "W3")]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [moe.forward_host(cfg, x_host, *w, stream=s) for s in streams]
+    torch.cuda.synchronize()
+    for out in outs:
+        assert moe.check_device_errors(out.workspace, streams[0]) == 0
+        for field in ("y", "topk_idx", "topk_w", "expert_counts", "dropped_mask", "f", "P", "L_aux"):
+            a, b = getattr(out, field), getattr(ref, field).cpu()
+            if a.dtype == torch.bfloat16:
+                a, b = a.view(torch.int16), b.view(torch.int16)
+            assert torch.equal(a, b), field
