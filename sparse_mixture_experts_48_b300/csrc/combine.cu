@@ -12,17 +12,19 @@
 // layer), §四 技术飞跃② (shared experts are always active).
 #include "common.cuh"
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kWarps = 4;
 
-__device__ __forceinline__ float4 ld_stream(const float4* p) {
+// The expert outputs are read once: L1 bypassed, L2 evict-first.
+__device__ __forceinline__ float4 ld_stream(const float4* p, uint64_t policy) {
   float4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p));
+               : "l"(p), "l"(policy));
   return v;
 }
 
@@ -57,6 +59,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineArgs a) {
   }
   const int64_t chunks = a.d / 4;   // 4 fp32 per 16-byte chunk
   const float4* O = (const float4*)a.o;
+  const uint64_t policy = l2_policy_evict_first();
   for (int64_t c0 = lane; c0 < chunks; c0 += 32 * U) {
     float4 v[NJ][U];
 #pragma unroll
@@ -64,7 +67,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineArgs a) {
       const int64_t c = c0 + 32 * u;
 #pragma unroll
       for (int j = 0; j < NJ; ++j)
-        if (row[j] >= 0 && c < chunks) v[j][u] = ld_stream(O + row[j] * chunks + c);
+        if (row[j] >= 0 && c < chunks) v[j][u] = ld_stream(O + row[j] * chunks + c, policy);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {

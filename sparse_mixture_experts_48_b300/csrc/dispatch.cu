@@ -20,6 +20,7 @@
 // 前馈网络原理与PyTorch实现" §2.3 (Switch load-balance loss).
 #include "common.cuh"
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -185,14 +186,6 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   if (lane == 0) a.seg.mtile_start[G] = mt_total;
 }
 
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 constexpr int kGatherWarps = 8;
 
 __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(GatherArgs a) {
@@ -216,6 +209,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(GatherArgs a)
   for (int j = 0; j < 8; ++j) slots[j] = __shfl_sync(0xffffffffu, my_slot, j);
   const int esz = a.dtype == MOE_DT_BF16 ? 2 : 4;
   const int64_t chunks = (int64_t)a.d * esz / 16;
+  const uint64_t policy = l2_policy_evict_first();   // x read once, the grouped copy written once
   const uint4* src = (const uint4*)((const uint8_t*)a.x + t * chunks * 16);
   uint4* dst = (uint4*)a.xperm;
   constexpr int U = 4;
@@ -224,7 +218,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(GatherArgs a)
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t c = c0 + u * 32;
-      if (c < chunks) v[u] = ld_stream(src + c);
+      if (c < chunks) v[u] = ld_stream_u4(src + c, policy);
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -233,7 +227,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(GatherArgs a)
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int64_t c = c0 + u * 32;
-          if (c < chunks) drow[c] = v[u];
+          if (c < chunks) st_stream_u4(drow + c, v[u], policy);
         }
       }
     }

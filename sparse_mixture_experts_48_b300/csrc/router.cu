@@ -154,14 +154,22 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
       }
     }
   }
+  // Per expert: selections (popc of the bit masks) and the sum of gate
+  // probabilities over the CTA's tokens, one warp per expert: lane l adds
+  // rows l and l + 32, then a fixed xor-tree over the lanes.
   const int nvalid = (int)(a.T - t0 < kRouterBM ? a.T - t0 : kRouterBM);
-  for (int e = tid; e < E; e += blockDim.x) {
-    int h = 0;
-    for (int qq = 0; qq < NW; ++qq) h += __popc(bits[e * NW + qq]);
-    a.hist[e * a.nblk + blk] = h;
+  const int lane = tid % 32, nwarps = blockDim.x / 32;
+  for (int e = tid / 32; e < E; e += nwarps) {
     float s = 0.f;
-    for (int r = 0; r < nvalid; ++r) s += sl[r * ldl + e];   // fixed order
-    a.psum[e * a.nblk + blk] = s;
+    for (int r = lane; r < nvalid; r += 32) s += sl[r * ldl + e];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) {
+      int h = 0;
+      for (int qq = 0; qq < NW; ++qq) h += __popc(bits[e * NW + qq]);
+      a.hist[e * a.nblk + blk] = h;
+      a.psum[e * a.nblk + blk] = s;
+    }
   }
 }
 
@@ -259,6 +267,7 @@ __global__ void __launch_bounds__(kThreadsBf16) router_bf16_kernel(const __grid_
   if (warp == kMmaWarps) {
     // ---------------- producer ----------------
     const uint16_t* W = (const uint16_t*)a.Wg;
+    const uint64_t x_policy = l2_policy_evict_first();   // x is streamed once
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
       if (tma_w) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
@@ -279,7 +288,8 @@ __global__ void __launch_bounds__(kThreadsBf16) router_bf16_kernel(const __grid_
       if (lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_expect_tx(fb, (uint32_t)(nsub * (L::XS + (tma_w ? L::WS : 0))));
-        for (int i = 0; i < nsub; ++i) tma_load_2d(smem_u32(xs + i * L::XS), &tmX, (k0 + i) * kBK, (int)t0, fb);
+        for (int i = 0; i < nsub; ++i)
+          tma_load_2d_hint(smem_u32(xs + i * L::XS), &tmX, (k0 + i) * kBK, (int)t0, fb, x_policy);
         if (tma_w)
           for (int i = 0; i < nsub; ++i)
             for (int b = 0; b < EP / L::WCOLS; ++b)
