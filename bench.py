@@ -74,6 +74,26 @@ def algorithmic(cfg, rows_A: int):
 
 
 # ---------------------------------------------------------------------------------------------
+# ranks: each runs an independent replica of the layer (the layer has no cross-GPU step)
+
+
+def max_over_ranks(ms: float, device, world: int) -> float:
+    """The slowest rank's time: the job's time for a step."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_rank: int, ms_per_step: float, world: int) -> float:
+    """Tokens/s of the whole job: every rank's tokens over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
+# ---------------------------------------------------------------------------------------------
 # DRAM traffic of the dominant kernel, from the committed ncu summary
 
 
@@ -306,12 +326,9 @@ def main():
     if status != 0:
         raise SystemExit(f"device error in the timed region: {moe.STATUS.get(status)}")
     ms_total = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, dev, world)
     ms_step = ms_total / K
-    value = world * cfg.T / (ms_step / 1e3)
+    value = replica_throughput(cfg.T, ms_step, world)
 
     # per-kernel durations from the stage events (on the launching stream)
     stage_ms = np.array([[ev[i][s].elapsed_time(ev[i][s + 1]) for s in range(moe.NUM_STAGES)] for i in range(K)])
@@ -380,15 +397,12 @@ def main():
             if st != 0:
                 raise SystemExit(f"device error in the end-to-end loop: {moe.STATUS.get(st)}")
         e_ms = e0.elapsed_time(e1) / K
-        if world > 1:
-            tt = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = max_over_ranks(e_ms, dev, world)
         ho = houts[0]
         bi = x_host.numel() * x_host.element_size()
         bo = sum(t.numel() * t.element_size() for t in (ho.y, ho.topk_idx, ho.topk_w, ho.expert_counts,
                                                          ho.dropped_mask, ho.f, ho.P, ho.L_aux))
-        e2e = {"value": world * cfg.T / (e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e_ms,
+        e2e = {"value": replica_throughput(cfg.T, e_ms, world), "unit": "tokens/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "how": "moe_forward_host, pinned host x in / all outputs out every step, 2 streams x 2 workspaces"}
 
