@@ -62,6 +62,8 @@ def _L() -> ctypes.CDLL:
         lib.oracle_layer_rows.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, i64, vp, vp, vp, vp,
                                           vp, vp, vp, vp, vp, vp]
         lib.oracle_balance.argtypes = [i64, i32, i32, dbl, vp, vp, vp, vp, vp]
+        lib.oracle_add_noise.argtypes = [i64, i32, vp, vp]
+        lib.oracle_route_health.argtypes = [i64, i32, i32, vp, vp]
         _lib = lib
     return _lib
 
@@ -179,6 +181,24 @@ def balance(n_pre: np.ndarray, probs: np.ndarray, k: int, alpha: float):
     return f, P, float(L[0])
 
 
+def add_noise(logits: np.ndarray, noise: np.ndarray) -> np.ndarray:
+    """logits + noise (noise: fp32 [T, E], the scaled Gaussian router noise)."""
+    out = np.array(logits, dtype=np.float64, order="C", copy=True)
+    nz = np.ascontiguousarray(noise, np.float32)
+    if nz.shape != out.shape:
+        raise ValueError("noise must have the logits' shape")
+    _L().oracle_add_noise(out.shape[0], out.shape[1], _p(out), _p(nz))
+    return out
+
+
+def route_health(n_pre: np.ndarray, T: int, k: int):
+    """(entropy of the selection shares, their variance, CV of the counts)."""
+    n = np.ascontiguousarray(n_pre, np.int32)
+    out = np.empty(3, np.float64)
+    _L().oracle_route_health(T, n.size, k, _p(n), _p(out))
+    return out
+
+
 # ---- the layer, chained ---------------------------------------------------------
 
 def routing(cfg, logits: np.ndarray) -> Dict[str, np.ndarray]:
@@ -189,7 +209,8 @@ def routing(cfg, logits: np.ndarray) -> Dict[str, np.ndarray]:
     C = capacity(logits.shape[0], cfg.E, cfg.capacity_factor)
     disp = dispatch(idx, cfg.E, C)
     f, P, L_aux = balance(disp["n_pre"], probs, cfg.k, cfg.alpha)
-    out = dict(probs=probs, topk_idx=idx, topk_w=w, capacity=C, f=f, P=P, L_aux=L_aux)
+    out = dict(probs=probs, topk_idx=idx, topk_w=w, capacity=C, f=f, P=P, L_aux=L_aux,
+               health=route_health(disp["n_pre"], logits.shape[0], cfg.k))
     out.update(disp)
     return out
 
@@ -199,8 +220,12 @@ def forward(cfg, inp: Dict, rows: Optional[Sequence[int]] = None,
     """The whole layer.  ``rows``: token rows whose output y is computed (all
     when None; routing and statistics always cover every token).  ``logits``:
     route on these logits instead of the oracle's own (used to compare the
-    integer decisions on the very fp32 logits another implementation made)."""
+    integer decisions on the very fp32 logits another implementation made;
+    they already contain any router noise).  ``inp["noise"]`` (optional):
+    router noise added to the oracle's own logits."""
     own = router_logits(inp["x"], inp["W_g"], inp["b_g"], cfg.dtype) if logits is None else None
+    if own is not None and inp.get("noise") is not None:
+        own = add_noise(own, inp["noise"])
     lg = own if logits is None else np.ascontiguousarray(logits, np.float64)
     out = routing(cfg, lg)
     out["logits"] = lg

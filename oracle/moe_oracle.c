@@ -266,3 +266,38 @@ void oracle_balance(int64_t T, int E, int k, double alpha, const int32_t* n_pre,
   }
   *L_aux = alpha * (double)E * L;
 }
+
+/* Router noise: the scores get Gaussian noise added before top-k, to
+ * encourage exploration of other experts ["Mixture of Experts混合专家模型架构原理
+ * 与路由策略实现", 门控网络的数学原理].  The pages give no formula beyond that.
+ * Reading: the caller's noise values (already scaled) are added to the logits,
+ * and everything after (gating, top-k, weights, P) uses the noisy logits.
+ * noise is fp32 [T, E]. */
+void oracle_add_noise(int64_t T, int E, double* logits, const float* noise) {
+  for (int64_t i = 0; i < T * E; ++i) logits[i] += (double)noise[i];
+}
+
+/* Routing-health statistics ["MoE混合专家模型：Transformer稀疏前馈网络原理与PyTorch
+ * 实现" §3.3: per-expert token counts, the entropy of the routing distribution
+ * against ln N, and the variance of expert utilisation / its coefficient of
+ * variation].  Reading: the distribution is the pre-capacity selection share
+ * f_e = n_e / (T k), so that uniform routing gives entropy ln E:
+ *   out[0] = H   = -sum_e f_e ln f_e   (terms with f_e = 0 add 0)
+ *   out[1] = Var = (1/E) sum_e (f_e - 1/E)^2
+ *   out[2] = CV  = std_e(n_e) / mean_e(n_e) = E sqrt(Var)
+ * T = 0 gives zeros. */
+void oracle_route_health(int64_t T, int E, int k, const int32_t* n_pre, double* out) {
+  out[0] = out[1] = out[2] = 0.0;
+  if (T <= 0) return;
+  const double tk = (double)T * (double)k;
+  double H = 0.0, var = 0.0;
+  for (int e = 0; e < E; ++e) {
+    const double f = (double)n_pre[e] / tk;
+    if (f > 0.0) H -= f * log(f);
+    var += (f - 1.0 / E) * (f - 1.0 / E);
+  }
+  var /= (double)E;
+  out[0] = H;
+  out[1] = var;
+  out[2] = (double)E * sqrt(var);
+}

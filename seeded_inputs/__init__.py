@@ -30,7 +30,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "libseeded.so")
 
-TAG = {"x": 1, "W_g": 2, "b_g": 3, "W1": 4, "b1": 5, "W2": 6, "b2": 7, "W3": 8}
+TAG = {"x": 1, "W_g": 2, "b_g": 3, "W1": 4, "b1": 5, "W2": 6, "b2": 7, "W3": 8, "noise": 9}
 
 RELU, GELU, SWIGLU = 0, 1, 2
 SOFTMAX, SIGMOID_NORM = 0, 1
@@ -175,6 +175,11 @@ def layer_inputs(cfg: LayerConfig, seed: int = 0) -> Dict[str, Optional[np.ndarr
     inp["b1"] = draw("b1", (G, f), cfg.bias_std) if cfg.ffn_bias else None
     inp["b2"] = draw("b2", (G, d), cfg.bias_std) if cfg.ffn_bias else None
     return inp
+
+
+def router_noise(cfg: LayerConfig, seed: int = 0, std: float = 1.0) -> np.ndarray:
+    """Scaled Gaussian router noise, fp32 [T, E]: std * N(0, 1)."""
+    return normal(cfg.T * cfg.E, seed, TAG["noise"], 0.0, std, F32).reshape(cfg.T, cfg.E)
 
 
 def x_only(cfg: LayerConfig, seed: int = 0) -> np.ndarray:

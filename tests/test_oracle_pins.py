@@ -320,3 +320,61 @@ def test_empty_batch():
     r = oracle.routing(cfg, np.zeros((0, 4)))
     assert r["counts"].tolist() == [0, 0, 0, 0] and r["L_aux"] == 0.0
     assert np.all(r["f"] == 0) and np.all(r["P"] == 0)
+
+
+# ---- router noise and routing-health statistics ------------------------------------
+
+def test_noise_alone_decides_routing_when_the_router_is_flat():
+    """All-zero W_g and b_g: the noisy scores are the noise itself, so top-k is
+    the k largest noise values (library argsort, ties impossible with
+    continuous noise) and the weights are the softmax of the selected noise."""
+    cfg = _cfg(T=40, d=16, E=7, k=3)
+    inp = _rand_inputs(cfg)
+    inp["W_g"] = np.zeros_like(inp["W_g"])
+    inp["b_g"] = np.zeros_like(inp["b_g"])
+    inp["noise"] = si.router_noise(cfg, seed=2, std=1.5)
+    out = oracle.forward(cfg, inp, rows=[0])
+    nz = inp["noise"].astype(np.float64)
+    expect = np.argsort(-nz, axis=1, kind="stable")[:, :3]
+    assert np.array_equal(out["topk_idx"], expect)
+    sel = np.take_along_axis(nz, expect, 1)
+    np.testing.assert_allclose(out["topk_w"], sp.softmax(sel, axis=1), rtol=1e-13, atol=0)
+    np.testing.assert_allclose(out["P"], sp.softmax(nz, axis=1).mean(0), rtol=1e-13, atol=0)
+
+
+def test_zero_noise_changes_nothing_and_noise_shifts_logits_exactly():
+    cfg = _cfg(T=25, d=16, E=5, k=2, dtype=si.BF16)
+    inp = _rand_inputs(cfg)
+    clean = oracle.forward(cfg, inp)
+    inp0 = dict(inp, noise=np.zeros((cfg.T, cfg.E), np.float32))
+    zero = oracle.forward(cfg, inp0)
+    for key in ("topk_idx", "topk_w", "counts", "f", "P", "y"):
+        assert np.array_equal(np.asarray(zero[key]), np.asarray(clean[key])), key
+    nz = si.router_noise(cfg, seed=4, std=0.7)
+    noisy = oracle.forward(cfg, dict(inp, noise=nz))
+    np.testing.assert_allclose(noisy["logits"], clean["logits"] + nz.astype(np.float64), rtol=0, atol=1e-15)
+
+
+def test_route_health_closed_forms():
+    E, k, T = 8, 2, 64
+    # uniform selections: entropy ln E, variance 0, CV 0
+    h = oracle.route_health(np.full(E, T * k // E, np.int32), T, k)
+    np.testing.assert_allclose(h, [np.log(E), 0.0, 0.0], rtol=1e-15, atol=1e-15)
+    # every selection on one expert (k = 1): entropy 0, CV = sqrt(E - 1)
+    n = np.zeros(E, np.int32)
+    n[3] = T
+    h = oracle.route_health(n, T, 1)
+    assert h[0] == 0.0
+    np.testing.assert_allclose(h[2], np.sqrt(E - 1), rtol=1e-14)
+    np.testing.assert_allclose(h[1], ((1 - 1 / E) ** 2 + (E - 1) / E ** 2) / E, rtol=1e-14)
+    # against library routines on random counts
+    rng = np.random.default_rng(9)
+    n = rng.integers(0, 50, size=E).astype(np.int32)
+    n[0] += 1
+    T = int(n.sum())
+    h = oracle.route_health(n, T, 1)
+    f = n / n.sum()
+    np.testing.assert_allclose(h[0], sp.entr(f).sum(), rtol=1e-13)
+    np.testing.assert_allclose(h[1], np.var(f), rtol=1e-13)
+    np.testing.assert_allclose(h[2], np.std(n) / np.mean(n), rtol=1e-13)
+    assert np.all(oracle.route_health(np.zeros(E, np.int32), 0, 2) == 0.0)
