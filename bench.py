@@ -250,6 +250,8 @@ def main():
     ap.add_argument("--T", type=int, default=0, help="override the token count (profiling runs)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop")
+    ap.add_argument("--noise-std", type=float, default=0.0,
+                    help="add seeded Gaussian router noise of this std before gating and top-k (0: none)")
     ap.add_argument("--gemm-one-cta", action="store_true",
                     help="bf16 expert GEMMs on the one-CTA tile kernel instead of the CTA-pair kernel")
     args = ap.parse_args()
@@ -291,6 +293,7 @@ def main():
 
     d = {k: to_dev(v) for k, v in inp.items()}
     args_in = [d[n] for n in ("x", "W_g", "b_g", "W1", "b1", "W2", "b2", "W3")]
+    noise = to_dev(si.router_noise(cfg, seed=rank, std=args.noise_std)) if args.noise_std > 0 else None
     out = moe.alloc_outputs(cfg, dev)
     ws = moe.alloc_workspace(cfg, dev)
     stream = torch.cuda.current_stream()
@@ -298,8 +301,8 @@ def main():
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)] for _ in range(K)]
 
     def step(i=None):
-        moe.forward(cfg, *args_in, out=out, workspace=ws, stage_events=ev[i] if i is not None else None,
-                    gemm_single_cta=args.gemm_one_cta)
+        moe.forward(cfg, *args_in, router_noise=noise, out=out, workspace=ws,
+                    stage_events=ev[i] if i is not None else None, gemm_single_cta=args.gemm_one_cta)
 
     for _ in range(W):
         step()
@@ -367,14 +370,15 @@ def main():
     if not args.no_e2e:
         x_host = torch.empty(d["x"].shape, dtype=d["x"].dtype, pin_memory=True)
         x_host.copy_(d["x"].cpu())
+        noise_host = noise.cpu().pin_memory() if noise is not None else None
         weights = args_in[1:]
         streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
         hws = [torch.empty((moe.host_workspace_size(cfg),), dtype=torch.uint8, device=dev) for _ in range(2)]
         houts = [moe.alloc_host_outputs(cfg) for _ in range(2)]
 
         def e2e_step(i):
-            moe.forward_host(cfg, x_host, *weights, out=houts[i % 2], workspace=hws[i % 2], stream=streams[i % 2],
-                             gemm_single_cta=args.gemm_one_cta)
+            moe.forward_host(cfg, x_host, *weights, router_noise_host=noise_host, out=houts[i % 2],
+                             workspace=hws[i % 2], stream=streams[i % 2], gemm_single_cta=args.gemm_one_cta)
 
         for i in range(W):
             e2e_step(i)
@@ -399,7 +403,7 @@ def main():
         e_ms = e0.elapsed_time(e1) / K
         e_ms = max_over_ranks(e_ms, dev, world)
         ho = houts[0]
-        bi = x_host.numel() * x_host.element_size()
+        bi = x_host.numel() * x_host.element_size() + (noise_host.numel() * 4 if noise_host is not None else 0)
         bo = sum(t.numel() * t.element_size() for t in (ho.y, ho.topk_idx, ho.topk_w, ho.expert_counts,
                                                          ho.dropped_mask, ho.f, ho.P, ho.L_aux))
         e2e = {"value": replica_throughput(cfg.T, e_ms, world), "unit": "tokens/s", "ms_per_step": e_ms,
@@ -421,6 +425,7 @@ def main():
             "config": {"workload": workload_desc(cfg), "T": cfg.T, "d_model": cfg.d, "d_ff": cfg.f, "E": cfg.E,
                        "k": cfg.k, "n_shared": cfg.S, "parallelism": "replicas" if world > 1 else "single GPU",
                        "expert_gemm": "one-CTA 128x256 tiles" if args.gemm_one_cta else "CTA-pair 256x256 tiles",
+                       "router_noise_std": args.noise_std,
                        "l2": "no flush: inputs larger than L2 (x %.0f MB, expert weights %.2f GB)" % (
                            inp["x"].nbytes / 1e6, sum(inp[n].nbytes for n in ("W1", "W2", "W3")
                                                       if inp[n] is not None) / 1e9)},

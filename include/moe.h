@@ -140,6 +140,11 @@ int64_t moe_capacity(const moe_config* cfg);
  * Inputs (device, read only):
  *   x, W_g, W1, W2 required; b_g, b1, b2 optional (NULL = no bias; biases are
  *   not used with SwiGLU); W3 required iff act == MOE_ACT_SWIGLU.
+ *   router_noise: optional fp32 [T, E], added to the router logits before
+ *   gating and top-k (Gaussian noise to encourage exploration, "Mixture of
+ *   Experts混合专家模型架构原理与路由策略实现", 门控网络的数学原理); the caller
+ *   draws and scales it.  Selection, weights, P and router_logits then all
+ *   use the noisy logits.  NULL = no noise.
  * Outputs (device, written):
  *   y [T, d] in dtype, or fp32 with MOE_FLAG_Y_F32 (must not overlap x),
  *   topk_idx int32 [T, k] (descending logit),
@@ -147,6 +152,10 @@ int64_t moe_capacity(const moe_config* cfg);
  *   dropped_mask uint8 [T, k] (1 = cut by capacity), f fp32 [E], P fp32 [E],
  *   L_aux fp32 [1].
  * Optional outputs (NULL = not written):
+ *   route_stats fp32 [3]: routing health of the pre-capacity selection shares
+ *   f_e = n_e / (T k) ("MoE混合专家模型：Transformer稀疏前馈网络原理与PyTorch实现"
+ *   §3.3): entropy -sum f ln f (ln E when uniform), variance (1/E) sum (f -
+ *   1/E)^2, and the coefficient of variation of the counts, E sqrt(variance);
  *   router_logits fp32 [T, E]; perm_token int32 [T*k]: token of each row of
  *   the expert-grouped order (experts ascending, tokens ascending inside an
  *   expert; entries past sum(expert_counts) are not written); slot int32 [T, k]:
@@ -157,13 +166,14 @@ int64_t moe_capacity(const moe_config* cfg);
  * expert_counts = f = P = 0 and L_aux = 0, and the per-token tensors (x, y,
  * topk_idx, topk_w, dropped_mask and the optional ones) may then be NULL. */
 moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
-                       const void* W1, const void* b1, const void* W2, const void* b2, const void* W3,
-                       void* y, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
-                       uint8_t* dropped_mask, float* f, float* P, float* L_aux, float* router_logits,
-                       int32_t* perm_token, int32_t* slot, void* workspace, size_t workspace_bytes,
-                       moe_stream stream, const moe_launch_opts* opts);
+                       const float* router_noise, const void* W1, const void* b1, const void* W2, const void* b2,
+                       const void* W3, void* y, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                       uint8_t* dropped_mask, float* f, float* P, float* L_aux, float* route_stats,
+                       float* router_logits, int32_t* perm_token, int32_t* slot, void* workspace,
+                       size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts);
 
-/* The same forward pass with HOST buffers: x_host and the outputs are host
+/* The same forward pass with HOST buffers: x_host, router_noise_host (or
+ * NULL) and the outputs (route_stats_host may be NULL) are host
  * memory (page-locked, e.g. cudaHostAlloc, for the copies to run
  * asynchronously; pageable memory works but its copies block the host).
  * Enqueued on `stream`: one host->device copy of x into the workspace,
@@ -176,10 +186,11 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
  * with the other's kernels; calls sharing a workspace must be ordered. */
 size_t moe_forward_host_workspace_size(const moe_config* cfg);
 moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const void* W_g, const void* b_g,
-                            const void* W1, const void* b1, const void* W2, const void* b2, const void* W3,
-                            void* y_host, int32_t* topk_idx_host, float* topk_w_host, int32_t* expert_counts_host,
-                            uint8_t* dropped_mask_host, float* f_host, float* P_host, float* L_aux_host,
-                            void* workspace, size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts);
+                            const float* router_noise_host, const void* W1, const void* b1, const void* W2,
+                            const void* b2, const void* W3, void* y_host, int32_t* topk_idx_host, float* topk_w_host,
+                            int32_t* expert_counts_host, uint8_t* dropped_mask_host, float* f_host, float* P_host,
+                            float* L_aux_host, float* route_stats_host, void* workspace, size_t workspace_bytes,
+                            moe_stream stream, const moe_launch_opts* opts);
 
 /* Waits for `stream`, then reports the device-side status of the last call
  * that used `workspace`: MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE, or

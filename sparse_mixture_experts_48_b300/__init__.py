@@ -98,11 +98,11 @@ def lib() -> ctypes.CDLL:
     L.moe_capacity.restype = i64
     L.moe_capacity.argtypes = [cfgp]
     L.moe_forward.restype = ctypes.c_int
-    L.moe_forward.argtypes = [cfgp] + [vp] * 8 + [vp] * 11 + [vp, sz, vp, optp]
+    L.moe_forward.argtypes = [cfgp] + [vp] * 9 + [vp] * 12 + [vp, sz, vp, optp]
     L.moe_forward_host_workspace_size.restype = sz
     L.moe_forward_host_workspace_size.argtypes = [cfgp]
     L.moe_forward_host.restype = ctypes.c_int
-    L.moe_forward_host.argtypes = [cfgp] + [vp] * 8 + [vp] * 8 + [vp, sz, vp, optp]
+    L.moe_forward_host.argtypes = [cfgp] + [vp] * 9 + [vp] * 9 + [vp, sz, vp, optp]
     L.moe_check_device_errors.restype = ctypes.c_int
     L.moe_check_device_errors.argtypes = [vp, vp]
     L.moe_grouped_gemm_workspace_size.restype = sz
@@ -191,6 +191,7 @@ class MoEOutput:
     f: torch.Tensor
     P: torch.Tensor
     L_aux: torch.Tensor
+    route_stats: Optional[torch.Tensor] = None   # entropy, variance, CV of the selection shares
     router_logits: Optional[torch.Tensor] = None
     perm_token: Optional[torch.Tensor] = None
     slot: Optional[torch.Tensor] = None
@@ -208,7 +209,8 @@ def alloc_outputs(cfg, device, debug: bool = False, y_f32: bool = False) -> MoEO
         dropped_mask=torch.empty((T, k), dtype=torch.uint8, device=device),
         f=torch.empty((E,), dtype=torch.float32, device=device),
         P=torch.empty((E,), dtype=torch.float32, device=device),
-        L_aux=torch.empty((1,), dtype=torch.float32, device=device))
+        L_aux=torch.empty((1,), dtype=torch.float32, device=device),
+        route_stats=torch.empty((3,), dtype=torch.float32, device=device))
     if debug:
         out.router_logits = torch.empty((T, E), dtype=torch.float32, device=device)
         out.perm_token = torch.full((max(T * k, 1),), -1, dtype=torch.int32, device=device)
@@ -223,7 +225,8 @@ def alloc_workspace(cfg, device) -> torch.Tensor:
     return torch.empty((n,), dtype=torch.uint8, device=device)
 
 
-def forward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutput] = None,
+def forward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3=None, *, router_noise: Optional[torch.Tensor] = None,
+            out: Optional[MoEOutput] = None,
             workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
             debug: bool = False, stage_events=None, timeout_ns: int = 0,
             y_f32: Optional[bool] = None, gemm_single_cta: bool = False) -> MoEOutput:
@@ -232,6 +235,8 @@ def forward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutpu
     ``y_f32``: write y in fp32 (default: the config's ``y_f32``, else its dtype).
     ``gemm_single_cta``: bf16 expert GEMMs on the one-CTA tile kernel instead
     of the default CTA-pair kernel.
+    ``router_noise``: fp32 [T, E] CUDA tensor added to the router logits before
+    gating and top-k (scaled Gaussian noise drawn by the caller).
 
     Asynchronous: returns once the kernels are enqueued.  Host-detected errors
     raise MoEError; device-side ones are reported by check_device_errors()."""
@@ -248,6 +253,7 @@ def forward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutpu
     _check(W2, "W2", (G, f, d), st)
     _check(b1, "b1", (G, f), st, required=False)
     _check(b2, "b2", (G, d), st, required=False)
+    _check(router_noise, "router_noise", (T, E), (torch.float32,), required=False)
     dev = x.device
     yf = bool(getattr(cfg, "y_f32", False)) if y_f32 is None else bool(y_f32)
     if out is None:
@@ -262,10 +268,11 @@ def forward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutpu
     ccfg = c_config(cfg, y_f32=yf)
     with torch.cuda.device(dev):
         status = lib().moe_forward(
-            ctypes.byref(ccfg), _ptr(x), _ptr(W_g), _ptr(b_g), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(W3),
-            _ptr(out.y), _ptr(out.topk_idx), _ptr(out.topk_w), _ptr(out.expert_counts), _ptr(out.dropped_mask),
-            _ptr(out.f), _ptr(out.P), _ptr(out.L_aux), _ptr(out.router_logits), _ptr(out.perm_token),
-            _ptr(out.slot), _ptr(workspace), workspace.numel(), _stream_handle(stream),
+            ctypes.byref(ccfg), _ptr(x), _ptr(W_g), _ptr(b_g), _ptr(router_noise), _ptr(W1), _ptr(b1), _ptr(W2),
+            _ptr(b2), _ptr(W3), _ptr(out.y), _ptr(out.topk_idx), _ptr(out.topk_w), _ptr(out.expert_counts),
+            _ptr(out.dropped_mask), _ptr(out.f), _ptr(out.P), _ptr(out.L_aux), _ptr(out.route_stats),
+            _ptr(out.router_logits), _ptr(out.perm_token), _ptr(out.slot), _ptr(workspace), workspace.numel(),
+            _stream_handle(stream),
             ctypes.byref(opts) if opts is not None else None)
     del keep
     if status != 0:
@@ -283,14 +290,16 @@ def alloc_host_outputs(cfg, y_f32: bool = False) -> MoEOutput:
         topk_w=torch.empty((T, k), dtype=torch.float32, **pin),
         expert_counts=torch.empty((E,), dtype=torch.int32, **pin),
         dropped_mask=torch.empty((T, k), dtype=torch.uint8, **pin), f=torch.empty((E,), dtype=torch.float32, **pin),
-        P=torch.empty((E,), dtype=torch.float32, **pin), L_aux=torch.empty((1,), dtype=torch.float32, **pin))
+        P=torch.empty((E,), dtype=torch.float32, **pin), L_aux=torch.empty((1,), dtype=torch.float32, **pin),
+        route_stats=torch.empty((3,), dtype=torch.float32, **pin))
 
 
 def host_workspace_size(cfg, y_f32: Optional[bool] = None) -> int:
     return int(lib().moe_forward_host_workspace_size(ctypes.byref(c_config(cfg, y_f32=y_f32))))
 
 
-def forward_host(cfg, x_host: torch.Tensor, W_g, b_g, W1, b1, W2, b2, W3=None, *, out: Optional[MoEOutput] = None,
+def forward_host(cfg, x_host: torch.Tensor, W_g, b_g, W1, b1, W2, b2, W3=None, *,
+                 router_noise_host: Optional[torch.Tensor] = None, out: Optional[MoEOutput] = None,
                  workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
                  y_f32: Optional[bool] = None, gemm_single_cta: bool = False) -> MoEOutput:
     """The layer on a host batch: x_host (page-locked CPU tensor) in, host
@@ -312,6 +321,10 @@ def forward_host(cfg, x_host: torch.Tensor, W_g, b_g, W1, b1, W2, b2, W3=None, *
     _check(W2, "W2", (G, f, d), st)
     _check(b1, "b1", (G, f), st, required=False)
     _check(b2, "b2", (G, d), st, required=False)
+    if router_noise_host is not None and (router_noise_host.is_cuda or tuple(router_noise_host.shape) != (T, E)
+                                          or router_noise_host.dtype != torch.float32
+                                          or not router_noise_host.is_contiguous()):
+        raise ValueError("router_noise_host must be a contiguous fp32 CPU tensor of shape (T, E)")
     yf = bool(getattr(cfg, "y_f32", False)) if y_f32 is None else bool(y_f32)
     if out is None:
         out = alloc_host_outputs(cfg, y_f32=yf)
@@ -323,9 +336,10 @@ def forward_host(cfg, x_host: torch.Tensor, W_g, b_g, W1, b1, W2, b2, W3=None, *
     ccfg = c_config(cfg, y_f32=yf)
     with torch.cuda.device(dev):
         status = lib().moe_forward_host(
-            ctypes.byref(ccfg), _ptr(x_host), _ptr(W_g), _ptr(b_g), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(W3),
-            _ptr(out.y), _ptr(out.topk_idx), _ptr(out.topk_w), _ptr(out.expert_counts), _ptr(out.dropped_mask),
-            _ptr(out.f), _ptr(out.P), _ptr(out.L_aux), _ptr(workspace), workspace.numel(), _stream_handle(stream),
+            ctypes.byref(ccfg), _ptr(x_host), _ptr(W_g), _ptr(b_g), _ptr(router_noise_host), _ptr(W1), _ptr(b1),
+            _ptr(W2), _ptr(b2), _ptr(W3), _ptr(out.y), _ptr(out.topk_idx), _ptr(out.topk_w), _ptr(out.expert_counts),
+            _ptr(out.dropped_mask), _ptr(out.f), _ptr(out.P), _ptr(out.L_aux), _ptr(out.route_stats),
+            _ptr(workspace), workspace.numel(), _stream_handle(stream),
             ctypes.byref(opts) if opts is not None else None)
     del keep
     if status != 0:

@@ -123,6 +123,30 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     a.offsets[E] = kept_total;
     *a.L_aux = (float)(a.alpha * (double)E * L);
   }
+  if (a.route_stats) {
+    // Routing health of the pre-capacity shares f_e = n_e / (T k): entropy
+    // -sum f ln f, variance (1/E) sum (f - 1/E)^2, CV = E sqrt(variance).
+    double H = 0.0, V = 0.0;
+    for (int i = 0; i < PE; ++i) {
+      const int e = e0 + i;
+      if (e < E && a.T > 0) {
+        const double fe = (double)s_npre[e] / Tk;
+        if (fe > 0.0) H -= fe * log(fe);
+        V += (fe - 1.0 / E) * (fe - 1.0 / E);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      H += __shfl_xor_sync(0xffffffffu, H, o);
+      V += __shfl_xor_sync(0xffffffffu, V, o);
+    }
+    if (lane == 0) {
+      V /= (double)E;
+      a.route_stats[0] = (float)H;
+      a.route_stats[1] = (float)V;
+      a.route_stats[2] = (float)((double)E * sqrt(V));
+    }
+  }
   // Segments of the grouped GEMMs: routed experts read the grouped copy of x,
   // shared experts read x itself and write rows T*k + s*T.  The offsets of
   // the routed segments are this warp's own (in registers / recomputed), so

@@ -12,6 +12,7 @@ struct RouterArgs {
   const void* x;    // [T, d]
   const void* Wg;   // [d, E]
   const void* bg;   // [E] or null
+  const float* noise;  // [T, E] fp32 added to the logits before gating, or null
   int64_t T;
   int d, E, k, gating, dtype;
   float* logits_out;   // [T, E] or null
@@ -41,6 +42,7 @@ struct ScanArgs {
   float* f;
   float* P;
   float* L_aux;
+  float* route_stats;  // [3] entropy, variance, CV of the selection shares, or null
   SegTable seg;
   int64_t rows_tk;     // T * k: first H / O row of the shared experts
   const uint32_t* err; // workspace status word: non-zero = an earlier stage failed

@@ -86,7 +86,7 @@ int64_t capacity_of(const moe_config* c) {
 
 // Device staging of moe_forward_host, placed after the moe_forward workspace.
 struct HostStage {
-  size_t x, y, idx, w, cnt, drop, f, P, L, total;
+  size_t x, y, idx, w, cnt, drop, f, P, L, noise, stats, total;
 };
 
 HostStage host_stage(const moe_config* c, size_t base) {
@@ -109,6 +109,8 @@ HostStage host_stage(const moe_config* c, size_t base) {
   h.f = take((size_t)c->E * 4);
   h.P = take((size_t)c->E * 4);
   h.L = take(4);
+  h.noise = take((size_t)c->T * c->E * 4);
+  h.stats = take(3 * 4);
   h.total = off;
   return h;
 }
@@ -151,10 +153,11 @@ int64_t moe_capacity(const moe_config* cfg) {
   return capacity_of(cfg);
 }
 
-moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, const void* b_g, const void* W1,
-                       const void* b1, const void* W2, const void* b2, const void* W3, void* y, int32_t* topk_idx,
-                       float* topk_w, int32_t* expert_counts, uint8_t* dropped_mask, float* f, float* P,
-                       float* L_aux, float* router_logits, int32_t* perm_token, int32_t* slot, void* workspace,
+moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
+                       const float* router_noise, const void* W1, const void* b1, const void* W2, const void* b2,
+                       const void* W3, void* y, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                       uint8_t* dropped_mask, float* f, float* P, float* L_aux, float* route_stats,
+                       float* router_logits, int32_t* perm_token, int32_t* slot, void* workspace,
                        size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts) {
   moe_status st = check_cfg(cfg);
   if (st != MOE_OK) return st;
@@ -168,7 +171,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   if (swiglu != (W3 != nullptr)) return MOE_ERR_INVALID_ARG;
   if (swiglu && (b1 || b2)) return MOE_ERR_INVALID_ARG;
   const void* all[] = {x, W_g, b_g, W1, b1, W2, b2, W3, y, topk_idx, topk_w, expert_counts, dropped_mask,
-                       f, P, L_aux, router_logits, perm_token, slot};
+                       f, P, L_aux, router_logits, perm_token, slot, router_noise, route_stats};
   for (const void* p : all)
     if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
   // y must not overlap x.
@@ -195,7 +198,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   // 1. router
   if (clk.mark(0) != cudaSuccess) return MOE_ERR_CUDA;
   RouterArgs ra;
-  ra.x = x; ra.Wg = W_g; ra.bg = b_g; ra.T = c.T; ra.d = c.d_model; ra.E = c.E; ra.k = c.k;
+  ra.x = x; ra.Wg = W_g; ra.bg = b_g; ra.noise = router_noise; ra.T = c.T; ra.d = c.d_model; ra.E = c.E; ra.k = c.k;
   ra.gating = c.gating; ra.dtype = c.dtype; ra.logits_out = router_logits; ra.topk_idx = topk_idx;
   ra.topk_w = topk_w; ra.lrank = ws + L.lrank; ra.hist = (int32_t*)(ws + L.hist); ra.psum = (float*)(ws + L.psum);
   ra.err = &hdr->err; ra.timeout_ns = timeout; ra.nblk = L.nblk;
@@ -207,6 +210,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   sa.T = c.T; sa.E = c.E; sa.k = c.k; sa.S = c.n_shared; sa.capacity = C; sa.alpha = c.alpha; sa.nblk = L.nblk;
   sa.hist = ra.hist; sa.psum = ra.psum; sa.base = (int32_t*)(ws + L.base); sa.n_pre = (int32_t*)(ws + L.npre);
   sa.counts = expert_counts; sa.offsets = (int32_t*)(ws + L.offsets); sa.f = f; sa.P = P; sa.L_aux = L_aux;
+  sa.route_stats = route_stats;
   sa.seg = seg; sa.rows_tk = L.rows_tk; sa.err = &hdr->err;
   if (launch_scan(sa, s) != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -255,10 +259,11 @@ size_t moe_forward_host_workspace_size(const moe_config* cfg) {
 }
 
 moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const void* W_g, const void* b_g,
-                            const void* W1, const void* b1, const void* W2, const void* b2, const void* W3,
-                            void* y_host, int32_t* topk_idx_host, float* topk_w_host, int32_t* expert_counts_host,
-                            uint8_t* dropped_mask_host, float* f_host, float* P_host, float* L_aux_host,
-                            void* workspace, size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts) {
+                            const float* router_noise_host, const void* W1, const void* b1, const void* W2,
+                            const void* b2, const void* W3, void* y_host, int32_t* topk_idx_host, float* topk_w_host,
+                            int32_t* expert_counts_host, uint8_t* dropped_mask_host, float* f_host, float* P_host,
+                            float* L_aux_host, float* route_stats_host, void* workspace, size_t workspace_bytes,
+                            moe_stream stream, const moe_launch_opts* opts) {
   moe_status st = check_cfg(cfg);
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
@@ -277,14 +282,21 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
   const size_t xbytes = (size_t)c.T * c.d_model * esz, ybytes = (size_t)c.T * c.d_model * (y_f32 ? 4 : 2);
   if (xbytes && cudaMemcpyAsync(ws + h.x, x_host, xbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  st = moe_forward(cfg, ws + h.x, W_g, b_g, W1, b1, W2, b2, W3, ws + h.y, (int32_t*)(ws + h.idx),
-                   (float*)(ws + h.w), (int32_t*)(ws + h.cnt), ws + h.drop, (float*)(ws + h.f), (float*)(ws + h.P),
-                   (float*)(ws + h.L), nullptr, nullptr, nullptr, workspace, L.total, stream, opts);
+  const size_t nbytes = (size_t)c.T * c.E * 4;
+  if (router_noise_host && nbytes &&
+      cudaMemcpyAsync(ws + h.noise, router_noise_host, nbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = moe_forward(cfg, ws + h.x, W_g, b_g, router_noise_host ? (const float*)(ws + h.noise) : nullptr, W1, b1, W2,
+                   b2, W3, ws + h.y, (int32_t*)(ws + h.idx), (float*)(ws + h.w), (int32_t*)(ws + h.cnt),
+                   ws + h.drop, (float*)(ws + h.f), (float*)(ws + h.P), (float*)(ws + h.L),
+                   route_stats_host ? (float*)(ws + h.stats) : nullptr, nullptr, nullptr, nullptr, workspace, L.total,
+                   stream, opts);
   if (st != MOE_OK) return st;
   struct Copy { void* dst; size_t off, bytes; } copies[] = {
       {y_host, h.y, ybytes},          {topk_idx_host, h.idx, tk * 4}, {topk_w_host, h.w, tk * 4},
       {expert_counts_host, h.cnt, (size_t)c.E * 4}, {dropped_mask_host, h.drop, tk},
-      {f_host, h.f, (size_t)c.E * 4}, {P_host, h.P, (size_t)c.E * 4}, {L_aux_host, h.L, 4}};
+      {f_host, h.f, (size_t)c.E * 4}, {P_host, h.P, (size_t)c.E * 4}, {L_aux_host, h.L, 4},
+      {route_stats_host, h.stats, route_stats_host ? (size_t)12 : 0}};
   for (const Copy& cp : copies)
     if (cp.bytes && cudaMemcpyAsync(cp.dst, ws + cp.off, cp.bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return MOE_ERR_CUDA;

@@ -81,6 +81,7 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
         float b = 0.f;
         if (a.bg) b = bf ? bf16_bits_to_f32(((const uint16_t*)a.bg)[e]) : ((const float*)a.bg)[e];
         l[e] += b;
+        if (a.noise) l[e] += a.noise[t * E + e];   // noisy scores: everything below uses them
         if (a.logits_out) a.logits_out[t * E + e] = l[e];
         insert(l[e], e);
       }

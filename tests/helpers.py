@@ -38,7 +38,7 @@ def device_inputs(inp):
 
 def run(cfg, dinp, debug=True, **kw):
     return moe.forward(cfg, dinp["x"], dinp["W_g"], dinp["b_g"], dinp["W1"], dinp["b1"], dinp["W2"],
-                       dinp["b2"], dinp["W3"], debug=debug, **kw)
+                       dinp["b2"], dinp["W3"], router_noise=dinp.get("noise"), debug=debug, **kw)
 
 
 def logit_scale(inp):
@@ -47,6 +47,8 @@ def logit_scale(inp):
     s = LOGIT_REL * (np.abs(x) @ np.abs(W))
     if inp["b_g"] is not None:
         s += 1e-6 * np.abs(si.as_f32(inp["b_g"]).astype(np.float64))[None, :]
+    if inp.get("noise") is not None:       # one more fp32 addition
+        s += 1e-6 * np.abs(inp["noise"].astype(np.float64))
     return s + 1e-30
 
 
@@ -58,6 +60,8 @@ def check_routing(cfg, inp, out, own_logits=None):
     gl = out.router_logits.cpu().numpy().astype(np.float64)
     if own_logits is None:
         own_logits = oracle.router_logits(inp["x"], inp["W_g"], inp["b_g"], cfg.dtype)
+        if inp.get("noise") is not None:
+            own_logits = oracle.add_noise(own_logits, inp["noise"])
     scale = logit_scale(inp)
     err = np.abs(gl - own_logits)
     assert np.all(err <= scale), f"logit error {err.max():.3e}, ratio {(err / scale).max():.3f}"
@@ -75,6 +79,8 @@ def check_routing(cfg, inp, out, own_logits=None):
     la = float(out.L_aux.cpu().numpy()[0])
     assert abs(la - ref["L_aux"]) <= LAUX_RTOL * abs(ref["L_aux"]) + 1e-12, (la, ref["L_aux"])
     assert int(out.expert_counts.sum()) == T * k - int(out.dropped_mask.sum())
+    if out.route_stats is not None:
+        np.testing.assert_allclose(out.route_stats.cpu().numpy(), ref["health"], rtol=2e-6, atol=1e-7)
 
     own_idx = oracle.topk(own_logits, k)
     diff = np.nonzero(np.any(own_idx != ref["topk_idx"], axis=1))[0]

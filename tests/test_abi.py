@@ -88,16 +88,16 @@ def _call_forward(L, cfg, **over):
     """moe_forward with fake, aligned, never-dereferenced pointers: every case
     here is rejected by the host checks before any CUDA call."""
     P = ctypes.c_void_p
-    args = dict(x=P(0x10000), W_g=P(0x20000), b_g=None, W1=P(0x30000), b1=None, W2=P(0x40000), b2=None,
-                W3=None, y=P(0x50000000), topk_idx=P(0x60000), topk_w=P(0x70000), counts=P(0x80000),
-                dropped=P(0x90000), f=P(0xA0000), Pp=P(0xB0000), L_aux=P(0xC0000), logits=None, perm=None,
-                slot=None, ws=P(0x100000), ws_bytes=moe.workspace_size(cfg))
+    args = dict(x=P(0x10000), W_g=P(0x20000), b_g=None, noise=None, W1=P(0x30000), b1=None, W2=P(0x40000),
+                b2=None, W3=None, y=P(0x50000000), topk_idx=P(0x60000), topk_w=P(0x70000), counts=P(0x80000),
+                dropped=P(0x90000), f=P(0xA0000), Pp=P(0xB0000), L_aux=P(0xC0000), stats=None, logits=None,
+                perm=None, slot=None, ws=P(0x100000), ws_bytes=moe.workspace_size(cfg))
     args.update(over)
     c = moe.c_config(cfg)
-    return L.moe_forward(ctypes.byref(c), args["x"], args["W_g"], args["b_g"], args["W1"], args["b1"],
-                         args["W2"], args["b2"], args["W3"], args["y"], args["topk_idx"], args["topk_w"],
-                         args["counts"], args["dropped"], args["f"], args["Pp"], args["L_aux"], args["logits"],
-                         args["perm"], args["slot"], args["ws"], args["ws_bytes"], None, None)
+    return L.moe_forward(ctypes.byref(c), args["x"], args["W_g"], args["b_g"], args["noise"], args["W1"],
+                         args["b1"], args["W2"], args["b2"], args["W3"], args["y"], args["topk_idx"], args["topk_w"],
+                         args["counts"], args["dropped"], args["f"], args["Pp"], args["L_aux"], args["stats"],
+                         args["logits"], args["perm"], args["slot"], args["ws"], args["ws_bytes"], None, None)
 
 
 def test_forward_host_checks(L):
@@ -108,6 +108,7 @@ def test_forward_host_checks(L):
     assert _call_forward(L, c, W3=P(0xD0000)) == 1                  # W3 without SwiGLU
     assert _call_forward(L, _cfg(act=moe.SWIGLU)) == 1             # SwiGLU without W3
     assert _call_forward(L, c, x=P(0x10008)) == 1                   # misaligned
+    assert _call_forward(L, c, noise=P(0xE0004)) == 1               # misaligned noise
     assert _call_forward(L, c, y=P(0x10000 + 64)) == 1              # y overlaps x
     assert _call_forward(L, c, ws_bytes=moe.workspace_size(c) - 1) == 3
     assert _call_forward(L, c, ws=None) == 3

@@ -80,6 +80,33 @@ def test_layer_small_one_cta_gemm(name):
     check_y(cfg, inp, out, gl, np.arange(cfg.T))
 
 
+@pytest.mark.parametrize("name,std", [("gpt2_top2_gelu_bf16", 1.0), ("skew_capacity_gelu_bf16", 0.5),
+                                      ("deepseek_shared_sigmoid_bf16", 2.0), ("tiny_top1_relu_f32", 1.0)])
+def test_layer_noisy_router(name, std):
+    """Gaussian router noise added before gating and top-k: routing, weights,
+    statistics and y follow the noisy logits."""
+    cfg = si.CONFIGS[name].replace(**SMALL[name])
+    inp = si.layer_inputs(cfg, seed=7)
+    inp["noise"] = si.router_noise(cfg, seed=7, std=std)
+    out = run(cfg, device_inputs(inp))
+    assert moe.check_device_errors(out.workspace) == 0
+    ref, gl, _ = check_routing(cfg, inp, out)
+    check_y(cfg, inp, out, gl, np.arange(cfg.T))
+    clean = run(cfg, device_inputs(dict(inp, noise=None)))
+    assert not torch.equal(out.topk_idx, clean.topk_idx)      # the noise really changes the routing
+
+
+def test_route_stats_closed_form_on_device():
+    """A flat router with k = E sends every token to every expert: uniform
+    shares, so the entropy is ln E and the variance and CV are 0."""
+    cfg = si.CONFIGS["gpt2_top2_gelu_bf16"].replace(T=200, d=128, f=128, E=4, k=4)
+    inp = si.layer_inputs(cfg, seed=8)
+    inp["W_g"] = np.zeros_like(inp["W_g"])
+    out = run(cfg, device_inputs(inp))
+    st = out.route_stats.cpu().numpy()
+    np.testing.assert_allclose(st, [np.log(4.0), 0.0, 0.0], rtol=1e-6, atol=1e-7)
+
+
 def test_all_tokens_choose_one_expert_with_capacity():
     cfg = si.CONFIGS["skew_capacity_gelu_bf16"].replace(T=260, d=128, f=128, E=8, k=1, capacity_factor=1.0)
     inp = si.layer_inputs(cfg, seed=3)
