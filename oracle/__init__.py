@@ -64,6 +64,11 @@ def _L() -> ctypes.CDLL:
         lib.oracle_balance.argtypes = [i64, i32, i32, dbl, vp, vp, vp, vp, vp]
         lib.oracle_add_noise.argtypes = [i64, i32, vp, vp]
         lib.oracle_route_health.argtypes = [i64, i32, i32, vp, vp]
+        lib.oracle_ec_capacity.restype = i64
+        lib.oracle_ec_capacity.argtypes = [i64, i32, i32, dbl]
+        lib.oracle_ec_select.argtypes = [i64, i32, i64, vp, vp]
+        lib.oracle_ec_layer_rows.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, vp, i64, vp, vp, vp, vp, vp,
+                                             vp, vp, vp, vp]
         _lib = lib
     return _lib
 
@@ -233,3 +238,46 @@ def forward(cfg, inp: Dict, rows: Optional[Sequence[int]] = None,
     out["rows"] = rows
     out["y"] = layer_rows(cfg, rows, inp, out["topk_idx"], out["topk_w"], out["dropped"])
     return out
+
+
+# ---- expert-choice routing ------------------------------------------------------------
+
+def ec_capacity(T: int, E: int, k: int, capacity_factor: float) -> int:
+    return int(_L().oracle_ec_capacity(T, E, k, capacity_factor))
+
+
+def ec_select(scores: np.ndarray, C: int) -> np.ndarray:
+    """[E, C] chosen tokens per expert (ascending), by score, ties to the lower token."""
+    sc = np.ascontiguousarray(scores, np.float64)
+    T, E = sc.shape
+    perm = np.empty((E, max(C, 0)), np.int32)
+    _L().oracle_ec_select(T, E, C, _p(sc), _p(perm))
+    return perm
+
+
+def ec_forward(cfg, inp: Dict, rows: Optional[Sequence[int]] = None,
+               scores: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """The layer with expert-choice routing.  ``scores``: select on these gate
+    probabilities [T, E] instead of the oracle's own (to compare decisions on
+    the very fp32 scores another implementation made); the weights of the sum
+    are the oracle's own fp64 gate probabilities either way."""
+    dt = cfg.dtype
+    lg = router_logits(inp["x"], inp["W_g"], inp["b_g"], dt)
+    if inp.get("noise") is not None:
+        lg = add_noise(lg, inp["noise"])
+    probs = gate_probs(lg, cfg.gating)
+    T = lg.shape[0]
+    C = ec_capacity(T, cfg.E, cfg.k, cfg.capacity_factor)
+    perm = ec_select(probs if scores is None else scores, C)
+    counts = np.full(cfg.E, C, np.int32)
+    P = probs.mean(axis=0) if T > 0 else np.zeros(cfg.E)
+    f = np.full(cfg.E, 1.0 / cfg.E) if T > 0 else np.zeros(cfg.E)
+    L_aux = cfg.alpha * cfg.E * float(np.sum(f * P))
+    rows = np.arange(T) if rows is None else np.asarray(rows, np.int64)
+    rows = np.ascontiguousarray(rows, np.int64)
+    y = np.empty((rows.size, cfg.d), np.float64)
+    _L().oracle_ec_layer_rows(cfg.d, cfg.f, cfg.E, cfg.S, cfg.act, dt, T, C, _p(rows), rows.size,
+                              _p(_stored(inp["x"], dt)), _p(_stored(inp["W1"], dt)), _p(_stored(inp["b1"], dt)),
+                              _p(_stored(inp["W2"], dt)), _p(_stored(inp["b2"], dt)), _p(_stored(inp["W3"], dt)),
+                              _p(np.ascontiguousarray(perm, np.int32)), _p(np.ascontiguousarray(probs)), _p(y))
+    return dict(logits=lg, probs=probs, capacity=C, perm=perm, counts=counts, f=f, P=P, L_aux=L_aux, rows=rows, y=y)

@@ -301,3 +301,77 @@ void oracle_route_health(int64_t T, int E, int k, const int32_t* n_pre, double* 
   out[1] = var;
   out[2] = (double)E * sqrt(var);
 }
+
+/* ---- expert-choice routing ---------------------------------------------------
+ * Each expert chooses the tokens it scores highest, instead of each token
+ * choosing experts ["MoE架构解析" §2.2: every expert gets the same load; a
+ * token may be chosen by several experts or by none].  Readings: the scores
+ * are the gate probabilities s[t,e] (softmax or normalised sigmoid over the
+ * experts, as for token choice); expert e takes the C tokens with the largest
+ * s[t,e], equal scores going to the lower token index, C = min(T, ceil(T cf /
+ * E)) with a capacity factor cf > 0, else min(T, ceil(T k / E)) (the compute
+ * of top-k token choice); a token's output is the sum over the experts that
+ * chose it, in ascending expert order, of s[t,e] times the expert's output
+ * (no renormalisation), plus the shared experts. */
+
+int64_t oracle_ec_capacity(int64_t T, int E, int k, double cf) {
+  double c = cf > 0.0 ? ceil((double)T * cf / (double)E) : ceil((double)T * (double)k / (double)E);
+  return (int64_t)c < T ? (int64_t)c : T;
+}
+
+/* perm[e*C + i]: the i-th chosen token of expert e, tokens ascending.
+ * Selection by a stable insertion sort of the token indices by score
+ * (descending, equal scores keep ascending token order), then the C chosen
+ * tokens listed in token order. */
+void oracle_ec_select(int64_t T, int E, int64_t C, const double* scores, int32_t* perm) {
+  int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+  uint8_t* chosen = (uint8_t*)malloc((size_t)(T > 0 ? T : 1));
+  for (int e = 0; e < E; ++e) {
+    for (int64_t t = 0; t < T; ++t) order[t] = (int32_t)t;
+    for (int64_t i = 1; i < T; ++i) {
+      int32_t key = order[i];
+      int64_t j = i - 1;
+      while (j >= 0 && scores[(int64_t)order[j] * E + e] < scores[(int64_t)key * E + e]) {
+        order[j + 1] = order[j];
+        --j;
+      }
+      order[j + 1] = key;
+    }
+    for (int64_t t = 0; t < T; ++t) chosen[t] = 0;
+    for (int64_t i = 0; i < C; ++i) chosen[order[i]] = 1;
+    int64_t n = 0;
+    for (int64_t t = 0; t < T; ++t)
+      if (chosen[t]) perm[(int64_t)e * C + n++] = (int32_t)t;
+  }
+  free(order);
+  free(chosen);
+}
+
+/* Layer output of expert-choice routing for the listed token rows. */
+void oracle_ec_layer_rows(int d, int f, int E, int S, int act, int dtype, int64_t T, int64_t C,
+                          const int64_t* rows, int64_t nrows, const void* x, const void* W1, const void* b1,
+                          const void* W2, const void* b2, const void* W3, const int32_t* perm,
+                          const double* scores, double* y) {
+  double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+  double* o = (double*)malloc(sizeof(double) * (size_t)d);
+  for (int64_t r = 0; r < nrows; ++r) {
+    const int64_t t = rows[r];
+    double* yr = y + r * d;
+    for (int i = 0; i < d; ++i) { xr[i] = ld(x, dtype, t * d + i); yr[i] = 0.0; }
+    for (int e = 0; e < E; ++e) {
+      int hit = 0;
+      for (int64_t i = 0; i < C; ++i)
+        if (perm[(int64_t)e * C + i] == t) { hit = 1; break; }
+      if (!hit) continue;
+      oracle_expert_ffn(d, f, act, dtype, e, xr, W1, b1, W2, b2, W3, o);
+      const double w = scores[t * E + e];
+      for (int i = 0; i < d; ++i) yr[i] += w * o[i];
+    }
+    for (int s = 0; s < S; ++s) {
+      oracle_expert_ffn(d, f, act, dtype, E + s, xr, W1, b1, W2, b2, W3, o);
+      for (int i = 0; i < d; ++i) yr[i] += o[i];
+    }
+  }
+  free(xr);
+  free(o);
+}

@@ -378,3 +378,73 @@ def test_route_health_closed_forms():
     np.testing.assert_allclose(h[1], np.var(f), rtol=1e-13)
     np.testing.assert_allclose(h[2], np.std(n) / np.mean(n), rtol=1e-13)
     assert np.all(oracle.route_health(np.zeros(E, np.int32), 0, 2) == 0.0)
+
+
+# ---- expert-choice routing ------------------------------------------------------------
+
+def test_ec_capacity():
+    assert oracle.ec_capacity(16384, 8, 2, 0.0) == 4096
+    assert oracle.ec_capacity(100, 8, 2, 1.25) == 16          # ceil(100 * 1.25 / 8)
+    assert oracle.ec_capacity(10, 2, 3, 0.0) == 10            # capped at T
+
+
+def test_ec_select_brute_force():
+    rng = np.random.default_rng(12)
+    for trial in range(60):
+        T, E = int(rng.integers(1, 12)), int(rng.integers(1, 6))
+        C = int(rng.integers(0, T + 1))
+        sc = rng.integers(0, 4, size=(T, E)).astype(np.float64) * 0.25     # many ties
+        if trial % 2:
+            sc = rng.random((T, E))
+        perm = oracle.ec_select(sc, C)
+        for e in range(E):
+            best = sorted(range(T), key=lambda t: (-sc[t, e], t))[:C]
+            assert perm[e].tolist() == sorted(best)
+
+
+def test_ec_flat_router_takes_the_first_tokens():
+    cfg = _cfg(T=20, d=16, E=4, k=2)
+    inp = _rand_inputs(cfg)
+    inp["W_g"] = np.zeros_like(inp["W_g"])
+    inp["b_g"] = np.zeros_like(inp["b_g"])
+    out = oracle.ec_forward(cfg, inp, rows=[0])
+    C = oracle.ec_capacity(cfg.T, cfg.E, cfg.k, 0.0)
+    assert C == 10
+    assert np.all(out["perm"] == np.arange(C)[None, :])
+    assert np.all(out["counts"] == C)
+    assert abs(out["L_aux"] - cfg.alpha) < 1e-17        # f = 1/E and P sums to 1
+
+
+@pytest.mark.parametrize("act", [si.GELU, si.SWIGLU])
+def test_ec_every_token_to_every_expert_is_the_dense_soft_mixture(act):
+    """C = T: every expert takes every token, so y = sum_e s[t,e] FFN_e(x_t)
+    (numpy matmuls); with identical experts and softmax scores that is FFN(x)."""
+    cfg = _cfg(T=9, d=16, f=24, E=3, k=2, act=act, capacity_factor=5.0, ffn_bias=(act != si.SWIGLU))
+    inp = _rand_inputs(cfg, seed=5)
+    out = oracle.ec_forward(cfg, inp)
+    assert out["capacity"] == cfg.T
+    x = si.as_f32(inp["x"]).astype(np.float64)
+    y = sum(out["probs"][:, e:e + 1] * _dense_ffn(cfg, inp, e, x) for e in range(cfg.E))
+    np.testing.assert_allclose(out["y"], y, rtol=1e-12, atol=1e-12)
+    for name in ("W1", "W2", "W3", "b1", "b2"):
+        if inp[name] is not None:
+            inp[name] = np.ascontiguousarray(np.broadcast_to(inp[name][:1], inp[name].shape))
+    out = oracle.ec_forward(cfg, inp)
+    np.testing.assert_allclose(out["y"], _dense_ffn(cfg, inp, 0, x), rtol=1e-12, atol=1e-12)
+
+
+def test_ec_orphan_tokens_get_only_the_shared_experts():
+    cfg = _cfg(T=12, d=16, f=24, E=3, k=1, S=1, act=si.SWIGLU, ffn_bias=False, capacity_factor=0.5)
+    inp = _rand_inputs(cfg, seed=6)
+    out = oracle.ec_forward(cfg, inp)
+    chosen = np.zeros(cfg.T, bool)
+    chosen[np.unique(out["perm"])] = True
+    assert (~chosen).sum() > 0
+    x = si.as_f32(inp["x"]).astype(np.float64)
+    shared = _dense_ffn(cfg, inp, cfg.E, x)
+    np.testing.assert_allclose(out["y"][~chosen], shared[~chosen], rtol=1e-12, atol=1e-12)
+    routed = out["y"] - shared
+    for t in np.nonzero(chosen)[0]:
+        expect = sum(out["probs"][t, e] * _dense_ffn(cfg, inp, e, x[t:t + 1])[0]
+                     for e in range(cfg.E) if t in out["perm"][e])
+        np.testing.assert_allclose(routed[t], expect, rtol=1e-12, atol=1e-12)
