@@ -252,12 +252,16 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop")
     ap.add_argument("--noise-std", type=float, default=0.0,
                     help="add seeded Gaussian router noise of this std before gating and top-k (0: none)")
+    ap.add_argument("--expert-choice", action="store_true",
+                    help="expert-choice routing: each expert takes its C = ceil(T k / E) best tokens")
     ap.add_argument("--gemm-one-cta", action="store_true",
                     help="bf16 expert GEMMs on the one-CTA tile kernel instead of the CTA-pair kernel")
     args = ap.parse_args()
     cfg = si.CONFIGS[args.workload]
     if args.T:
         cfg = cfg.replace(T=args.T)
+    if args.expert_choice:
+        cfg = cfg.replace(expert_choice=True)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
 
@@ -426,6 +430,7 @@ def main():
                        "k": cfg.k, "n_shared": cfg.S, "parallelism": "replicas" if world > 1 else "single GPU",
                        "expert_gemm": "one-CTA 128x256 tiles" if args.gemm_one_cta else "CTA-pair 256x256 tiles",
                        "router_noise_std": args.noise_std,
+                       "routing": "expert choice" if args.expert_choice else "token choice",
                        "l2": "no flush: inputs larger than L2 (x %.0f MB, expert weights %.2f GB)" % (
                            inp["x"].nbytes / 1e6, sum(inp[n].nbytes for n in ("W1", "W2", "W3")
                                                       if inp[n] is not None) / 1e9)},

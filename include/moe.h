@@ -100,6 +100,20 @@ typedef struct {
 /* y is written in fp32 whatever `dtype` is (e.g. for an fp32 residual stream).
  * Without it y has the storage dtype and carries that dtype's final rounding. */
 #define MOE_FLAG_Y_F32 1
+/* Expert-choice routing ("MoE架构解析" §2.2): instead of each token choosing
+ * its top-k experts, each expert chooses the C tokens with the largest gate
+ * probability s[t,e] (softmax, or normalised sigmoid, over the experts; equal
+ * probabilities: lower token index first), C = min(T, ceil(T cf / E)) with a
+ * capacity factor cf > 0, else min(T, ceil(T k / E)).  Every expert gets the
+ * same load; a token may be chosen by several experts or by none.
+ *   y[t] = sum over the experts e that chose t, ascending, of s[t,e] o_e(t),
+ *          plus the shared experts; a token no expert chose gets only those.
+ * Outputs: expert_counts = C for every expert; f_e = 1/E; P and L_aux as for
+ * token choice; route_stats of the shares; perm_token [E*C]: the chosen tokens
+ * of each expert, ascending; router_logits: the probabilities s[t,e] the
+ * experts chose on.  topk_idx, topk_w, dropped_mask and slot are not used
+ * (may be NULL). */
+#define MOE_FLAG_EXPERT_CHOICE 2
 
 /* Launch options; pass NULL for defaults. */
 typedef struct {
@@ -133,7 +147,8 @@ moe_status moe_validate_config(const moe_config* cfg);
 size_t moe_workspace_size(const moe_config* cfg);
 
 /* Expert capacity C = ceil(T * capacity_factor / E) computed in double, or -1
- * when capacity_factor <= 0 (no limit) ("MoE架构解析" §三 关键技术①). */
+ * when capacity_factor <= 0 (no limit) ("MoE架构解析" §三 关键技术①).  With
+ * MOE_FLAG_EXPERT_CHOICE: the tokens each expert chooses (see that flag). */
 int64_t moe_capacity(const moe_config* cfg);
 
 /* The layer's forward pass (steps 1-7 above).

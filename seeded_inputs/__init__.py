@@ -55,6 +55,7 @@ class LayerConfig:
     ffn_bias: bool = True
     router_bias_std: float = 0.01
     bias_std: float = 0.01
+    expert_choice: bool = False       # each expert chooses its tokens instead
 
     def replace(self, **kw) -> "LayerConfig":
         return dataclasses.replace(self, **kw)

@@ -28,6 +28,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 RELU, GELU, SWIGLU, NONE = 0, 1, 2, 3
 FLAG_Y_F32 = 1
+FLAG_EXPERT_CHOICE = 2
 SOFTMAX, SIGMOID_NORM = 0, 1
 F32, BF16 = 0, 1
 NUM_STAGES = 6
@@ -57,6 +58,7 @@ class MoEConfig:
     capacity_factor: float = 0.0
     alpha: float = 0.01
     y_f32: bool = False        # write y in fp32 whatever dtype is
+    expert_choice: bool = False  # each expert chooses its tokens (see moe.h)
 
 
 class _CConfig(ctypes.Structure):
@@ -123,9 +125,9 @@ def exported_symbols() -> Sequence[str]:
 
 def c_config(cfg, y_f32: Optional[bool] = None) -> _CConfig:
     yf = bool(getattr(cfg, "y_f32", False)) if y_f32 is None else bool(y_f32)
+    flags = (FLAG_Y_F32 if yf else 0) | (FLAG_EXPERT_CHOICE if getattr(cfg, "expert_choice", False) else 0)
     return _CConfig(int(cfg.T), int(cfg.d), int(cfg.f), int(cfg.E), int(cfg.k), int(cfg.S), int(cfg.act),
-                    int(cfg.gating), int(cfg.dtype), float(cfg.capacity_factor), float(cfg.alpha),
-                    FLAG_Y_F32 if yf else 0)
+                    int(cfg.gating), int(cfg.dtype), float(cfg.capacity_factor), float(cfg.alpha), flags)
 
 
 def validate(cfg) -> int:
@@ -212,8 +214,11 @@ def alloc_outputs(cfg, device, debug: bool = False, y_f32: bool = False) -> MoEO
         L_aux=torch.empty((1,), dtype=torch.float32, device=device),
         route_stats=torch.empty((3,), dtype=torch.float32, device=device))
     if debug:
+        rows = T * k
+        if getattr(cfg, "expert_choice", False):
+            rows = max(rows, E * capacity(cfg))
         out.router_logits = torch.empty((T, E), dtype=torch.float32, device=device)
-        out.perm_token = torch.full((max(T * k, 1),), -1, dtype=torch.int32, device=device)
+        out.perm_token = torch.full((max(rows, 1),), -1, dtype=torch.int32, device=device)
         out.slot = torch.empty((T, k), dtype=torch.int32, device=device)
     return out
 

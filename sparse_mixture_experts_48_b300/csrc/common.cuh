@@ -24,10 +24,14 @@ struct WsHeader {
 
 // Byte offsets of the regions inside the caller's workspace.
 struct WsLayout {
-  size_t hdr, hist, psum, base, lrank, npre, offsets, seg, slot, xperm, h, o, total;
+  size_t hdr, hist, psum, base, lrank, npre, offsets, seg, slot, xperm, h, o;
+  size_t ec_scores, ec_bits, ec_tokrow, ec_wrow, ec_perm;   // expert choice only
+  size_t total;
   int64_t nblk;      // router CTAs
-  int64_t rows_tk;   // T * k (rows reserved for routed assignments)
-  int64_t rows_all;  // T * k + S * T
+  int64_t rows_tk;   // rows of routed assignments: T * k, or E * C for expert choice
+  int64_t rows_all;  // rows_tk + S * T
+  int64_t ec_C;      // expert choice: tokens per expert; -1 for token choice
+  int EW;            // words of the per-token expert mask
   int G;             // E + S weight slabs / segments
 };
 

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   // their selection counts (the rank base of each CTA's tokens), the expert's
   // total selections n_e, and the sum of its gate probabilities.  Loads of
   // kScanU chunks are issued before their scans.
+  const bool ec = a.ec_C >= 0;   // expert choice: n_e = C for every expert, no ranks
   for (int e = warp; e < E; e += nwarps) {
     int run = 0;
     double ps = 0.0;
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
 #pragma unroll
       for (int u = 0; u < kScanU; ++u) {
         const int64_t b = b0 + 32 * u + lane;
-        v[u] = b < a.nblk ? a.hist[e * a.nblk + b] : 0;
+        v[u] = (b < a.nblk && !ec) ? a.hist[e * a.nblk + b] : 0;
         p[u] = b < a.nblk ? a.psum[e * a.nblk + b] : 0.f;
       }
 #pragma unroll
@@ -71,11 +72,12 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
         const int64_t b = b0 + 32 * u + lane;
         int tot;
         const int ex = warp_excl_scan(v[u], lane, &tot);
-        if (b < a.nblk) a.base[e * a.nblk + b] = run + ex;
+        if (b < a.nblk && !ec) a.base[e * a.nblk + b] = run + ex;
         run += tot;
         ps += (double)p[u];
       }
     }
+    if (ec) run = (int)a.ec_C;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
     if (lane == 0) {
@@ -99,7 +101,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   }
   int kept_total;
   int off = warp_excl_scan(cnt_local, lane, &kept_total);
-  const double Tk = (double)a.T * (double)a.k;
+  // f divides by all selections: T k for token choice, E C for expert choice.
+  const double Tk = ec ? (double)E * (double)a.ec_C : (double)a.T * (double)a.k;
   double L = 0.0;
   for (int i = 0; i < PE; ++i) {
     const int e = e0 + i;

@@ -24,6 +24,7 @@ struct RouterArgs {
   float* psum;         // [E, nblk] sum of gate probabilities per router CTA
   uint32_t* err;       // workspace status word
   int64_t timeout_ns;  // limit of every device-side wait
+  float* scores_em;    // expert choice: gate probabilities [E, T] (no top-k), else null
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 
@@ -44,8 +45,9 @@ struct ScanArgs {
   float* L_aux;
   float* route_stats;  // [3] entropy, variance, CV of the selection shares, or null
   SegTable seg;
-  int64_t rows_tk;     // T * k: first H / O row of the shared experts
+  int64_t rows_tk;     // T * k (E * C for expert choice): first H / O row of the shared experts
   const uint32_t* err; // workspace status word: non-zero = an earlier stage failed
+  int64_t ec_C;        // expert choice: every expert has exactly this many selections; -1 otherwise
 };
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
 
@@ -79,6 +81,43 @@ struct CombineArgs {
   const uint32_t* err;  // non-zero: skip (an earlier stage failed)
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+
+// Expert-choice routing (ec_routing.cu).
+struct EcSelectArgs {
+  const float* scores_em;  // [E, T] gate probabilities
+  int64_t T, C;
+  int E, EW;               // EW = ceil(E / 32) words of the per-token expert mask
+  int32_t* perm;           // [E * C] chosen tokens, grouped by expert, tokens ascending
+  float* w_row;            // [E * C] gate weight of each grouped row
+  int32_t* tok_row;        // [T, E] grouped row of (token, expert) where chosen
+  uint32_t* bits;          // [T, EW] choosing experts of each token (zeroed by the caller)
+  const uint32_t* err;
+};
+cudaError_t launch_ec_select(const EcSelectArgs& a, cudaStream_t s);
+
+struct EcGatherArgs {
+  const void* x;
+  const int32_t* perm;
+  int64_t rows;
+  int d, esz;
+  void* xperm;
+  const uint32_t* err;
+};
+cudaError_t launch_ec_gather(const EcGatherArgs& a, cudaStream_t s);
+
+struct EcCombineArgs {
+  const float* o;          // expert outputs, fp32
+  const uint32_t* bits;
+  const int32_t* tok_row;
+  const float* w_row;
+  int64_t T;
+  int E, EW, S, d;
+  int64_t rows_routed;     // E * C: first row of the shared experts
+  bool y_f32;
+  void* y;
+  const uint32_t* err;
+};
+cudaError_t launch_ec_combine(const EcCombineArgs& a, cudaStream_t s);
 
 // Grouped GEMM over the segment table.
 struct GemmArgs {

@@ -18,6 +18,14 @@ constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Expert choice: tokens per expert, min(T, ceil(T cf / E)), or min(T, ceil(T k / E))
+// without a capacity factor (the compute of top-k token choice).
+int64_t ec_capacity_of(const moe_config* c) {
+  const double v = c->capacity_factor > 0.0 ? ceil((double)c->T * c->capacity_factor / (double)c->E)
+                                            : ceil((double)c->T * (double)c->k / (double)c->E);
+  return (int64_t)v < c->T ? (int64_t)v : c->T;
+}
+
 moe_status check_cfg(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->T < 0 || c->d_model <= 0 || c->d_ff <= 0 || c->E <= 0 || c->k <= 0 || c->n_shared < 0)
@@ -26,13 +34,14 @@ moe_status check_cfg(const moe_config* c) {
   if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_GELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (c->gating != MOE_GATE_SOFTMAX && c->gating != MOE_GATE_SIGMOID_NORM) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_DT_F32 && c->dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
-  if (c->flags & ~(int64_t)MOE_FLAG_Y_F32) return MOE_ERR_INVALID_ARG;
+  if (c->flags & ~(int64_t)(MOE_FLAG_Y_F32 | MOE_FLAG_EXPERT_CHOICE)) return MOE_ERR_INVALID_ARG;
   if (!isfinite(c->capacity_factor) || !isfinite(c->alpha)) return MOE_ERR_INVALID_ARG;
   if (c->E > kMaxE || c->k > kMaxK || c->n_shared > kMaxShared) return MOE_ERR_UNSUPPORTED;
   if (c->dtype == MOE_DT_BF16 && (c->d_model % 64 != 0 || c->d_ff % 64 != 0)) return MOE_ERR_UNSUPPORTED;
   if (c->dtype == MOE_DT_F32 && (c->d_model % 4 != 0 || c->d_ff % 4 != 0)) return MOE_ERR_UNSUPPORTED;
   // Row indices of the grouped buffers are int32 (and TMA coordinates).
-  const int64_t rows_all = c->T * (int64_t)c->k + (int64_t)c->n_shared * c->T;
+  const int64_t routed = (c->flags & MOE_FLAG_EXPERT_CHOICE) ? (int64_t)c->E * ec_capacity_of(c) : c->T * (int64_t)c->k;
+  const int64_t rows_all = routed + (int64_t)c->n_shared * c->T;
   if (rows_all >= ((int64_t)1 << 31) - 2 * kGemmBM) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -40,8 +49,11 @@ moe_status check_cfg(const moe_config* c) {
 WsLayout layout(const moe_config* c) {
   WsLayout L;
   const size_t esz = c->dtype == MOE_DT_BF16 ? 2 : 4;
+  const bool ec = (c->flags & MOE_FLAG_EXPERT_CHOICE) != 0;
   L.nblk = (c->T + kRouterBM - 1) / kRouterBM;
-  L.rows_tk = c->T * (int64_t)c->k;
+  L.ec_C = ec ? ec_capacity_of(c) : -1;
+  L.EW = (c->E + 31) / 32;
+  L.rows_tk = ec ? (int64_t)c->E * L.ec_C : c->T * (int64_t)c->k;
   L.rows_all = L.rows_tk + (int64_t)c->n_shared * c->T;
   L.G = c->E + c->n_shared;
   size_t off = 0;
@@ -62,6 +74,11 @@ WsLayout layout(const moe_config* c) {
   L.xperm = take((size_t)L.rows_tk * c->d_model * esz);
   L.h = take((size_t)L.rows_all * c->d_ff * esz);
   L.o = take((size_t)L.rows_all * c->d_model * 4);
+  L.ec_scores = take(ec ? (size_t)c->E * c->T * 4 : 0);
+  L.ec_bits = take(ec ? (size_t)c->T * L.EW * 4 : 0);
+  L.ec_tokrow = take(ec ? (size_t)c->T * c->E * 4 : 0);
+  L.ec_wrow = take(ec ? (size_t)L.rows_tk * 4 : 0);
+  L.ec_perm = take(ec ? (size_t)L.rows_tk * 4 : 0);
   L.total = off;
   return L;
 }
@@ -150,6 +167,7 @@ size_t moe_workspace_size(const moe_config* cfg) {
 
 int64_t moe_capacity(const moe_config* cfg) {
   if (check_cfg(cfg) != MOE_OK) return -1;
+  if (cfg->flags & MOE_FLAG_EXPERT_CHOICE) return ec_capacity_of(cfg);
   return capacity_of(cfg);
 }
 
@@ -166,8 +184,10 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   // Required tensors.  With T == 0 the per-token tensors hold no elements and
   // may be NULL (allocators hand out NULL for empty buffers).
   const bool empty = c.T == 0;
+  const bool ec = (c.flags & MOE_FLAG_EXPERT_CHOICE) != 0;   // topk_idx, topk_w, dropped_mask unused
   if (!W_g || !W1 || !W2 || !expert_counts || !f || !P || !L_aux) return MOE_ERR_INVALID_ARG;
-  if (!empty && (!x || !y || !topk_idx || !topk_w || !dropped_mask)) return MOE_ERR_INVALID_ARG;
+  if (!empty && (!x || !y)) return MOE_ERR_INVALID_ARG;
+  if (!empty && !ec && (!topk_idx || !topk_w || !dropped_mask)) return MOE_ERR_INVALID_ARG;
   if (swiglu != (W3 != nullptr)) return MOE_ERR_INVALID_ARG;
   if (swiglu && (b1 || b2)) return MOE_ERR_INVALID_ARG;
   const void* all[] = {x, W_g, b_g, W1, b1, W2, b2, W3, y, topk_idx, topk_w, expert_counts, dropped_mask,
@@ -194,6 +214,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   StageClock clk{opts, s};
 
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ec && c.T > 0 && cudaMemsetAsync(ws + L.ec_bits, 0, (size_t)c.T * L.EW * 4, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   // 1. router
   if (clk.mark(0) != cudaSuccess) return MOE_ERR_CUDA;
@@ -202,12 +224,22 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   ra.gating = c.gating; ra.dtype = c.dtype; ra.logits_out = router_logits; ra.topk_idx = topk_idx;
   ra.topk_w = topk_w; ra.lrank = ws + L.lrank; ra.hist = (int32_t*)(ws + L.hist); ra.psum = (float*)(ws + L.psum);
   ra.err = &hdr->err; ra.timeout_ns = timeout; ra.nblk = L.nblk;
+  ra.scores_em = ec ? (float*)(ws + L.ec_scores) : nullptr;
   if (launch_router(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
 
-  // 2. scan: ranks, capacity, offsets, statistics, segment table
+  // 2. scan: ranks, capacity, offsets, statistics, segment table (expert
+  //    choice: first each expert's choice of tokens)
   if (clk.mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ec) {
+    EcSelectArgs ea;
+    ea.scores_em = (const float*)(ws + L.ec_scores); ea.T = c.T; ea.C = L.ec_C; ea.E = c.E; ea.EW = L.EW;
+    ea.perm = (int32_t*)(ws + L.ec_perm); ea.w_row = (float*)(ws + L.ec_wrow); ea.tok_row = (int32_t*)(ws + L.ec_tokrow);
+    ea.bits = (uint32_t*)(ws + L.ec_bits); ea.err = &hdr->err;
+    if (c.T > 0 && launch_ec_select(ea, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   ScanArgs sa;
-  sa.T = c.T; sa.E = c.E; sa.k = c.k; sa.S = c.n_shared; sa.capacity = C; sa.alpha = c.alpha; sa.nblk = L.nblk;
+  sa.T = c.T; sa.E = c.E; sa.k = c.k; sa.S = c.n_shared; sa.capacity = ec ? -1 : C; sa.alpha = c.alpha;
+  sa.nblk = L.nblk; sa.ec_C = L.ec_C;
   sa.hist = ra.hist; sa.psum = ra.psum; sa.base = (int32_t*)(ws + L.base); sa.n_pre = (int32_t*)(ws + L.npre);
   sa.counts = expert_counts; sa.offsets = (int32_t*)(ws + L.offsets); sa.f = f; sa.P = P; sa.L_aux = L_aux;
   sa.route_stats = route_stats;
@@ -216,11 +248,20 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
 
   // 3. gather into the expert-grouped buffer
   if (clk.mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ec) {
+    EcGatherArgs eg;
+    eg.x = x; eg.perm = (const int32_t*)(ws + L.ec_perm); eg.rows = c.T > 0 ? L.rows_tk : 0; eg.d = c.d_model;
+    eg.esz = (int)esz; eg.xperm = ws + L.xperm; eg.err = &hdr->err;
+    if (launch_ec_gather(eg, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (perm_token && L.rows_tk > 0 &&
+        cudaMemcpyAsync(perm_token, ws + L.ec_perm, (size_t)L.rows_tk * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   GatherArgs ga;
   ga.x = x; ga.T = c.T; ga.d = c.d_model; ga.E = c.E; ga.k = c.k; ga.dtype = c.dtype; ga.capacity = C;
   ga.topk_idx = topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.offsets = sa.offsets; ga.slot = slot_buf;
   ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm; ga.err = &hdr->err; ga.nblk = L.nblk;
-  if (launch_gather(ga, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!ec && launch_gather(ga, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 4./5. expert GEMMs
   const int64_t max_mtiles = (L.rows_tk + kGemmBM - 1) / kGemmBM + c.E +
@@ -248,7 +289,16 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   CombineArgs ca;
   ca.o = (const float*)(ws + L.o); ca.T = c.T; ca.d = c.d_model; ca.k = c.k; ca.S = c.n_shared; ca.y_f32 = y_f32;
   ca.rows_tk = L.rows_tk; ca.slot = slot_buf; ca.topk_w = topk_w; ca.y = y; ca.err = &hdr->err;
-  if (launch_combine(ca, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ec) {
+    EcCombineArgs ek;
+    ek.o = (const float*)(ws + L.o); ek.bits = (const uint32_t*)(ws + L.ec_bits);
+    ek.tok_row = (const int32_t*)(ws + L.ec_tokrow); ek.w_row = (const float*)(ws + L.ec_wrow); ek.T = c.T;
+    ek.E = c.E; ek.EW = L.EW; ek.S = c.n_shared; ek.d = c.d_model; ek.rows_routed = L.rows_tk; ek.y_f32 = y_f32;
+    ek.y = y; ek.err = &hdr->err;
+    if (launch_ec_combine(ek, s) != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (launch_combine(ca, s) != cudaSuccess) {
+    return MOE_ERR_CUDA;
+  }
   if (clk.mark(6) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -268,9 +318,10 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
   const bool empty = c.T == 0;
+  const bool ec = (c.flags & MOE_FLAG_EXPERT_CHOICE) != 0;
   if (!expert_counts_host || !f_host || !P_host || !L_aux_host) return MOE_ERR_INVALID_ARG;
-  if (!empty && (!x_host || !y_host || !topk_idx_host || !topk_w_host || !dropped_mask_host))
-    return MOE_ERR_INVALID_ARG;
+  if (!empty && (!x_host || !y_host)) return MOE_ERR_INVALID_ARG;
+  if (!empty && !ec && (!topk_idx_host || !topk_w_host || !dropped_mask_host)) return MOE_ERR_INVALID_ARG;
   const WsLayout L = layout(&c);
   const HostStage h = host_stage(&c, L.total);
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < h.total) return MOE_ERR_WORKSPACE;
@@ -298,7 +349,7 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
       {f_host, h.f, (size_t)c.E * 4}, {P_host, h.P, (size_t)c.E * 4}, {L_aux_host, h.L, 4},
       {route_stats_host, h.stats, route_stats_host ? (size_t)12 : 0}};
   for (const Copy& cp : copies)
-    if (cp.bytes && cudaMemcpyAsync(cp.dst, ws + cp.off, cp.bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (cp.dst && cp.bytes && cudaMemcpyAsync(cp.dst, ws + cp.off, cp.bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return MOE_ERR_CUDA;
   return MOE_OK;
 }

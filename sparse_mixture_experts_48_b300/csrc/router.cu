@@ -82,8 +82,8 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
         if (a.bg) b = bf ? bf16_bits_to_f32(((const uint16_t*)a.bg)[e]) : ((const float*)a.bg)[e];
         l[e] += b;
         if (a.noise) l[e] += a.noise[t * E + e];   // noisy scores: everything below uses them
-        if (a.logits_out) a.logits_out[t * E + e] = l[e];
-        insert(l[e], e);
+        if (a.logits_out && !a.scores_em) a.logits_out[t * E + e] = l[e];
+        insert(l[e], e);                           // (expert choice uses only the maximum, val[0])
       }
     }
     // Butterfly merge: take the partner's whole list, then insert it
@@ -121,7 +121,13 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
     if (valid) {
       const float rz = 1.f / z;
       for (int e = q; e < E; e += kTPT) l[e] *= rz;
-      if (q == 0) {
+      if (a.scores_em) {
+        // Expert choice: the experts choose on these gate probabilities.
+        for (int e = q; e < E; e += kTPT) {
+          a.scores_em[(int64_t)e * a.T + t] = l[e];
+          if (a.logits_out) a.logits_out[t * E + e] = l[e];
+        }
+      } else if (q == 0) {
         float g[8], zsel = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
