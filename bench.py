@@ -65,10 +65,13 @@ def algorithmic(cfg, rows_A: int):
     g1 = 2.0 * rows_A * d * f * (m - 1)         # x W1 (and x W3)
     g2 = 2.0 * rows_A * f * d                   # h W2
     kept = rows_A - cfg.S * T
+    # token choice reads each token's row once and writes it to each kept
+    # slot; expert choice reads one x row per grouped row
+    gather_read = kept * d * b if getattr(cfg, "expert_choice", False) else T * d * b
     return {
         "gemm1_flop": g1, "gemm2_flop": g2,
         "router_bytes": T * d * b + d * E * b + T * cfg.k * 8.0,
-        "gather_bytes": T * d * b + kept * d * b,
+        "gather_bytes": gather_read + kept * d * b,
         "combine_bytes": rows_A * d * 4.0 + T * d * b,
     }
 
