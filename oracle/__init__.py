@@ -64,6 +64,7 @@ def _L() -> ctypes.CDLL:
         lib.oracle_balance.argtypes = [i64, i32, i32, dbl, vp, vp, vp, vp, vp]
         lib.oracle_add_noise.argtypes = [i64, i32, vp, vp]
         lib.oracle_route_health.argtypes = [i64, i32, i32, vp, vp]
+        lib.oracle_backward.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32, dbl, dbl] + [vp] * 21
         lib.oracle_ec_capacity.restype = i64
         lib.oracle_ec_capacity.argtypes = [i64, i32, i32, dbl]
         lib.oracle_ec_select.argtypes = [i64, i32, i64, vp, vp]
@@ -281,3 +282,30 @@ def ec_forward(cfg, inp: Dict, rows: Optional[Sequence[int]] = None,
                               _p(_stored(inp["W2"], dt)), _p(_stored(inp["b2"], dt)), _p(_stored(inp["W3"], dt)),
                               _p(np.ascontiguousarray(perm, np.int32)), _p(np.ascontiguousarray(probs)), _p(y))
     return dict(logits=lg, probs=probs, capacity=C, perm=perm, counts=counts, f=f, P=P, L_aux=L_aux, rows=rows, y=y)
+
+
+# ---- backward pass ------------------------------------------------------------------
+
+def backward(cfg, inp: Dict, dy: np.ndarray, dL_aux: float = 1.0) -> Dict[str, np.ndarray]:
+    """Gradients of sum_t <dy_t, y_t> + dL_aux * L_aux (token choice), fp64."""
+    dt = cfg.dtype
+    lg = router_logits(inp["x"], inp["W_g"], inp["b_g"], dt)
+    if inp.get("noise") is not None:
+        lg = add_noise(lg, inp["noise"])
+    r = routing(cfg, lg)
+    T, d, f, E, S, k = cfg.T, cfg.d, cfg.f, cfg.E, cfg.S, cfg.k
+    G = E + S
+    out = dict(dx=np.empty((T, d)), dW_g=np.empty((d, E)), db_g=np.empty(E), dW1=np.empty((G, d, f)),
+               db1=np.empty((G, f)), dW2=np.empty((G, f, d)), db2=np.empty((G, d)),
+               dW3=np.empty((G, d, f)) if cfg.act == SWIGLU else None)
+    dyc = np.ascontiguousarray(dy, np.float64)
+    _L().oracle_backward(T, d, f, E, k, S, cfg.act, cfg.gating, dt, cfg.alpha, dL_aux,
+                         _p(_stored(inp["x"], dt)), _p(_stored(inp["W_g"], dt)), _p(np.ascontiguousarray(lg)),
+                         _p(_stored(inp["W1"], dt)), _p(_stored(inp["b1"], dt)), _p(_stored(inp["W2"], dt)),
+                         _p(_stored(inp["b2"], dt)), _p(_stored(inp["W3"], dt)),
+                         _p(np.ascontiguousarray(r["topk_idx"], np.int32)), _p(np.ascontiguousarray(r["topk_w"])),
+                         _p(np.ascontiguousarray(r["dropped"], np.uint8)), _p(np.ascontiguousarray(r["n_pre"], np.int32)),
+                         _p(dyc), _p(out["dx"]), _p(out["dW_g"]), _p(out["db_g"]), _p(out["dW1"]), _p(out["db1"]),
+                         _p(out["dW2"]), _p(out["db2"]), _p(out["dW3"]))
+    out["routing"] = r
+    return out

@@ -375,3 +375,178 @@ void oracle_ec_layer_rows(int d, int f, int E, int S, int act, int dtype, int64_
   free(xr);
   free(o);
 }
+
+/* ---- backward pass ---------------------------------------------------------------
+ * Gradients of the scalar  L = sum_t <dy_t, y_t> + dL_aux * L_aux  with respect
+ * to x, W_g, b_g, W1, b1, W2, b2, W3 (token-choice routing), for training the
+ * layer with the load-balance term added to the main loss ["MoE混合专家模型：
+ * Transformer稀疏前馈网络原理与PyTorch实现" §4.3: the aux loss joins the main loss
+ * before one backward; "手撕一个极简 MoE-FFN" §七].  Written out from the forward
+ * by the chain rule:
+ *  - selection, the capacity cut and f are piecewise constant: no gradient;
+ *  - y_t = sum_{kept j} w_j o_j + sum_s o_s:  dw_j = <dy_t, o_j>,  do_j = w_j dy_t;
+ *  - o = W2^T h + b2:  dh = W2 do,  dW2 += h do^T,  db2 += do;
+ *  - h = act(a), a = W1^T x + b1:  da = act'(a) dh;  SwiGLU h = silu(a) u with
+ *    u = W3^T x:  da = dh u silu'(a),  du = dh silu(a);
+ *  - dx += W1 da (+ W3 du),  dW1 += x da^T,  dW3 += x du^T,  db1 += da;
+ *  - renormalised weights w_j = g_j / sum_sel g:  dg_i = (dw_i - sum_j w_j dw_j) /
+ *    sum_sel g on the selected experts; softmax g = p: dl = p (dg - <p, dg>);
+ *    normalised sigmoid: the selected sigmoids, dl_i = dg_i s_i (1 - s_i);
+ *  - L_aux = alpha E sum_e f_e P_e with P_e = mean_t p_te: dp_te = dL_aux alpha E
+ *    f_e / T, through softmax as above, or through p = s / sum s for sigmoid;
+ *  - l = x W_g + b_g (+ noise): dW_g += x dl^T, db_g += dl, dx += W_g dl.
+ * All outputs are fp64 and are overwritten.  dy is fp64 [T, d]. */
+static double gelu_grad(double z) {
+  /* d/dz [z Phi(z)] = Phi(z) + z phi(z), phi the standard normal density */
+  return 0.5 * (1.0 + erf(z / sqrt(2.0))) + z * exp(-0.5 * z * z) / sqrt(2.0 * acos(-1.0));
+}
+static double sig(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+void oracle_backward(int64_t T, int d, int f, int E, int k, int S, int act, int gating, int dtype, double alpha,
+                     double dL_aux, const void* x, const void* W_g, const double* logits, const void* W1,
+                     const void* b1, const void* W2, const void* b2, const void* W3, const int32_t* idx,
+                     const double* w, const uint8_t* dropped, const int32_t* n_pre, const double* dy, double* dx,
+                     double* dWg, double* dbg, double* dW1, double* db1, double* dW2, double* db2, double* dW3) {
+  const int G = E + S;
+  memset(dx, 0, sizeof(double) * (size_t)(T * d));
+  memset(dWg, 0, sizeof(double) * (size_t)d * E);
+  memset(dbg, 0, sizeof(double) * (size_t)E);
+  memset(dW1, 0, sizeof(double) * (size_t)G * d * f);
+  memset(db1, 0, sizeof(double) * (size_t)G * f);
+  memset(dW2, 0, sizeof(double) * (size_t)G * f * d);
+  memset(db2, 0, sizeof(double) * (size_t)G * d);
+  if (dW3) memset(dW3, 0, sizeof(double) * (size_t)G * d * f);
+  double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+  double* a = (double*)malloc(sizeof(double) * (size_t)f);
+  double* u = (double*)malloc(sizeof(double) * (size_t)f);
+  double* h = (double*)malloc(sizeof(double) * (size_t)f);
+  double* dh = (double*)malloc(sizeof(double) * (size_t)f);
+  double* da = (double*)malloc(sizeof(double) * (size_t)f);
+  double* du = (double*)malloc(sizeof(double) * (size_t)f);
+  double* o = (double*)malloc(sizeof(double) * (size_t)d);
+  double* p = (double*)malloc(sizeof(double) * (size_t)E);
+  double* dl = (double*)malloc(sizeof(double) * (size_t)E);
+  double* dp = (double*)malloc(sizeof(double) * (size_t)E);
+  double* dw = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+  const int swiglu = act == OACT_SWIGLU;
+  for (int64_t t = 0; t < T; ++t) {
+    const double* dyt = dy + t * d;
+    for (int i = 0; i < d; ++i) xr[i] = ld(x, dtype, t * d + i);
+    /* experts: routed (kept) and shared */
+    for (int j = 0; j < k + S; ++j) {
+      int g;
+      double wj;
+      if (j < k) {
+        dw[j] = 0.0;
+        if (dropped[t * k + j]) continue;
+        g = idx[t * k + j];
+        wj = w[t * k + j];
+      } else {
+        g = E + (j - k);
+        wj = 1.0;
+      }
+      const int64_t w1o = (int64_t)g * d * f, w2o = (int64_t)g * f * d;
+      for (int c = 0; c < f; ++c) { a[c] = (b1 && !swiglu) ? ld(b1, dtype, (int64_t)g * f + c) : 0.0; u[c] = 0.0; }
+      for (int i = 0; i < d; ++i) {
+        for (int c = 0; c < f; ++c) a[c] += xr[i] * ld(W1, dtype, w1o + (int64_t)i * f + c);
+        if (swiglu)
+          for (int c = 0; c < f; ++c) u[c] += xr[i] * ld(W3, dtype, w1o + (int64_t)i * f + c);
+      }
+      for (int c = 0; c < f; ++c) h[c] = swiglu ? oracle_act(OACT_SWIGLU, a[c]) * u[c] : oracle_act(act, a[c]);
+      /* o and dw_j = <dy, o> */
+      if (j < k) {
+        for (int c = 0; c < d; ++c) o[c] = (b2 && !swiglu) ? ld(b2, dtype, (int64_t)g * d + c) : 0.0;
+        for (int r = 0; r < f; ++r)
+          for (int c = 0; c < d; ++c) o[c] += h[r] * ld(W2, dtype, w2o + (int64_t)r * d + c);
+        double s = 0.0;
+        for (int c = 0; c < d; ++c) s += dyt[c] * o[c];
+        dw[j] = s;
+      }
+      /* do = wj dy; dh = W2 do; dW2 += h do^T; db2 += do */
+      for (int r = 0; r < f; ++r) {
+        double s = 0.0;
+        for (int c = 0; c < d; ++c) {
+          const double doc = wj * dyt[c];
+          s += ld(W2, dtype, w2o + (int64_t)r * d + c) * doc;
+          dW2[w2o + (int64_t)r * d + c] += h[r] * doc;
+        }
+        dh[r] = s;
+      }
+      if (b2 && !swiglu)
+        for (int c = 0; c < d; ++c) db2[(int64_t)g * d + c] += wj * dyt[c];
+      /* activation */
+      for (int r = 0; r < f; ++r) {
+        if (swiglu) {
+          const double sa = sig(a[r]);
+          da[r] = dh[r] * u[r] * (sa + a[r] * sa * (1.0 - sa));
+          du[r] = dh[r] * a[r] * sa;
+        } else if (act == OACT_RELU) {
+          da[r] = a[r] > 0.0 ? dh[r] : 0.0;
+        } else {
+          da[r] = dh[r] * gelu_grad(a[r]);
+        }
+      }
+      /* dx, dW1, dW3, db1 */
+      for (int i = 0; i < d; ++i) {
+        double s = 0.0;
+        for (int r = 0; r < f; ++r) {
+          s += ld(W1, dtype, w1o + (int64_t)i * f + r) * da[r];
+          dW1[w1o + (int64_t)i * f + r] += xr[i] * da[r];
+          if (swiglu) {
+            s += ld(W3, dtype, w1o + (int64_t)i * f + r) * du[r];
+            dW3[w1o + (int64_t)i * f + r] += xr[i] * du[r];
+          }
+        }
+        dx[t * d + i] += s;
+      }
+      if (b1 && !swiglu)
+        for (int r = 0; r < f; ++r) db1[(int64_t)g * f + r] += da[r];
+    }
+    /* router: through the renormalised weights, then the aux term */
+    const double* l = logits + t * E;
+    oracle_gate_probs(1, E, gating, l, p);
+    for (int e = 0; e < E; ++e) dl[e] = 0.0;
+    double zsel = 0.0, wdw = 0.0;
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[t * k + j];
+      zsel += gating == OGATE_SOFTMAX ? p[e] : sig(l[e]);
+      wdw += w[t * k + j] * dw[j];
+    }
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[t * k + j];
+      if (gating == OGATE_SOFTMAX) {
+        /* w = softmax of the selected logits: dl_i = w_i (dw_i - sum w dw) */
+        dl[e] += w[t * k + j] * (dw[j] - wdw);
+      } else {
+        const double se = sig(l[e]);
+        dl[e] += (dw[j] - wdw) / zsel * se * (1.0 - se);
+      }
+    }
+    if (dL_aux != 0.0) {
+      for (int e = 0; e < E; ++e) dp[e] = dL_aux * alpha * E * ((double)n_pre[e] / ((double)T * k)) / (double)T;
+      double s = 0.0;
+      for (int e = 0; e < E; ++e) s += p[e] * dp[e];
+      if (gating == OGATE_SOFTMAX) {
+        for (int e = 0; e < E; ++e) dl[e] += p[e] * (dp[e] - s);
+      } else {
+        /* p = sig / sum sig:  dsig_e = (dp_e - sum_e' p_e' dp_e') / sum sig;  dl = dsig s (1 - s) */
+        double zs = 0.0;
+        for (int e = 0; e < E; ++e) zs += sig(l[e]);
+        for (int e = 0; e < E; ++e) {
+          const double se = sig(l[e]);
+          dl[e] += (dp[e] - s) / zs * se * (1.0 - se);
+        }
+      }
+    }
+    for (int e = 0; e < E; ++e) {
+      dbg[e] += dl[e];
+      for (int i = 0; i < d; ++i) dWg[(int64_t)i * E + e] += xr[i] * dl[e];
+    }
+    for (int i = 0; i < d; ++i) {
+      double s = 0.0;
+      for (int e = 0; e < E; ++e) s += ld(W_g, dtype, (int64_t)i * E + e) * dl[e];
+      dx[t * d + i] += s;
+    }
+  }
+  free(xr); free(a); free(u); free(h); free(dh); free(da); free(du); free(o); free(p); free(dl); free(dp); free(dw);
+}

@@ -1,0 +1,82 @@
+"""The oracle's backward pass against central finite differences of its own
+forward pass, in fp64 on tiny layers.
+
+The scalar is L = sum_t <dy_t, y_t> + dL_aux * L_aux.  Routing (top-k and the
+capacity cut) is piecewise constant, so a coordinate is only checked when its
+perturbation leaves every routing decision unchanged.  Inputs are stored in
+fp32, so each perturbed value is the fp32 neighbour actually stored, and the
+difference quotient divides by that stored difference."""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+
+
+def _cfg(**kw):
+    base = dict(name="bwd", T=7, d=8, f=12, E=4, k=2, S=0, act=si.GELU, gating=si.SOFTMAX, dtype=si.F32)
+    base.update(kw)
+    return si.LayerConfig(**base)
+
+
+def _loss(cfg, inp, dy, dL_aux):
+    out = oracle.forward(cfg, inp)
+    return float(np.sum(dy * out["y"]) + dL_aux * out["L_aux"]), out
+
+
+def _fd_check(cfg, inp, dy, dL_aux, names, n_coords=5, seed=0, h=2.0 ** -10):
+    g = oracle.backward(cfg, inp, dy, dL_aux)
+    _, base = _loss(cfg, inp, dy, dL_aux)
+    rng = np.random.default_rng(seed)
+    key = {"x": "dx", "W_g": "dW_g", "b_g": "db_g", "W1": "dW1", "b1": "db1", "W2": "dW2", "b2": "db2", "W3": "dW3"}
+    checked = 0
+    for name in names:
+        arr = inp[name]
+        flat = arr.reshape(-1)
+        for i in rng.choice(flat.size, size=min(n_coords, flat.size), replace=False):
+            v0 = flat[i]
+            vp, vm = np.float32(v0 + h), np.float32(v0 - h)
+            flat[i] = vp
+            lp, op = _loss(cfg, inp, dy, dL_aux)
+            flat[i] = vm
+            lm, om = _loss(cfg, inp, dy, dL_aux)
+            flat[i] = v0
+            same = all(np.array_equal(o["topk_idx"], base["topk_idx"]) and np.array_equal(o["dropped"], base["dropped"])
+                       for o in (op, om))
+            if not same:
+                continue
+            fd = (lp - lm) / (float(vp) - float(vm))
+            an = g[key[name]].reshape(-1)[i]
+            scale = max(1.0, np.abs(g[key[name]]).max())
+            assert abs(fd - an) <= 2e-5 * scale, (name, i, fd, an)
+            checked += 1
+    assert checked >= len(names) * n_coords // 2
+    return g
+
+
+def test_backward_gelu_softmax_capacity_bias_noise():
+    cfg = _cfg(capacity_factor=0.9, router_bias_std=0.5)
+    inp = si.layer_inputs(cfg, seed=3)
+    inp["noise"] = si.router_noise(cfg, seed=3, std=0.3)
+    dy = np.random.default_rng(1).standard_normal((cfg.T, cfg.d))
+    g = _fd_check(cfg, inp, dy, 0.7, ["x", "W_g", "b_g", "W1", "b1", "W2", "b2"])
+    assert g["routing"]["dropped"].sum() > 0          # the capacity cut is exercised
+
+
+def test_backward_swiglu_sigmoid_shared():
+    cfg = _cfg(act=si.SWIGLU, gating=si.SIGMOID_NORM, S=1, k=3, E=5, ffn_bias=False)
+    inp = si.layer_inputs(cfg, seed=4)
+    dy = np.random.default_rng(2).standard_normal((cfg.T, cfg.d))
+    _fd_check(cfg, inp, dy, 1.3, ["x", "W_g", "b_g", "W1", "W2", "W3"], seed=1)
+
+
+def test_backward_only_aux_reaches_only_the_router():
+    """dy = 0: the expert weights get no gradient, the router only through L_aux."""
+    cfg = _cfg(act=si.SWIGLU, ffn_bias=False)
+    inp = si.layer_inputs(cfg, seed=5)
+    g = oracle.backward(cfg, inp, np.zeros((cfg.T, cfg.d)), 1.0)
+    for key in ("dW1", "dW2", "dW3"):
+        assert np.all(g[key] == 0.0)
+    assert np.abs(g["dW_g"]).max() > 0
+    g0 = oracle.backward(cfg, inp, np.zeros((cfg.T, cfg.d)), 0.0)
+    assert np.all(g0["dW_g"] == 0.0) and np.all(g0["dx"] == 0.0)
