@@ -207,6 +207,28 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
                             float* L_aux_host, float* route_stats_host, void* workspace, size_t workspace_bytes,
                             moe_stream stream, const moe_launch_opts* opts);
 
+/* Backward pass of the layer (token choice, bf16): gradients of
+ *   L = sum_t <dy_t, y_t> + dL_aux * L_aux
+ * (the load-balance loss joins the main loss before one backward, "MoE混合专家
+ * 模型：Transformer稀疏前馈网络原理与PyTorch实现" §4.3) with respect to x, W_g,
+ * b_g, W1, b1, W2, b2 and W3.  The forward pass is recomputed inside (nothing
+ * is kept between calls); routing, the capacity cut and f carry no gradient;
+ * the renormalised top-k weights and L_aux (through P) carry the router's.
+ * Inputs: as moe_forward (device), plus dy [T, d] bf16 and the scalar dL_aux
+ * (1.0 when L_aux is added to the loss as is).
+ * Outputs (device, fp32, overwritten): dx [T, d], dW_g [d, E], db_g [E] (iff
+ * b_g), dW1 [E+S, d, f], db1 [E+S, f] (iff b1), dW2 [E+S, f, d], db2 [E+S, d]
+ * (iff b2), dW3 [E+S, d, f] (iff SwiGLU).
+ * workspace: >= moe_backward_workspace_size(cfg) bytes, 256-byte aligned.
+ * MOE_ERR_UNSUPPORTED for fp32 layers and for MOE_FLAG_EXPERT_CHOICE.
+ * Deterministic: bitwise the same gradients for the same inputs. */
+size_t moe_backward_workspace_size(const moe_config* cfg);
+moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
+                        const float* router_noise, const void* W1, const void* b1, const void* W2, const void* b2,
+                        const void* W3, const void* dy, float dL_aux, float* dx, float* dW_g, float* db_g,
+                        float* dW1, float* db1, float* dW2, float* db2, float* dW3, void* workspace,
+                        size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts);
+
 /* Waits for `stream`, then reports the device-side status of the last call
  * that used `workspace`: MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE, or
  * MOE_ERR_CUDA if the stream itself reports an error.  Synchronising. */

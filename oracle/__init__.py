@@ -286,12 +286,18 @@ def ec_forward(cfg, inp: Dict, rows: Optional[Sequence[int]] = None,
 
 # ---- backward pass ------------------------------------------------------------------
 
-def backward(cfg, inp: Dict, dy: np.ndarray, dL_aux: float = 1.0) -> Dict[str, np.ndarray]:
-    """Gradients of sum_t <dy_t, y_t> + dL_aux * L_aux (token choice), fp64."""
+def backward(cfg, inp: Dict, dy: np.ndarray, dL_aux: float = 1.0,
+             logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """Gradients of sum_t <dy_t, y_t> + dL_aux * L_aux (token choice), fp64.
+    ``logits``: route on (and differentiate the gating at) these logits instead
+    of the oracle's own, as in forward()."""
     dt = cfg.dtype
-    lg = router_logits(inp["x"], inp["W_g"], inp["b_g"], dt)
-    if inp.get("noise") is not None:
-        lg = add_noise(lg, inp["noise"])
+    if logits is None:
+        lg = router_logits(inp["x"], inp["W_g"], inp["b_g"], dt)
+        if inp.get("noise") is not None:
+            lg = add_noise(lg, inp["noise"])
+    else:
+        lg = np.ascontiguousarray(logits, np.float64)
     r = routing(cfg, lg)
     T, d, f, E, S, k = cfg.T, cfg.d, cfg.f, cfg.E, cfg.S, cfg.k
     G = E + S

@@ -105,6 +105,10 @@ def lib() -> ctypes.CDLL:
     L.moe_forward_host_workspace_size.argtypes = [cfgp]
     L.moe_forward_host.restype = ctypes.c_int
     L.moe_forward_host.argtypes = [cfgp] + [vp] * 9 + [vp] * 9 + [vp, sz, vp, optp]
+    L.moe_backward_workspace_size.restype = sz
+    L.moe_backward_workspace_size.argtypes = [cfgp]
+    L.moe_backward.restype = ctypes.c_int
+    L.moe_backward.argtypes = [cfgp] + [vp] * 10 + [ctypes.c_float] + [vp] * 9 + [sz, vp, optp]
     L.moe_check_device_errors.restype = ctypes.c_int
     L.moe_check_device_errors.argtypes = [vp, vp]
     L.moe_grouped_gemm_workspace_size.restype = sz
@@ -119,7 +123,8 @@ def lib() -> ctypes.CDLL:
 
 def exported_symbols() -> Sequence[str]:
     return ("moe_status_string", "moe_validate_config", "moe_workspace_size", "moe_capacity", "moe_forward",
-            "moe_forward_host_workspace_size", "moe_forward_host", "moe_check_device_errors",
+            "moe_forward_host_workspace_size", "moe_forward_host", "moe_backward_workspace_size", "moe_backward",
+            "moe_check_device_errors",
             "moe_grouped_gemm_workspace_size", "moe_grouped_gemm", "moe_grouped_gemm_noalloc")
 
 
@@ -350,6 +355,64 @@ def forward_host(cfg, x_host: torch.Tensor, W_g, b_g, W1, b1, W2, b2, W3=None, *
     if status != 0:
         raise MoEError(status, "moe_forward_host")
     return out
+
+
+@dataclasses.dataclass
+class MoEGrads:
+    dx: torch.Tensor
+    dW_g: torch.Tensor
+    db_g: Optional[torch.Tensor]
+    dW1: torch.Tensor
+    db1: Optional[torch.Tensor]
+    dW2: torch.Tensor
+    db2: Optional[torch.Tensor]
+    dW3: Optional[torch.Tensor]
+    workspace: Optional[torch.Tensor] = None
+
+
+def backward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3, dy, dL_aux: float = 1.0, *,
+             router_noise: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> MoEGrads:
+    """Gradients of sum <dy, y> + dL_aux * L_aux (moe_backward; fp32 outputs).
+    Recomputes the forward pass inside; asynchronous like forward()."""
+    if not torch.cuda.is_available():
+        raise RuntimeError("the MoE layer runs on a CUDA device; none is available")
+    T, d, f, E, S = cfg.T, cfg.d, cfg.f, cfg.E, cfg.S
+    G = E + S
+    st = _STORE[cfg.dtype]
+    _check(x, "x", (T, d), st)
+    _check(dy, "dy", (T, d), st)
+    _check(W_g, "W_g", (d, E), st)
+    _check(b_g, "b_g", (E,), st, required=False)
+    _check(W1, "W1", (G, d, f), st)
+    _check(W3, "W3", (G, d, f), st, required=cfg.act == SWIGLU)
+    _check(W2, "W2", (G, f, d), st)
+    _check(b1, "b1", (G, f), st, required=False)
+    _check(b2, "b2", (G, d), st, required=False)
+    _check(router_noise, "router_noise", (T, E), (torch.float32,), required=False)
+    dev = W1.device
+    z = dict(dtype=torch.float32, device=dev)
+    g = MoEGrads(dx=torch.empty((T, d), **z), dW_g=torch.empty((d, E), **z),
+                 db_g=torch.empty((E,), **z) if b_g is not None else None, dW1=torch.empty((G, d, f), **z),
+                 db1=torch.empty((G, f), **z) if b1 is not None else None, dW2=torch.empty((G, f, d), **z),
+                 db2=torch.empty((G, d), **z) if b2 is not None else None,
+                 dW3=torch.empty((G, d, f), **z) if cfg.act == SWIGLU else None)
+    ccfg = c_config(cfg)
+    if workspace is None:
+        n = int(lib().moe_backward_workspace_size(ctypes.byref(ccfg)))
+        if n == 0:
+            raise MoEError(2, "moe_backward_workspace_size")
+        workspace = torch.empty((n,), dtype=torch.uint8, device=dev)
+    g.workspace = workspace
+    with torch.cuda.device(dev):
+        status = lib().moe_backward(
+            ctypes.byref(ccfg), _ptr(x), _ptr(W_g), _ptr(b_g), _ptr(router_noise), _ptr(W1), _ptr(b1), _ptr(W2),
+            _ptr(b2), _ptr(W3), _ptr(dy), float(dL_aux), _ptr(g.dx), _ptr(g.dW_g), _ptr(g.db_g), _ptr(g.dW1),
+            _ptr(g.db1), _ptr(g.dW2), _ptr(g.db2), _ptr(g.dW3), _ptr(workspace), workspace.numel(),
+            _stream_handle(stream), None)
+    if status != 0:
+        raise MoEError(status, "moe_backward")
+    return g
 
 
 def check_device_errors(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:

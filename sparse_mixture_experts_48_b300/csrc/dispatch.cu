@@ -91,13 +91,16 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   // Phase 2, one warp: lane l owns experts [l * PE, (l + 1) * PE).
   const int PE = (E + 31) / 32;
   const int e0 = lane * PE;
+  // Rows a routed segment occupies: its kept count, padded to a.pad_rows.
+  const int pad = a.pad_rows > 1 ? a.pad_rows : 1;
+  auto seg_rows = [&](int n) {
+    const int c = (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
+    return (c + pad - 1) / pad * pad;
+  };
   int cnt_local = 0;
   for (int i = 0; i < PE; ++i) {
     const int e = e0 + i;
-    if (e < E) {
-      const int n = s_npre[e];
-      cnt_local += (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
-    }
+    if (e < E) cnt_local += seg_rows(s_npre[e]);
   }
   int kept_total;
   int off = warp_excl_scan(cnt_local, lane, &kept_total);
@@ -112,7 +115,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       a.n_pre[e] = n;
       a.counts[e] = c;
       a.offsets[e] = off;
-      off += c;
+      off += seg_rows(n);
       const double fe = a.T > 0 ? (double)n / Tk : 0.0;
       const double Pe = a.T > 0 ? s_psum[e] / (double)a.T : 0.0;
       a.f[e] = (float)fe;
@@ -163,10 +166,9 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     if (g < G) {
       int rows;
       if (g < E) {
-        const int n = s_npre[g];
-        rows = (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
+        rows = seg_rows(s_npre[g]);
       } else {
-        rows = failed ? 0 : (int)a.T;
+        rows = failed ? 0 : (int)(pad > 1 ? a.shared_stride : a.T);
       }
       mt_local += (rows + kGemmBM - 1) / kGemmBM;
     }
@@ -177,10 +179,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   int row_local = 0;
   for (int i = 0; i < PG; ++i) {
     const int g = g0 + i;
-    if (g < E) {
-      const int n = s_npre[g];
-      row_local += (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
-    }
+    if (g < E) row_local += seg_rows(s_npre[g]);
   }
   int row_total;
   int orow_r = warp_excl_scan(row_local, lane, &row_total);
@@ -189,15 +188,14 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     if (g < G) {
       int rows, orow, arow, asrc;
       if (g < E) {
-        const int n = s_npre[g];
-        rows = (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
+        rows = seg_rows(s_npre[g]);
         orow = orow_r;
         orow_r += rows;
         arow = orow;
         asrc = 0;
       } else {
-        rows = failed ? 0 : (int)a.T;
-        orow = (int)(a.rows_tk + (int64_t)(g - E) * a.T);
+        rows = failed ? 0 : (int)(pad > 1 ? a.shared_stride : a.T);
+        orow = (int)(a.rows_tk + (int64_t)(g - E) * a.shared_stride);
         arow = 0;
         asrc = 1;
       }

@@ -92,7 +92,20 @@ __device__ __forceinline__ void map_tile(const Ctl& c, int G, int n_tiles, int t
   m = local - n * mtg;
 }
 
-template <bool SWIGLU, bool OUT_F32>
+// 32 fp32 values (as bits) -> 32 bf16 at dst (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const uint32_t (&v)[32]) {
+  uint32_t p[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+}
+
+// SAVE_PRE (expert GEMM 1 of the backward pass's forward recomputation): the
+// pre-activations a = x W1 + b1 (and u = x W3 for SwiGLU) are also stored, in
+// bf16, at the output's rows and columns (a.pre_a, a.pre_u).
+template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3, GemmArgs a) {
@@ -299,6 +312,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint32_t u[32];
           tmem_ld32(tbase + 128u + (uint32_t)(ch * 32), u);
           tmem_wait_ld();
+          if (SAVE_PRE && valid && col0 < a.N) {
+            store_bf16x32((uint16_t*)a.pre_a + orow * a.N + col0, v);
+            store_bf16x32((uint16_t*)a.pre_u + orow * a.N + col0, u);
+          }
           if (valid && col0 < a.N) {
             uint32_t p[16];
 #pragma unroll
@@ -321,6 +338,12 @@ __global__ void __launch_bounds__(THREADS, 1)
               const uint16_t* bp = bias + (int64_t)wslab * a.N + col0;
 #pragma unroll
               for (int i = 0; i < 32; ++i) f[i] += bf16_bits_to_f32(bp[i]);
+            }
+            if (SAVE_PRE) {
+              uint32_t fb[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) fb[i] = __float_as_uint(f[i]);
+              store_bf16x32((uint16_t*)a.pre_a + orow * a.N + col0, fb);
             }
             if (a.act == MOE_ACT_RELU) {
 #pragma unroll
@@ -365,10 +388,10 @@ bool map_weights(CUtensorMap* m, const void* ptr, int G, int K, int N) {
   return tmap_bf16_3d(m, ptr, G, K, N, 64, BK);
 }
 
-template <bool SWIGLU, bool OUT_F32>
+template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE = false>
 cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtensorMap& mA1, const CUtensorMap& mB,
                         const CUtensorMap& mB3, int64_t max_pair_tiles, cudaStream_t s) {
-  auto kernel = gemm_pair_kernel<SWIGLU, OUT_F32>;
+  auto kernel = gemm_pair_kernel<SWIGLU, OUT_F32, SAVE_PRE>;
   static int max_clusters = -1;   // per kernel instantiation, per process (one device type)
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -420,7 +443,11 @@ cudaError_t launch_grouped_gemm_pair(const GemmArgs& a, cudaStream_t s) {
   // a.max_mtiles bounds the 128-row tiles, hence also the 256-row pair tiles.
   const int64_t max_pair_tiles = a.max_mtiles * ((a.N + bn - 1) / bn);
   cudaError_t e;
-  if (swiglu)
+  if (a.pre_a && swiglu)
+    e = launch_pair<true, false, true>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
+  else if (a.pre_a)
+    e = launch_pair<false, false, true>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
+  else if (swiglu)
     e = launch_pair<true, false>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
   else if (a.out_f32)
     e = launch_pair<false, true>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);

@@ -48,6 +48,8 @@ struct ScanArgs {
   int64_t rows_tk;     // T * k (E * C for expert choice): first H / O row of the shared experts
   const uint32_t* err; // workspace status word: non-zero = an earlier stage failed
   int64_t ec_C;        // expert choice: every expert has exactly this many selections; -1 otherwise
+  int pad_rows;        // routed segments padded to multiples of this many rows (1: packed)
+  int64_t shared_stride;  // rows between shared segments (T, or T padded)
 };
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
 
@@ -141,9 +143,112 @@ struct GemmArgs {
   uint32_t* err;
   int64_t timeout_ns;
   bool single_cta;      // bf16: the one-CTA 128 x 256 tile kernel instead of the CTA-pair kernel
+  void* pre_a;          // if set (pair kernel, bf16 out): pre-activations a = A B + bias, [rows, N] bf16
+  void* pre_u;          // SwiGLU with pre_a: u = A B3, [rows, N] bf16
 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_grouped_gemm_pair(const GemmArgs& a, cudaStream_t s);
+
+// Expert GEMMs of the backward pass (grouped_gemm_bwd.cu).
+struct BwdGemmArgs {
+  int G, Gw;               // segments, weight slabs
+  SegTable seg;            // rows (padded to 64-row multiples), w, out_row, a_src
+  int M, N, K;             // dgrad: reduction K, output columns N; wgrad: slab M x N
+  const void* A;           // dgrad: [rows_A, K] (dO, or dA); wgrad: X [rows_A, M]
+  const void* A2;          // dgrad second phase (dU), or wgrad: x [rows_A2, M] for a_src 1
+  int64_t rows_A, rows_A2;
+  const void* B;           // dgrad: weight slabs [Gw, N, K]; wgrad: D [rows_B, N]
+  int64_t rows_B;
+  const void* B2;          // dgrad second phase (W3)
+  void* C;                 // dgrad: fp32 [rows, N] or dA bf16; wgrad: fp32 [Gw, M, N]
+  void* C2;                // dgrad SwiGLU: dU bf16
+  const void* pre_a;       // dgrad with act_bwd: saved pre-activations [rows, N] bf16
+  const void* pre_u;
+  int act;
+  bool act_bwd;            // dgrad epilogue: activation backward (dH -> dA, dU)
+  bool x_from_asrc;        // wgrad: segments with a_src 1 read X rows from A2 starting at row 0
+  int64_t max_tiles;       // upper bound of the pair tiles
+  uint32_t* err;
+  int64_t timeout_ns;
+};
+cudaError_t launch_gemm_dgrad(const BwdGemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_wgrad(const BwdGemmArgs& a, cudaStream_t s);
+
+// Backward-pass kernels around the GEMMs (moe_backward.cu).
+struct PadZeroArgs {
+  void* buf;               // grouped buffer
+  int64_t row_bytes;       // multiple of 16
+  int G, E;
+  int64_t T;
+  const int32_t* counts;   // kept rows of the routed segments
+  SegTable seg;            // rows = padded rows, out_row
+};
+cudaError_t launch_pad_zero(const PadZeroArgs& a, cudaStream_t s);
+
+struct CombineBwdArgs {
+  const void* dy;          // [T, d] bf16
+  const float* o;          // expert outputs [rows, d] fp32
+  const int32_t* slot;     // [T, k]
+  const float* topk_w;
+  int64_t T;
+  int d, k, S;
+  int64_t rows_routed, shared_stride;   // shared expert s, token t: row rows_routed + s * shared_stride + t
+  void* dO;                // [rows, d] bf16
+  float* dw;               // [T, k]
+  const uint32_t* err;
+};
+cudaError_t launch_combine_bwd(const CombineBwdArgs& a, cudaStream_t s);
+
+struct RouterBwdArgs {
+  const float* logits;     // [T, E] (noisy) router logits
+  const int32_t* topk_idx;
+  const float* topk_w;
+  const float* dw;
+  const int32_t* n_pre;    // [E] selections before the capacity cut
+  int64_t T;
+  int E, k, gating;
+  double alpha;
+  float dL_aux;
+  float* dl;               // [T, E]
+  const uint32_t* err;
+};
+cudaError_t launch_router_bwd(const RouterBwdArgs& a, cudaStream_t s);
+
+struct DxArgs {
+  const float* dxp;        // [rows, d] gradients of the grouped rows
+  const int32_t* slot;
+  const float* dl;
+  const void* Wg;          // [d, E] bf16
+  int64_t T;
+  int d, k, E, S;
+  int64_t rows_routed, shared_stride;
+  float* dx;               // [T, d]
+  const uint32_t* err;
+};
+cudaError_t launch_dx(const DxArgs& a, cudaStream_t s);
+
+struct DwgArgs {
+  const void* x;           // [T, d] bf16
+  const float* dl;         // [T, E]
+  int64_t T;
+  int d, E;
+  int64_t nchunk;
+  float* part;             // [nchunk, d, E]
+  float* bpart;            // [nchunk, E]
+  float* dWg;              // [d, E]
+  float* dbg;              // [E] or null
+};
+int64_t dwg_chunks(int64_t T);
+cudaError_t launch_dwg(const DwgArgs& a, cudaStream_t s);
+
+struct ColsumArgs {
+  const void* buf;         // grouped [rows, N] bf16
+  SegTable seg;
+  int G;
+  int64_t N;
+  float* out;              // [Gw, N]
+};
+cudaError_t launch_colsum(const ColsumArgs& a, cudaStream_t s);
 
 // Builds a segment table from row offsets (standalone grouped GEMM entry point).
 cudaError_t launch_segments_from_offsets(const int32_t* offsets, int G, int64_t M, SegTable seg, uint32_t* err,

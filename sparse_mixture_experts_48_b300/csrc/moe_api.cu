@@ -132,6 +132,76 @@ HostStage host_stage(const moe_config* c, size_t base) {
   return h;
 }
 
+// Workspace of moe_backward: the forward recomputation in a padded grouped
+// layout (every routed segment padded to whole 128-row blocks, the shared
+// segments to T rounded up to 128, padding rows zero) and the gradients.
+struct BwdLayout {
+  size_t hdr, hist, psum, base, lrank, npre, offsets, seg, slot, idx, w, drop, cnt, f, P, L, logits;
+  size_t xperm, pre_a, pre_u, h, o, dO, dA, dU, dxp, dw, dl, part, bpart, total;
+  int64_t nblk, Tpad, rows_routed, rows_all, nchunk;
+  int G;
+};
+
+BwdLayout bwd_layout(const moe_config* c) {
+  BwdLayout L;
+  const bool swiglu = c->act == MOE_ACT_SWIGLU;
+  const int64_t T = c->T;
+  L.G = c->E + c->n_shared;
+  L.nblk = (T + kRouterBM - 1) / kRouterBM;
+  L.Tpad = (T + 127) / 128 * 128;
+  L.rows_routed = (T * c->k + 127) / 128 * 128 + 128 * (int64_t)c->E;   // >= sum of padded segments
+  L.rows_all = L.rows_routed + (int64_t)c->n_shared * L.Tpad;
+  L.nchunk = dwg_chunks(T);
+  const size_t d = c->d_model, f = c->d_ff, tk = (size_t)T * c->k, ra = (size_t)L.rows_all;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align_up(off + (bytes ? bytes : 1), 256);
+    return at;
+  };
+  L.hdr = take(sizeof(WsHeader));
+  L.hist = take((size_t)L.nblk * c->E * 4);
+  L.psum = take((size_t)L.nblk * c->E * 4);
+  L.base = take((size_t)L.nblk * c->E * 4);
+  L.lrank = take(tk);
+  L.npre = take((size_t)c->E * 4);
+  L.offsets = take((size_t)(c->E + 1) * 4);
+  L.seg = take((size_t)(6 * L.G + 1) * 4);
+  L.slot = take(tk * 4);
+  L.idx = take(tk * 4);
+  L.w = take(tk * 4);
+  L.drop = take(tk);
+  L.cnt = take((size_t)c->E * 4);
+  L.f = take((size_t)c->E * 4);
+  L.P = take((size_t)c->E * 4);
+  L.L = take(4);
+  L.logits = take((size_t)T * c->E * 4);
+  L.xperm = take((size_t)L.rows_routed * d * 2);
+  L.pre_a = take(ra * f * 2);
+  L.pre_u = take(swiglu ? ra * f * 2 : 0);
+  L.h = take(ra * f * 2);
+  L.o = take(ra * d * 4);
+  L.dO = take(ra * d * 2);
+  L.dA = take(ra * f * 2);
+  L.dU = take(swiglu ? ra * f * 2 : 0);
+  L.dxp = take(ra * d * 4);
+  L.dw = take(tk * 4);
+  L.dl = take((size_t)T * c->E * 4);
+  L.part = take((size_t)L.nchunk * d * c->E * 4);
+  L.bpart = take((size_t)L.nchunk * c->E * 4);
+  L.total = off;
+  return L;
+}
+
+moe_status check_bwd_cfg(const moe_config* c) {
+  moe_status st = check_cfg(c);
+  if (st != MOE_OK) return st;
+  if (c->dtype != MOE_DT_BF16 || (c->flags & MOE_FLAG_EXPERT_CHOICE)) return MOE_ERR_UNSUPPORTED;
+  const BwdLayout L = bwd_layout(c);
+  if (L.rows_all >= ((int64_t)1 << 31) - 2 * kGemmBM) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
 struct StageClock {
   const moe_launch_opts* o;
   cudaStream_t s;
@@ -239,7 +309,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   }
   ScanArgs sa;
   sa.T = c.T; sa.E = c.E; sa.k = c.k; sa.S = c.n_shared; sa.capacity = ec ? -1 : C; sa.alpha = c.alpha;
-  sa.nblk = L.nblk; sa.ec_C = L.ec_C;
+  sa.nblk = L.nblk; sa.ec_C = L.ec_C; sa.pad_rows = 1; sa.shared_stride = c.T;
   sa.hist = ra.hist; sa.psum = ra.psum; sa.base = (int32_t*)(ws + L.base); sa.n_pre = (int32_t*)(ws + L.npre);
   sa.counts = expert_counts; sa.offsets = (int32_t*)(ws + L.offsets); sa.f = f; sa.P = P; sa.L_aux = L_aux;
   sa.route_stats = route_stats;
@@ -351,6 +421,164 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
   for (const Copy& cp : copies)
     if (cp.dst && cp.bytes && cudaMemcpyAsync(cp.dst, ws + cp.off, cp.bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+size_t moe_backward_workspace_size(const moe_config* cfg) {
+  if (check_bwd_cfg(cfg) != MOE_OK) return 0;
+  return bwd_layout(cfg).total;
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
+                        const float* router_noise, const void* W1, const void* b1, const void* W2, const void* b2,
+                        const void* W3, const void* dy, float dL_aux, float* dx, float* dW_g, float* db_g,
+                        float* dW1, float* db1, float* dW2, float* db2, float* dW3, void* workspace,
+                        size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts) {
+  moe_status st = check_bwd_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config& c = *cfg;
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  const bool empty = c.T == 0;
+  if (!W_g || !W1 || !W2 || !dW_g || !dW1 || !dW2) return MOE_ERR_INVALID_ARG;
+  if (!empty && (!x || !dy || !dx)) return MOE_ERR_INVALID_ARG;
+  if (swiglu != (W3 != nullptr) || swiglu != (dW3 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (swiglu && (b1 || b2)) return MOE_ERR_INVALID_ARG;
+  if ((b_g != nullptr) != (db_g != nullptr) || (b1 != nullptr) != (db1 != nullptr) ||
+      (b2 != nullptr) != (db2 != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!isfinite(dL_aux)) return MOE_ERR_INVALID_ARG;
+  const void* all[] = {x, W_g, b_g, router_noise, W1, b1, W2, b2, W3, dy, dx, dW_g, db_g, dW1, db1, dW2, db2, dW3};
+  for (const void* p : all)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  const BwdLayout L = bwd_layout(&c);
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  const int64_t timeout = (opts && opts->wait_timeout_ns > 0) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = (uint8_t*)workspace;
+  WsHeader* hdr = (WsHeader*)(ws + L.hdr);
+  const SegTable seg = seg_table(ws, L.seg, L.G);
+  const int64_t C = capacity_of(&c);
+  const int d = c.d_model, f = c.d_ff, E = c.E, k = c.k, S = c.n_shared, G = L.G;
+  const int64_t T = c.T;
+
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (T == 0) {
+    // No tokens: every gradient is zero.
+    struct Z { void* p; size_t bytes; } zs[] = {
+        {dW_g, (size_t)d * E * 4}, {db_g, (size_t)E * 4}, {dW1, (size_t)G * d * f * 4}, {db1, (size_t)G * f * 4},
+        {dW2, (size_t)G * f * d * 4}, {db2, (size_t)G * d * 4}, {dW3, (size_t)G * d * f * 4}};
+    for (const Z& z : zs)
+      if (z.p && cudaMemsetAsync(z.p, 0, z.bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  // ---- forward recomputation (padded grouped layout) ----
+  RouterArgs ra;
+  memset(&ra, 0, sizeof(ra));
+  ra.x = x; ra.Wg = W_g; ra.bg = b_g; ra.noise = router_noise; ra.T = T; ra.d = d; ra.E = E; ra.k = k;
+  ra.gating = c.gating; ra.dtype = c.dtype; ra.logits_out = (float*)(ws + L.logits);
+  ra.topk_idx = (int32_t*)(ws + L.idx); ra.topk_w = (float*)(ws + L.w); ra.lrank = ws + L.lrank;
+  ra.hist = (int32_t*)(ws + L.hist); ra.psum = (float*)(ws + L.psum); ra.err = &hdr->err; ra.timeout_ns = timeout;
+  ra.nblk = L.nblk;
+  if (launch_router(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
+  ScanArgs sa;
+  memset(&sa, 0, sizeof(sa));
+  sa.T = T; sa.E = E; sa.k = k; sa.S = S; sa.capacity = C; sa.alpha = c.alpha; sa.nblk = L.nblk; sa.ec_C = -1;
+  sa.pad_rows = 128; sa.shared_stride = L.Tpad; sa.hist = ra.hist; sa.psum = ra.psum;
+  sa.base = (int32_t*)(ws + L.base); sa.n_pre = (int32_t*)(ws + L.npre); sa.counts = (int32_t*)(ws + L.cnt);
+  sa.offsets = (int32_t*)(ws + L.offsets); sa.f = (float*)(ws + L.f); sa.P = (float*)(ws + L.P);
+  sa.L_aux = (float*)(ws + L.L); sa.route_stats = nullptr; sa.seg = seg; sa.rows_tk = L.rows_routed;
+  sa.err = &hdr->err;
+  if (launch_scan(sa, s) != cudaSuccess) return MOE_ERR_CUDA;
+  GatherArgs ga;
+  memset(&ga, 0, sizeof(ga));
+  ga.x = x; ga.T = T; ga.d = d; ga.E = E; ga.k = k; ga.dtype = c.dtype; ga.capacity = C;
+  ga.topk_idx = ra.topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.nblk = L.nblk; ga.offsets = sa.offsets;
+  ga.slot = (int32_t*)(ws + L.slot); ga.dropped = ws + L.drop; ga.perm_token = nullptr; ga.xperm = ws + L.xperm;
+  ga.err = &hdr->err;
+  if (launch_gather(ga, s) != cudaSuccess) return MOE_ERR_CUDA;
+  PadZeroArgs pz;
+  pz.buf = ws + L.xperm; pz.row_bytes = (int64_t)d * 2; pz.G = E; pz.E = E; pz.T = T; pz.counts = sa.counts;
+  pz.seg = seg;
+  if (launch_pad_zero(pz, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const int64_t max_mtiles = L.rows_all / kGemmBM + G;
+  GemmArgs g1;
+  memset(&g1, 0, sizeof(g1));
+  g1.dtype = c.dtype; g1.act = c.act; g1.G = G; g1.K = d; g1.N = f; g1.a_from_out_rows = false; g1.seg = seg;
+  g1.A0 = ws + L.xperm; g1.rows_A0 = L.rows_routed; g1.A1 = S > 0 ? x : nullptr; g1.rows_A1 = T;
+  g1.B = W1; g1.B3 = W3; g1.Gw = G; g1.bias = b1; g1.C = ws + L.h; g1.max_mtiles = T > 0 ? max_mtiles : 0;
+  g1.err = &hdr->err; g1.timeout_ns = timeout; g1.pre_a = ws + L.pre_a; g1.pre_u = swiglu ? ws + L.pre_u : nullptr;
+  if (launch_grouped_gemm(g1, s) != cudaSuccess) return MOE_ERR_CUDA;
+  GemmArgs g2 = g1;
+  g2.act = MOE_ACT_NONE; g2.K = f; g2.N = d; g2.a_from_out_rows = true; g2.A0 = ws + L.h; g2.rows_A0 = L.rows_all;
+  g2.A1 = nullptr; g2.rows_A1 = 0; g2.B = W2; g2.B3 = nullptr; g2.bias = b2; g2.C = ws + L.o; g2.out_f32 = true;
+  g2.pre_a = nullptr; g2.pre_u = nullptr;
+  if (launch_grouped_gemm(g2, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // ---- backward ----
+  CombineBwdArgs cb;
+  cb.dy = dy; cb.o = (const float*)(ws + L.o); cb.slot = ga.slot; cb.topk_w = ra.topk_w; cb.T = T; cb.d = d;
+  cb.k = k; cb.S = S; cb.rows_routed = L.rows_routed; cb.shared_stride = L.Tpad; cb.dO = ws + L.dO;
+  cb.dw = (float*)(ws + L.dw); cb.err = &hdr->err;
+  if (launch_combine_bwd(cb, s) != cudaSuccess) return MOE_ERR_CUDA;
+  pz.buf = ws + L.dO; pz.G = G;
+  if (launch_pad_zero(pz, s) != cudaSuccess) return MOE_ERR_CUDA;
+  RouterBwdArgs rb;
+  rb.logits = (const float*)(ws + L.logits); rb.topk_idx = ra.topk_idx; rb.topk_w = ra.topk_w;
+  rb.dw = cb.dw; rb.n_pre = sa.n_pre; rb.T = T; rb.E = E; rb.k = k; rb.gating = c.gating; rb.alpha = c.alpha;
+  rb.dL_aux = dL_aux; rb.dl = (float*)(ws + L.dl); rb.err = &hdr->err;
+  if (launch_router_bwd(rb, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // dH = dO W2^T, activation backward -> dA (, dU)
+  BwdGemmArgs bg;
+  memset(&bg, 0, sizeof(bg));
+  bg.G = G; bg.Gw = G; bg.seg = seg; bg.act = c.act; bg.err = &hdr->err; bg.timeout_ns = timeout;
+  const int64_t dgrad_tiles = T > 0 ? (L.rows_all / 256 + G) * ((int64_t)(f + 255) / 256) : 0;
+  bg.K = d; bg.N = f; bg.A = ws + L.dO; bg.rows_A = L.rows_all; bg.B = W2; bg.C = ws + L.dA;
+  bg.C2 = swiglu ? ws + L.dU : nullptr; bg.pre_a = ws + L.pre_a; bg.pre_u = swiglu ? ws + L.pre_u : nullptr;
+  bg.act_bwd = true; bg.max_tiles = dgrad_tiles;
+  if (launch_gemm_dgrad(bg, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // dX of the grouped rows = dA W1^T (+ dU W3^T)
+  BwdGemmArgs bx = bg;
+  bx.K = f; bx.N = d; bx.A = ws + L.dA; bx.A2 = swiglu ? ws + L.dU : nullptr; bx.B = W1; bx.B2 = swiglu ? W3 : nullptr;
+  bx.C = ws + L.dxp; bx.C2 = nullptr; bx.pre_a = nullptr; bx.pre_u = nullptr; bx.act_bwd = false;
+  bx.max_tiles = T > 0 ? (L.rows_all / 256 + G) * ((int64_t)(d + 255) / 256) : 0;
+  if (launch_gemm_dgrad(bx, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // weight gradients: dW2 = H^T dO, dW1 = X^T dA, dW3 = X^T dU
+  BwdGemmArgs bw;
+  memset(&bw, 0, sizeof(bw));
+  bw.G = G; bw.Gw = G; bw.seg = seg; bw.err = &hdr->err; bw.timeout_ns = timeout;
+  bw.M = f; bw.N = d; bw.A = ws + L.h; bw.rows_A = L.rows_all; bw.B = ws + L.dO; bw.rows_B = L.rows_all; bw.C = dW2;
+  bw.x_from_asrc = false; bw.max_tiles = (int64_t)G * ((f + 255) / 256) * ((d + 255) / 256);
+  if (launch_gemm_wgrad(bw, s) != cudaSuccess) return MOE_ERR_CUDA;
+  BwdGemmArgs bw1 = bw;
+  bw1.M = d; bw1.N = f; bw1.A = ws + L.xperm; bw1.rows_A = L.rows_routed; bw1.A2 = S > 0 ? x : nullptr;
+  bw1.rows_A2 = T;
+  bw1.x_from_asrc = true; bw1.B = ws + L.dA; bw1.C = dW1;
+  bw1.max_tiles = (int64_t)G * ((d + 255) / 256) * ((f + 255) / 256);
+  if (launch_gemm_wgrad(bw1, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (swiglu) {
+    BwdGemmArgs bw3 = bw1;
+    bw3.B = ws + L.dU; bw3.C = dW3;
+    if (launch_gemm_wgrad(bw3, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (b1) {
+    ColsumArgs cs;
+    cs.buf = ws + L.dA; cs.seg = seg; cs.G = G; cs.N = f; cs.out = db1;
+    if (launch_colsum(cs, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (b2) {
+    ColsumArgs cs;
+    cs.buf = ws + L.dO; cs.seg = seg; cs.G = G; cs.N = d; cs.out = db2;
+    if (launch_colsum(cs, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  DxArgs dxa;
+  dxa.dxp = (const float*)(ws + L.dxp); dxa.slot = ga.slot; dxa.dl = rb.dl; dxa.Wg = W_g; dxa.T = T; dxa.d = d;
+  dxa.k = k; dxa.E = E; dxa.S = S; dxa.rows_routed = L.rows_routed; dxa.shared_stride = L.Tpad; dxa.dx = dx;
+  dxa.err = &hdr->err;
+  if (launch_dx(dxa, s) != cudaSuccess) return MOE_ERR_CUDA;
+  DwgArgs dg;
+  dg.x = x; dg.dl = rb.dl; dg.T = T; dg.d = d; dg.E = E; dg.nchunk = L.nchunk; dg.part = (float*)(ws + L.part);
+  dg.bpart = (float*)(ws + L.bpart); dg.dWg = dW_g; dg.dbg = db_g;
+  if (launch_dwg(dg, s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

@@ -1,0 +1,112 @@
+"""moe_backward on the GPU against the oracle's fp64 backward pass.
+
+Both route on the GPU's own fp32 logits (taken from a forward call, which
+computes the very same logits), so every routing decision agrees.  The GPU
+keeps several bf16 intermediates (dO, the pre-activations, H, dA, dU) like the
+forward keeps H, so each gradient tensor is checked by its relative Frobenius error
+(<= 1e-2; <= 2e-2 for every expert slab of a weight gradient), and dx and the
+router gradients also by max-abs error (<= 5e-2 RMS)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+import sparse_mixture_experts_48_b300 as moe
+from helpers import device_inputs, run
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    ("gelu_bias_capacity", "gpt2_top2_gelu_bf16", dict(T=300, d=256, f=512, capacity_factor=1.0), 0.0),
+    ("swiglu_mixtral", "mixtral_swiglu_bf16", dict(T=260, d=512, f=1024), 0.0),
+    ("sigmoid_shared_fine", "deepseek_shared_sigmoid_bf16", dict(T=300, d=512, f=320), 0.0),
+    ("relu_noise", "gpt2_top2_gelu_bf16", dict(T=200, d=192, f=448, act=si.RELU, E=5, k=3), 0.8),
+    ("one_token", "mixtral_swiglu_bf16", dict(T=1, d=256, f=256, S=1), 0.0),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from sparse_mixture_experts_48_b300 import build
+    build.build()
+
+
+def _close(name, got, ref, fro_tol=1e-2, max_tol=5e-2):
+    """Relative Frobenius error of the whole tensor <= fro_tol.  Stacked weight
+    gradients (one slab per expert): also each slab's relative Frobenius error
+    <= 2 fro_tol, so one wrong slab or tile cannot hide in the total.  A slab
+    entry is a sum of x_r dA_r over the expert's rows, so with few rows the
+    entries are heavy-tailed products and a max-abs bound against the RMS says
+    little; dx, dW_g, db_g get max-abs error <= max_tol RMS."""
+    got = got.cpu().numpy().astype(np.float64)
+    if np.sqrt(np.mean(ref ** 2)) == 0.0:
+        assert np.all(got == 0.0), name
+        return
+    fro = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    assert fro <= fro_tol, f"{name}: rel. Frobenius {fro:.2e}"
+    if name in ("dW1", "dW2", "dW3", "db1", "db2"):
+        for g, (gs, rs) in enumerate(zip(got.reshape(got.shape[0], -1), ref.reshape(ref.shape[0], -1))):
+            nr = np.linalg.norm(rs)
+            if nr == 0.0:
+                assert np.all(gs == 0.0), (name, g)
+                continue
+            sf = float(np.linalg.norm(gs - rs) / nr)
+            assert sf <= 2 * fro_tol, f"{name}[{g}]: rel. Frobenius {sf:.2e}"
+    else:
+        mx = float(np.abs(got - ref).max()) / float(np.sqrt(np.mean(ref ** 2)))
+        assert mx <= max_tol, f"{name}: max/RMS {mx:.2e}"
+
+
+# The router's logit gradient of a token with k = 2 is w0 w1 (dw0 - dw1), with
+# dw_j = <dy, O_j>: when the two dot products nearly cancel, the bf16-level
+# error of O (about 2^-9 of |dw|) becomes a large part of the difference.  Over
+# many tokens that averages out; for a handful of tokens the router gradients
+# (dW_g, db_g) get a 5x looser relative bound.
+FEW_TOKENS = 32
+
+
+@pytest.mark.parametrize("label,base,over,noise", CASES, ids=[c[0] for c in CASES])
+def test_backward_matches_oracle(label, base, over, noise):
+    cfg = si.CONFIGS[base].replace(**over)
+    inp = si.layer_inputs(cfg, seed=21)
+    if noise:
+        inp["noise"] = si.router_noise(cfg, seed=21, std=noise)
+    dinp = device_inputs(inp)
+    dy = si.normal(cfg.T * cfg.d, 21, 30, dtype=si.BF16).reshape(cfg.T, cfg.d)
+    fwd = run(cfg, dinp)                               # the GPU's own logits
+    gl = fwd.router_logits.cpu().numpy().astype(np.float64)
+    g = moe.backward(cfg, dinp["x"], dinp["W_g"], dinp["b_g"], dinp["W1"], dinp["b1"], dinp["W2"], dinp["b2"],
+                     dinp["W3"], device_inputs({"dy": dy})["dy"], dL_aux=1.0, router_noise=dinp.get("noise"))
+    assert moe.check_device_errors(g.workspace) == 0
+    ref = oracle.backward(cfg, inp, si.as_f32(dy).astype(np.float64), 1.0, logits=gl)
+    for name in ("dx", "dW_g", "db_g", "dW1", "db1", "dW2", "db2", "dW3"):
+        if getattr(g, name) is None:          # the layer has no such parameter
+            continue
+        loose = name in ("dW_g", "db_g") and cfg.T < FEW_TOKENS
+        _close(name, getattr(g, name), ref[name], *((5e-2, 2.5e-1) if loose else ()))
+    if cfg.capacity_factor > 0:
+        assert ref["routing"]["dropped"].sum() > 0
+
+
+def test_backward_is_deterministic():
+    cfg = si.CONFIGS["deepseek_shared_sigmoid_bf16"].replace(T=300, d=512, f=320)
+    dinp = device_inputs(si.layer_inputs(cfg, seed=22))
+    dy = device_inputs({"dy": si.normal(cfg.T * cfg.d, 22, 30, dtype=si.BF16).reshape(cfg.T, cfg.d)})["dy"]
+    args = [dinp[n] for n in ("x", "W_g", "b_g", "W1", "b1", "W2", "b2", "W3")]
+    a = moe.backward(cfg, *args, dy)
+    b = moe.backward(cfg, *args, dy)
+    torch.cuda.synchronize()
+    for name in ("dx", "dW_g", "dW1", "dW2", "dW3"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+def test_backward_empty_batch_gives_zero_weight_gradients():
+    cfg = si.CONFIGS["gpt2_top2_gelu_bf16"].replace(T=0, d=128, f=128)
+    inp = si.layer_inputs(cfg.replace(T=1), seed=23)
+    dinp = device_inputs(inp)
+    x = dinp["x"][:0]
+    g = moe.backward(cfg, x, dinp["W_g"], dinp["b_g"], dinp["W1"], dinp["b1"], dinp["W2"], dinp["b2"], None, x)
+    torch.cuda.synchronize()
+    for name in ("dW_g", "db_g", "dW1", "db1", "dW2", "db2"):
+        assert torch.all(getattr(g, name) == 0), name
