@@ -241,6 +241,53 @@ def run_reference(args, cfg):
 
 
 # ---------------------------------------------------------------------------------------------
+# backward pass
+
+
+def run_backward(args, cfg, d, dev, world, rank, local):
+    """Times moe_backward (the forward recomputed inside, then all gradients) on
+    the same workload; prints one JSON line with tokens/s of the training step
+    and the GEMM throughput (forward 2 A d f m + backward 2 A d f (2 m - 1))."""
+    import torch
+    import sparse_mixture_experts_48_b300 as moe
+    dy = d["x"].clone()                       # any [T, d] bf16 upstream gradient
+    args_in = [d[n] for n in ("x", "W_g", "b_g", "W1", "b1", "W2", "b2", "W3")]
+    g = moe.backward(cfg, *args_in, dy)
+    ws = g.workspace
+    for _ in range(args.warmup):
+        moe.backward(cfg, *args_in, dy, workspace=ws)
+    if moe.check_device_errors(ws) != 0:
+        raise SystemExit("device error in the backward warm-up")
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record()
+        for _ in range(args.steps):
+            moe.backward(cfg, *args_in, dy, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+    if moe.check_device_errors(ws) != 0:
+        raise SystemExit("device error in the backward timed region")
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev, world)
+    fwd = moe.forward(cfg, *args_in)
+    torch.cuda.synchronize()
+    rows_A = int(fwd.expert_counts.sum().item()) + cfg.S * cfg.T
+    m = cfg.n_mats
+    flop = 2.0 * rows_A * cfg.d * cfg.f * m + 2.0 * rows_A * cfg.d * cfg.f * (2 * m - 1)
+    peaks, kind = load_peaks()
+    tf = flop / (ms / 1e3) / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": "MoE-layer backward (forward recomputation + gradients) tokens/s on 1 B300",
+            "value": replica_throughput(cfg.T, ms, world), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_desc(cfg), "T": cfg.T},
+            "gemm_flop_per_step": flop, "gemm_tflops": round(tf, 1),
+            "frac_of_bf16_sustained": round(tf / float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])), 4),
+            "peak_source": kind, "clocks": clocks.summary()}), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
 
 
 def main():
@@ -257,6 +304,8 @@ def main():
                     help="add seeded Gaussian router noise of this std before gating and top-k (0: none)")
     ap.add_argument("--expert-choice", action="store_true",
                     help="expert-choice routing: each expert takes its C = ceil(T k / E) best tokens")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (moe_backward: forward recomputation + gradients) instead")
     ap.add_argument("--gemm-one-cta", action="store_true",
                     help="bf16 expert GEMMs on the one-CTA tile kernel instead of the CTA-pair kernel")
     args = ap.parse_args()
@@ -301,6 +350,8 @@ def main():
     d = {k: to_dev(v) for k, v in inp.items()}
     args_in = [d[n] for n in ("x", "W_g", "b_g", "W1", "b1", "W2", "b2", "W3")]
     noise = to_dev(si.router_noise(cfg, seed=rank, std=args.noise_std)) if args.noise_std > 0 else None
+    if args.backward:
+        return run_backward(args, cfg, d, dev, world, rank, local)
     out = moe.alloc_outputs(cfg, dev)
     ws = moe.alloc_workspace(cfg, dev)
     stream = torch.cuda.current_stream()

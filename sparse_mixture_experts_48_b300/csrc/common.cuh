@@ -67,6 +67,21 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
   return *reinterpret_cast<uint16_t*>(&h);
 }
 
+// 32 consecutive bf16 at p (64 bytes, 16-byte aligned) -> fp32, four 16-byte loads.
+__device__ __forceinline__ void load_bf16x32(const uint16_t* p, float (&f)[32]) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = q[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      f[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
 }

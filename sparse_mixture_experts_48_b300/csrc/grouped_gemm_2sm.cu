@@ -335,9 +335,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
             if (bias) {
-              const uint16_t* bp = bias + (int64_t)wslab * a.N + col0;
+              float bv[32];
+              load_bf16x32(bias + (int64_t)wslab * a.N + col0, bv);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) f[i] += bf16_bits_to_f32(bp[i]);
+              for (int i = 0; i < 32; ++i) f[i] += bv[i];
             }
             if (SAVE_PRE) {
               uint32_t fb[32];

@@ -334,23 +334,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!valid || col0 >= a.N) continue;
         if (MODE == kDgradAct) {
           // dH -> dA (and dU) from the saved pre-activations.
-          const uint16_t* pa = (const uint16_t*)a.pre_a + orow * a.N + col0;
+          // Row offsets are multiples of N (a multiple of 64) and col0 of 32:
+          // the 32 pre-activations are 64 aligned bytes, four vector loads.
+          float av[32];
+          load_bf16x32((const uint16_t*)a.pre_a + orow * a.N + col0, av);
           uint32_t da[32], du[32];
           if (a.act == MOE_ACT_SWIGLU) {
-            const uint16_t* pu = (const uint16_t*)a.pre_u + orow * a.N + col0;
+            float uv[32];
+            load_bf16x32((const uint16_t*)a.pre_u + orow * a.N + col0, uv);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float dh = __uint_as_float(v[i]);
-              const float av = bf16_bits_to_f32(pa[i]), uv = bf16_bits_to_f32(pu[i]);
-              da[i] = __float_as_uint(dh * uv * silu_grad(av));
-              du[i] = __float_as_uint(dh * silu(av));
+              da[i] = __float_as_uint(dh * uv[i] * silu_grad(av[i]));
+              du[i] = __float_as_uint(dh * silu(av[i]));
             }
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float dh = __uint_as_float(v[i]);
-              const float av = bf16_bits_to_f32(pa[i]);
-              const float gr = a.act == MOE_ACT_RELU ? (av > 0.f ? 1.f : 0.f) : gelu_grad(av);
+              const float gr = a.act == MOE_ACT_RELU ? (av[i] > 0.f ? 1.f : 0.f) : gelu_grad(av[i]);
               da[i] = __float_as_uint(dh * gr);
             }
           }

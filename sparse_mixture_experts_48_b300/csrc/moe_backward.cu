@@ -10,7 +10,8 @@
 //                the selected sigmoids) plus the L_aux term through P
 //                (dp_te = dL_aux alpha E f_e / T).
 //   dx           per token: sum of the grouped-row gradients of its kept
-//                assignments and shared experts, plus dl_t W_g^T.
+//                assignments and shared experts, plus dl_t W_g^T (8 tokens
+//                per warp share the W_g rows).
 //   dWg          x^T dl and sum_t dl, in T-chunks, then the chunks in order.
 //   colsum       bias gradients: column sums of dO / dA over a segment.
 //   pad_zero     the padding rows of a grouped buffer (segments padded to
@@ -129,37 +130,88 @@ __global__ void router_bwd_kernel(RouterBwdArgs a) {
 }
 
 // ---- dx ---------------------------------------------------------------------------
+// A warp handles kDxTok consecutive tokens, so every W_g row it loads (for the
+// dl W_g^T term) serves all of them; a lane owns 4 consecutive columns.
 constexpr int kMaxE = 256;
 
+template <int kDxTok>
 __global__ void __launch_bounds__(kWarps * 32) dx_kernel(DxArgs a) {
-  __shared__ float s_dl[kWarps][kMaxE];
+  __shared__ float s_dl[kWarps][kDxTok][kMaxE];
+  __shared__ int s_slot[kWarps][kDxTok][8];
   const int lane = threadIdx.x % 32, wl = threadIdx.x / 32;
-  const int64_t t = (int64_t)blockIdx.x * kWarps + wl;
-  if (t >= a.T || *(volatile const uint32_t*)a.err != 0u) return;
+  const int64_t t0 = ((int64_t)blockIdx.x * kWarps + wl) * kDxTok;
+  if (t0 >= a.T || *(volatile const uint32_t*)a.err != 0u) return;
   const int d = a.d, k = a.k, E = a.E;
-  for (int e = lane; e < E; e += 32) s_dl[wl][e] = a.dl[t * E + e];
+  const int nt = a.T - t0 < kDxTok ? (int)(a.T - t0) : kDxTok;
+  for (int i = lane; i < kDxTok * E; i += 32) {
+    const int tt = i / E, e = i % E;
+    s_dl[wl][tt][e] = tt < nt ? a.dl[(t0 + tt) * E + e] : 0.f;
+  }
+  for (int i = lane; i < kDxTok * 8; i += 32) {
+    const int tt = i / 8, j = i % 8;
+    s_slot[wl][tt][j] = (tt < nt && j < k) ? a.slot[(t0 + tt) * k + j] : -1;
+  }
   __syncwarp();
-  int slots[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) slots[j] = j < k ? a.slot[t * k + j] : -1;
   const uint16_t* Wg = (const uint16_t*)a.Wg;
-  for (int c = lane; c < d; c += 32) {
-    float acc = 0.f;
+  const bool wvec = (E % 8) == 0;   // rows of W_g in 16-byte pieces
+  for (int c = 4 * lane; c < d; c += 128) {
+    float r[kDxTok][4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (slots[j] >= 0) acc += a.dxp[(int64_t)slots[j] * d + c];
-    for (int s = 0; s < a.S; ++s) acc += a.dxp[(a.rows_routed + (int64_t)s * a.shared_stride + t) * d + c];
-    float r = 0.f;
-    for (int e = 0; e < E; ++e) r = fmaf(s_dl[wl][e], bf16_bits_to_f32(Wg[(int64_t)c * E + e]), r);
-    a.dx[t * d + c] = acc + r;
+    for (int tt = 0; tt < kDxTok; ++tt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) r[tt][q] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint16_t* wr = Wg + (int64_t)(c + q) * E;
+      for (int e0 = 0; e0 < E; e0 += 8) {
+        float wv[8];
+        if (wvec) {
+          const uint4 w = *reinterpret_cast<const uint4*>(wr + e0);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            wv[2 * j] = __uint_as_float(ww[j] << 16);
+            wv[2 * j + 1] = __uint_as_float(ww[j] & 0xffff0000u);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) wv[j] = e0 + j < E ? bf16_bits_to_f32(wr[e0 + j]) : 0.f;
+        }
+#pragma unroll
+        for (int tt = 0; tt < kDxTok; ++tt)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (e0 + j < E) r[tt][q] = fmaf(s_dl[wl][tt][e0 + j], wv[j], r[tt][q]);
+      }
+    }
+    for (int tt = 0; tt < nt; ++tt) {
+      const int64_t t = t0 + tt;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int sl = s_slot[wl][tt][j];
+        if (sl >= 0) {
+          const float4 v = *reinterpret_cast<const float4*>(a.dxp + (int64_t)sl * d + c);
+          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+      }
+      for (int s = 0; s < a.S; ++s) {
+        const float4 v =
+            *reinterpret_cast<const float4*>(a.dxp + (a.rows_routed + (int64_t)s * a.shared_stride + t) * d + c);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      *reinterpret_cast<float4*>(a.dx + t * d + c) =
+          make_float4(acc.x + r[tt][0], acc.y + r[tt][1], acc.z + r[tt][2], acc.w + r[tt][3]);
+    }
   }
 }
 
 // ---- dW_g, db_g -------------------------------------------------------------------
 constexpr int kDwgChunk = 256;   // tokens per chunk
-constexpr int kDwgEB = 8;        // experts per pass
 
 // part[chunk][i][e] = sum_{t in chunk} x[t][i] dl[t][e];  bpart[chunk][e] = sum_{t in chunk} dl[t][e]
+// kDwgEB experts per pass over the chunk.
+template <int kDwgEB>
 __global__ void dwg_partial_kernel(DwgArgs a) {
   __shared__ float s_dl[kDwgChunk][kDwgEB];
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -243,14 +295,26 @@ cudaError_t launch_router_bwd(const RouterBwdArgs& a, cudaStream_t s) {
 cudaError_t launch_dx(const DxArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
   if (a.E > kMaxE || a.k > 8) return cudaErrorInvalidValue;
-  dx_kernel<<<(unsigned)((a.T + kWarps - 1) / kWarps), kWarps * 32, 0, s>>>(a);
+  // Many experts make the dl W_g^T term heavy: 8 tokens per warp share the
+  // W_g rows; with few experts one token per warp keeps more warps busy.
+  if (a.E > 16) {
+    const int64_t per_cta = (int64_t)kWarps * 8;
+    dx_kernel<8><<<(unsigned)((a.T + per_cta - 1) / per_cta), kWarps * 32, 0, s>>>(a);
+  } else {
+    dx_kernel<1><<<(unsigned)((a.T + kWarps - 1) / kWarps), kWarps * 32, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 int64_t dwg_chunks(int64_t T) { return (T + kDwgChunk - 1) / kDwgChunk; }
 cudaError_t launch_dwg(const DwgArgs& a, cudaStream_t s) {
   if (a.T > 0) {
     dim3 grid((unsigned)((a.d + 127) / 128), (unsigned)a.nchunk);
-    dwg_partial_kernel<<<grid, 128, 0, s>>>(a);
+    if (a.E <= 8)
+      dwg_partial_kernel<8><<<grid, 128, 0, s>>>(a);
+    else if (a.E <= 16)
+      dwg_partial_kernel<16><<<grid, 128, 0, s>>>(a);
+    else
+      dwg_partial_kernel<32><<<grid, 128, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
