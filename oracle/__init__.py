@@ -11,6 +11,9 @@ order the pages give them:
   -> capacity / drops / grouped order -> expert FFNs + gate-weighted sum (+
   shared experts) -> balance statistics f, P, L_aux.
 
+``fp8_forward`` runs the same layer with E4M3 expert weights and activations
+(per-output-unit weight scales, per-row activation scales) for the FP8 path.
+
 Every function takes the STORED input values (fp32 arrays, or uint16 arrays
 of bf16 bits) and widens them to double itself.
 """
@@ -70,6 +73,14 @@ def _L() -> ctypes.CDLL:
         lib.oracle_ec_select.argtypes = [i64, i32, i64, vp, vp]
         lib.oracle_ec_layer_rows.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, vp, i64, vp, vp, vp, vp, vp,
                                              vp, vp, vp, vp]
+        u8 = ctypes.c_uint8
+        lib.oracle_bf16_round.restype = dbl
+        lib.oracle_bf16_round.argtypes = [dbl]
+        lib.oracle_e4m3_value.restype = dbl
+        lib.oracle_e4m3_value.argtypes = [u8]
+        lib.oracle_e4m3_encode.argtypes = [i64, vp, vp]
+        lib.oracle_quantize_rows.argtypes = [i64, i64, vp, vp, vp]
+        lib.oracle_fp8_layer_rows.argtypes = [i32, i32, i32, i32, i32, i32, vp, i64] + [vp] * 14
         _lib = lib
     return _lib
 
@@ -314,4 +325,97 @@ def backward(cfg, inp: Dict, dy: np.ndarray, dL_aux: float = 1.0,
                          _p(dyc), _p(out["dx"]), _p(out["dW_g"]), _p(out["db_g"]), _p(out["dW1"]), _p(out["db1"]),
                          _p(out["dW2"]), _p(out["db2"]), _p(out["dW3"]))
     out["routing"] = r
+    return out
+
+
+# ---- FP8 (E4M3) experts ----------------------------------------------------------
+
+def _as_f32_values(a: np.ndarray) -> np.ndarray:
+    """Stored values as fp32 (bf16 bits widen exactly)."""
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32)
+    return np.ascontiguousarray(a, np.float32)
+
+
+def bf16_round(v: float) -> float:
+    """Nearest bf16 value (ties to even) of a double."""
+    return float(_L().oracle_bf16_round(float(v)))
+
+
+def e4m3_value(code: int) -> float:
+    return float(_L().oracle_e4m3_value(int(code)))
+
+
+def e4m3_values(codes: np.ndarray) -> np.ndarray:
+    table = np.array([e4m3_value(c) for c in range(256)], np.float64)
+    return table[np.asarray(codes, np.uint8)]
+
+
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    """fp32 values -> E4M3 codes (nearest, ties to even, saturating at 448)."""
+    x = np.ascontiguousarray(v, np.float32)
+    q = np.empty(x.shape, np.uint8)
+    _L().oracle_e4m3_encode(x.size, _p(x), _p(q))
+    return q
+
+
+def quantize_rows(v: np.ndarray):
+    """Per-row E4M3 quantisation of a [rows, cols] matrix of stored values (fp32,
+    or uint16 bf16 bits): (codes uint8 [rows, cols], decoding scales fp32 [rows])."""
+    x = np.ascontiguousarray(_as_f32_values(np.asarray(v)))
+    if x.ndim == 1:
+        x = x.reshape(1, -1)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty(rows, np.float32)
+    _L().oracle_quantize_rows(rows, cols, _p(x), _p(q), _p(s))
+    return q, s
+
+
+def quantize_weights(W: np.ndarray):
+    """Stacked [G, in, out] weights -> (codes [G, out, in], scales [G, out]): one
+    scale per output unit of each expert."""
+    G, K, N = W.shape
+    Wt = np.ascontiguousarray(np.swapaxes(_as_f32_values(W), 1, 2)).reshape(G * N, K)
+    q, s = quantize_rows(Wt)
+    return q.reshape(G, N, K), s.reshape(G, N)
+
+
+def quantize_experts(cfg, inp: Dict) -> Dict[str, np.ndarray]:
+    out = {}
+    out["W1q"], out["s1"] = quantize_weights(inp["W1"])
+    out["W2q"], out["s2"] = quantize_weights(inp["W2"])
+    if inp.get("W3") is not None:
+        out["W3q"], out["s3"] = quantize_weights(inp["W3"])
+    return out
+
+
+def fp8_forward(cfg, inp: Dict, rows: Optional[Sequence[int]] = None, logits: Optional[np.ndarray] = None,
+                wq: Optional[Dict[str, np.ndarray]] = None) -> Dict[str, np.ndarray]:
+    """The layer with FP8 experts: routing, statistics and gate weights exactly as
+    ``forward`` (on the bf16 inputs); the expert FFNs on per-token quantised x,
+    per-(expert, output unit) quantised weights (``wq``: the oracle's own
+    ``quantize_experts`` when None) and per-row quantised h."""
+    own = router_logits(inp["x"], inp["W_g"], inp["b_g"], cfg.dtype) if logits is None else None
+    if own is not None and inp.get("noise") is not None:
+        own = add_noise(own, inp["noise"])
+    lg = own if logits is None else np.ascontiguousarray(logits, np.float64)
+    out = routing(cfg, lg)
+    out["logits"] = lg
+    wq = quantize_experts(cfg, inp) if wq is None else wq
+    xq, xs = quantize_rows(inp["x"])
+    rows = np.arange(cfg.T) if rows is None else np.asarray(rows, np.int64)
+    rows = np.ascontiguousarray(rows, np.int64)
+    out["rows"] = rows
+    y = np.empty((rows.size, cfg.d), np.float64)
+    b1 = None if inp.get("b1") is None else np.ascontiguousarray(_as_f32_values(inp["b1"]))
+    b2 = None if inp.get("b2") is None else np.ascontiguousarray(_as_f32_values(inp["b2"]))
+    _L().oracle_fp8_layer_rows(cfg.d, cfg.f, cfg.E, cfg.k, cfg.S, cfg.act, _p(rows), rows.size, _p(xq), _p(xs),
+                               _p(wq["W1q"]), _p(wq["s1"]), _p(wq.get("W3q")), _p(wq.get("s3")), _p(b1),
+                               _p(wq["W2q"]), _p(wq["s2"]), _p(b2),
+                               _p(np.ascontiguousarray(out["topk_idx"], np.int32)),
+                               _p(np.ascontiguousarray(out["topk_w"], np.float64)),
+                               _p(np.ascontiguousarray(out["dropped"], np.uint8)), _p(y))
+    out["y"] = y
+    out["xq"], out["xs"] = xq, xs
     return out

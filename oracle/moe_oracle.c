@@ -550,3 +550,150 @@ void oracle_backward(int64_t T, int d, int f, int E, int k, int S, int act, int 
   }
   free(xr); free(a); free(u); free(h); free(dh); free(da); free(du); free(o); free(p); free(dl); free(dp); free(dw);
 }
+
+/* ---- FP8 (E4M3) experts ---------------------------------------------------------
+ * ["MoE混合专家模型：Transformer稀疏前馈网络原理与PyTorch实现" §5.2: the expert
+ * parameters are quantised from 16-bit to 8-bit floats, which halves their memory
+ * at a usually acceptable loss of quality.]  The pages name the format only.
+ * Readings:
+ *  - the 8-bit format is E4M3 (1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ *    bits, subnormals, no infinities, largest finite value 448, S.1111.111 NaN);
+ *  - encoding rounds to the nearest value, ties to the even mantissa, and
+ *    saturates at +-448;
+ *  - a vector v has one scale pair: a = max(max_i |v_i|, 2^-60), the encoding
+ *    factor r = fl32(448 / a) and the decoding scale s = fl32(a / 448);
+ *    q_i = e4m3(fl32(v_i * r)), decoded value s * value(q_i);
+ *  - weights: one vector per (expert, output unit), i.e. per column of the
+ *    [in, out] slab, stored transposed as [out, in]; activations: one vector per
+ *    row of x and per row of the hidden activations h;
+ *  - the products of the expert GEMMs are exact and summed in fp64 here; the
+ *    scales multiply the sum; h is rounded to bf16 (nearest, ties to even)
+ *    before its quantisation, as it is held in bf16 between the two GEMMs. */
+static double round_bits(double v, int sig_bits, int min_exp) {
+  /* nearest value with sig_bits significant bits (ties to even); quantum never
+   * below 2^min_exp */
+  if (v == 0.0 || isnan(v)) return v;
+  int e;
+  frexp(v, &e);                       /* |v| in [2^(e-1), 2^e) */
+  int qe = e - sig_bits;
+  if (qe < min_exp) qe = min_exp;
+  return ldexp(rint(ldexp(v, -qe)), qe);   /* rint: ties to even in the default mode */
+}
+
+double oracle_bf16_round(double v) { return round_bits(v, 8, -133); }
+
+double oracle_e4m3_value(uint8_t c) {
+  const int E = (c >> 3) & 15, m = c & 7;
+  if (E == 15 && m == 7) return NAN;
+  const double v = E == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), E - 10);
+  return (c & 0x80) ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode1(float x) {
+  const double v = x;
+  if (isnan(v)) return 0x7F;
+  const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  double a = fabs(v);
+  if (a >= 448.0) return sign | 0x7E;                 /* saturate */
+  a = round_bits(a, 4, -9);                            /* 4 significant bits; subnormal quantum 2^-9 */
+  if (a >= 448.0) return sign | 0x7E;
+  if (a == 0.0) return sign;
+  if (a < ldexp(1.0, -6)) return sign | (uint8_t)ldexp(a, 9);        /* subnormal: m * 2^-9 */
+  int e;
+  const double fr = frexp(a, &e);                      /* a = (2 fr) 2^(e-1), 2 fr in [1, 2) */
+  const int E = e - 1 + 7, m = (int)((2.0 * fr - 1.0) * 8.0);
+  return sign | (uint8_t)(E << 3) | (uint8_t)m;
+}
+
+void oracle_e4m3_encode(int64_t n, const float* x, uint8_t* q) {
+  for (int64_t i = 0; i < n; ++i) q[i] = oracle_e4m3_encode1(x[i]);
+}
+
+void oracle_quantize_rows(int64_t rows, int64_t cols, const float* v, uint8_t* q, float* s) {
+  const float floor_a = (float)ldexp(1.0, -60);
+  for (int64_t r = 0; r < rows; ++r) {
+    const float* vr = v + r * cols;
+    float a = 0.0f;
+    for (int64_t i = 0; i < cols; ++i) {
+      const float m = fabsf(vr[i]);
+      if (m > a) a = m;
+    }
+    if (a < floor_a) a = floor_a;
+    const float rr = 448.0f / a;
+    const float ss = a / 448.0f;
+    for (int64_t i = 0; i < cols; ++i) {
+      const float p = vr[i] * rr;
+      q[r * cols + i] = oracle_e4m3_encode1(p);
+    }
+    s[r] = ss;
+  }
+}
+
+/* Expert g on one quantised row xq (scale xs): o = W2-GEMM of the quantised h.
+ * Weights: Wq [G, out, in] e4m3 with scales [G, out]; biases fp32 or NULL. */
+void oracle_fp8_expert_ffn(int d, int f, int act, int g, const uint8_t* xq, float xs, const uint8_t* W1q,
+                           const float* s1, const uint8_t* W3q, const float* s3, const float* b1,
+                           const uint8_t* W2q, const float* s2, const float* b2, double* out) {
+  double* xv = (double*)malloc(sizeof(double) * (size_t)d);
+  float* hb = (float*)malloc(sizeof(float) * (size_t)f);
+  uint8_t* hq = (uint8_t*)malloc((size_t)f);
+  double* hv = (double*)malloc(sizeof(double) * (size_t)f);
+  for (int i = 0; i < d; ++i) xv[i] = oracle_e4m3_value(xq[i]);
+  for (int j = 0; j < f; ++j) {
+    const uint8_t* w1 = W1q + ((int64_t)g * f + j) * d;
+    double acc = 0.0;
+    for (int i = 0; i < d; ++i) acc += xv[i] * oracle_e4m3_value(w1[i]);
+    double a = (double)xs * (double)s1[(int64_t)g * f + j] * acc;
+    double h;
+    if (act == OACT_SWIGLU) {
+      const uint8_t* w3 = W3q + ((int64_t)g * f + j) * d;
+      double acc3 = 0.0;
+      for (int i = 0; i < d; ++i) acc3 += xv[i] * oracle_e4m3_value(w3[i]);
+      const double u = (double)xs * (double)s3[(int64_t)g * f + j] * acc3;
+      h = oracle_act(OACT_SWIGLU, a) * u;
+    } else {
+      if (b1) a += (double)b1[(int64_t)g * f + j];
+      h = oracle_act(act, a);
+    }
+    hb[j] = (float)oracle_bf16_round(h);    /* exact in fp32 */
+  }
+  float hs;
+  oracle_quantize_rows(1, f, hb, hq, &hs);
+  for (int j = 0; j < f; ++j) hv[j] = oracle_e4m3_value(hq[j]);
+  for (int c = 0; c < d; ++c) {
+    const uint8_t* w2 = W2q + ((int64_t)g * d + c) * f;
+    double acc = 0.0;
+    for (int j = 0; j < f; ++j) acc += hv[j] * oracle_e4m3_value(w2[j]);
+    out[c] = (double)hs * (double)s2[(int64_t)g * d + c] * acc;
+    if (b2 && act != OACT_SWIGLU) out[c] += (double)b2[(int64_t)g * d + c];
+  }
+  free(xv);
+  free(hb);
+  free(hq);
+  free(hv);
+}
+
+/* The layer output of the listed token rows with FP8 experts: x quantised per
+ * token row (xq [T, d], xs [T]), then as oracle_layer_rows. */
+void oracle_fp8_layer_rows(int d, int f, int E, int k, int S, int act, const int64_t* rows, int64_t nrows,
+                           const uint8_t* xq, const float* xs, const uint8_t* W1q, const float* s1,
+                           const uint8_t* W3q, const float* s3, const float* b1, const uint8_t* W2q,
+                           const float* s2, const float* b2, const int32_t* idx, const double* w,
+                           const uint8_t* dropped, double* y) {
+  double* o = (double*)malloc(sizeof(double) * (size_t)d);
+  for (int64_t r = 0; r < nrows; ++r) {
+    const int64_t t = rows[r];
+    double* yr = y + r * d;
+    for (int i = 0; i < d; ++i) yr[i] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      if (dropped[t * k + j]) continue;
+      oracle_fp8_expert_ffn(d, f, act, idx[t * k + j], xq + t * d, xs[t], W1q, s1, W3q, s3, b1, W2q, s2, b2, o);
+      for (int i = 0; i < d; ++i) yr[i] += w[t * k + j] * o[i];
+    }
+    for (int s = 0; s < S; ++s) {
+      oracle_fp8_expert_ffn(d, f, act, E + s, xq + t * d, xs[t], W1q, s1, W3q, s3, b1, W2q, s2, b2, o);
+      for (int i = 0; i < d; ++i) yr[i] += o[i];
+    }
+  }
+  free(o);
+}
