@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--T TOKENS] [--no-cpu] [--no-e2e]
+                    [--noise-std S] [--expert-choice] [--backward] [--fp8] [--gemm-one-cta]
 
 A step is one whole forward pass of the layer (router, scan, gather, expert
 GEMM 1, expert GEMM 2, combine) over one batch of T synthetic tokens.  The
@@ -36,6 +37,7 @@ sys.path.insert(0, ROOT)
 import seeded_inputs as si  # noqa: E402
 
 METRIC = "MoE-layer tokens/s on 1 B300; grouped-GEMM TFLOPS as % of bf16 peak"
+METRIC_FP8 = "MoE-layer tokens/s on 1 B300 with FP8 (E4M3) experts; grouped-GEMM TFLOPS as % of fp8 peak"
 DEFAULT_WORKLOAD = "mixtral_swiglu_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
@@ -68,12 +70,19 @@ def algorithmic(cfg, rows_A: int):
     # token choice reads each token's row once and writes it to each kept
     # slot; expert choice reads one x row per grouped row
     gather_read = kept * d * b if getattr(cfg, "expert_choice", False) else T * d * b
-    return {
+    out = {
         "gemm1_flop": g1, "gemm2_flop": g2,
         "router_bytes": T * d * b + d * E * b + T * cfg.k * 8.0,
         "gather_bytes": gather_read + kept * d * b,
         "combine_bytes": rows_A * d * 4.0 + T * d * b,
     }
+    if getattr(cfg, "fp8_experts", False):
+        # x read in bf16, one E4M3 code per element written per kept slot (and
+        # once in token order for the shared experts), one scale per row
+        out["gather_bytes"] = T * d * b + kept * (d + 4.0) + (T * (d + 4.0) if cfg.S else 0.0)
+        # H read in bf16, codes and one scale per row written
+        out["quantize_h_bytes"] = rows_A * (f * 3.0 + 4.0)
+    return out
 
 
 # ---------------------------------------------------------------------------------------------
@@ -308,12 +317,20 @@ def main():
                     help="time the backward pass (moe_backward: forward recomputation + gradients) instead")
     ap.add_argument("--gemm-one-cta", action="store_true",
                     help="bf16 expert GEMMs on the one-CTA tile kernel instead of the CTA-pair kernel")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 (E4M3) expert weights and activations (moe_forward_fp8); the weights are "
+                         "quantised once before the timed region")
     args = ap.parse_args()
     cfg = si.CONFIGS[args.workload]
     if args.T:
         cfg = cfg.replace(T=args.T)
     if args.expert_choice:
         cfg = cfg.replace(expert_choice=True)
+    if args.fp8:
+        if args.expert_choice or args.backward or args.gemm_one_cta or args.impl == "reference":
+            raise SystemExit("--fp8 runs the token-choice forward on the CTA-pair GEMM of our implementation")
+        cfg = cfg.replace(fp8_experts=True)
+        args.no_cpu = True
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
 
@@ -356,11 +373,18 @@ def main():
     ws = moe.alloc_workspace(cfg, dev)
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)] for _ in range(K)]
+    fp8 = args.fp8
+    n_ev = moe.NUM_STAGES + (2 if fp8 else 1)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K)]
+    experts8 = moe.quantize_experts_fp8(d["W1"], d["W2"], d["W3"]) if fp8 else None
 
     def step(i=None):
-        moe.forward(cfg, *args_in, router_noise=noise, out=out, workspace=ws,
-                    stage_events=ev[i] if i is not None else None, gemm_single_cta=args.gemm_one_cta)
+        if fp8:
+            moe.forward_fp8(cfg, d["x"], d["W_g"], d["b_g"], experts8, d["b1"], d["b2"], router_noise=noise,
+                            out=out, workspace=ws, stage_events=ev[i] if i is not None else None)
+        else:
+            moe.forward(cfg, *args_in, router_noise=noise, out=out, workspace=ws,
+                        stage_events=ev[i] if i is not None else None, gemm_single_cta=args.gemm_one_cta)
 
     for _ in range(W):
         step()
@@ -391,8 +415,15 @@ def main():
     ms_step = ms_total / K
     value = replica_throughput(cfg.T, ms_step, world)
 
-    # per-kernel durations from the stage events (on the launching stream)
-    stage_ms = np.array([[ev[i][s].elapsed_time(ev[i][s + 1]) for s in range(moe.NUM_STAGES)] for i in range(K)])
+    # per-kernel durations from the stage events (on the launching stream);
+    # with FP8 experts event 7 splits [4, 5) into the H quantisation and GEMM 2
+    if fp8:
+        spans = [(0, 1), (1, 2), (2, 3), (3, 4), (7, 5), (5, 6), (4, 7)]
+        names = list(moe.STAGE_NAMES) + ["quantize_h"]
+    else:
+        spans = [(s, s + 1) for s in range(moe.NUM_STAGES)]
+        names = list(moe.STAGE_NAMES)
+    stage_ms = np.array([[ev[i][a].elapsed_time(ev[i][b]) for a, b in spans] for i in range(K)])
     stage_avg = stage_ms.mean(axis=0)
     rows_A = int(out.expert_counts.sum().item()) + cfg.S * cfg.T
     alg = algorithmic(cfg, rows_A)
@@ -400,24 +431,35 @@ def main():
     hbm = float(peaks["hbm_gbs"])
     tc_burst = float(peaks["bf16_tflops"])
     tc_sust = float(peaks.get("bf16_tflops_sustained", tc_burst))
+    tc_tag = "bf16"
+    if fp8:
+        # E4M3 tensor-core peak: the measured bf16 figures times the nominal
+        # dense ratio 4.5 / 2.25 PFLOP/s
+        tc_burst, tc_sust, tc_tag = 2.0 * tc_burst, 2.0 * tc_sust, "fp8"
     kernels = {}
-    for s, name in enumerate(moe.STAGE_NAMES):
+    for s, name in enumerate(names):
         kernels[name] = {"ms": round(float(stage_avg[s]), 5)}
-    for name, key in (("router", "router_bytes"), ("gather", "gather_bytes"), ("combine", "combine_bytes")):
-        gbs = alg[key] / (stage_avg[moe.STAGE_NAMES.index(name)] / 1e3) / 1e9
+    hbm_kernels = [("router", "router_bytes"), ("gather", "gather_bytes"), ("combine", "combine_bytes")]
+    if fp8:
+        hbm_kernels.append(("quantize_h", "quantize_h_bytes"))
+    for name, key in hbm_kernels:
+        gbs = alg[key] / (stage_avg[names.index(name)] / 1e3) / 1e9
         kernels[name].update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4), "bytes": alg[key]})
     for name, key in (("expert_gemm1", "gemm1_flop"), ("expert_gemm2", "gemm2_flop")):
-        tf = alg[key] / (stage_avg[moe.STAGE_NAMES.index(name)] / 1e3) / 1e12
-        kernels[name].update({"TFLOP/s": round(tf, 1), "frac_bf16_sustained": round(tf / tc_sust, 4),
-                              "frac_bf16_burst": round(tf / tc_burst, 4), "flop": alg[key]})
+        tf = alg[key] / (stage_avg[names.index(name)] / 1e3) / 1e12
+        kernels[name].update({"TFLOP/s": round(tf, 1), f"frac_{tc_tag}_sustained": round(tf / tc_sust, 4),
+                              f"frac_{tc_tag}_burst": round(tf / tc_burst, 4), "flop": alg[key]})
     gemm_ms = stage_avg[3] + stage_avg[4]
     gemm_tf = (alg["gemm1_flop"] + alg["gemm2_flop"]) / (gemm_ms / 1e3) / 1e12
     dom = "expert_gemm1"
     dom_tf = kernels[dom]["TFLOP/s"]
-    traffic = measured_traffic(cfg, dom, args.gemm_one_cta)
+    traffic = None if fp8 else measured_traffic(cfg, dom, args.gemm_one_cta)
+    src = ("measured bf16_tflops_sustained x 2 (nominal E4M3 / bf16 dense ratio)" if fp8 else
+           "measured bf16_tflops_sustained (cuBLAS bf16, back to back)")
+    if peak_kind != "measured":
+        src = src.replace("measured", "fallback")
     roofline = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": tc_sust, "unit": "TFLOP/s",
-                "frac": round(dom_tf / tc_sust, 4), "traffic": traffic,
-                "peak_source": f"{peak_kind} bf16_tflops_sustained (cuBLAS bf16, back to back)",
+                "frac": round(dom_tf / tc_sust, 4), "traffic": traffic, "peak_source": src,
                 "frac_of_burst_peak": round(dom_tf / tc_burst, 4)}
 
     # End to end through the public API with host buffers (moe_forward_host):
@@ -435,8 +477,13 @@ def main():
         houts = [moe.alloc_host_outputs(cfg) for _ in range(2)]
 
         def e2e_step(i):
-            moe.forward_host(cfg, x_host, *weights, router_noise_host=noise_host, out=houts[i % 2],
-                             workspace=hws[i % 2], stream=streams[i % 2], gemm_single_cta=args.gemm_one_cta)
+            if fp8:
+                moe.forward_fp8_host(cfg, x_host, d["W_g"], d["b_g"], experts8, d["b1"], d["b2"],
+                                     router_noise_host=noise_host, out=houts[i % 2], workspace=hws[i % 2],
+                                     stream=streams[i % 2])
+            else:
+                moe.forward_host(cfg, x_host, *weights, router_noise_host=noise_host, out=houts[i % 2],
+                                 workspace=hws[i % 2], stream=streams[i % 2], gemm_single_cta=args.gemm_one_cta)
 
         for i in range(W):
             e2e_step(i)
@@ -466,7 +513,8 @@ def main():
                                                          ho.dropped_mask, ho.f, ho.P, ho.L_aux))
         e2e = {"value": replica_throughput(cfg.T, e_ms, world), "unit": "tokens/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "how": "moe_forward_host, pinned host x in / all outputs out every step, 2 streams x 2 workspaces"}
+               "how": ("moe_forward_fp8_host" if fp8 else "moe_forward_host") +
+                      ", pinned host x in / all outputs out every step, 2 streams x 2 workspaces"}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -477,24 +525,27 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+            "metric": METRIC_FP8 if fp8 else METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": W,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if cfg.dtype == si.BF16 else "f32", "data": "synthetic",
+            "dtype": "e4m3" if fp8 else ("bf16" if cfg.dtype == si.BF16 else "f32"), "data": "synthetic",
             "config": {"workload": workload_desc(cfg), "T": cfg.T, "d_model": cfg.d, "d_ff": cfg.f, "E": cfg.E,
                        "k": cfg.k, "n_shared": cfg.S, "parallelism": "replicas" if world > 1 else "single GPU",
                        "expert_gemm": "one-CTA 128x256 tiles" if args.gemm_one_cta else "CTA-pair 256x256 tiles",
                        "router_noise_std": args.noise_std,
                        "routing": "expert choice" if args.expert_choice else "token choice",
+                       "experts": ("FP8 E4M3 weights (one scale per output unit) and activations (one scale "
+                                   "per row); router, x, y in bf16" if fp8 else "bf16"),
                        "l2": "no flush: inputs larger than L2 (x %.0f MB, expert weights %.2f GB)" % (
                            inp["x"].nbytes / 1e6, sum(inp[n].nbytes for n in ("W1", "W2", "W3")
                                                       if inp[n] is not None) / 1e9)},
-            "grouped_gemm": {"tflops": round(gemm_tf, 1), "frac_of_bf16_sustained": round(gemm_tf / tc_sust, 4),
-                             "frac_of_bf16_burst": round(gemm_tf / tc_burst, 4), "ms": round(float(gemm_ms), 4)},
+            "grouped_gemm": {"tflops": round(gemm_tf, 1), f"frac_of_{tc_tag}_sustained": round(gemm_tf / tc_sust, 4),
+                             f"frac_of_{tc_tag}_burst": round(gemm_tf / tc_burst, 4), "ms": round(float(gemm_ms), 4)},
             "roofline": roofline,
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": moe.NUM_STAGES * K,
+            "gpu_launches": (moe.NUM_STAGES + (1 if fp8 else 0)) * K,
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)

@@ -114,13 +114,21 @@ typedef struct {
  * experts chose on.  topk_idx, topk_w, dropped_mask and slot are not used
  * (may be NULL). */
 #define MOE_FLAG_EXPERT_CHOICE 2
+/* FP8 experts: the expert weights are E4M3 codes with scales (moe_fp8_experts,
+ * made by moe_quantize_weights_fp8) and the layer runs through
+ * moe_forward_fp8; moe_workspace_size then sizes that call's workspace.
+ * Needs dtype == MOE_DT_BF16 (x, y, W_g, b1, b2 stay bf16) and token choice. */
+#define MOE_FLAG_FP8_EXPERTS 4
 
 /* Launch options; pass NULL for defaults. */
 typedef struct {
   /* If non-NULL: created events recorded on `stream` around the kernels.
    * moe_forward: MOE_NUM_STAGES + 1 events; event i just before stage i,
-   * event MOE_NUM_STAGES after the last.  moe_grouped_gemm: 2 events, before
-   * and after the GEMM kernel. */
+   * event MOE_NUM_STAGES after the last.  moe_forward_fp8: MOE_NUM_STAGES + 2
+   * events; the extra one (index MOE_NUM_STAGES + 1) is recorded after the
+   * hidden activations' quantisation, between events 4 and 5 (so [4, 7) is
+   * that kernel and [7, 5) the second expert GEMM).  moe_grouped_gemm: 2
+   * events, before and after the GEMM kernel. */
   moe_event* stage_events;
   /* Limit of every device-side wait in nanoseconds; 0 = 2 s.  A wait that
    * runs out makes the kernel stop cleanly and records MOE_ERR_TIMEOUT. */
@@ -228,6 +236,79 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
                         const void* W3, const void* dy, float dL_aux, float* dx, float* dW_g, float* db_g,
                         float* dW1, float* db1, float* dW2, float* db2, float* dW3, void* workspace,
                         size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts);
+
+/* ---- FP8 (E4M3) experts ---------------------------------------------------------
+ * "MoE混合专家模型：Transformer稀疏前馈网络原理与PyTorch实现" §5.2: expert parameters
+ * quantised from 16-bit to 8-bit floats halve their memory at a usually
+ * acceptable loss of quality.  Format E4M3 (1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits; largest finite 448).  A vector v is quantised with one scale
+ * pair: a = max(max_i |v_i|, 2^-60), encoding factor r = fl32(448 / a), decoding
+ * scale s = fl32(a / 448), codes q_i = e4m3(fl32(v_i r)) rounded to nearest with
+ * ties to even and saturating at +-448; v_i ~ s value(q_i).
+ *
+ * Quantise weight slabs W [G, K, N] (bf16, the layer's [in, out] layout), one
+ * vector per (slab, output column n): codes Wq [G, N, K] (transposed: K-major)
+ * and decoding scales [G, N] fp32.  Device pointers, Wq 16-byte aligned;
+ * K a multiple of 16; G <= 65535.  Asynchronous on `stream`. */
+moe_status moe_quantize_weights_fp8(const void* W, int64_t G, int64_t K, int64_t N, uint8_t* Wq, float* scale,
+                                    moe_stream stream);
+
+/* Quantise the rows of X [rows, cols] (bf16), one vector per row: codes
+ * Q [rows, cols] and decoding scales [rows] fp32.  cols a multiple of 16;
+ * device pointers, 16-byte aligned.  The layer applies this to the hidden
+ * activations between its two expert GEMMs, and to x while grouping it. */
+moe_status moe_quantize_rows_fp8(const void* X, int64_t rows, int64_t cols, uint8_t* Q, float* scale,
+                                 moe_stream stream);
+
+/* FP8 expert weights, all device pointers (slabs: E routed, then S shared). */
+typedef struct {
+  const uint8_t* W1;  /* [E+S, f, d] codes of W1 (moe_quantize_weights_fp8 of [E+S, d, f]) */
+  const float* s1;    /* [E+S, f] */
+  const uint8_t* W3;  /* SwiGLU only, as W1; else NULL */
+  const float* s3;
+  const uint8_t* W2;  /* [E+S, d, f] codes of W2 ([E+S, f, d]) */
+  const float* s2;    /* [E+S, d] */
+} moe_fp8_experts;
+
+/* The layer with FP8 experts (cfg->flags must include MOE_FLAG_FP8_EXPERTS).
+ * Routing, statistics and gate weights are moe_forward's, on the bf16 x and
+ * W_g.  Each token row of x is quantised (one scale per row) while it is
+ * grouped; expert GEMM 1 multiplies E4M3 codes on the tensor cores (fp32
+ * accumulation), scales by the row's and the output unit's decoding scales,
+ * adds b1 (bf16, not with SwiGLU) and applies the activation; the hidden
+ * activations are held in bf16, then quantised per row; expert GEMM 2 the
+ * same with W2 and b2; the combine is moe_forward's (fp32 expert outputs).
+ * Arguments as moe_forward, with the expert weights in `w`.  d and f
+ * multiples of 64. */
+moe_status moe_forward_fp8(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
+                           const float* router_noise, const moe_fp8_experts* w, const void* b1, const void* b2,
+                           void* y, int32_t* topk_idx, float* topk_w, int32_t* expert_counts, uint8_t* dropped_mask,
+                           float* f, float* P, float* L_aux, float* route_stats, float* router_logits,
+                           int32_t* perm_token, int32_t* slot, void* workspace, size_t workspace_bytes,
+                           moe_stream stream, const moe_launch_opts* opts);
+
+/* moe_forward_fp8 with HOST buffers, as moe_forward_host is moe_forward
+ * with host buffers (the FP8 expert weights stay device pointers);
+ * workspace: >= moe_forward_host_workspace_size(cfg) bytes. */
+moe_status moe_forward_fp8_host(const moe_config* cfg, const void* x_host, const void* W_g, const void* b_g,
+                                const float* router_noise_host, const moe_fp8_experts* w, const void* b1,
+                                const void* b2, void* y_host, int32_t* topk_idx_host, float* topk_w_host,
+                                int32_t* expert_counts_host, uint8_t* dropped_mask_host, float* f_host, float* P_host,
+                                float* L_aux_host, float* route_stats_host, void* workspace, size_t workspace_bytes,
+                                moe_stream stream, const moe_launch_opts* opts);
+
+/* Where an intermediate of moe_forward / moe_forward_fp8 lies in the
+ * workspace after a call (for inspection and tests): *offset and *bytes of
+ * region `region` for `cfg`.  MOE_ERR_INVALID_ARG for an invalid cfg or a
+ * region the cfg does not have.  Rows are those of the expert-grouped order
+ * (T*k routed rows, then S*T shared rows). */
+#define MOE_REGION_XPERM 1     /* grouped copy of x [T*k, d]: dtype, or E4M3 codes */
+#define MOE_REGION_X_SCALE 2   /* FP8: decoding scale of each grouped row [T*k] fp32 */
+#define MOE_REGION_H 3         /* hidden activations [T*k + S*T, f] (bf16 with FP8) */
+#define MOE_REGION_H_CODES 4   /* FP8: E4M3 codes of H [T*k + S*T, f] */
+#define MOE_REGION_H_SCALE 5   /* FP8: decoding scale of each row of H [T*k + S*T] fp32 */
+#define MOE_REGION_O 6         /* expert outputs [T*k + S*T, d] fp32 */
+moe_status moe_workspace_region(const moe_config* cfg, int32_t region, size_t* offset, size_t* bytes);
 
 /* Waits for `stream`, then reports the device-side status of the last call
  * that used `workspace`: MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE, or

@@ -81,12 +81,17 @@ def _L() -> ctypes.CDLL:
         lib.oracle_e4m3_encode.argtypes = [i64, vp, vp]
         lib.oracle_quantize_rows.argtypes = [i64, i64, vp, vp, vp]
         lib.oracle_fp8_layer_rows.argtypes = [i32, i32, i32, i32, i32, i32, vp, i64] + [vp] * 14
+        lib.oracle_fp8_hidden.argtypes = [i32, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp]
+        lib.oracle_fp8_out.argtypes = [i32, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp, vp]
         _lib = lib
     return _lib
 
 
 def _p(a: Optional[np.ndarray]):
-    return None if a is None else a.ctypes.data
+    """Pointer to a's data that keeps a alive for the call: arguments such as
+    _p(np.ascontiguousarray(v, np.int32)) may be temporaries, whose buffers
+    would otherwise be freed before the C function reads them."""
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
 def _stored(a: Optional[np.ndarray], dtype: int) -> Optional[np.ndarray]:
@@ -390,6 +395,29 @@ def quantize_experts(cfg, inp: Dict) -> Dict[str, np.ndarray]:
     return out
 
 
+def _bias_f32(inp: Dict, name: str):
+    return None if inp.get(name) is None else np.ascontiguousarray(_as_f32_values(inp[name]))
+
+
+def fp8_hidden(cfg, g: int, xq_row: np.ndarray, xs: float, wq: Dict[str, np.ndarray], inp: Dict) -> np.ndarray:
+    """Hidden activations [f] (fp64, before the bf16 rounding) of FP8 expert g
+    on one quantised row."""
+    h = np.empty(cfg.f, np.float64)
+    xr = np.ascontiguousarray(xq_row, np.uint8)
+    _L().oracle_fp8_hidden(cfg.d, cfg.f, cfg.act, int(g), _p(xr), float(xs), _p(wq["W1q"]), _p(wq["s1"]),
+                           _p(wq.get("W3q")), _p(wq.get("s3")), _p(_bias_f32(inp, "b1")), _p(h))
+    return h
+
+
+def fp8_out(cfg, g: int, hq_row: np.ndarray, hs: float, wq: Dict[str, np.ndarray], inp: Dict) -> np.ndarray:
+    """Output [d] of FP8 expert g from one quantised hidden row."""
+    o = np.empty(cfg.d, np.float64)
+    hr = np.ascontiguousarray(hq_row, np.uint8)
+    _L().oracle_fp8_out(cfg.d, cfg.f, cfg.act, int(g), _p(hr), float(hs), _p(wq["W2q"]), _p(wq["s2"]),
+                        _p(_bias_f32(inp, "b2")), _p(o))
+    return o
+
+
 def fp8_forward(cfg, inp: Dict, rows: Optional[Sequence[int]] = None, logits: Optional[np.ndarray] = None,
                 wq: Optional[Dict[str, np.ndarray]] = None) -> Dict[str, np.ndarray]:
     """The layer with FP8 experts: routing, statistics and gate weights exactly as
@@ -408,8 +436,7 @@ def fp8_forward(cfg, inp: Dict, rows: Optional[Sequence[int]] = None, logits: Op
     rows = np.ascontiguousarray(rows, np.int64)
     out["rows"] = rows
     y = np.empty((rows.size, cfg.d), np.float64)
-    b1 = None if inp.get("b1") is None else np.ascontiguousarray(_as_f32_values(inp["b1"]))
-    b2 = None if inp.get("b2") is None else np.ascontiguousarray(_as_f32_values(inp["b2"]))
+    b1, b2 = _bias_f32(inp, "b1"), _bias_f32(inp, "b2")
     _L().oracle_fp8_layer_rows(cfg.d, cfg.f, cfg.E, cfg.k, cfg.S, cfg.act, _p(rows), rows.size, _p(xq), _p(xs),
                                _p(wq["W1q"]), _p(wq["s1"]), _p(wq.get("W3q")), _p(wq.get("s3")), _p(b1),
                                _p(wq["W2q"]), _p(wq["s2"]), _p(b2),

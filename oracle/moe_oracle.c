@@ -605,6 +605,17 @@ uint8_t oracle_e4m3_encode1(float x) {
   return sign | (uint8_t)(E << 3) | (uint8_t)m;
 }
 
+/* value(code) for all 256 codes, filled from oracle_e4m3_value on first use. */
+static const double* e4m3_table(void) {
+  static double tab[256];
+  static int ready = 0;
+  if (!ready) {
+    for (int c = 0; c < 256; ++c) tab[c] = oracle_e4m3_value((uint8_t)c);
+    ready = 1;
+  }
+  return tab;
+}
+
 void oracle_e4m3_encode(int64_t n, const float* x, uint8_t* q) {
   for (int64_t i = 0; i < n; ++i) q[i] = oracle_e4m3_encode1(x[i]);
 }
@@ -629,48 +640,65 @@ void oracle_quantize_rows(int64_t rows, int64_t cols, const float* v, uint8_t* q
   }
 }
 
-/* Expert g on one quantised row xq (scale xs): o = W2-GEMM of the quantised h.
- * Weights: Wq [G, out, in] e4m3 with scales [G, out]; biases fp32 or NULL. */
-void oracle_fp8_expert_ffn(int d, int f, int act, int g, const uint8_t* xq, float xs, const uint8_t* W1q,
-                           const float* s1, const uint8_t* W3q, const float* s3, const float* b1,
-                           const uint8_t* W2q, const float* s2, const float* b2, double* out) {
+/* First half of FP8 expert g on one quantised row xq (scale xs): the hidden
+ * activations h [f] in fp64, before their bf16 rounding.
+ * Weights: Wq [G, out, in] E4M3 codes with scales [G, out]; b1 fp32 or NULL. */
+void oracle_fp8_hidden(int d, int f, int act, int g, const uint8_t* xq, float xs, const uint8_t* W1q,
+                       const float* s1, const uint8_t* W3q, const float* s3, const float* b1, double* h) {
+  const double* V = e4m3_table();
   double* xv = (double*)malloc(sizeof(double) * (size_t)d);
-  float* hb = (float*)malloc(sizeof(float) * (size_t)f);
-  uint8_t* hq = (uint8_t*)malloc((size_t)f);
-  double* hv = (double*)malloc(sizeof(double) * (size_t)f);
-  for (int i = 0; i < d; ++i) xv[i] = oracle_e4m3_value(xq[i]);
+  for (int i = 0; i < d; ++i) xv[i] = V[xq[i]];
   for (int j = 0; j < f; ++j) {
     const uint8_t* w1 = W1q + ((int64_t)g * f + j) * d;
     double acc = 0.0;
-    for (int i = 0; i < d; ++i) acc += xv[i] * oracle_e4m3_value(w1[i]);
+    for (int i = 0; i < d; ++i) acc += xv[i] * V[w1[i]];
     double a = (double)xs * (double)s1[(int64_t)g * f + j] * acc;
-    double h;
     if (act == OACT_SWIGLU) {
       const uint8_t* w3 = W3q + ((int64_t)g * f + j) * d;
       double acc3 = 0.0;
-      for (int i = 0; i < d; ++i) acc3 += xv[i] * oracle_e4m3_value(w3[i]);
+      for (int i = 0; i < d; ++i) acc3 += xv[i] * V[w3[i]];
       const double u = (double)xs * (double)s3[(int64_t)g * f + j] * acc3;
-      h = oracle_act(OACT_SWIGLU, a) * u;
+      h[j] = oracle_act(OACT_SWIGLU, a) * u;
     } else {
       if (b1) a += (double)b1[(int64_t)g * f + j];
-      h = oracle_act(act, a);
+      h[j] = oracle_act(act, a);
     }
-    hb[j] = (float)oracle_bf16_round(h);    /* exact in fp32 */
   }
-  float hs;
-  oracle_quantize_rows(1, f, hb, hq, &hs);
-  for (int j = 0; j < f; ++j) hv[j] = oracle_e4m3_value(hq[j]);
+  free(xv);
+}
+
+/* Second half: expert output o [d] from the quantised hidden row hq (scale hs). */
+void oracle_fp8_out(int d, int f, int act, int g, const uint8_t* hq, float hs, const uint8_t* W2q,
+                    const float* s2, const float* b2, double* out) {
+  const double* V = e4m3_table();
+  double* hv = (double*)malloc(sizeof(double) * (size_t)f);
+  for (int j = 0; j < f; ++j) hv[j] = V[hq[j]];
   for (int c = 0; c < d; ++c) {
     const uint8_t* w2 = W2q + ((int64_t)g * d + c) * f;
     double acc = 0.0;
-    for (int j = 0; j < f; ++j) acc += hv[j] * oracle_e4m3_value(w2[j]);
+    for (int j = 0; j < f; ++j) acc += hv[j] * V[w2[j]];
     out[c] = (double)hs * (double)s2[(int64_t)g * d + c] * acc;
     if (b2 && act != OACT_SWIGLU) out[c] += (double)b2[(int64_t)g * d + c];
   }
-  free(xv);
+  free(hv);
+}
+
+/* FP8 expert g on one quantised row: hidden, bf16 rounding, per-row
+ * quantisation of h, output. */
+void oracle_fp8_expert_ffn(int d, int f, int act, int g, const uint8_t* xq, float xs, const uint8_t* W1q,
+                           const float* s1, const uint8_t* W3q, const float* s3, const float* b1,
+                           const uint8_t* W2q, const float* s2, const float* b2, double* out) {
+  double* h = (double*)malloc(sizeof(double) * (size_t)f);
+  float* hb = (float*)malloc(sizeof(float) * (size_t)f);
+  uint8_t* hq = (uint8_t*)malloc((size_t)f);
+  oracle_fp8_hidden(d, f, act, g, xq, xs, W1q, s1, W3q, s3, b1, h);
+  for (int j = 0; j < f; ++j) hb[j] = (float)oracle_bf16_round(h[j]);    /* exact in fp32 */
+  float hs;
+  oracle_quantize_rows(1, f, hb, hq, &hs);
+  oracle_fp8_out(d, f, act, g, hq, hs, W2q, s2, b2, out);
+  free(h);
   free(hb);
   free(hq);
-  free(hv);
 }
 
 /* The layer output of the listed token rows with FP8 experts: x quantised per

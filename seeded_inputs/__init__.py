@@ -56,6 +56,7 @@ class LayerConfig:
     router_bias_std: float = 0.01
     bias_std: float = 0.01
     expert_choice: bool = False       # each expert chooses its tokens instead
+    fp8_experts: bool = False         # expert weights held as E4M3 codes
 
     def replace(self, **kw) -> "LayerConfig":
         return dataclasses.replace(self, **kw)

@@ -29,6 +29,8 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 RELU, GELU, SWIGLU, NONE = 0, 1, 2, 3
 FLAG_Y_F32 = 1
 FLAG_EXPERT_CHOICE = 2
+FLAG_FP8_EXPERTS = 4
+REGION_XPERM, REGION_X_SCALE, REGION_H, REGION_H_CODES, REGION_H_SCALE, REGION_O = 1, 2, 3, 4, 5, 6
 SOFTMAX, SIGMOID_NORM = 0, 1
 F32, BF16 = 0, 1
 NUM_STAGES = 6
@@ -59,6 +61,7 @@ class MoEConfig:
     alpha: float = 0.01
     y_f32: bool = False        # write y in fp32 whatever dtype is
     expert_choice: bool = False  # each expert chooses its tokens (see moe.h)
+    fp8_experts: bool = False    # E4M3 expert weights (forward_fp8)
 
 
 class _CConfig(ctypes.Structure):
@@ -71,6 +74,11 @@ class _CConfig(ctypes.Structure):
 class _COpts(ctypes.Structure):
     _fields_ = [("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("wait_timeout_ns", ctypes.c_int64),
                 ("flags", ctypes.c_int64)]
+
+
+class _CFp8(ctypes.Structure):
+    _fields_ = [("W1", ctypes.c_void_p), ("s1", ctypes.c_void_p), ("W3", ctypes.c_void_p),
+                ("s3", ctypes.c_void_p), ("W2", ctypes.c_void_p), ("s2", ctypes.c_void_p)]
 
 
 OPT_GEMM_SINGLE_CTA = 1
@@ -117,6 +125,18 @@ def lib() -> ctypes.CDLL:
     L.moe_grouped_gemm.argtypes = [i32, i32, i32, vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, optp]
     L.moe_grouped_gemm_noalloc.restype = ctypes.c_int
     L.moe_grouped_gemm_noalloc.argtypes = [i32, i32, i32, vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, optp]
+    L.moe_quantize_weights_fp8.restype = ctypes.c_int
+    L.moe_quantize_weights_fp8.argtypes = [vp, i64, i64, i64, vp, vp, vp]
+    L.moe_quantize_rows_fp8.restype = ctypes.c_int
+    L.moe_quantize_rows_fp8.argtypes = [vp, i64, i64, vp, vp, vp]
+    L.moe_forward_fp8.restype = ctypes.c_int
+    L.moe_forward_fp8.argtypes = [cfgp] + [vp] * 4 + [ctypes.POINTER(_CFp8)] + [vp] * 2 + [vp] * 12 + [vp, sz, vp,
+                                                                                                       optp]
+    L.moe_forward_fp8_host.restype = ctypes.c_int
+    L.moe_forward_fp8_host.argtypes = [cfgp] + [vp] * 4 + [ctypes.POINTER(_CFp8)] + [vp] * 2 + [vp] * 9 + [vp, sz,
+                                                                                                           vp, optp]
+    L.moe_workspace_region.restype = ctypes.c_int
+    L.moe_workspace_region.argtypes = [cfgp, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     _lib_handle = L
     return L
 
@@ -125,12 +145,15 @@ def exported_symbols() -> Sequence[str]:
     return ("moe_status_string", "moe_validate_config", "moe_workspace_size", "moe_capacity", "moe_forward",
             "moe_forward_host_workspace_size", "moe_forward_host", "moe_backward_workspace_size", "moe_backward",
             "moe_check_device_errors",
-            "moe_grouped_gemm_workspace_size", "moe_grouped_gemm", "moe_grouped_gemm_noalloc")
+            "moe_grouped_gemm_workspace_size", "moe_grouped_gemm", "moe_grouped_gemm_noalloc",
+            "moe_quantize_weights_fp8", "moe_quantize_rows_fp8", "moe_forward_fp8", "moe_forward_fp8_host",
+            "moe_workspace_region")
 
 
 def c_config(cfg, y_f32: Optional[bool] = None) -> _CConfig:
     yf = bool(getattr(cfg, "y_f32", False)) if y_f32 is None else bool(y_f32)
     flags = (FLAG_Y_F32 if yf else 0) | (FLAG_EXPERT_CHOICE if getattr(cfg, "expert_choice", False) else 0)
+    flags |= FLAG_FP8_EXPERTS if getattr(cfg, "fp8_experts", False) else 0
     return _CConfig(int(cfg.T), int(cfg.d), int(cfg.f), int(cfg.E), int(cfg.k), int(cfg.S), int(cfg.act),
                     int(cfg.gating), int(cfg.dtype), float(cfg.capacity_factor), float(cfg.alpha), flags)
 
@@ -476,3 +499,159 @@ def grouped_gemm_noalloc(dtype: int, act: int, seg_offsets: torch.Tensor, A: tor
     if status != 0:
         raise MoEError(status, "moe_grouped_gemm_noalloc")
     return C
+
+
+# ---- FP8 (E4M3) experts ------------------------------------------------------------
+
+@dataclasses.dataclass
+class Fp8Experts:
+    """Expert weights as E4M3 codes, K-major, with one fp32 decoding scale per
+    (expert, output unit): W1/W3 [E+S, f, d] with s1/s3 [E+S, f]; W2 [E+S, d, f]
+    with s2 [E+S, d]."""
+    W1: torch.Tensor
+    s1: torch.Tensor
+    W2: torch.Tensor
+    s2: torch.Tensor
+    W3: Optional[torch.Tensor] = None
+    s3: Optional[torch.Tensor] = None
+
+
+def quantize_weights_fp8(W: torch.Tensor, stream: Optional[torch.cuda.Stream] = None):
+    """bf16 weight slabs [G, K, N] -> (codes uint8 [G, N, K], scales fp32 [G, N])."""
+    if W.dim() != 3:
+        raise ValueError("W must be [G, K, N]")
+    _check(W, "W", tuple(W.shape), _STORE[BF16])
+    G, K, N = W.shape
+    Q = torch.empty((G, N, K), dtype=torch.uint8, device=W.device)
+    sc = torch.empty((G, N), dtype=torch.float32, device=W.device)
+    with torch.cuda.device(W.device):
+        st = lib().moe_quantize_weights_fp8(_ptr(W), G, K, N, _ptr(Q), _ptr(sc), _stream_handle(stream))
+    if st != 0:
+        raise MoEError(st, "moe_quantize_weights_fp8")
+    return Q, sc
+
+
+def quantize_rows_fp8(X: torch.Tensor, stream: Optional[torch.cuda.Stream] = None):
+    """bf16 rows [rows, cols] -> (codes uint8 [rows, cols], scales fp32 [rows])."""
+    if X.dim() != 2:
+        raise ValueError("X must be [rows, cols]")
+    _check(X, "X", tuple(X.shape), _STORE[BF16])
+    rows, cols = X.shape
+    Q = torch.empty((rows, cols), dtype=torch.uint8, device=X.device)
+    sc = torch.empty((rows,), dtype=torch.float32, device=X.device)
+    with torch.cuda.device(X.device):
+        st = lib().moe_quantize_rows_fp8(_ptr(X), rows, cols, _ptr(Q), _ptr(sc), _stream_handle(stream))
+    if st != 0:
+        raise MoEError(st, "moe_quantize_rows_fp8")
+    return Q, sc
+
+
+def quantize_experts_fp8(W1: torch.Tensor, W2: torch.Tensor, W3: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> Fp8Experts:
+    q1, s1 = quantize_weights_fp8(W1, stream)
+    q2, s2 = quantize_weights_fp8(W2, stream)
+    q3, s3 = quantize_weights_fp8(W3, stream) if W3 is not None else (None, None)
+    return Fp8Experts(W1=q1, s1=s1, W2=q2, s2=s2, W3=q3, s3=s3)
+
+
+def _fp8_cfg(cfg):
+    return dataclasses.replace(cfg, fp8_experts=True) if not getattr(cfg, "fp8_experts", False) else cfg
+
+
+def forward_fp8(cfg, x, W_g, b_g, experts: Fp8Experts, b1=None, b2=None, *,
+                router_noise: Optional[torch.Tensor] = None, out: Optional[MoEOutput] = None,
+                workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+                debug: bool = False, stage_events=None, timeout_ns: int = 0,
+                y_f32: Optional[bool] = None) -> MoEOutput:
+    """The layer with FP8 experts (moe_forward_fp8): routing as forward(), the
+    expert GEMMs on E4M3 codes.  ``stage_events``: NUM_STAGES + 2 events (the
+    last one after the hidden activations' quantisation)."""
+    if not torch.cuda.is_available():
+        raise RuntimeError("the MoE layer runs on a CUDA device; none is available")
+    cfg = _fp8_cfg(cfg)
+    T, d, f, E, k, S = cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S
+    G = E + S
+    st = _STORE[cfg.dtype]
+    u8, f32 = (torch.uint8,), (torch.float32,)
+    _check(x, "x", (T, d), st)
+    _check(W_g, "W_g", (d, E), st)
+    _check(b_g, "b_g", (E,), st, required=False)
+    _check(experts.W1, "W1 codes", (G, f, d), u8)
+    _check(experts.s1, "s1", (G, f), f32)
+    _check(experts.W2, "W2 codes", (G, d, f), u8)
+    _check(experts.s2, "s2", (G, d), f32)
+    _check(experts.W3, "W3 codes", (G, f, d), u8, required=cfg.act == SWIGLU)
+    _check(experts.s3, "s3", (G, f), f32, required=cfg.act == SWIGLU)
+    _check(b1, "b1", (G, f), st, required=False)
+    _check(b2, "b2", (G, d), st, required=False)
+    _check(router_noise, "router_noise", (T, E), (torch.float32,), required=False)
+    dev = x.device
+    yf = bool(getattr(cfg, "y_f32", False)) if y_f32 is None else bool(y_f32)
+    if out is None:
+        out = alloc_outputs(cfg, dev, debug=debug, y_f32=yf)
+    if workspace is None:
+        workspace = out.workspace if out.workspace is not None else alloc_workspace(cfg, dev)
+    out.workspace = workspace
+    opts, keep = _opts(stage_events, timeout_ns, 0)
+    ccfg = c_config(cfg, y_f32=yf)
+    w = _fp8_struct(experts)
+    with torch.cuda.device(dev):
+        status = lib().moe_forward_fp8(
+            ctypes.byref(ccfg), _ptr(x), _ptr(W_g), _ptr(b_g), _ptr(router_noise), ctypes.byref(w), _ptr(b1),
+            _ptr(b2), _ptr(out.y), _ptr(out.topk_idx), _ptr(out.topk_w), _ptr(out.expert_counts),
+            _ptr(out.dropped_mask), _ptr(out.f), _ptr(out.P), _ptr(out.L_aux), _ptr(out.route_stats),
+            _ptr(out.router_logits), _ptr(out.perm_token), _ptr(out.slot), _ptr(workspace), workspace.numel(),
+            _stream_handle(stream), ctypes.byref(opts) if opts is not None else None)
+    del keep
+    if status != 0:
+        raise MoEError(status, "moe_forward_fp8")
+    return out
+
+
+def _fp8_struct(experts: Fp8Experts) -> _CFp8:
+    return _CFp8(experts.W1.data_ptr(), experts.s1.data_ptr(),
+                 experts.W3.data_ptr() if experts.W3 is not None else None,
+                 experts.s3.data_ptr() if experts.s3 is not None else None,
+                 experts.W2.data_ptr(), experts.s2.data_ptr())
+
+
+def forward_fp8_host(cfg, x_host: torch.Tensor, W_g, b_g, experts: Fp8Experts, b1=None, b2=None, *,
+                     router_noise_host: Optional[torch.Tensor] = None, out: Optional[MoEOutput] = None,
+                     workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+                     y_f32: Optional[bool] = None) -> MoEOutput:
+    """forward_fp8 on a host batch (moe_forward_fp8_host): x_host and the
+    outputs are page-locked CPU tensors, the weights CUDA tensors."""
+    if not torch.cuda.is_available():
+        raise RuntimeError("the MoE layer runs on a CUDA device; none is available")
+    cfg = _fp8_cfg(cfg)
+    T, d = cfg.T, cfg.d
+    if x_host.is_cuda or not x_host.is_contiguous() or tuple(x_host.shape) != (T, d) or \
+            x_host.dtype not in _STORE[cfg.dtype]:
+        raise ValueError("x_host must be a contiguous CPU tensor of shape (T, d) in the config's dtype")
+    yf = bool(getattr(cfg, "y_f32", False)) if y_f32 is None else bool(y_f32)
+    if out is None:
+        out = alloc_host_outputs(cfg, y_f32=yf)
+    dev = experts.W1.device
+    if workspace is None:
+        workspace = torch.empty((host_workspace_size(cfg, yf),), dtype=torch.uint8, device=dev)
+    out.workspace = workspace
+    ccfg = c_config(cfg, y_f32=yf)
+    w = _fp8_struct(experts)
+    with torch.cuda.device(dev):
+        status = lib().moe_forward_fp8_host(
+            ctypes.byref(ccfg), _ptr(x_host), _ptr(W_g), _ptr(b_g), _ptr(router_noise_host), ctypes.byref(w),
+            _ptr(b1), _ptr(b2), _ptr(out.y), _ptr(out.topk_idx), _ptr(out.topk_w), _ptr(out.expert_counts),
+            _ptr(out.dropped_mask), _ptr(out.f), _ptr(out.P), _ptr(out.L_aux), _ptr(out.route_stats),
+            _ptr(workspace), workspace.numel(), _stream_handle(stream), None)
+    if status != 0:
+        raise MoEError(status, "moe_forward_fp8_host")
+    return out
+
+
+def workspace_region(cfg, region: int):
+    """(offset, bytes) of an intermediate in the workspace of ``cfg``'s call."""
+    off, n = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    st = lib().moe_workspace_region(ctypes.byref(c_config(cfg)), int(region), ctypes.byref(off), ctypes.byref(n))
+    if st != 0:
+        raise MoEError(st, "moe_workspace_region")
+    return int(off.value), int(n.value)

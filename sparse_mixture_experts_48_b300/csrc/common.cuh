@@ -26,6 +26,7 @@ struct WsHeader {
 struct WsLayout {
   size_t hdr, hist, psum, base, lrank, npre, offsets, seg, slot, xperm, h, o;
   size_t ec_scores, ec_bits, ec_tokrow, ec_wrow, ec_perm;   // expert choice only
+  size_t xs_perm, xq, xs_tok, hq, hs;                       // FP8 experts only
   size_t total;
   int64_t nblk;      // router CTAs
   int64_t rows_tk;   // rows of routed assignments: T * k, or E * C for expert choice
@@ -84,6 +85,53 @@ __device__ __forceinline__ void load_bf16x32(const uint16_t* p, float (&f)[32]) 
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+}
+
+// ---- E4M3 (8-bit float: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+// largest finite 448) --------------------------------------------------------------
+constexpr float kE4M3Max = 448.f;
+
+// Scale pair of a vector whose largest magnitude is amax: encoding factor
+// r = 448 / a and decoding scale s = a / 448, a = max(amax, 2^-60), both
+// rounded once to fp32.
+__device__ __forceinline__ void e4m3_scales(float amax, float& r, float& s) {
+  const float a = fmaxf(amax, 0x1p-60f);
+  r = __fdiv_rn(kE4M3Max, a);
+  s = __fdiv_rn(a, kE4M3Max);
+}
+
+// Four fp32 values (already multiplied by r) -> four E4M3 codes, nearest with
+// ties to even, saturating at +-448; v0 in the lowest byte.
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
+  uint16_t lo, hi;
+  // The first source lands in the upper byte of the 16-bit result.
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(v1), "f"(v0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(v3), "f"(v2));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// 8 bf16 (one 16-byte word) -> 8 E4M3 codes (8 bytes) with encoding factor r.
+__device__ __forceinline__ uint2 e4m3x8_from_bf16(const uint4 v, float r) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __fmul_rn(__uint_as_float(w[j] << 16), r);
+    f[2 * j + 1] = __fmul_rn(__uint_as_float(w[j] & 0xffff0000u), r);
+  }
+  return make_uint2(e4m3x4(f[0], f[1], f[2], f[3]), e4m3x4(f[4], f[5], f[6], f[7]));
+}
+
+// Largest |bf16| of one 16-byte word.
+__device__ __forceinline__ float amax_bf16x8(const uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
+    m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xffff0000u)));
+  }
+  return m;
 }
 
 }  // namespace moe

@@ -232,6 +232,34 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(GatherArgs a)
   int slots[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) slots[j] = __shfl_sync(0xffffffffu, my_slot, j);
+  if (a.fp8) {
+    // FP8 experts: quantise the bf16 row on the way.  Pass 1 finds its largest
+    // magnitude; pass 2 re-reads the row (now in L1 / L2) and writes 16 codes
+    // per 16-byte store to every kept slot (and to the token-order copy that
+    // the shared experts read).
+    const int64_t words = a.d / 8;
+    const uint4* src = (const uint4*)a.x + t * words;
+    float m = 0.f;
+    for (int64_t c = lane; c < words; c += 32) m = fmaxf(m, amax_bf16x8(src[c]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float r, sc;
+    e4m3_scales(m, r, sc);
+    const int64_t ow = a.d / 16;
+    uint4* dst = (uint4*)a.xperm;
+    for (int64_t c = lane; c < ow; c += 32) {
+      const uint2 lo = e4m3x8_from_bf16(src[2 * c], r);
+      const uint2 hi = e4m3x8_from_bf16(src[2 * c + 1], r);
+      const uint4 q = make_uint4(lo.x, lo.y, hi.x, hi.y);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < k && slots[j] >= 0) dst[(int64_t)slots[j] * ow + c] = q;
+      if (a.xq) reinterpret_cast<uint4*>(a.xq)[t * ow + c] = q;
+    }
+    if (lane < k && my_slot >= 0) a.xs_perm[my_slot] = sc;
+    if (lane == 0 && a.xs_tok) a.xs_tok[t] = sc;
+    return;
+  }
   const int esz = a.dtype == MOE_DT_BF16 ? 2 : 4;
   const int64_t chunks = (int64_t)a.d * esz / 16;
   const uint64_t policy = l2_policy_evict_first();   // x read once, the grouped copy written once

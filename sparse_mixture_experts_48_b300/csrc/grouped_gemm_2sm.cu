@@ -24,7 +24,13 @@
 //               drained accumulators are released on the leader's tempty
 //               barrier (16 arrivals: both CTAs' epilogue warps).
 // Rows past a segment's end are computed but never stored; B boxes past N are
-// zero-filled by TMA (their columns are never stored).  Every wait is bounded;
+// zero-filled by TMA (their columns are never stored).
+//
+// FP8 instantiation: A and B hold E4M3 codes, both K-major (B stored [N, K] per
+// slab), a k-block is 128 codes (128 bytes: the same 32 KB stage), and the
+// leader issues M256 N256 K32 kind::f8f6f4 MMAs.  K needs only be a multiple
+// of 64: TMA fills the codes past K with zeros.  The epilogue multiplies each
+// accumulator by its row's and its column's decoding scales.  Every wait is bounded;
 // set-up and tear-down meet at cluster barriers that both CTAs always reach.
 //
 // Sources: "手撕一个极简 MoE-FFN" §四 (Expert = w2(act(w1 x))), §六 (group the
@@ -58,6 +64,8 @@ constexpr int TMEM_COLS = 512;                  // two 256-column accumulators
 constexpr int MAX_G = 264;
 constexpr uint32_t kWhere = 0x400;
 constexpr uint32_t kIdescPair = idesc_bf16(BMP, MMA_N);
+constexpr uint32_t kIdescPairF8 = idesc_e4m3(BMP, MMA_N);
+constexpr int BK8 = 128;                        // E4M3 codes per k-block (128 bytes)
 
 struct Ctl {
   uint64_t full[STAGES];    // leader: both CTAs' copies of the stage have landed
@@ -102,10 +110,23 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const uint32_t (&v)
   for (int i = 0; i < 4; ++i) d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
 }
 
+// v[i] <- v[i] * ra * s[i] for 32 consecutive column scales s (16-byte aligned).
+__device__ __forceinline__ void scale_acc32(uint32_t (&v)[32], float ra, const float* s) {
+  const float4* s4 = reinterpret_cast<const float4*>(s);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 q = s4[i];
+    v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) * (ra * q.x));
+    v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) * (ra * q.y));
+    v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) * (ra * q.z));
+    v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) * (ra * q.w));
+  }
+}
+
 // SAVE_PRE (expert GEMM 1 of the backward pass's forward recomputation): the
 // pre-activations a = x W1 + b1 (and u = x W3 for SwiGLU) are also stored, in
 // bf16, at the output's rows and columns (a.pre_a, a.pre_u).
-template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE>
+template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE, bool FP8 = false>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3, GemmArgs a) {
@@ -122,7 +143,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int G = a.G;
   const int n_tiles = (a.N + BN_OUT - 1) / BN_OUT;
-  const int nkb = a.K / BK;
+  const int nkb = FP8 ? (a.K + BK8 - 1) / BK8 : a.K / BK;
   const uint64_t limit = (uint64_t)a.timeout_ns;
   const uint64_t drain_limit = limit > 2000000000ull ? limit : 2000000000ull;
 
@@ -223,9 +244,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t fb = full_leader + (uint32_t)(stage * 8);
           const uint32_t sa = base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
-          tma_load_2d_pair(sa, amap, kb * BK, arow, fb);
-          tma_load_3d_pair(sb, bmap, bcol, kb * BK, wslab, fb);
-          tma_load_3d_pair(sb + B_BOX_BYTES, bmap, bcol + 64, kb * BK, wslab, fb);
+          if (FP8) {
+            // A: 128 rows x 128 codes; B: this CTA's 128 columns (rows of the
+            // [N, K] slab) x 128 codes.
+            tma_load_2d_pair(sa, amap, kb * BK8, arow, fb);
+            tma_load_3d_pair(sb, bmap, kb * BK8, bcol, wslab, fb);
+          } else {
+            tma_load_2d_pair(sa, amap, kb * BK, arow, fb);
+            tma_load_3d_pair(sb, bmap, bcol, kb * BK, wslab, fb);
+            tma_load_3d_pair(sb + B_BOX_BYTES, bmap, bcol + 64, kb * BK, wslab, fb);
+          }
           issued[stage] = true;
           issued_phase[stage] = phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -259,14 +287,24 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint32_t sa = base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
+          if (FP8) {
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            // A: K-major, 8-row groups 1024 B apart; a K step of 16 is 32 bytes.
-            const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
-            // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row k groups
-            // 1024 B apart (SBO); a K step of 16 rows is 2048 bytes.
-            const uint64_t bd = smem_desc(sb + kk * 2048, B_BOX_BYTES, 1024);
-            mma_bf16_cta2<kIdescPair>(d_tmem, ad, bd, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < BK8 / 32; ++kk) {
+              // A and B K-major, 8-row groups 1024 B apart; a K step of 32 codes is 32 bytes.
+              const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc(sb + kk * 32, 16, 1024);
+              mma_f8_cta2<kIdescPairF8>(d_tmem, ad, bd, (kb | kk) != 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              // A: K-major, 8-row groups 1024 B apart; a K step of 16 is 32 bytes.
+              const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+              // B: N-major, 64-column boxes 8 KB apart (LBO), 8-row k groups
+              // 1024 B apart (SBO); a K step of 16 rows is 2048 bytes.
+              const uint64_t bd = smem_desc(sb + kk * 2048, B_BOX_BYTES, 1024);
+              mma_bf16_cta2<kIdescPair>(d_tmem, ad, bd, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           mma_commit_cta2(smem_u32(&c.empty[stage]), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -303,6 +341,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int wslab = c.w[g];
       const int n0 = n * BN_OUT;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * MMA_N);
+      float ra = 0.f;                       // FP8: this row's decoding scale
+      if (FP8 && valid) ra = (c.asrc[g] ? a.a_scale1 : a.a_scale0)[c.arow[g] + grow];
       constexpr int CHUNKS = BN_OUT / 32;   // 32-column chunks per tile
       for (int ch = half * (CHUNKS / 2); ch < (half + 1) * (CHUNKS / 2); ++ch) {
         const int col0 = n0 + ch * 32;
@@ -312,6 +352,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint32_t u[32];
           tmem_ld32(tbase + 128u + (uint32_t)(ch * 32), u);
           tmem_wait_ld();
+          if (FP8 && valid && col0 < a.N) {
+            scale_acc32(v, ra, a.b_scale + (int64_t)wslab * a.N + col0);
+            scale_acc32(u, ra, a.b3_scale + (int64_t)wslab * a.N + col0);
+          }
           if (SAVE_PRE && valid && col0 < a.N) {
             store_bf16x32((uint16_t*)a.pre_a + orow * a.N + col0, v);
             store_bf16x32((uint16_t*)a.pre_u + orow * a.N + col0, u);
@@ -331,6 +375,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else {
           tmem_wait_ld();
           if (valid && col0 < a.N) {
+            if (FP8) scale_acc32(v, ra, a.b_scale + (int64_t)wslab * a.N + col0);
             float f[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
@@ -389,10 +434,10 @@ bool map_weights(CUtensorMap* m, const void* ptr, int G, int K, int N) {
   return tmap_bf16_3d(m, ptr, G, K, N, 64, BK);
 }
 
-template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE = false>
+template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE = false, bool FP8 = false>
 cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtensorMap& mA1, const CUtensorMap& mB,
                         const CUtensorMap& mB3, int64_t max_pair_tiles, cudaStream_t s) {
-  auto kernel = gemm_pair_kernel<SWIGLU, OUT_F32, SAVE_PRE>;
+  auto kernel = gemm_pair_kernel<SWIGLU, OUT_F32, SAVE_PRE, FP8>;
   static int max_clusters = -1;   // per kernel instantiation, per process (one device type)
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -422,8 +467,42 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtenso
 
 }  // namespace
 
+// FP8 experts: E4M3 codes, A [rows, K], B [Gw, N, K].
+static cudaError_t launch_pair_fp8(const GemmArgs& a, cudaStream_t s) {
+  if (a.G > MAX_G || a.K % 64 != 0 || a.N % 64 != 0) return cudaErrorInvalidValue;
+  if (a.out_f32 && a.act == MOE_ACT_SWIGLU) return cudaErrorInvalidValue;
+  if (a.pre_a || !a.a_scale0 || !a.b_scale || (a.A1 && !a.a_scale1)) return cudaErrorInvalidValue;
+  const bool swiglu = a.act == MOE_ACT_SWIGLU;
+  if (swiglu && (!a.B3 || !a.b3_scale)) return cudaErrorInvalidValue;
+  CUtensorMap mA0, mA1, mB, mB3;
+  if (!tmap_u8_2d(&mA0, a.A0, a.rows_A0, a.K, BMC)) return cudaErrorInvalidValue;
+  if (a.A1) {
+    if (!tmap_u8_2d(&mA1, a.A1, a.rows_A1, a.K, BMC)) return cudaErrorInvalidValue;
+  } else {
+    mA1 = mA0;
+  }
+  if (!tmap_u8_3d(&mB, a.B, a.Gw, a.N, a.K, 128)) return cudaErrorInvalidValue;
+  if (swiglu) {
+    if (!tmap_u8_3d(&mB3, a.B3, a.Gw, a.N, a.K, 128)) return cudaErrorInvalidValue;
+  } else {
+    mB3 = mB;
+  }
+  const int bn = swiglu ? 128 : 256;
+  const int64_t max_pair_tiles = a.max_mtiles * ((a.N + bn - 1) / bn);
+  cudaError_t e;
+  if (swiglu)
+    e = launch_pair<true, false, false, true>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
+  else if (a.out_f32)
+    e = launch_pair<false, true, false, true>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
+  else
+    e = launch_pair<false, false, false, true>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_grouped_gemm_pair(const GemmArgs& a, cudaStream_t s) {
   if (a.max_mtiles <= 0) return cudaSuccess;
+  if (a.fp8) return launch_pair_fp8(a, s);
   if (a.G > MAX_G || a.K % BK != 0 || a.N % 64 != 0) return cudaErrorInvalidValue;
   if (a.out_f32 && a.act == MOE_ACT_SWIGLU) return cudaErrorInvalidValue;
   CUtensorMap mA0, mA1, mB, mB3;

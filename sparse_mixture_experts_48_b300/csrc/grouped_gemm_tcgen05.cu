@@ -355,7 +355,7 @@ int sm_count() {
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.dtype == MOE_DT_F32) return launch_grouped_gemm_f32(a, s);
-  if (!a.single_cta) return launch_grouped_gemm_pair(a, s);
+  if (!a.single_cta || a.fp8) return launch_grouped_gemm_pair(a, s);
   if (a.max_mtiles <= 0) return cudaSuccess;
   if (a.G > MAX_G || a.K % BK != 0 || a.N % 64 != 0) return cudaErrorInvalidValue;
   if (a.out_f32 && a.act == MOE_ACT_SWIGLU) return cudaErrorInvalidValue;

@@ -68,8 +68,40 @@ struct GatherArgs {
   int32_t* perm_token;  // [T*k] or null
   void* xperm;          // [T*k, d]
   const uint32_t* err;  // non-zero: skip (the ranks are not valid)
+  // FP8 experts: x (bf16) is quantised per token row on the way; xperm holds
+  // E4M3 codes, xs_perm [T*k] each grouped row's decoding scale, and (shared
+  // experts) xq [T, d] / xs_tok [T] the quantised rows in token order.
+  bool fp8;
+  float* xs_perm;
+  uint8_t* xq;
+  float* xs_tok;
 };
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
+
+// Per-row E4M3 quantisation of bf16 rows (fp8.cu): row r of X -> codes Q[r]
+// and decoding scale scale[r].  Rows [0, rows0) are live only below *live0
+// (when live0 is set: the kept routed rows of H); rows [row1, row1 + rows1)
+// follow (the shared experts' rows of H).
+struct QuantRowsArgs {
+  const void* X;        // [., cols] bf16
+  uint8_t* Q;           // [., cols]
+  float* scale;         // [.]
+  int64_t cols;
+  int64_t rows0;
+  const int32_t* live0; // or null: all rows0 rows
+  int64_t row1, rows1;
+  const uint32_t* err;  // or null
+};
+cudaError_t launch_quantize_rows(const QuantRowsArgs& a, cudaStream_t s);
+
+// Weight slabs W [G, K, N] bf16 -> Q [G, N, K] E4M3 with one scale per (g, n).
+struct QuantWeightsArgs {
+  const void* W;
+  uint8_t* Q;
+  float* scale;
+  int64_t G, K, N;
+};
+cudaError_t launch_quantize_weights(const QuantWeightsArgs& a, cudaStream_t s);
 
 struct CombineArgs {
   const float* o;       // [rows_all, d] expert outputs, fp32
@@ -145,6 +177,16 @@ struct GemmArgs {
   bool single_cta;      // bf16: the one-CTA 128 x 256 tile kernel instead of the CTA-pair kernel
   void* pre_a;          // if set (pair kernel, bf16 out): pre-activations a = A B + bias, [rows, N] bf16
   void* pre_u;          // SwiGLU with pre_a: u = A B3, [rows, N] bf16
+  // FP8 experts (pair kernel): A0 / A1 hold E4M3 codes with one decoding scale
+  // per row (a_scale0 / a_scale1, indexed like the A rows); B / B3 hold E4M3
+  // codes stored [Gw, N, K] (K-major) with one scale per (slab, column)
+  // (b_scale / b3_scale, [Gw, N]).  The epilogue multiplies the accumulator by
+  // both scales before the bias and the activation.
+  bool fp8;
+  const float* a_scale0;
+  const float* a_scale1;
+  const float* b_scale;
+  const float* b3_scale;
 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_grouped_gemm_pair(const GemmArgs& a, cudaStream_t s);

@@ -34,7 +34,9 @@ moe_status check_cfg(const moe_config* c) {
   if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_GELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (c->gating != MOE_GATE_SOFTMAX && c->gating != MOE_GATE_SIGMOID_NORM) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_DT_F32 && c->dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
-  if (c->flags & ~(int64_t)(MOE_FLAG_Y_F32 | MOE_FLAG_EXPERT_CHOICE)) return MOE_ERR_INVALID_ARG;
+  if (c->flags & ~(int64_t)(MOE_FLAG_Y_F32 | MOE_FLAG_EXPERT_CHOICE | MOE_FLAG_FP8_EXPERTS)) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & MOE_FLAG_FP8_EXPERTS) && (c->dtype != MOE_DT_BF16 || (c->flags & MOE_FLAG_EXPERT_CHOICE)))
+    return MOE_ERR_UNSUPPORTED;
   if (!isfinite(c->capacity_factor) || !isfinite(c->alpha)) return MOE_ERR_INVALID_ARG;
   if (c->E > kMaxE || c->k > kMaxK || c->n_shared > kMaxShared) return MOE_ERR_UNSUPPORTED;
   if (c->dtype == MOE_DT_BF16 && (c->d_model % 64 != 0 || c->d_ff % 64 != 0)) return MOE_ERR_UNSUPPORTED;
@@ -71,7 +73,8 @@ WsLayout layout(const moe_config* c) {
   L.offsets = take((size_t)(c->E + 1) * 4);
   L.seg = take((size_t)(6 * L.G + 1) * 4);
   L.slot = take((size_t)L.rows_tk * 4);
-  L.xperm = take((size_t)L.rows_tk * c->d_model * esz);
+  const bool fp8 = (c->flags & MOE_FLAG_FP8_EXPERTS) != 0;
+  L.xperm = take((size_t)L.rows_tk * c->d_model * (fp8 ? 1 : esz));
   L.h = take((size_t)L.rows_all * c->d_ff * esz);
   L.o = take((size_t)L.rows_all * c->d_model * 4);
   L.ec_scores = take(ec ? (size_t)c->E * c->T * 4 : 0);
@@ -79,6 +82,12 @@ WsLayout layout(const moe_config* c) {
   L.ec_tokrow = take(ec ? (size_t)c->T * c->E * 4 : 0);
   L.ec_wrow = take(ec ? (size_t)L.rows_tk * 4 : 0);
   L.ec_perm = take(ec ? (size_t)L.rows_tk * 4 : 0);
+  const bool sh8 = fp8 && c->n_shared > 0;
+  L.xs_perm = take(fp8 ? (size_t)L.rows_tk * 4 : 0);
+  L.xq = take(sh8 ? (size_t)c->T * c->d_model : 0);
+  L.xs_tok = take(sh8 ? (size_t)c->T * 4 : 0);
+  L.hq = take(fp8 ? (size_t)L.rows_all * c->d_ff : 0);
+  L.hs = take(fp8 ? (size_t)L.rows_all * 4 : 0);
   L.total = off;
   return L;
 }
@@ -196,7 +205,7 @@ BwdLayout bwd_layout(const moe_config* c) {
 moe_status check_bwd_cfg(const moe_config* c) {
   moe_status st = check_cfg(c);
   if (st != MOE_OK) return st;
-  if (c->dtype != MOE_DT_BF16 || (c->flags & MOE_FLAG_EXPERT_CHOICE)) return MOE_ERR_UNSUPPORTED;
+  if (c->dtype != MOE_DT_BF16 || (c->flags & (MOE_FLAG_EXPERT_CHOICE | MOE_FLAG_FP8_EXPERTS))) return MOE_ERR_UNSUPPORTED;
   const BwdLayout L = bwd_layout(c);
   if (L.rows_all >= ((int64_t)1 << 31) - 2 * kGemmBM) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -241,15 +250,25 @@ int64_t moe_capacity(const moe_config* cfg) {
   return capacity_of(cfg);
 }
 
-moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
-                       const float* router_noise, const void* W1, const void* b1, const void* W2, const void* b2,
-                       const void* W3, void* y, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
-                       uint8_t* dropped_mask, float* f, float* P, float* L_aux, float* route_stats,
-                       float* router_logits, int32_t* perm_token, int32_t* slot, void* workspace,
-                       size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts) {
+// The layer; q8 != NULL: FP8 experts (W1, W2, W3 are then q8's codes).
+static moe_status forward_impl(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
+                               const float* router_noise, const void* W1, const void* b1, const void* W2,
+                               const void* b2, const void* W3, const moe_fp8_experts* q8, void* y,
+                               int32_t* topk_idx, float* topk_w, int32_t* expert_counts, uint8_t* dropped_mask,
+                               float* f, float* P, float* L_aux, float* route_stats, float* router_logits,
+                               int32_t* perm_token, int32_t* slot, void* workspace, size_t workspace_bytes,
+                               moe_stream stream, const moe_launch_opts* opts) {
   moe_status st = check_cfg(cfg);
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
+  const bool fp8 = (c.flags & MOE_FLAG_FP8_EXPERTS) != 0;
+  if (fp8 != (q8 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (fp8) {
+    if (!q8->s1 || !q8->s2 || (q8->W3 != nullptr) != (q8->s3 != nullptr)) return MOE_ERR_INVALID_ARG;
+    const void* sc[] = {q8->s1, q8->s2, q8->s3};
+    for (const void* p : sc)
+      if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  }
   const bool swiglu = c.act == MOE_ACT_SWIGLU;
   // Required tensors.  With T == 0 the per-token tensors hold no elements and
   // may be NULL (allocators hand out NULL for empty buffers).
@@ -328,9 +347,17 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
       return MOE_ERR_CUDA;
   }
   GatherArgs ga;
+  memset(&ga, 0, sizeof(ga));
   ga.x = x; ga.T = c.T; ga.d = c.d_model; ga.E = c.E; ga.k = c.k; ga.dtype = c.dtype; ga.capacity = C;
   ga.topk_idx = topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.offsets = sa.offsets; ga.slot = slot_buf;
   ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm; ga.err = &hdr->err; ga.nblk = L.nblk;
+  const bool sh8 = fp8 && c.n_shared > 0;
+  if (fp8) {
+    ga.fp8 = true;
+    ga.xs_perm = (float*)(ws + L.xs_perm);
+    ga.xq = sh8 ? ws + L.xq : nullptr;
+    ga.xs_tok = sh8 ? (float*)(ws + L.xs_tok) : nullptr;
+  }
   if (!ec && launch_gather(ga, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 4./5. expert GEMMs
@@ -344,6 +371,12 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   g1.B = W1; g1.B3 = W3; g1.Gw = L.G; g1.bias = b1; g1.C = ws + L.h; g1.max_mtiles = c.T > 0 ? max_mtiles : 0;
   g1.err = &hdr->err; g1.timeout_ns = timeout;
   g1.single_cta = opts && (opts->flags & MOE_OPT_GEMM_SINGLE_CTA);
+  if (fp8) {
+    g1.fp8 = true;
+    g1.A1 = sh8 ? ws + L.xq : nullptr;
+    g1.a_scale0 = (const float*)(ws + L.xs_perm); g1.a_scale1 = sh8 ? (const float*)(ws + L.xs_tok) : nullptr;
+    g1.B = q8->W1; g1.B3 = q8->W3; g1.b_scale = q8->s1; g1.b3_scale = q8->s3;
+  }
   if (clk.mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_grouped_gemm(g1, s) != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -352,6 +385,19 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   g2.A0 = ws + L.h; g2.rows_A0 = L.rows_all > 0 ? L.rows_all : 1; g2.A1 = nullptr; g2.rows_A1 = 0;
   g2.B = W2; g2.B3 = nullptr; g2.bias = b2; g2.C = ws + L.o; g2.out_f32 = true;
   if (clk.mark(4) != cudaSuccess) return MOE_ERR_CUDA;
+  if (fp8) {
+    // H (bf16) -> E4M3 codes with one scale per row: the kept routed rows and the shared rows.
+    QuantRowsArgs qa;
+    qa.X = ws + L.h; qa.Q = ws + L.hq; qa.scale = (float*)(ws + L.hs); qa.cols = c.d_ff;
+    qa.rows0 = c.T > 0 ? L.rows_tk : 0; qa.live0 = sa.offsets + c.E;
+    qa.row1 = L.rows_tk; qa.rows1 = (int64_t)c.n_shared * c.T; qa.err = &hdr->err;
+    if (launch_quantize_rows(qa, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (opts && opts->stage_events && cudaEventRecord((cudaEvent_t)opts->stage_events[MOE_NUM_STAGES + 1], s) !=
+                                          cudaSuccess)
+      return MOE_ERR_CUDA;
+    g2.A0 = ws + L.hq; g2.a_scale0 = (const float*)(ws + L.hs); g2.a_scale1 = nullptr;
+    g2.B = q8->W2; g2.b_scale = q8->s2; g2.b3_scale = nullptr;
+  }
   if (launch_grouped_gemm(g2, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 6. combine
@@ -373,19 +419,90 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, co
   return MOE_OK;
 }
 
+moe_status moe_forward(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
+                       const float* router_noise, const void* W1, const void* b1, const void* W2, const void* b2,
+                       const void* W3, void* y, int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                       uint8_t* dropped_mask, float* f, float* P, float* L_aux, float* route_stats,
+                       float* router_logits, int32_t* perm_token, int32_t* slot, void* workspace,
+                       size_t workspace_bytes, moe_stream stream, const moe_launch_opts* opts) {
+  if (cfg && (cfg->flags & MOE_FLAG_FP8_EXPERTS)) return MOE_ERR_INVALID_ARG;   // moe_forward_fp8
+  return forward_impl(cfg, x, W_g, b_g, router_noise, W1, b1, W2, b2, W3, nullptr, y, topk_idx, topk_w,
+                      expert_counts, dropped_mask, f, P, L_aux, route_stats, router_logits, perm_token, slot,
+                      workspace, workspace_bytes, stream, opts);
+}
+
+moe_status moe_forward_fp8(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,
+                           const float* router_noise, const moe_fp8_experts* w, const void* b1, const void* b2,
+                           void* y, int32_t* topk_idx, float* topk_w, int32_t* expert_counts, uint8_t* dropped_mask,
+                           float* f, float* P, float* L_aux, float* route_stats, float* router_logits,
+                           int32_t* perm_token, int32_t* slot, void* workspace, size_t workspace_bytes,
+                           moe_stream stream, const moe_launch_opts* opts) {
+  if (!cfg || !(cfg->flags & MOE_FLAG_FP8_EXPERTS) || !w) return MOE_ERR_INVALID_ARG;
+  return forward_impl(cfg, x, W_g, b_g, router_noise, w->W1, b1, w->W2, b2, w->W3, w, y, topk_idx, topk_w,
+                      expert_counts, dropped_mask, f, P, L_aux, route_stats, router_logits, perm_token, slot,
+                      workspace, workspace_bytes, stream, opts);
+}
+
+moe_status moe_quantize_weights_fp8(const void* W, int64_t G, int64_t K, int64_t N, uint8_t* Wq, float* scale,
+                                    moe_stream stream) {
+  if (G < 0 || K < 0 || N < 0) return MOE_ERR_INVALID_ARG;
+  if (G == 0 || K == 0 || N == 0) return MOE_OK;
+  if (!W || !Wq || !scale || !aligned16(W) || !aligned16(Wq) || !aligned16(scale)) return MOE_ERR_INVALID_ARG;
+  if (K % 16 != 0 || G > 65535) return MOE_ERR_UNSUPPORTED;
+  QuantWeightsArgs a;
+  a.W = W; a.Q = Wq; a.scale = scale; a.G = G; a.K = K; a.N = N;
+  return launch_quantize_weights(a, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_quantize_rows_fp8(const void* X, int64_t rows, int64_t cols, uint8_t* Q, float* scale,
+                                 moe_stream stream) {
+  if (rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return MOE_OK;
+  if (!X || !Q || !scale || !aligned16(X) || !aligned16(Q) || !aligned16(scale)) return MOE_ERR_INVALID_ARG;
+  if (cols % 16 != 0 || rows >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  QuantRowsArgs a;
+  a.X = X; a.Q = Q; a.scale = scale; a.cols = cols; a.rows0 = rows; a.live0 = nullptr; a.row1 = rows;
+  a.rows1 = 0; a.err = nullptr;
+  return launch_quantize_rows(a, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_workspace_region(const moe_config* cfg, int32_t region, size_t* offset, size_t* bytes) {
+  if (check_cfg(cfg) != MOE_OK || !offset || !bytes) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout(cfg);
+  const bool fp8 = (cfg->flags & MOE_FLAG_FP8_EXPERTS) != 0;
+  const size_t esz = cfg->dtype == MOE_DT_BF16 ? 2 : 4;
+  const size_t d = cfg->d_model, f = cfg->d_ff, tk = (size_t)L.rows_tk, ra = (size_t)L.rows_all;
+  switch (region) {
+    case MOE_REGION_XPERM: *offset = L.xperm; *bytes = tk * d * (fp8 ? 1 : esz); return MOE_OK;
+    case MOE_REGION_H: *offset = L.h; *bytes = ra * f * esz; return MOE_OK;
+    case MOE_REGION_O: *offset = L.o; *bytes = ra * d * 4; return MOE_OK;
+    default: break;
+  }
+  if (!fp8) return MOE_ERR_INVALID_ARG;
+  switch (region) {
+    case MOE_REGION_X_SCALE: *offset = L.xs_perm; *bytes = tk * 4; return MOE_OK;
+    case MOE_REGION_H_CODES: *offset = L.hq; *bytes = ra * f; return MOE_OK;
+    case MOE_REGION_H_SCALE: *offset = L.hs; *bytes = ra * 4; return MOE_OK;
+    default: return MOE_ERR_INVALID_ARG;
+  }
+}
+
 size_t moe_forward_host_workspace_size(const moe_config* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
   return host_stage(cfg, layout(cfg).total).total;
 }
 
-moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const void* W_g, const void* b_g,
-                            const float* router_noise_host, const void* W1, const void* b1, const void* W2,
-                            const void* b2, const void* W3, void* y_host, int32_t* topk_idx_host, float* topk_w_host,
-                            int32_t* expert_counts_host, uint8_t* dropped_mask_host, float* f_host, float* P_host,
-                            float* L_aux_host, float* route_stats_host, void* workspace, size_t workspace_bytes,
-                            moe_stream stream, const moe_launch_opts* opts) {
+// moe_forward_host / moe_forward_fp8_host (q8 != NULL).
+static moe_status forward_host_impl(const moe_config* cfg, const void* x_host, const void* W_g, const void* b_g,
+                                    const float* router_noise_host, const void* W1, const void* b1, const void* W2,
+                                    const void* b2, const void* W3, const moe_fp8_experts* q8, void* y_host,
+                                    int32_t* topk_idx_host, float* topk_w_host, int32_t* expert_counts_host,
+                                    uint8_t* dropped_mask_host, float* f_host, float* P_host, float* L_aux_host,
+                                    float* route_stats_host, void* workspace, size_t workspace_bytes,
+                                    moe_stream stream, const moe_launch_opts* opts) {
   moe_status st = check_cfg(cfg);
   if (st != MOE_OK) return st;
+  if (((cfg->flags & MOE_FLAG_FP8_EXPERTS) != 0) != (q8 != nullptr)) return MOE_ERR_INVALID_ARG;
   const moe_config& c = *cfg;
   const bool empty = c.T == 0;
   const bool ec = (c.flags & MOE_FLAG_EXPERT_CHOICE) != 0;
@@ -407,11 +524,11 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
   if (router_noise_host && nbytes &&
       cudaMemcpyAsync(ws + h.noise, router_noise_host, nbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  st = moe_forward(cfg, ws + h.x, W_g, b_g, router_noise_host ? (const float*)(ws + h.noise) : nullptr, W1, b1, W2,
-                   b2, W3, ws + h.y, (int32_t*)(ws + h.idx), (float*)(ws + h.w), (int32_t*)(ws + h.cnt),
-                   ws + h.drop, (float*)(ws + h.f), (float*)(ws + h.P), (float*)(ws + h.L),
-                   route_stats_host ? (float*)(ws + h.stats) : nullptr, nullptr, nullptr, nullptr, workspace, L.total,
-                   stream, opts);
+  st = forward_impl(cfg, ws + h.x, W_g, b_g, router_noise_host ? (const float*)(ws + h.noise) : nullptr, W1, b1,
+                    W2, b2, W3, q8, ws + h.y, (int32_t*)(ws + h.idx), (float*)(ws + h.w), (int32_t*)(ws + h.cnt),
+                    ws + h.drop, (float*)(ws + h.f), (float*)(ws + h.P), (float*)(ws + h.L),
+                    route_stats_host ? (float*)(ws + h.stats) : nullptr, nullptr, nullptr, nullptr, workspace,
+                    L.total, stream, opts);
   if (st != MOE_OK) return st;
   struct Copy { void* dst; size_t off, bytes; } copies[] = {
       {y_host, h.y, ybytes},          {topk_idx_host, h.idx, tk * 4}, {topk_w_host, h.w, tk * 4},
@@ -422,6 +539,30 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
     if (cp.dst && cp.bytes && cudaMemcpyAsync(cp.dst, ws + cp.off, cp.bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const void* W_g, const void* b_g,
+                            const float* router_noise_host, const void* W1, const void* b1, const void* W2,
+                            const void* b2, const void* W3, void* y_host, int32_t* topk_idx_host, float* topk_w_host,
+                            int32_t* expert_counts_host, uint8_t* dropped_mask_host, float* f_host, float* P_host,
+                            float* L_aux_host, float* route_stats_host, void* workspace, size_t workspace_bytes,
+                            moe_stream stream, const moe_launch_opts* opts) {
+  if (cfg && (cfg->flags & MOE_FLAG_FP8_EXPERTS)) return MOE_ERR_INVALID_ARG;   // moe_forward_fp8_host
+  return forward_host_impl(cfg, x_host, W_g, b_g, router_noise_host, W1, b1, W2, b2, W3, nullptr, y_host,
+                           topk_idx_host, topk_w_host, expert_counts_host, dropped_mask_host, f_host, P_host,
+                           L_aux_host, route_stats_host, workspace, workspace_bytes, stream, opts);
+}
+
+moe_status moe_forward_fp8_host(const moe_config* cfg, const void* x_host, const void* W_g, const void* b_g,
+                                const float* router_noise_host, const moe_fp8_experts* w, const void* b1,
+                                const void* b2, void* y_host, int32_t* topk_idx_host, float* topk_w_host,
+                                int32_t* expert_counts_host, uint8_t* dropped_mask_host, float* f_host, float* P_host,
+                                float* L_aux_host, float* route_stats_host, void* workspace, size_t workspace_bytes,
+                                moe_stream stream, const moe_launch_opts* opts) {
+  if (!cfg || !(cfg->flags & MOE_FLAG_FP8_EXPERTS) || !w) return MOE_ERR_INVALID_ARG;
+  return forward_host_impl(cfg, x_host, W_g, b_g, router_noise_host, w->W1, b1, w->W2, b2, w->W3, w, y_host,
+                           topk_idx_host, topk_w_host, expert_counts_host, dropped_mask_host, f_host, P_host,
+                           L_aux_host, route_stats_host, workspace, workspace_bytes, stream, opts);
 }
 
 size_t moe_backward_workspace_size(const moe_config* cfg) {

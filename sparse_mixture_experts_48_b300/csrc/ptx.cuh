@@ -159,5 +159,9 @@ bool tmap_bf16_2d_swizzle(CUtensorMap* m, const void* ptr, int64_t rows, int64_t
                           int row_bytes);
 // Stacked bf16 matrices [G, rows, cols], box box_cols x box_rows x 1, 128-byte swizzle.
 bool tmap_bf16_3d(CUtensorMap* m, const void* ptr, int G, int64_t rows, int64_t cols, int box_cols, int box_rows);
+// Byte matrices (E4M3 codes): row-major [rows, cols] and stacked [G, rows, cols],
+// box 128 bytes x box_rows (x 1), 128-byte swizzle.
+bool tmap_u8_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows);
+bool tmap_u8_3d(CUtensorMap* m, const void* ptr, int G, int64_t rows, int64_t cols, int box_rows);
 
 }  // namespace moe

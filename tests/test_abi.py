@@ -23,7 +23,7 @@ def L():
 def _declared():
     src = open(os.path.join(ROOT, "include", "moe.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_exports_every_declared_entry_point(L):
@@ -134,3 +134,53 @@ def test_grouped_gemm_host_checks(L):
              P(0x100000), ws, None, None) == 1
     assert f(moe.BF16, moe.NONE, 4, P(0x800), 256, 128, 128, P(0x1000), P(0x2000), None, None, P(0x3000),
              P(0x100000), ws - 1, None, None) == 3
+
+
+def test_fp8_config_rules(L):
+    c8 = _cfg(fp8_experts=True)
+    assert moe.validate(c8) == 0
+    assert moe.workspace_size(c8) > 0 and moe.workspace_size(c8) != moe.workspace_size(_cfg())
+    assert moe.validate(_cfg(fp8_experts=True, dtype=moe.F32, d=64, f=64)) == 2
+    assert moe.validate(_cfg(fp8_experts=True, expert_choice=True)) == 2
+    # FP8 regions exist only with the flag
+    assert moe.workspace_region(c8, moe.REGION_H_CODES)[1] == (4096 * 2) * 3072
+    with pytest.raises(moe.MoEError):
+        moe.workspace_region(_cfg(), moe.REGION_H_CODES)
+    assert moe.workspace_region(_cfg(), moe.REGION_H)[1] == (4096 * 2) * 3072 * 2
+    # the flag routes to moe_forward_fp8: moe_forward refuses it, the host path and the backward too
+    assert _call_forward(L, c8, ws_bytes=moe.workspace_size(c8)) == 1
+    assert L.moe_forward_host_workspace_size(ctypes.byref(moe.c_config(c8))) > moe.workspace_size(c8)
+    assert L.moe_backward_workspace_size(ctypes.byref(moe.c_config(c8))) == 0
+
+
+def _call_forward_fp8(L, cfg, w, **over):
+    P = ctypes.c_void_p
+    args = dict(x=P(0x10000), W_g=P(0x20000), y=P(0x50000000), ws=P(0x100000), ws_bytes=moe.workspace_size(cfg))
+    args.update(over)
+    c = moe.c_config(cfg)
+    wp = ctypes.byref(w) if w is not None else None
+    return L.moe_forward_fp8(ctypes.byref(c), args["x"], args["W_g"], None, None, wp, None, None, args["y"],
+                             P(0x60000), P(0x70000), P(0x80000), P(0x90000), P(0xA0000), P(0xB0000), P(0xC0000),
+                             None, None, None, None, args["ws"], args["ws_bytes"], None, None)
+
+
+def test_forward_fp8_host_checks(L):
+    c8 = _cfg(fp8_experts=True)
+    w = moe._CFp8(0x30000, 0x31000, None, None, 0x40000, 0x41000)
+    assert _call_forward_fp8(L, c8, None) == 1                            # no weights
+    assert _call_forward_fp8(L, _cfg(), w, ws_bytes=moe.workspace_size(_cfg())) == 1   # flag missing
+    assert _call_forward_fp8(L, c8, moe._CFp8(0x30000, None, None, None, 0x40000, 0x41000)) == 1  # no s1
+    assert _call_forward_fp8(L, c8, moe._CFp8(0x30000, 0x31004, None, None, 0x40000, 0x41000)) == 1  # misaligned
+    assert _call_forward_fp8(L, c8, w, ws_bytes=moe.workspace_size(c8) - 1) == 3
+    assert _call_forward_fp8(L, c8, w, x=None) == 1
+
+
+def test_quantize_host_checks(L):
+    P = ctypes.c_void_p
+    assert L.moe_quantize_weights_fp8(P(0x1000), 2, 100, 64, P(0x2000), P(0x3000), None) == 2     # K % 16
+    assert L.moe_quantize_weights_fp8(P(0x1000), 2, 64, 64, None, P(0x3000), None) == 1
+    assert L.moe_quantize_weights_fp8(P(0x1008), 2, 64, 64, P(0x2000), P(0x3000), None) == 1       # misaligned
+    assert L.moe_quantize_weights_fp8(None, 0, 64, 64, None, None, None) == 0                      # empty
+    assert L.moe_quantize_rows_fp8(P(0x1000), 4, 40, P(0x2000), P(0x3000), None) == 2              # cols % 16
+    assert L.moe_quantize_rows_fp8(P(0x1000), -1, 64, P(0x2000), P(0x3000), None) == 1
+    assert L.moe_quantize_rows_fp8(None, 0, 64, None, None, None) == 0

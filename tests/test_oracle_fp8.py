@@ -164,3 +164,38 @@ def test_fp8_layer_is_close_to_the_unquantised_layer(base):
     y = oracle.forward(cfg, inp)["y"]
     rel = np.linalg.norm(y8 - y) / np.linalg.norm(y)
     assert 1e-3 < rel < 8e-2, rel
+
+
+@pytest.mark.parametrize("act", [si.GELU, si.SWIGLU])
+def test_fp8_expert_halves_against_numpy(act):
+    """fp8_hidden and fp8_out (the two halves of one FP8 expert) against numpy
+    matmuls on the decoded operands, repeated while other arrays are allocated
+    and freed: the wrappers' argument buffers (the fp32 biases are converted
+    on the fly) must stay alive through each call."""
+    cfg = si.CONFIGS["gpt2_top2_gelu_bf16"].replace(T=4, d=128, f=192, E=3, act=act)
+    inp = si.layer_inputs(cfg, seed=12)
+    if act == si.SWIGLU:
+        inp["b1"] = inp["b2"] = None
+    wq = oracle.quantize_experts(cfg, inp)
+    xq, xs = oracle.quantize_rows(inp["x"])
+    g = 2
+    W1d = oracle.e4m3_values(wq["W1q"][g]) * wq["s1"][g][:, None]             # [f, d]
+    a = W1d @ (oracle.e4m3_values(xq[1]) * float(xs[1]))
+    if act == si.SWIGLU:
+        u = (oracle.e4m3_values(wq["W3q"][g]) * wq["s3"][g][:, None]) @ (oracle.e4m3_values(xq[1]) * float(xs[1]))
+        h_ref = a / (1.0 + np.exp(-a)) * u
+    else:
+        from scipy.special import erf
+        a = a + si.as_f32(inp["b1"])[g]
+        h_ref = 0.5 * a * (1.0 + erf(a / np.sqrt(2.0)))
+    hq, hs = oracle.quantize_rows(_bf16_round_array(h_ref).astype(np.float32))
+    o_ref = (oracle.e4m3_values(wq["W2q"][g]) * wq["s2"][g][:, None]) @ (oracle.e4m3_values(hq[0]) * float(hs[0]))
+    if act != si.SWIGLU:
+        o_ref = o_ref + si.as_f32(inp["b2"])[g]
+    for i in range(50):
+        churn = [np.ones(500 + 7 * i) for _ in range(4)]
+        h = oracle.fp8_hidden(cfg, g, xq[1], xs[1], wq, inp)
+        o = oracle.fp8_out(cfg, g, hq[0], hs[0], wq, inp)
+        del churn
+        np.testing.assert_allclose(h, h_ref, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-14)
