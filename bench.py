@@ -377,6 +377,13 @@ def main():
     n_ev = moe.NUM_STAGES + (2 if fp8 else 1)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K)]
     experts8 = moe.quantize_experts_fp8(d["W1"], d["W2"], d["W3"]) if fp8 else None
+    if fp8:
+        # the layer keeps only the E4M3 codes and scales of the expert weights
+        torch.cuda.synchronize()
+        for n in ("W1", "W2", "W3"):
+            d[n] = None
+        args_in = None
+        torch.cuda.empty_cache()
 
     def step(i=None):
         if fp8:
@@ -453,7 +460,7 @@ def main():
     gemm_tf = (alg["gemm1_flop"] + alg["gemm2_flop"]) / (gemm_ms / 1e3) / 1e12
     dom = "expert_gemm1"
     dom_tf = kernels[dom]["TFLOP/s"]
-    traffic = None if fp8 else measured_traffic(cfg, dom, args.gemm_one_cta)
+    traffic = measured_traffic(cfg, dom + ("_fp8" if fp8 else ""), args.gemm_one_cta)
     src = ("measured bf16_tflops_sustained x 2 (nominal E4M3 / bf16 dense ratio)" if fp8 else
            "measured bf16_tflops_sustained (cuBLAS bf16, back to back)")
     if peak_kind != "measured":
@@ -471,7 +478,7 @@ def main():
         x_host = torch.empty(d["x"].shape, dtype=d["x"].dtype, pin_memory=True)
         x_host.copy_(d["x"].cpu())
         noise_host = noise.cpu().pin_memory() if noise is not None else None
-        weights = args_in[1:]
+        weights = args_in[1:] if args_in is not None else None
         streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
         hws = [torch.empty((moe.host_workspace_size(cfg),), dtype=torch.uint8, device=dev) for _ in range(2)]
         houts = [moe.alloc_host_outputs(cfg) for _ in range(2)]
@@ -538,7 +545,7 @@ def main():
                                    "per row); router, x, y in bf16" if fp8 else "bf16"),
                        "l2": "no flush: inputs larger than L2 (x %.0f MB, expert weights %.2f GB)" % (
                            inp["x"].nbytes / 1e6, sum(inp[n].nbytes for n in ("W1", "W2", "W3")
-                                                      if inp[n] is not None) / 1e9)},
+                                                      if inp[n] is not None) / (2e9 if fp8 else 1e9))},
             "grouped_gemm": {"tflops": round(gemm_tf, 1), f"frac_of_{tc_tag}_sustained": round(gemm_tf / tc_sust, 4),
                              f"frac_of_{tc_tag}_burst": round(gemm_tf / tc_burst, 4), "ms": round(float(gemm_ms), 4)},
             "roofline": roofline,
