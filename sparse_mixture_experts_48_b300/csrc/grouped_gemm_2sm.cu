@@ -84,8 +84,17 @@ struct Ctl {
   int asrc[MAX_G];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// fp32 outputs (expert GEMM 2) stage each epilogue warp's 32 x 32 tile in
+// shared memory for a TMA store: 4 KB per warp, paid for with one ring stage.
+constexpr int kStageTileBytes = 32 * 32 * 4;
+template <bool OUT_F32>
+constexpr int ring_stages() { return OUT_F32 ? STAGES - 1 : STAGES; }
+template <bool OUT_F32>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)ring_stages<OUT_F32>() * STAGE_BYTES + sizeof(Ctl) +
+         (OUT_F32 ? 1024 + (size_t)EPI_WARPS * kStageTileBytes : 0);
+}
+static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ void map_tile(const Ctl& c, int G, int n_tiles, int tile, int& g, int& m, int& n) {
   int lo = 0, hi = G - 1;
@@ -129,13 +138,17 @@ __device__ __forceinline__ void scale_acc32(uint32_t (&v)[32], float ra, const f
 template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE, bool FP8 = false>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3, GemmArgs a) {
+                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3,
+                     const __grid_constant__ CUtensorMap tmC, GemmArgs a) {
   constexpr int BN_OUT = SWIGLU ? 128 : 256;   // output columns per pair tile
+  constexpr int NST = ring_stages<OUT_F32>();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;            // 1 KB aligned ring for the 128-byte swizzle
   uint8_t* ring = smem_raw + (base - raw);
-  Ctl& c = *reinterpret_cast<Ctl*>(ring + STAGES * STAGE_BYTES);
+  Ctl& c = *reinterpret_cast<Ctl*>(ring + NST * STAGE_BYTES);
+  // OUT_F32: the epilogue warps' TMA-store tiles, 1 KB aligned (128-byte swizzle)
+  const uint32_t stg = (base + (uint32_t)(NST * STAGE_BYTES + sizeof(Ctl)) + 1023u) & ~1023u;
   volatile uint32_t* abort = &c.abort;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -181,7 +194,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 31) c.mt[G] = incl;
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&c.full[s]), 1);
       mbar_init(smem_u32(&c.empty[s]), 1);
     }
@@ -221,9 +234,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t full_leader = mapa_shared(smem_u32(&c.full[0]), 0);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_phase[STAGES];
-      bool issued[STAGES];
-      for (int s = 0; s < STAGES; ++s) { issued[s] = false; issued_phase[s] = 0; }
+      uint32_t issued_phase[NST];
+      bool issued[NST];
+      for (int s = 0; s < NST; ++s) { issued[s] = false; issued_phase[s] = 0; }
       for (int tile = pair; tile < total; tile += npairs) {
         int g, m, n;
         map_tile(c, G, n_tiles, tile, g, m, n);
@@ -256,14 +269,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           issued[stage] = true;
           issued_phase[stage] = phase;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
       }
       // Both CTAs' copies complete on the leader's barriers: the leader
       // waits for every stage it armed before the pair may tear down.
       if (rank == 0)
-        for (int s = 0; s < STAGES; ++s)
+        for (int s = 0; s < NST; ++s)
           if (issued[s]) mbar_drain(smem_u32(&c.full[s]), issued_phase[s], drain_limit);
     }
   } else if (warp == 1) {
@@ -307,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
           mma_commit_cta2(smem_u32(&c.empty[stage]), 0x3);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         mma_commit_cta2(smem_u32(&c.tfull[acc]), 0x3);
@@ -343,6 +356,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * MMA_N);
       float ra = 0.f;                       // FP8: this row's decoding scale
       if (FP8 && valid) ra = (c.asrc[g] ? a.a_scale1 : a.a_scale0)[c.arow[g] + grow];
+      // fp32 output: a warp whose 32 rows all lie inside the segment stores
+      // each 32 x 32 chunk with one TMA store (a partial warp stores its valid
+      // rows itself, so no store reaches the next segment's rows).
+      const int wrow0 = m * BMP + (int)rank * BMC + q * 32;
+      const bool tma_st = OUT_F32 && a.rows_C > 0 && wrow0 + 31 < c.rows[g];
+      const uint32_t wbuf = stg + (uint32_t)((warp - 2) * kStageTileBytes);
       constexpr int CHUNKS = BN_OUT / 32;   // 32-column chunks per tile
       for (int ch = half * (CHUNKS / 2); ch < (half + 1) * (CHUNKS / 2); ++ch) {
         const int col0 = n0 + ch * 32;
@@ -398,7 +417,26 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) f[i] = gelu_erf(f[i]);
             }
-            if (OUT_F32) {
+            if (OUT_F32 && tma_st) {
+              // Row `lane` of the warp's tile, 16-byte chunk i at lane * 128 + ((i ^ (lane & 7)) << 4):
+              // the 128-byte swizzle the tensor map reads back.  The buffer is
+              // reused once the previous chunk's store has read it.
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint32_t at = wbuf + (uint32_t)(lane * 128) + ((uint32_t)(i ^ (lane & 7)) << 4);
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(at), "f"(f[4 * i]), "f"(f[4 * i + 1]),
+                             "f"(f[4 * i + 2]), "f"(f[4 * i + 3])
+                             : "memory");
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmC, wbuf, col0, (int)(c.orow[g] + wrow0));
+                bulk_commit_group();
+              }
+            } else if (OUT_F32) {
               float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.C) + orow * a.N + col0);
 #pragma unroll
               for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
@@ -417,6 +455,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader + (uint32_t)(acc * 8));
     }
+    // The tiles' TMA stores have completed before the CTA's shared memory goes.
+    if (OUT_F32 && lane == 0) bulk_wait_all();
   }
 
   // ---- tear-down: both CTAs here, nothing in flight, then free TMEM ----
@@ -438,6 +478,11 @@ template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE = false, bool FP8 = false>
 cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtensorMap& mA1, const CUtensorMap& mB,
                         const CUtensorMap& mB3, int64_t max_pair_tiles, cudaStream_t s) {
   auto kernel = gemm_pair_kernel<SWIGLU, OUT_F32, SAVE_PRE, FP8>;
+  constexpr size_t kSmemBytes = smem_bytes<OUT_F32>();
+  // C as an fp32 tensor map for the TMA-store epilogue (else an unused copy of A's)
+  CUtensorMap mC = mA0;
+  GemmArgs args = a;
+  if (!OUT_F32 || a.rows_C <= 0 || !tmap_f32_2d(&mC, a.C, a.rows_C, a.N, 32)) args.rows_C = 0;
   static int max_clusters = -1;   // per kernel instantiation, per process (one device type)
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -462,7 +507,7 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtenso
   }
   const int64_t pairs = max_pair_tiles < max_clusters ? max_pair_tiles : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kernel, mA0, mA1, mB, mB3, a);
+  return cudaLaunchKernelEx(&cfg, kernel, mA0, mA1, mB, mB3, mC, args);
 }
 
 }  // namespace

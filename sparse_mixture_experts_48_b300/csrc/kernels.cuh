@@ -182,6 +182,8 @@ struct GemmArgs {
   // codes stored [Gw, N, K] (K-major) with one scale per (slab, column)
   // (b_scale / b3_scale, [Gw, N]).  The epilogue multiplies the accumulator by
   // both scales before the bias and the activation.
+  int64_t rows_C;       // rows of C; > 0 with out_f32 lets the pair kernel store whole 32-row
+                        // warp tiles by TMA (0: per-thread stores only)
   bool fp8;
   const float* a_scale0;
   const float* a_scale1;

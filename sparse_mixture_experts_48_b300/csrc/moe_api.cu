@@ -383,7 +383,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   GemmArgs g2 = g1;
   g2.act = MOE_ACT_NONE; g2.K = c.d_ff; g2.N = c.d_model; g2.a_from_out_rows = true;
   g2.A0 = ws + L.h; g2.rows_A0 = L.rows_all > 0 ? L.rows_all : 1; g2.A1 = nullptr; g2.rows_A1 = 0;
-  g2.B = W2; g2.B3 = nullptr; g2.bias = b2; g2.C = ws + L.o; g2.out_f32 = true;
+  g2.B = W2; g2.B3 = nullptr; g2.bias = b2; g2.C = ws + L.o; g2.out_f32 = true; g2.rows_C = L.rows_all;
   if (clk.mark(4) != cudaSuccess) return MOE_ERR_CUDA;
   if (fp8) {
     // H (bf16) -> E4M3 codes with one scale per row: the kept routed rows and the shared rows.
@@ -652,7 +652,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
   GemmArgs g2 = g1;
   g2.act = MOE_ACT_NONE; g2.K = f; g2.N = d; g2.a_from_out_rows = true; g2.A0 = ws + L.h; g2.rows_A0 = L.rows_all;
   g2.A1 = nullptr; g2.rows_A1 = 0; g2.B = W2; g2.B3 = nullptr; g2.bias = b2; g2.C = ws + L.o; g2.out_f32 = true;
-  g2.pre_a = nullptr; g2.pre_u = nullptr;
+  g2.pre_a = nullptr; g2.pre_u = nullptr; g2.rows_C = L.rows_all;
   if (launch_grouped_gemm(g2, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // ---- backward ----

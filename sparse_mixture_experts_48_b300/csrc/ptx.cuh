@@ -152,7 +152,25 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
 // Row-major bf16 matrix [rows, cols] (cols contiguous), box box_cols x box_rows,
 // 128-byte swizzle, zero fill outside the matrix.  False if it cannot be encoded
 // (unaligned base or stride, or no driver entry point).
+// TMA store of a box from this CTA's shared memory to global memory, tracked by
+// the issuing thread's bulk-async groups.  The source follows the tensor map's
+// swizzle; the generic-proxy writes that filled it must be fenced first.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(c0),
+               "r"(c1), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The source shared memory of every committed group has been read.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Every committed group has completed its writes.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 bool tmap_bf16_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows);
+// Row-major fp32 [rows, cols] (cols a multiple of 4), box 32 columns (128
+// bytes) x box_rows, 128-byte swizzle: the layout of an fp32 epilogue tile.
+bool tmap_f32_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows);
 // As tmap_bf16_2d with the swizzle chosen by the box row size: 16 bytes none,
 // 32 / 64 / 128 bytes the matching swizzle mode.
 bool tmap_bf16_2d_swizzle(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows,
