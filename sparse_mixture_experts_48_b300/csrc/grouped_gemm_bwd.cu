@@ -73,13 +73,24 @@ struct Ctl {
   int orow[MAX_G];
   int asrc[MAX_G];
 };
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-
-__device__ __forceinline__ float silu_grad(float a) {
-  const float s = 1.f / (1.f + __expf(-a));
-  return s + a * s * (1.f - s);
+// fp32 outputs (dgrad of the grouped rows, weight gradients) leave through
+// shared memory and TMA stores: a 4 KB 32 x 32 tile per epilogue warp, paid
+// for with one ring stage.
+constexpr int kStageTileBytes = 32 * 32 * 4;
+// (The activation backward stages its two bf16 32 x 32 outputs, dA and dU, in
+// the same 4 KB per warp.)
+template <int MODE>
+constexpr int ring_stages() { return STAGES - 1; }
+template <int MODE>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)ring_stages<MODE>() * STAGE_BYTES + sizeof(Ctl) + 1024 + (size_t)EPI_WARPS * kStageTileBytes;
 }
+static_assert(smem_bytes<kDgradF32>() <= 227 * 1024 && smem_bytes<kDgradAct>() <= 227 * 1024,
+              "shared memory per CTA");
+
+// sigma(a) with the fast divide (0 for a below about -87, where 1 + e^-a
+// leaves the divide's range; sigma is below 1e-37 there).
+__device__ __forceinline__ float sigmoid_fast(float a) { return __fdividef(1.f, 1.f + __expf(-a)); }
 __device__ __forceinline__ float gelu_grad(float z) {
   // d/dz [z Phi(z)] = Phi(z) + z phi(z)
   return 0.5f * (1.f + erff(z * 0.70710678118654752f)) + z * 0.39894228040143268f * __expf(-0.5f * z * z);
@@ -89,13 +100,17 @@ template <int MODE, bool TWO_PHASE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
-                    BwdGemmArgs a) {
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, BwdGemmArgs a,
+                    int tma_store) {
   constexpr bool WGRAD = MODE == kWgrad;
+  constexpr int NST = ring_stages<MODE>();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* ring = smem_raw + (base - raw);
-  Ctl& c = *reinterpret_cast<Ctl*>(ring + STAGES * STAGE_BYTES);
+  Ctl& c = *reinterpret_cast<Ctl*>(ring + NST * STAGE_BYTES);
+  // fp32 outputs: the epilogue warps' TMA-store tiles, 1 KB aligned (128-byte swizzle)
+  const uint32_t stg = (base + (uint32_t)(NST * STAGE_BYTES + sizeof(Ctl)) + 1023u) & ~1023u;
   volatile uint32_t* abort = &c.abort;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -139,7 +154,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 31) c.mt[G] = incl;
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&c.full[s]), 1);
       mbar_init(smem_u32(&c.empty[s]), 1);
     }
@@ -182,6 +197,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     g = lo;
     const int local = tile - c.mt[g];
+    if (WGRAD && a.M > a.N) {
+      // Pairs running at the same time share the larger operand's column
+      // block (X^T rows m) and sweep the smaller one's, which stays in L2.
+      m = local / n_tiles;
+      n = local - m * n_tiles;
+      return;
+    }
     const int mtg = WGRAD ? m_tiles_w : (c.mt[g + 1] - c.mt[g]) / n_tiles;
     n = local / mtg;
     m = local - n * mtg;
@@ -194,9 +216,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t full_leader = mapa_shared(smem_u32(&c.full[0]), 0);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_phase[STAGES];
-      bool issued[STAGES];
-      for (int s = 0; s < STAGES; ++s) { issued[s] = false; issued_phase[s] = 0; }
+      uint32_t issued_phase[NST];
+      bool issued[NST];
+      for (int s = 0; s < NST; ++s) { issued[s] = false; issued_phase[s] = 0; }
       for (int tile = pair; tile < total; tile += npairs) {
         int g, m, n;
         map_tile(tile, g, m, n);
@@ -234,12 +256,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           issued[stage] = true;
           issued_phase[stage] = phase;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
       }
       if (rank == 0)
-        for (int s = 0; s < STAGES; ++s)
+        for (int s = 0; s < NST; ++s)
           if (issued[s]) mbar_drain(smem_u32(&c.full[s]), issued_phase[s], drain_limit);
     }
   } else if (warp == 1) {
@@ -282,7 +304,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mma_bf16_cta2<kId>(d_tmem, ad, bd, (kb | k4) != 0 ? 1u : 0u);
           }
           mma_commit_cta2(smem_u32(&c.empty[stage]), 0x3);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         mma_commit_cta2(smem_u32(&c.tfull[acc]), 0x3);
@@ -303,6 +325,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int nkb = tile_kb(g);
       const int acc = it & 1;
       const uint32_t aphase = (uint32_t)(it >> 1) & 1u;
+      if (MODE == kDgradAct) {
+        // While the tile's MMAs run, pull this thread's pre-activations (its
+        // row, its half of the tile's columns) into L2 for the epilogue.
+        const int grow = m * BMP + (int)rank * BMC + row;
+        const int c0 = n * MMA_N + half * 128;
+        const int ncols = a.N - c0 < 128 ? a.N - c0 : 128;
+        if (grow < c.rows[g] && ncols > 0) {
+          const size_t off = ((size_t)(c.orow[g] + grow) * a.N + c0) * 2;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((const uint8_t*)a.pre_a + off),
+                       "r"(ncols * 2)
+                       : "memory");
+          if (a.act == MOE_ACT_SWIGLU)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((const uint8_t*)a.pre_u + off),
+                         "r"(ncols * 2)
+                         : "memory");
+        }
+      }
       bool ok = mbar_wait_i(smem_u32(&c.tfull[acc]), aphase, abort, limit, a.err, kWhere + 4);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -312,15 +351,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Output row of this thread and whether it is stored.
       int64_t orow;
       bool valid;
+      // First output row of this warp's 32 and whether all 32 are stored (then
+      // an fp32 output leaves by TMA store, one 32 x 32 box per chunk).
+      int64_t wrow0;
+      bool wfull;
       if (WGRAD) {
         const int mr = m * BMP + (int)rank * BMC + row;
         valid = mr < a.M;
         orow = (int64_t)c.w[g] * a.M + mr;          // dW[g] is [M, N]
+        wrow0 = (int64_t)c.w[g] * a.M + m * BMP + (int)rank * BMC + q * 32;
+        wfull = m * BMP + (int)rank * BMC + q * 32 + 31 < a.M;
       } else {
         const int grow = m * BMP + (int)rank * BMC + row;
         valid = grow < c.rows[g];
         orow = (int64_t)c.orow[g] + grow;
+        wrow0 = (int64_t)c.orow[g] + m * BMP + (int)rank * BMC + q * 32;
+        wfull = m * BMP + (int)rank * BMC + q * 32 + 31 < c.rows[g];
       }
+      const bool tma_st = tma_store && wfull;
+      const uint32_t wbuf = stg + (uint32_t)((warp - 2) * kStageTileBytes);
       for (int ch = half * 4; ch < half * 4 + 4; ++ch) {
         const int col0 = n0 + ch * 32;
         uint32_t v[32];
@@ -344,9 +393,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             load_bf16x32((const uint16_t*)a.pre_u + orow * a.N + col0, uv);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
+              // silu(a) = a s, silu'(a) = s (1 + a (1 - s)), s = sigma(a)
               const float dh = __uint_as_float(v[i]);
-              da[i] = __float_as_uint(dh * uv[i] * silu_grad(av[i]));
-              du[i] = __float_as_uint(dh * silu(av[i]));
+              const float sg = sigmoid_fast(av[i]);
+              da[i] = __float_as_uint(dh * uv[i] * (sg * (1.f + av[i] * (1.f - sg))));
+              du[i] = __float_as_uint(dh * (av[i] * sg));
             }
           } else {
 #pragma unroll
@@ -356,18 +407,65 @@ __global__ void __launch_bounds__(THREADS, 1)
               da[i] = __float_as_uint(dh * gr);
             }
           }
-          uint32_t p[16];
+          uint32_t p[16], pu[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(__uint_as_float(da[2 * i]), __uint_as_float(da[2 * i + 1]));
-          uint4* dst = reinterpret_cast<uint4*>((uint16_t*)a.C + orow * a.N + col0);
+          const bool two = a.act == MOE_ACT_SWIGLU;
+          if (two) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
-          if (a.act == MOE_ACT_SWIGLU) {
+            for (int i = 0; i < 16; ++i) pu[i] = pack_bf16x2(__uint_as_float(du[2 * i]), __uint_as_float(du[2 * i + 1]));
+          }
+          if (tma_st) {
+            // 32 rows x 64 bytes per output, 16-byte chunk j of row `lane` at
+            // lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4): the 64-byte swizzle.
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(__uint_as_float(du[2 * i]), __uint_as_float(du[2 * i + 1]));
-            uint4* dst2 = reinterpret_cast<uint4*>((uint16_t*)a.C2 + orow * a.N + col0);
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t at = (uint32_t)(lane * 64) + ((uint32_t)(j ^ ((lane >> 1) & 3)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(wbuf + at), "r"(p[4 * j]),
+                           "r"(p[4 * j + 1]), "r"(p[4 * j + 2]), "r"(p[4 * j + 3])
+                           : "memory");
+              if (two)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(wbuf + 2048u + at), "r"(pu[4 * j]),
+                             "r"(pu[4 * j + 1]), "r"(pu[4 * j + 2]), "r"(pu[4 * j + 3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, wbuf, col0, (int)wrow0);
+              if (two) tma_store_2d(&tmC2, wbuf + 2048u, col0, (int)wrow0);
+              bulk_commit_group();
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>((uint16_t*)a.C + orow * a.N + col0);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst2[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+            if (two) {
+              uint4* dst2 = reinterpret_cast<uint4*>((uint16_t*)a.C2 + orow * a.N + col0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst2[i] = make_uint4(pu[4 * i], pu[4 * i + 1], pu[4 * i + 2], pu[4 * i + 3]);
+            }
+          }
+        } else if (tma_st) {
+          // Row `lane` of the warp's tile, 16-byte chunk i at lane * 128 + ((i ^ (lane & 7)) << 4)
+          // (the tensor map's 128-byte swizzle); the buffer is reused once the
+          // previous chunk's store has read it.
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t at = wbuf + (uint32_t)(lane * 128) + ((uint32_t)(i ^ (lane & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(at), "r"(v[4 * i]), "r"(v[4 * i + 1]),
+                         "r"(v[4 * i + 2]), "r"(v[4 * i + 3])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, wbuf, col0, (int)wrow0);
+            bulk_commit_group();
           }
         } else {
           float4* dst = reinterpret_cast<float4*>((float*)a.C + orow * a.N + col0);
@@ -381,6 +479,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader + (uint32_t)(acc * 8));
     }
+    // The tiles' TMA stores have completed before the CTA's shared memory goes.
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -396,6 +496,22 @@ template <int MODE, bool TWO_PHASE>
 cudaError_t launch_mode(const BwdGemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mA2, const CUtensorMap& mB,
                         const CUtensorMap& mB2, int64_t max_tiles, cudaStream_t s) {
   auto kernel = gemm_bwd_kernel<MODE, TWO_PHASE>;
+  constexpr size_t kSmemBytes = smem_bytes<MODE>();
+  // fp32 output as a tensor map for the TMA-store epilogue: dgrad rows of the
+  // grouped order, or the stacked weight gradients [Gw * M, N].
+  // The activation backward's bf16 outputs dA (and dU) likewise, 32 x 32 boxes
+  // of 64-byte rows.
+  CUtensorMap mC = mA, mC2 = mA;
+  int tma_store = 0;
+  if (MODE != kDgradAct) {
+    const int64_t rows_c = MODE == kWgrad ? (int64_t)a.Gw * a.M : a.rows_A;
+    tma_store = tmap_f32_2d(&mC, a.C, rows_c, a.N, 32) ? 1 : 0;
+  } else {
+    tma_store = tmap_bf16_2d_swizzle(&mC, a.C, a.rows_A, a.N, 32, 32, 64) &&
+                        (a.act != MOE_ACT_SWIGLU || tmap_bf16_2d_swizzle(&mC2, a.C2, a.rows_A, a.N, 32, 32, 64))
+                    ? 1
+                    : 0;
+  }
   static int max_clusters = -1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -421,7 +537,7 @@ cudaError_t launch_mode(const BwdGemmArgs& a, const CUtensorMap& mA, const CUten
   const int64_t pairs = max_tiles < max_clusters ? max_tiles : max_clusters;
   if (pairs <= 0) return cudaSuccess;
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kernel, mA, mA2, mB, mB2, a);
+  return cudaLaunchKernelEx(&cfg, kernel, mA, mA2, mB, mB2, mC, mC2, a, tma_store);
 }
 
 }  // namespace
