@@ -86,15 +86,39 @@ struct Ctl {
 
 // fp32 outputs (expert GEMM 2) stage each epilogue warp's 32 x 32 tile in
 // shared memory for a TMA store: 4 KB per warp, paid for with one ring stage.
+// SAVE_PRE (the backward's recomputed GEMM 1) stages its three bf16 32 x 32
+// tiles (H, pre_a, pre_u: 2 KB each) the same way.
 constexpr int kStageTileBytes = 32 * 32 * 4;
-template <bool OUT_F32>
-constexpr int ring_stages() { return OUT_F32 ? STAGES - 1 : STAGES; }
-template <bool OUT_F32>
+constexpr int kStageBf16Bytes = 32 * 32 * 2;
+template <bool OUT_F32, bool SAVE_PRE>
+constexpr int ring_stages() { return (OUT_F32 || SAVE_PRE) ? STAGES - 1 : STAGES; }
+template <bool OUT_F32, bool SAVE_PRE>
+constexpr int warp_stage_bytes() { return OUT_F32 ? kStageTileBytes : SAVE_PRE ? 3 * kStageBf16Bytes : 0; }
+template <bool OUT_F32, bool SAVE_PRE>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)ring_stages<OUT_F32>() * STAGE_BYTES + sizeof(Ctl) +
-         (OUT_F32 ? 1024 + (size_t)EPI_WARPS * kStageTileBytes : 0);
+  return 1024 + (size_t)ring_stages<OUT_F32, SAVE_PRE>() * STAGE_BYTES + sizeof(Ctl) +
+         (warp_stage_bytes<OUT_F32, SAVE_PRE>() ? 1024 + (size_t)EPI_WARPS * warp_stage_bytes<OUT_F32, SAVE_PRE>() : 0);
 }
-static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "shared memory per CTA");
+static_assert(smem_bytes<false, false>() <= 227 * 1024 && smem_bytes<true, false>() <= 227 * 1024 &&
+                  smem_bytes<false, true>() <= 227 * 1024,
+              "shared memory per CTA");
+
+// 16 packed bf16 pairs (one thread's 32 columns) into row `lane` of a 32 x 32
+// bf16 staging tile laid out with the 64-byte swizzle: 16-byte chunk j at
+// lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4).
+__device__ __forceinline__ void stage_bf16_row(uint32_t buf, int lane, const uint32_t (&p)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t at = buf + (uint32_t)(lane * 64) + ((uint32_t)(j ^ ((lane >> 1) & 3)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(at), "r"(p[4 * j]), "r"(p[4 * j + 1]),
+                 "r"(p[4 * j + 2]), "r"(p[4 * j + 3])
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void pack_row(const uint32_t (&v)[32], uint32_t (&p)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+}
 
 __device__ __forceinline__ void map_tile(const Ctl& c, int G, int n_tiles, int tile, int& g, int& m, int& n) {
   int lo = 0, hi = G - 1;
@@ -139,9 +163,10 @@ template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE, bool FP8 = false>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3,
-                     const __grid_constant__ CUtensorMap tmC, GemmArgs a) {
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
+                     const __grid_constant__ CUtensorMap tmU, GemmArgs a) {
   constexpr int BN_OUT = SWIGLU ? 128 : 256;   // output columns per pair tile
-  constexpr int NST = ring_stages<OUT_F32>();
+  constexpr int NST = ring_stages<OUT_F32, SAVE_PRE>();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;            // 1 KB aligned ring for the 128-byte swizzle
@@ -360,8 +385,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // each 32 x 32 chunk with one TMA store (a partial warp stores its valid
       // rows itself, so no store reaches the next segment's rows).
       const int wrow0 = m * BMP + (int)rank * BMC + q * 32;
-      const bool tma_st = OUT_F32 && a.rows_C > 0 && wrow0 + 31 < c.rows[g];
-      const uint32_t wbuf = stg + (uint32_t)((warp - 2) * kStageTileBytes);
+      const bool tma_st = (OUT_F32 || SAVE_PRE) && a.rows_C > 0 && wrow0 + 31 < c.rows[g];
+      const uint32_t wbuf = stg + (uint32_t)((warp - 2) * warp_stage_bytes<OUT_F32, SAVE_PRE>());
       constexpr int CHUNKS = BN_OUT / 32;   // 32-column chunks per tile
       for (int ch = half * (CHUNKS / 2); ch < (half + 1) * (CHUNKS / 2); ++ch) {
         const int col0 = n0 + ch * 32;
@@ -375,7 +400,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             scale_acc32(v, ra, a.b_scale + (int64_t)wslab * a.N + col0);
             scale_acc32(u, ra, a.b3_scale + (int64_t)wslab * a.N + col0);
           }
-          if (SAVE_PRE && valid && col0 < a.N) {
+          if (SAVE_PRE && valid && col0 < a.N && !tma_st) {
             store_bf16x32((uint16_t*)a.pre_a + orow * a.N + col0, v);
             store_bf16x32((uint16_t*)a.pre_u + orow * a.N + col0, u);
           }
@@ -387,9 +412,30 @@ __global__ void __launch_bounds__(THREADS, 1)
               const float h1 = silu(__uint_as_float(v[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
               p[i] = pack_bf16x2(h0, h1);
             }
-            uint4* dst = reinterpret_cast<uint4*>(C + orow * a.N + col0);
+            if (SAVE_PRE && tma_st) {
+              // H, pre_a, pre_u of the warp's 32 rows leave by three TMA stores.
+              uint32_t pa[16], pu[16];
+              pack_row(v, pa);
+              pack_row(u, pu);
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+              stage_bf16_row(wbuf, lane, p);
+              stage_bf16_row(wbuf + kStageBf16Bytes, lane, pa);
+              stage_bf16_row(wbuf + 2 * kStageBf16Bytes, lane, pu);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                const int r0 = (int)(c.orow[g] + wrow0);
+                tma_store_2d(&tmC, wbuf, col0, r0);
+                tma_store_2d(&tmP, wbuf + kStageBf16Bytes, col0, r0);
+                tma_store_2d(&tmU, wbuf + 2 * kStageBf16Bytes, col0, r0);
+                bulk_commit_group();
+              }
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(C + orow * a.N + col0);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+            }
           }
         } else {
           tmem_wait_ld();
@@ -404,11 +450,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) f[i] += bv[i];
             }
+            uint32_t pa[16];             // SAVE_PRE: the pre-activations, packed
             if (SAVE_PRE) {
               uint32_t fb[32];
 #pragma unroll
               for (int i = 0; i < 32; ++i) fb[i] = __float_as_uint(f[i]);
-              store_bf16x32((uint16_t*)a.pre_a + orow * a.N + col0, fb);
+              if (tma_st)
+                pack_row(fb, pa);
+              else
+                store_bf16x32((uint16_t*)a.pre_a + orow * a.N + col0, fb);
             }
             if (a.act == MOE_ACT_RELU) {
 #pragma unroll
@@ -440,6 +490,22 @@ __global__ void __launch_bounds__(THREADS, 1)
               float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.C) + orow * a.N + col0);
 #pragma unroll
               for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+            } else if (SAVE_PRE && tma_st) {
+              uint32_t p[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+              stage_bf16_row(wbuf, lane, p);
+              stage_bf16_row(wbuf + kStageBf16Bytes, lane, pa);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                const int r0 = (int)(c.orow[g] + wrow0);
+                tma_store_2d(&tmC, wbuf, col0, r0);
+                tma_store_2d(&tmP, wbuf + kStageBf16Bytes, col0, r0);
+                bulk_commit_group();
+              }
             } else {
               uint32_t p[16];
 #pragma unroll
@@ -456,7 +522,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive_cluster(tempty_leader + (uint32_t)(acc * 8));
     }
     // The tiles' TMA stores have completed before the CTA's shared memory goes.
-    if (OUT_F32 && lane == 0) bulk_wait_all();
+    if ((OUT_F32 || SAVE_PRE) && lane == 0) bulk_wait_all();
   }
 
   // ---- tear-down: both CTAs here, nothing in flight, then free TMEM ----
@@ -478,11 +544,22 @@ template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE = false, bool FP8 = false>
 cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtensorMap& mA1, const CUtensorMap& mB,
                         const CUtensorMap& mB3, int64_t max_pair_tiles, cudaStream_t s) {
   auto kernel = gemm_pair_kernel<SWIGLU, OUT_F32, SAVE_PRE, FP8>;
-  constexpr size_t kSmemBytes = smem_bytes<OUT_F32>();
-  // C as an fp32 tensor map for the TMA-store epilogue (else an unused copy of A's)
-  CUtensorMap mC = mA0;
+  constexpr size_t kSmemBytes = smem_bytes<OUT_F32, SAVE_PRE>();
+  // C (fp32), or H and the pre-activations (bf16, 64-byte rows), as tensor maps
+  // for the TMA-store epilogue (else unused copies of A's)
+  CUtensorMap mC = mA0, mP = mA0, mU = mA0;
   GemmArgs args = a;
-  if (!OUT_F32 || a.rows_C <= 0 || !tmap_f32_2d(&mC, a.C, a.rows_C, a.N, 32)) args.rows_C = 0;
+  bool ok_maps = a.rows_C > 0;
+  if (OUT_F32) {
+    ok_maps = ok_maps && tmap_f32_2d(&mC, a.C, a.rows_C, a.N, 32);
+  } else if (SAVE_PRE) {
+    ok_maps = ok_maps && tmap_bf16_2d_swizzle(&mC, a.C, a.rows_C, a.N, 32, 32, 64) &&
+              tmap_bf16_2d_swizzle(&mP, a.pre_a, a.rows_C, a.N, 32, 32, 64) &&
+              (!SWIGLU || tmap_bf16_2d_swizzle(&mU, a.pre_u, a.rows_C, a.N, 32, 32, 64));
+  } else {
+    ok_maps = false;
+  }
+  if (!ok_maps) args.rows_C = 0;
   static int max_clusters = -1;   // per kernel instantiation, per process (one device type)
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -507,7 +584,7 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtenso
   }
   const int64_t pairs = max_pair_tiles < max_clusters ? max_pair_tiles : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kernel, mA0, mA1, mB, mB3, mC, args);
+  return cudaLaunchKernelEx(&cfg, kernel, mA0, mA1, mB, mB3, mC, mP, mU, args);
 }
 
 }  // namespace

@@ -648,6 +648,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
   g1.A0 = ws + L.xperm; g1.rows_A0 = L.rows_routed; g1.A1 = S > 0 ? x : nullptr; g1.rows_A1 = T;
   g1.B = W1; g1.B3 = W3; g1.Gw = G; g1.bias = b1; g1.C = ws + L.h; g1.max_mtiles = T > 0 ? max_mtiles : 0;
   g1.err = &hdr->err; g1.timeout_ns = timeout; g1.pre_a = ws + L.pre_a; g1.pre_u = swiglu ? ws + L.pre_u : nullptr;
+  g1.rows_C = L.rows_all;
   if (launch_grouped_gemm(g1, s) != cudaSuccess) return MOE_ERR_CUDA;
   GemmArgs g2 = g1;
   g2.act = MOE_ACT_NONE; g2.K = f; g2.N = d; g2.a_from_out_rows = true; g2.A0 = ws + L.h; g2.rows_A0 = L.rows_all;
