@@ -90,17 +90,23 @@ struct Ctl {
 // tiles (H, pre_a, pre_u: 2 KB each) the same way.
 constexpr int kStageTileBytes = 32 * 32 * 4;
 constexpr int kStageBf16Bytes = 32 * 32 * 2;
-template <bool OUT_F32, bool SAVE_PRE>
-constexpr int ring_stages() { return (OUT_F32 || SAVE_PRE) ? STAGES - 1 : STAGES; }
-template <bool OUT_F32, bool SAVE_PRE>
-constexpr int warp_stage_bytes() { return OUT_F32 ? kStageTileBytes : SAVE_PRE ? 3 * kStageBf16Bytes : 0; }
-template <bool OUT_F32, bool SAVE_PRE>
-constexpr size_t smem_bytes() {
-  return 1024 + (size_t)ring_stages<OUT_F32, SAVE_PRE>() * STAGE_BYTES + sizeof(Ctl) +
-         (warp_stage_bytes<OUT_F32, SAVE_PRE>() ? 1024 + (size_t)EPI_WARPS * warp_stage_bytes<OUT_F32, SAVE_PRE>() : 0);
+// The FP8 GEMM 1 (bf16 H out) stages its H tile too: its main loop per tile is
+// half the bf16 one's, so per-thread stores would weigh twice as much.
+template <bool OUT_F32, bool SAVE_PRE, bool FP8>
+constexpr int warp_stage_bytes() {
+  return OUT_F32 ? kStageTileBytes : SAVE_PRE ? 3 * kStageBf16Bytes : FP8 ? kStageBf16Bytes : 0;
 }
-static_assert(smem_bytes<false, false>() <= 227 * 1024 && smem_bytes<true, false>() <= 227 * 1024 &&
-                  smem_bytes<false, true>() <= 227 * 1024,
+template <bool OUT_F32, bool SAVE_PRE, bool FP8>
+constexpr int ring_stages() { return warp_stage_bytes<OUT_F32, SAVE_PRE, FP8>() ? STAGES - 1 : STAGES; }
+template <bool OUT_F32, bool SAVE_PRE, bool FP8>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)ring_stages<OUT_F32, SAVE_PRE, FP8>() * STAGE_BYTES + sizeof(Ctl) +
+         (warp_stage_bytes<OUT_F32, SAVE_PRE, FP8>()
+              ? 1024 + (size_t)EPI_WARPS * warp_stage_bytes<OUT_F32, SAVE_PRE, FP8>()
+              : 0);
+}
+static_assert(smem_bytes<false, false, false>() <= 227 * 1024 && smem_bytes<true, false, false>() <= 227 * 1024 &&
+                  smem_bytes<false, true, false>() <= 227 * 1024 && smem_bytes<false, false, true>() <= 227 * 1024,
               "shared memory per CTA");
 
 // 16 packed bf16 pairs (one thread's 32 columns) into row `lane` of a 32 x 32
@@ -166,7 +172,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
                      const __grid_constant__ CUtensorMap tmU, GemmArgs a) {
   constexpr int BN_OUT = SWIGLU ? 128 : 256;   // output columns per pair tile
-  constexpr int NST = ring_stages<OUT_F32, SAVE_PRE>();
+  constexpr int NST = ring_stages<OUT_F32, SAVE_PRE, FP8>();
+  constexpr bool STAGE_H = !OUT_F32 && (SAVE_PRE || FP8);   // bf16 H leaves by TMA store
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;            // 1 KB aligned ring for the 128-byte swizzle
@@ -385,8 +392,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // each 32 x 32 chunk with one TMA store (a partial warp stores its valid
       // rows itself, so no store reaches the next segment's rows).
       const int wrow0 = m * BMP + (int)rank * BMC + q * 32;
-      const bool tma_st = (OUT_F32 || SAVE_PRE) && a.rows_C > 0 && wrow0 + 31 < c.rows[g];
-      const uint32_t wbuf = stg + (uint32_t)((warp - 2) * warp_stage_bytes<OUT_F32, SAVE_PRE>());
+      const bool tma_st = (OUT_F32 || STAGE_H) && a.rows_C > 0 && wrow0 + 31 < c.rows[g];
+      const uint32_t wbuf = stg + (uint32_t)((warp - 2) * warp_stage_bytes<OUT_F32, SAVE_PRE, FP8>());
       constexpr int CHUNKS = BN_OUT / 32;   // 32-column chunks per tile
       for (int ch = half * (CHUNKS / 2); ch < (half + 1) * (CHUNKS / 2); ++ch) {
         const int col0 = n0 + ch * 32;
@@ -412,23 +419,27 @@ __global__ void __launch_bounds__(THREADS, 1)
               const float h1 = silu(__uint_as_float(v[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
               p[i] = pack_bf16x2(h0, h1);
             }
-            if (SAVE_PRE && tma_st) {
-              // H, pre_a, pre_u of the warp's 32 rows leave by three TMA stores.
-              uint32_t pa[16], pu[16];
-              pack_row(v, pa);
-              pack_row(u, pu);
+            if (STAGE_H && tma_st) {
+              // H (and with SAVE_PRE pre_a, pre_u) of the warp's 32 rows leave by TMA stores.
               if (lane == 0) bulk_wait_read_all();
               __syncwarp();
               stage_bf16_row(wbuf, lane, p);
-              stage_bf16_row(wbuf + kStageBf16Bytes, lane, pa);
-              stage_bf16_row(wbuf + 2 * kStageBf16Bytes, lane, pu);
+              if (SAVE_PRE) {
+                uint32_t pa[16], pu[16];
+                pack_row(v, pa);
+                pack_row(u, pu);
+                stage_bf16_row(wbuf + kStageBf16Bytes, lane, pa);
+                stage_bf16_row(wbuf + 2 * kStageBf16Bytes, lane, pu);
+              }
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
                 const int r0 = (int)(c.orow[g] + wrow0);
                 tma_store_2d(&tmC, wbuf, col0, r0);
-                tma_store_2d(&tmP, wbuf + kStageBf16Bytes, col0, r0);
-                tma_store_2d(&tmU, wbuf + 2 * kStageBf16Bytes, col0, r0);
+                if (SAVE_PRE) {
+                  tma_store_2d(&tmP, wbuf + kStageBf16Bytes, col0, r0);
+                  tma_store_2d(&tmU, wbuf + 2 * kStageBf16Bytes, col0, r0);
+                }
                 bulk_commit_group();
               }
             } else {
@@ -490,20 +501,20 @@ __global__ void __launch_bounds__(THREADS, 1)
               float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.C) + orow * a.N + col0);
 #pragma unroll
               for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
-            } else if (SAVE_PRE && tma_st) {
+            } else if (STAGE_H && tma_st) {
               uint32_t p[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
               if (lane == 0) bulk_wait_read_all();
               __syncwarp();
               stage_bf16_row(wbuf, lane, p);
-              stage_bf16_row(wbuf + kStageBf16Bytes, lane, pa);
+              if (SAVE_PRE) stage_bf16_row(wbuf + kStageBf16Bytes, lane, pa);
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
                 const int r0 = (int)(c.orow[g] + wrow0);
                 tma_store_2d(&tmC, wbuf, col0, r0);
-                tma_store_2d(&tmP, wbuf + kStageBf16Bytes, col0, r0);
+                if (SAVE_PRE) tma_store_2d(&tmP, wbuf + kStageBf16Bytes, col0, r0);
                 bulk_commit_group();
               }
             } else {
@@ -522,7 +533,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive_cluster(tempty_leader + (uint32_t)(acc * 8));
     }
     // The tiles' TMA stores have completed before the CTA's shared memory goes.
-    if ((OUT_F32 || SAVE_PRE) && lane == 0) bulk_wait_all();
+    if ((OUT_F32 || STAGE_H) && lane == 0) bulk_wait_all();
   }
 
   // ---- tear-down: both CTAs here, nothing in flight, then free TMEM ----
@@ -544,7 +555,7 @@ template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE = false, bool FP8 = false>
 cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtensorMap& mA1, const CUtensorMap& mB,
                         const CUtensorMap& mB3, int64_t max_pair_tiles, cudaStream_t s) {
   auto kernel = gemm_pair_kernel<SWIGLU, OUT_F32, SAVE_PRE, FP8>;
-  constexpr size_t kSmemBytes = smem_bytes<OUT_F32, SAVE_PRE>();
+  constexpr size_t kSmemBytes = smem_bytes<OUT_F32, SAVE_PRE, FP8>();
   // C (fp32), or H and the pre-activations (bf16, 64-byte rows), as tensor maps
   // for the TMA-store epilogue (else unused copies of A's)
   CUtensorMap mC = mA0, mP = mA0, mU = mA0;
@@ -556,6 +567,8 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtenso
     ok_maps = ok_maps && tmap_bf16_2d_swizzle(&mC, a.C, a.rows_C, a.N, 32, 32, 64) &&
               tmap_bf16_2d_swizzle(&mP, a.pre_a, a.rows_C, a.N, 32, 32, 64) &&
               (!SWIGLU || tmap_bf16_2d_swizzle(&mU, a.pre_u, a.rows_C, a.N, 32, 32, 64));
+  } else if (FP8) {
+    ok_maps = ok_maps && tmap_bf16_2d_swizzle(&mC, a.C, a.rows_C, a.N, 32, 32, 64);
   } else {
     ok_maps = false;
   }

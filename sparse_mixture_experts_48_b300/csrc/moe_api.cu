@@ -376,6 +376,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
     g1.A1 = sh8 ? ws + L.xq : nullptr;
     g1.a_scale0 = (const float*)(ws + L.xs_perm); g1.a_scale1 = sh8 ? (const float*)(ws + L.xs_tok) : nullptr;
     g1.B = q8->W1; g1.B3 = q8->W3; g1.b_scale = q8->s1; g1.b3_scale = q8->s3;
+    g1.rows_C = L.rows_all;
   }
   if (clk.mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_grouped_gemm(g1, s) != cudaSuccess) return MOE_ERR_CUDA;
