@@ -552,7 +552,9 @@ def main():
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": (moe.NUM_STAGES + (1 if fp8 else 0)) * K,
+            # router, scan, gather, GEMM 1, GEMM 2, combine; + the H quantisation with FP8
+            # experts; + the per-expert selection with expert choice
+            "gpu_launches": (moe.NUM_STAGES + (1 if fp8 else 0) + (1 if args.expert_choice else 0)) * K,
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)
