@@ -285,14 +285,22 @@ def run_backward(args, cfg, d, dev, world, rank, local):
     flop = 2.0 * rows_A * cfg.d * cfg.f * m + 2.0 * rows_A * cfg.d * cfg.f * (2 * m - 1)
     peaks, kind = load_peaks()
     tf = flop / (ms / 1e3) / 1e12
+    sust = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     if rank == 0:
         print(json.dumps({
             "metric": "MoE-layer backward (forward recomputation + gradients) tokens/s on 1 B300",
             "value": replica_throughput(cfg.T, ms, world), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
             "config": {"workload": workload_desc(cfg), "T": cfg.T},
             "gemm_flop_per_step": flop, "gemm_tflops": round(tf, 1),
-            "frac_of_bf16_sustained": round(tf / float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])), 4),
+            "frac_of_bf16_sustained": round(tf / sust, 4),
+            # the call's GEMM work over the whole call's time: a lower bound of
+            # the GEMMs' own rate (their share of the call is about 96 %)
+            "roofline": {"bound": "tensor", "kernel": "all expert GEMMs of the call (timed as the whole call)",
+                         "achieved": round(tf, 1), "peak": sust, "unit": "TFLOP/s", "frac": round(tf / sust, 4),
+                         "traffic": None,
+                         "peak_source": f"{kind} bf16_tflops_sustained (cuBLAS bf16, back to back)"},
             "peak_source": kind, "clocks": clocks.summary()}), flush=True)
 
 
