@@ -487,6 +487,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   cluster_sync_all();
   tc_fence_after();
+  abort_grace(a.err);
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
   }

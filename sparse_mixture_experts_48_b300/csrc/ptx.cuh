@@ -120,6 +120,17 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
   return r;
 }
 // Every thread of every CTA of the cluster arrives, then waits (release / acquire).
+// After an abort in a CTA pair, a copy the peer issued before it stopped may
+// still be landing in this CTA's shared memory or on its barriers (the pair's
+// copies complete on the leader's barriers, which only the leader drains).
+// A CTA that sees the status word set waits this long (bounded) before its
+// shared memory and TMEM are released; copies land within microseconds.
+__device__ __forceinline__ void abort_grace(const uint32_t* err) {
+  if (*(volatile const uint32_t*)err == 0u) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < 50000ull) __nanosleep(1000);
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
