@@ -325,6 +325,8 @@ def main():
                     help="time the backward pass (moe_backward: forward recomputation + gradients) instead")
     ap.add_argument("--gemm-one-cta", action="store_true",
                     help="bf16 expert GEMMs on the one-CTA tile kernel instead of the CTA-pair kernel")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the layer captured in a CUDA graph and replayed (reported under 'graph')")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 (E4M3) expert weights and activations (moe_forward_fp8); the weights are "
                          "quantised once before the timed region")
@@ -477,6 +479,30 @@ def main():
                 "frac": round(dom_tf / tc_sust, 4), "traffic": traffic, "peak_source": src,
                 "frac_of_burst_peak": round(dom_tf / tc_burst, 4)}
 
+    # The same step captured once in a CUDA graph and replayed: no host-side
+    # launch work per step (what bounds small layers).
+    graph = None
+    if args.graph:
+        if fp8:
+            fg = moe.ForwardGraph(cfg, d["x"], d["W_g"], d["b_g"], experts=experts8, router_noise=noise)
+        else:
+            fg = moe.ForwardGraph(cfg, *args_in, router_noise=noise, gemm_single_cta=args.gemm_one_cta)
+        for _ in range(W):
+            fg.replay()
+        torch.cuda.synchronize()
+        barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(K):
+            fg.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        st = moe.check_device_errors(fg.out.workspace)
+        if st != 0:
+            raise SystemExit(f"device error in the graph loop: {moe.STATUS.get(st)}")
+        g_ms = max_over_ranks(g0.elapsed_time(g1) / K, dev, world)
+        graph = {"value": replica_throughput(cfg.T, g_ms, world), "unit": "tokens/s", "ms_per_step": g_ms}
+
     # End to end through the public API with host buffers (moe_forward_host):
     # every step copies its x from page-locked host memory in and all outputs
     # back out.  Steps alternate two streams and two workspaces, so one step's
@@ -560,6 +586,7 @@ def main():
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "graph": graph,
             # router, scan, gather, GEMM 1, GEMM 2, combine; + the H quantisation with FP8
             # experts; + the per-expert selection with expert choice
             "gpu_launches": (moe.NUM_STAGES + (1 if fp8 else 0) + (1 if args.expert_choice else 0)) * K,

@@ -655,3 +655,55 @@ def workspace_region(cfg, region: int):
     if st != 0:
         raise MoEError(st, "moe_workspace_region")
     return int(off.value), int(n.value)
+
+
+# ---- CUDA graphs ------------------------------------------------------------------
+
+class ForwardGraph:
+    """One whole forward pass (forward() or, with ``experts``, forward_fp8())
+    captured once in a CUDA graph and replayed: every kernel of the layer runs
+    again on the same buffers without host-side launch work, which is what
+    bounds small layers.  Update the inputs in place (``x.copy_(...)``) before
+    ``replay()``; the outputs are in ``out``.
+
+    The capture runs one warm-up call first (first-use kernel attributes and
+    the device's cluster occupancy are queried then, outside the capture)."""
+
+    def __init__(self, cfg, x, W_g, b_g, W1=None, b1=None, W2=None, b2=None, W3=None, *,
+                 experts: Optional[Fp8Experts] = None, router_noise: Optional[torch.Tensor] = None,
+                 debug: bool = False, y_f32: Optional[bool] = None, gemm_single_cta: bool = False):
+        self.cfg = _fp8_cfg(cfg) if experts is not None else cfg
+        self.stream = torch.cuda.Stream(device=x.device)
+        yf = bool(getattr(cfg, "y_f32", False)) if y_f32 is None else bool(y_f32)
+        self.out = alloc_outputs(self.cfg, x.device, debug=debug, y_f32=yf)
+        self.out.workspace = alloc_workspace(self.cfg, x.device)
+        if experts is not None:
+            def call():
+                forward_fp8(self.cfg, x, W_g, b_g, experts, b1, b2, router_noise=router_noise, out=self.out,
+                            workspace=self.out.workspace, stream=self.stream, y_f32=yf)
+        else:
+            def call():
+                forward(self.cfg, x, W_g, b_g, W1, b1, W2, b2, W3, router_noise=router_noise, out=self.out,
+                        workspace=self.out.workspace, stream=self.stream, y_f32=yf,
+                        gemm_single_cta=gemm_single_cta)
+        self.stream.wait_stream(torch.cuda.current_stream(x.device))
+        with torch.cuda.stream(self.stream):
+            call()
+        self.stream.synchronize()
+        status = check_device_errors(self.out.workspace, self.stream)
+        if status != 0:
+            raise MoEError(status, "ForwardGraph warm-up")
+        self.graph = torch.cuda.CUDAGraph()
+        # relaxed: the launchers set kernel attributes (not stream work) while capturing
+        with torch.cuda.graph(self.graph, stream=self.stream, capture_error_mode="relaxed"):
+            call()
+
+    def replay(self) -> MoEOutput:
+        """Enqueue the captured forward on the graph's stream, ordered after
+        the current stream's work (and the current stream after it)."""
+        cur = torch.cuda.current_stream(self.stream.device)
+        self.stream.wait_stream(cur)
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()
+        cur.wait_stream(self.stream)
+        return self.out
