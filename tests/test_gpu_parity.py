@@ -198,3 +198,22 @@ def test_forward_host_matches_device_forward(name):
             if a.dtype == torch.bfloat16:
                 a, b = a.view(torch.int16), b.view(torch.int16)
             assert torch.equal(a, b), field
+
+
+@pytest.mark.parametrize("base,over", [
+    ("gpt2_top2_gelu_bf16", dict(T=20000, d=128, f=128)),                       # softmax, bias, E = 8
+    ("deepseek_shared_sigmoid_bf16", dict(T=12345, d=128, f=128, S=1)),       # sigmoid, E = 64, ragged tail
+    ("skew_capacity_gelu_bf16", dict(T=30000, d=64, f=128, capacity_factor=1.1)),   # drops
+], ids=["softmax_e8", "sigmoid_e64", "skew_capacity"])
+def test_router_more_tiles_than_sms(base, over):
+    """More 64-token router tiles than SMs (several CTAs per SM, and a second
+    wave): every routing decision, the statistics and sampled rows of y."""
+    cfg = si.CONFIGS[base].replace(**over)
+    inp = si.layer_inputs(cfg, seed=61)
+    dinp = device_inputs(inp)
+    out = run(cfg, dinp)
+    torch.cuda.synchronize()
+    assert moe.check_device_errors(out.workspace) == 0
+    ref, gl, _ = check_routing(cfg, inp, out)
+    rows = np.random.default_rng(3).choice(cfg.T, size=64, replace=False)
+    check_y(cfg, inp, out, gl, rows)
