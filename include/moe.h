@@ -66,7 +66,7 @@ typedef struct CUevent_st* moe_event;   /* a cudaEvent_t */
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1, /* NULL where a tensor is required, bad sizes, aliasing, misalignment */
-  MOE_ERR_UNSUPPORTED = 2, /* a valid layer this build does not run (e.g. k > 8, d % 64 for bf16) */
+  MOE_ERR_UNSUPPORTED = 2, /* a valid layer this library does not run (e.g. k > 8, d % 64 for bf16) */
   MOE_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than moe_workspace_size() */
   MOE_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch error, sticky error) */
   MOE_ERR_TIMEOUT = 5,     /* a device-side wait exceeded its limit; outputs are not valid */
@@ -145,7 +145,7 @@ typedef struct {
 /* Human-readable name of a status.  Never NULL. */
 const char* moe_status_string(moe_status s);
 
-/* MOE_OK if the config describes a layer this build runs, else the reason. */
+/* MOE_OK if the config describes a layer this library runs, else the reason. */
 moe_status moe_validate_config(const moe_config* cfg);
 
 /* Device workspace bytes moe_forward needs for `cfg` (0 if cfg is invalid).
