@@ -28,39 +28,16 @@ constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kMaxCachedT = 32768;   // keys kept in shared memory up to this T (128 KB)
 
-// Block-wide exclusive scan of one int per thread; returns the block total.
-__device__ int block_excl_scan(int v, int* s_warp, int* excl) {
-  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-  int incl = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += n;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kSelWarps ? s_warp[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, wi, off);
-      if (lane >= off) wi += n;
-    }
-    if (lane < kSelWarps) s_warp[lane] = wi - w;   // exclusive warp offsets
-    if (lane == 31) s_warp[32] = wi;               // block total
-  }
-  __syncthreads();
-  *excl = s_warp[warp] + incl - v;
-  const int total = s_warp[32];
-  __syncthreads();
-  return total;
-}
+// Histogram privatised per group of kHistWarps warps: the top bytes of
+// probabilities fall into a handful of bins, and 1024 threads adding into one
+// histogram would serialise on them.
+constexpr int kHistGroups = 8;
+constexpr int kHistWarps = kSelWarps / kHistGroups;
 
 __global__ void __launch_bounds__(kSelThreads) ec_select_kernel(EcSelectArgs a) {
   extern __shared__ uint32_t s_keys[];            // cached keys (T <= kMaxCachedT)
   __shared__ int s_hist[256];
-  __shared__ int s_warp[33];
+  __shared__ int s_hpart[kHistGroups][256];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining;
   const int e = blockIdx.x;
@@ -86,22 +63,55 @@ __global__ void __launch_bounds__(kSelThreads) ec_select_kernel(EcSelectArgs a) 
   if (C > 0) {
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      for (int i = threadIdx.x; i < 256; i += kSelThreads) s_hist[i] = 0;
+      for (int i = threadIdx.x; i < kHistGroups * 256; i += kSelThreads) (&s_hpart[0][0])[i] = 0;
       __syncthreads();
       const uint32_t prefix = s_prefix;
+      int* hp = s_hpart[(threadIdx.x / 32) / kHistWarps];
       for (int64_t t = threadIdx.x; t < T; t += kSelThreads) {
         const uint32_t k = key(t);
-        if ((k & mask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255u], 1);
+        if ((k & mask) == prefix) atomicAdd(&hp[(k >> shift) & 255u], 1);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int rem = s_remaining, cum = 0, b = 255;
-        for (; b > 0; --b) {
-          if (cum + s_hist[b] >= rem) break;
-          cum += s_hist[b];
+      for (int i = threadIdx.x; i < 256; i += kSelThreads) {
+        int h = 0;
+#pragma unroll
+        for (int g = 0; g < kHistGroups; ++g) h += s_hpart[g][i];
+        s_hist[i] = h;
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        // The bin holding the rem-th largest key, searched from the top: lane
+        // l owns bins 255 - 8l .. 248 - 8l; a scan over the lanes gives the
+        // keys in the higher bins, and the first lane whose bins reach rem
+        // names the bin (and the keys of that bin still to take).
+        const int ln = threadIdx.x;
+        const int rem = s_remaining;
+        int cnt[8], local = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          cnt[j] = s_hist[255 - (8 * ln + j)];
+          local += cnt[j];
         }
-        s_remaining = rem - cum;
-        s_prefix = prefix | ((uint32_t)b << shift);
+        int incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (ln >= off) incl += v;
+        }
+        int cum = incl - local, bin = -1;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (bin < 0) {
+            if (cum + cnt[j] >= rem) bin = 255 - (8 * ln + j);
+            else cum += cnt[j];
+          }
+        }
+        const uint32_t found = __ballot_sync(0xffffffffu, bin >= 0);
+        // the keys that match the prefix always number at least rem: bin 0 at the latest
+        if (found != 0u && ln == __ffs(found) - 1) {
+          s_remaining = rem - cum;
+          s_prefix = prefix | ((uint32_t)bin << shift);
+        }
       }
       mask |= 255u << shift;
       __syncthreads();
@@ -111,28 +121,83 @@ __global__ void __launch_bounds__(kSelThreads) ec_select_kernel(EcSelectArgs a) 
   const int need_eq = C > 0 ? s_remaining : 0;
 
   // Chosen tokens in token order: key > thr, or key == thr among the first
-  // need_eq such tokens.  Two running block scans (equal keys, chosen).
-  int eq_base = 0, pos_base = 0;
-  for (int64_t t0 = 0; t0 < T; t0 += kSelThreads) {
-    const int64_t t = t0 + threadIdx.x;
-    const uint32_t k = t < T ? key(t) : 0u;
-    const bool gt = C > 0 && t < T && k > thr;
-    const bool eq = C > 0 && t < T && k == thr;
-    int eq_ex;
-    const int eq_tot = block_excl_scan(eq ? 1 : 0, s_warp, &eq_ex);
-    const bool take = gt || (eq && eq_base + eq_ex < need_eq);
-    int pos_ex;
-    const int pos_tot = block_excl_scan(take ? 1 : 0, s_warp, &pos_ex);
-    if (take) {
-      const int64_t row = (int64_t)e * C + pos_base + pos_ex;
-      a.perm[row] = (int32_t)t;
-      a.w_row[row] = __uint_as_float(k);
-      a.tok_row[t * a.E + e] = (int32_t)row;
-      atomicOr(&a.bits[t * a.EW + e / 32], 1u << (e % 32));
+  // need_eq such tokens.  Warp w owns the contiguous tokens [w B, (w + 1) B):
+  // it counts its keys above and equal to the threshold, one scan over the 32
+  // warps places every warp's equal keys and chosen tokens, and each warp then
+  // walks its block again in order, ranking with ballots.
+  const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
+  const int64_t B = ((T + kSelWarps - 1) / kSelWarps + 31) / 32 * 32;
+  const int64_t wb = (int64_t)wid * B;
+  int gt = 0, eq = 0;
+  if (C > 0)
+    for (int64_t t = wb + lane; t < wb + B && t < T; t += 32) {
+      const uint32_t k = key(t);
+      gt += k > thr;
+      eq += k == thr;
     }
-    eq_base += eq_tot;
-    pos_base += pos_tot;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    gt += __shfl_xor_sync(0xffffffffu, gt, off);
+    eq += __shfl_xor_sync(0xffffffffu, eq, off);
   }
+  __shared__ int s_eq[kSelWarps], s_take[kSelWarps];
+  if (lane == 0) s_eq[wid] = eq;
+  __syncthreads();
+  if (wid == 0) {
+    // equal keys before each warp, then how many of its own it takes, then
+    // the chosen tokens before each warp
+    const int ne = lane < kSelWarps ? s_eq[lane] : 0;
+    int ni = ne;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, ni, off);
+      if (lane >= off) ni += v;
+    }
+    const int eq_before = ni - ne;
+    int take_eq = need_eq - eq_before;
+    take_eq = take_eq < 0 ? 0 : (take_eq > ne ? ne : take_eq);
+    if (lane < kSelWarps) s_take[lane] = take_eq;
+  }
+  __syncthreads();
+  const int my_take_eq = s_take[wid];
+  const int my_count = gt + my_take_eq;
+  __shared__ int s_pos[kSelWarps];
+  if (lane == 0) s_pos[wid] = my_count;
+  __syncthreads();
+  if (wid == 0) {
+    int v = lane < kSelWarps ? s_pos[lane] : 0;
+    int vi = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, vi, off);
+      if (lane >= off) vi += u;
+    }
+    __syncwarp();
+    if (lane < kSelWarps) s_pos[lane] = vi - v;
+  }
+  __syncthreads();
+  int pos = s_pos[wid];
+  int eq_seen = 0;
+  const uint32_t lt = (1u << lane) - 1u;
+  if (C > 0)
+    for (int64_t t0 = wb; t0 < wb + B && t0 < T; t0 += 32) {
+      const int64_t t = t0 + lane;
+      const uint32_t k = t < T && t < wb + B ? key(t) : 0u;
+      const bool in = t < T && t < wb + B;
+      const bool g = in && k > thr, q = in && k == thr;
+      const uint32_t qb = __ballot_sync(0xffffffffu, q);
+      const bool take = g || (q && eq_seen + __popc(qb & lt) < my_take_eq);
+      const uint32_t tb = __ballot_sync(0xffffffffu, take);
+      if (take) {
+        const int64_t row = (int64_t)e * C + pos + __popc(tb & lt);
+        a.perm[row] = (int32_t)t;
+        a.w_row[row] = __uint_as_float(k);
+        a.tok_row[t * a.E + e] = (int32_t)row;
+        atomicOr(&a.bits[t * a.EW + e / 32], 1u << (e % 32));
+      }
+      eq_seen += __popc(qb);
+      pos += __popc(tb);
+    }
 }
 
 constexpr int kGatherWarps = 8;
@@ -192,17 +257,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32) ec_combine_kernel(EcCombin
   const int64_t chunks = a.d / 4;
   const float4* O = (const float4*)a.o;
   const uint64_t policy = l2_policy_evict_first();
+  constexpr int kBatch = 4;   // sources whose loads are in flight together
   for (int64_t c = lane; c < chunks; c += 32) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < n; ++j) {
-      const uint4 u = ld_stream_u4(O + s_row[wl][j] * chunks + c, policy);
-      const float4 v = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
-                                   __uint_as_float(u.w));
-      const float w = s_w[wl][j];
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+    for (int j0 = 0; j0 < n; j0 += kBatch) {
+      uint4 u[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b)
+        if (j0 + b < n) u[b] = ld_stream_u4(O + s_row[wl][j0 + b] * chunks + c, policy);
+      // accumulated in source order, as one load at a time would
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (j0 + b < n) {
+          const float w = s_w[wl][j0 + b];
+          acc.x = fmaf(w, __uint_as_float(u[b].x), acc.x);
+          acc.y = fmaf(w, __uint_as_float(u[b].y), acc.y);
+          acc.z = fmaf(w, __uint_as_float(u[b].z), acc.z);
+          acc.w = fmaf(w, __uint_as_float(u[b].w), acc.w);
+        }
+      }
     }
     if (a.y_f32) {
       reinterpret_cast<float4*>(a.y)[t * chunks + c] = acc;
