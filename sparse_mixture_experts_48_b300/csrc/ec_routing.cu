@@ -232,58 +232,74 @@ __global__ void __launch_bounds__(kCombineWarps * 32) ec_combine_kernel(EcCombin
   const int lane = threadIdx.x % 32, wl = threadIdx.x / 32;
   const int64_t t = (int64_t)blockIdx.x * kCombineWarps + wl;
   if (t >= a.T || *(volatile const uint32_t*)a.err != 0u) return;
-  // The token's sources in order: choosing experts ascending, then the shared experts.
+  // The token's sources in order: choosing experts ascending, then the shared
+  // experts.  Lane l looks at expert w * 32 + l of mask word w; a ballot
+  // places the chosen ones in expert order.
   int n = 0;
+  const uint32_t lt = (1u << lane) - 1u;
   for (int w = 0; w < a.EW; ++w) {
-    uint32_t bits = a.bits[t * a.EW + w];
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1u;
-      if (lane == 0) {
-        const int64_t row = a.tok_row[t * a.E + w * 32 + b];
-        s_row[wl][n] = row;
-        s_w[wl][n] = a.w_row[row];
-      }
-      ++n;
+    const uint32_t word = a.bits[t * a.EW + w];
+    const bool chosen = (word >> lane) & 1u;
+    if (chosen) {
+      const int64_t row = a.tok_row[t * a.E + w * 32 + lane];
+      const int at = n + __popc(word & lt);
+      s_row[wl][at] = row;
+      s_w[wl][at] = a.w_row[row];
     }
+    n += __popc(word);
   }
-  if (lane == 0)
-    for (int s = 0; s < a.S; ++s) {
-      s_row[wl][n + s] = a.rows_routed + (int64_t)s * a.T + t;
-      s_w[wl][n + s] = 1.f;
-    }
+  if (lane < a.S) {
+    s_row[wl][n + lane] = a.rows_routed + (int64_t)lane * a.T + t;
+    s_w[wl][n + lane] = 1.f;
+  }
   n += a.S;
   __syncwarp();
   const int64_t chunks = a.d / 4;
   const float4* O = (const float4*)a.o;
   const uint64_t policy = l2_policy_evict_first();
   constexpr int kBatch = 4;   // sources whose loads are in flight together
-  for (int64_t c = lane; c < chunks; c += 32) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int U = 2;        // 16-byte chunks per lane per pass
+  for (int64_t c0 = lane; c0 < chunks; c0 += 32 * U) {
+    float4 acc[U];
+#pragma unroll
+    for (int v = 0; v < U; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j0 = 0; j0 < n; j0 += kBatch) {
-      uint4 u[kBatch];
+      uint4 u[kBatch][U];
 #pragma unroll
       for (int b = 0; b < kBatch; ++b)
-        if (j0 + b < n) u[b] = ld_stream_u4(O + s_row[wl][j0 + b] * chunks + c, policy);
+#pragma unroll
+        for (int v = 0; v < U; ++v)
+          if (j0 + b < n && c0 + 32 * v < chunks)
+            u[b][v] = ld_stream_u4(O + s_row[wl][j0 + b] * chunks + c0 + 32 * v, policy);
       // accumulated in source order, as one load at a time would
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         if (j0 + b < n) {
           const float w = s_w[wl][j0 + b];
-          acc.x = fmaf(w, __uint_as_float(u[b].x), acc.x);
-          acc.y = fmaf(w, __uint_as_float(u[b].y), acc.y);
-          acc.z = fmaf(w, __uint_as_float(u[b].z), acc.z);
-          acc.w = fmaf(w, __uint_as_float(u[b].w), acc.w);
+#pragma unroll
+          for (int v = 0; v < U; ++v) {
+            if (c0 + 32 * v < chunks) {
+              acc[v].x = fmaf(w, __uint_as_float(u[b][v].x), acc[v].x);
+              acc[v].y = fmaf(w, __uint_as_float(u[b][v].y), acc[v].y);
+              acc[v].z = fmaf(w, __uint_as_float(u[b][v].z), acc[v].z);
+              acc[v].w = fmaf(w, __uint_as_float(u[b][v].w), acc[v].w);
+            }
+          }
         }
       }
     }
-    if (a.y_f32) {
-      reinterpret_cast<float4*>(a.y)[t * chunks + c] = acc;
-    } else {
-      uint2 out;
-      out.x = pack_bf16x2(acc.x, acc.y);
-      out.y = pack_bf16x2(acc.z, acc.w);
-      reinterpret_cast<uint2*>(a.y)[t * chunks + c] = out;
+#pragma unroll
+    for (int v = 0; v < U; ++v) {
+      const int64_t c = c0 + 32 * v;
+      if (c >= chunks) continue;
+      if (a.y_f32) {
+        reinterpret_cast<float4*>(a.y)[t * chunks + c] = acc[v];
+      } else {
+        uint2 out;
+        out.x = pack_bf16x2(acc[v].x, acc[v].y);
+        out.y = pack_bf16x2(acc[v].z, acc[v].w);
+        reinterpret_cast<uint2*>(a.y)[t * chunks + c] = out;
+      }
     }
   }
 }
