@@ -223,3 +223,22 @@ def test_fp8_full_size_sampled():
     ex, out = run_fp8(cfg, inp)
     rows = np.random.default_rng(7).choice(cfg.T, size=6, replace=False)
     check_layer(cfg, inp, ex, out, rows=rows, stages=False)
+
+
+def test_fp8_host_buffers_match_device_call():
+    """moe_forward_fp8_host (x in, outputs out through pinned host memory)
+    gives bitwise the outputs of moe_forward_fp8 on device buffers."""
+    cfg = si.CONFIGS["deepseek_shared_sigmoid_bf16"].replace(T=300, d=256, f=192)
+    inp = si.layer_inputs(cfg, seed=34)
+    inp["noise"] = si.router_noise(cfg, seed=34, std=0.3)
+    dinp = device_inputs(inp)
+    ex = moe.quantize_experts_fp8(dinp["W1"], dinp["W2"], dinp.get("W3"))
+    dev = moe.forward_fp8(cfg, dinp["x"], dinp["W_g"], dinp["b_g"], ex, dinp["b1"], dinp["b2"],
+                          router_noise=dinp["noise"])
+    x_host = dinp["x"].cpu().pin_memory()
+    host = moe.forward_fp8_host(cfg, x_host, dinp["W_g"], dinp["b_g"], ex, dinp["b1"], dinp["b2"],
+                                router_noise_host=dinp["noise"].cpu().pin_memory())
+    torch.cuda.synchronize()
+    assert moe.check_device_errors(host.workspace) == 0
+    for n in ("y", "topk_idx", "topk_w", "expert_counts", "dropped_mask", "f", "P", "L_aux", "route_stats"):
+        assert torch.equal(getattr(dev, n).cpu(), getattr(host, n)), n
