@@ -83,6 +83,7 @@ def _L() -> ctypes.CDLL:
         lib.oracle_fp8_layer_rows.argtypes = [i32, i32, i32, i32, i32, i32, vp, i64] + [vp] * 14
         lib.oracle_fp8_hidden.argtypes = [i32, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp]
         lib.oracle_fp8_out.argtypes = [i32, i32, i32, i32, vp, ctypes.c_float, vp, vp, vp, vp]
+        lib.oracle_fp8_ec_layer_rows.argtypes = [i32, i32, i32, i32, i32, i64, i64, vp, i64] + [vp] * 13
         _lib = lib
     return _lib
 
@@ -446,3 +447,25 @@ def fp8_forward(cfg, inp: Dict, rows: Optional[Sequence[int]] = None, logits: Op
     out["y"] = y
     out["xq"], out["xs"] = xq, xs
     return out
+
+
+def fp8_ec_forward(cfg, inp: Dict, rows: Optional[Sequence[int]] = None, scores: Optional[np.ndarray] = None,
+                   wq: Optional[Dict[str, np.ndarray]] = None) -> Dict[str, np.ndarray]:
+    """Expert-choice routing (as ``ec_forward``) with FP8 experts (as
+    ``fp8_forward``): the choosing experts' outputs from the token's quantised
+    row, weighted by the oracle's own fp64 gate probabilities."""
+    ref = ec_forward(cfg, inp, rows=[], scores=scores)
+    wq = quantize_experts(cfg, inp) if wq is None else wq
+    xq, xs = quantize_rows(inp["x"])
+    T = ref["probs"].shape[0]
+    rows = np.arange(T) if rows is None else np.asarray(rows, np.int64)
+    rows = np.ascontiguousarray(rows, np.int64)
+    y = np.empty((rows.size, cfg.d), np.float64)
+    b1, b2 = _bias_f32(inp, "b1"), _bias_f32(inp, "b2")
+    _L().oracle_fp8_ec_layer_rows(cfg.d, cfg.f, cfg.E, cfg.S, cfg.act, T, ref["capacity"], _p(rows), rows.size,
+                                  _p(xq), _p(xs), _p(wq["W1q"]), _p(wq["s1"]), _p(wq.get("W3q")), _p(wq.get("s3")),
+                                  _p(b1), _p(wq["W2q"]), _p(wq["s2"]), _p(b2),
+                                  _p(np.ascontiguousarray(ref["perm"], np.int32)),
+                                  _p(np.ascontiguousarray(ref["probs"])), _p(y))
+    ref.update(rows=rows, y=y, xq=xq, xs=xs)
+    return ref

@@ -725,3 +725,33 @@ void oracle_fp8_layer_rows(int d, int f, int E, int k, int S, int act, const int
   }
   free(o);
 }
+
+/* Expert-choice layer output with FP8 experts: as oracle_ec_layer_rows, each
+ * choosing expert's output from the token's quantised row (xq [T, d], xs [T])
+ * through oracle_fp8_expert_ffn. */
+void oracle_fp8_ec_layer_rows(int d, int f, int E, int S, int act, int64_t T, int64_t C, const int64_t* rows,
+                              int64_t nrows, const uint8_t* xq, const float* xs, const uint8_t* W1q,
+                              const float* s1, const uint8_t* W3q, const float* s3, const float* b1,
+                              const uint8_t* W2q, const float* s2, const float* b2, const int32_t* perm,
+                              const double* scores, double* y) {
+  double* o = (double*)malloc(sizeof(double) * (size_t)d);
+  for (int64_t r = 0; r < nrows; ++r) {
+    const int64_t t = rows[r];
+    double* yr = y + r * d;
+    for (int i = 0; i < d; ++i) yr[i] = 0.0;
+    for (int e = 0; e < E; ++e) {
+      int hit = 0;
+      for (int64_t i = 0; i < C; ++i)
+        if (perm[(int64_t)e * C + i] == t) { hit = 1; break; }
+      if (!hit) continue;
+      oracle_fp8_expert_ffn(d, f, act, e, xq + t * d, xs[t], W1q, s1, W3q, s3, b1, W2q, s2, b2, o);
+      const double w = scores[t * E + e];
+      for (int i = 0; i < d; ++i) yr[i] += w * o[i];
+    }
+    for (int s = 0; s < S; ++s) {
+      oracle_fp8_expert_ffn(d, f, act, E + s, xq + t * d, xs[t], W1q, s1, W3q, s3, b1, W2q, s2, b2, o);
+      for (int i = 0; i < d; ++i) yr[i] += o[i];
+    }
+  }
+  free(o);
+}

@@ -199,3 +199,23 @@ def test_fp8_expert_halves_against_numpy(act):
         del churn
         np.testing.assert_allclose(h, h_ref, rtol=1e-12, atol=1e-14)
         np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-14)
+
+
+def test_fp8_expert_choice_every_token_to_every_expert_is_the_fp8_soft_mixture():
+    """C = T: every expert takes every token, so y = sum_e p_e FFN8_e(x), each
+    FP8 expert output composed here from fp8_hidden, the bf16 rounding of h,
+    its quantisation and fp8_out."""
+    cfg = si.CONFIGS["gpt2_top2_gelu_bf16"].replace(T=5, d=64, f=96, E=3, k=3, expert_choice=True,
+                                                   capacity_factor=3.0)
+    inp = si.layer_inputs(cfg, seed=13)
+    ref = oracle.fp8_ec_forward(cfg, inp)
+    assert ref["capacity"] == cfg.T
+    wq = oracle.quantize_experts(cfg, inp)
+    xq, xs = oracle.quantize_rows(inp["x"])
+    for t in range(cfg.T):
+        want = np.zeros(cfg.d)
+        for e in range(cfg.E):
+            h = oracle.fp8_hidden(cfg, e, xq[t], xs[t], wq, inp)
+            hq, hs = oracle.quantize_rows(_bf16_round_array(h).astype(np.float32))
+            want += ref["probs"][t, e] * oracle.fp8_out(cfg, e, hq[0], hs[0], wq, inp)
+        np.testing.assert_allclose(ref["y"][t], want, rtol=1e-12, atol=1e-14)
