@@ -80,6 +80,10 @@ def algorithmic(cfg, rows_A: int):
         # x read in bf16, one E4M3 code per element written per kept slot (and
         # once in token order for the shared experts), one scale per row
         out["gather_bytes"] = T * d * b + kept * (d + 4.0) + (T * (d + 4.0) if cfg.S else 0.0)
+        if getattr(cfg, "expert_choice", False):
+            # expert choice: x quantised once per token, then each grouped row
+            # copies its token's codes and scale
+            out["gather_bytes"] = T * d * b + T * (d + 4.0) + 2.0 * kept * (d + 4.0)
         # H read in bf16, codes and one scale per row written
         out["quantize_h_bytes"] = rows_A * (f * 3.0 + 4.0)
     return out
@@ -337,8 +341,8 @@ def main():
     if args.expert_choice:
         cfg = cfg.replace(expert_choice=True)
     if args.fp8:
-        if args.expert_choice or args.backward or args.gemm_one_cta or args.impl == "reference":
-            raise SystemExit("--fp8 runs the token-choice forward on the CTA-pair GEMM of our implementation")
+        if args.backward or args.gemm_one_cta or args.impl == "reference":
+            raise SystemExit("--fp8 runs the forward on the CTA-pair GEMM of our implementation")
         cfg = cfg.replace(fp8_experts=True)
         args.no_cpu = True
     if args.warmup < 3 and args.impl == "ours":
@@ -588,8 +592,10 @@ def main():
             "e2e": e2e,
             "graph": graph,
             # router, scan, gather, GEMM 1, GEMM 2, combine; + the H quantisation with FP8
-            # experts; + the per-expert selection with expert choice
-            "gpu_launches": (moe.NUM_STAGES + (1 if fp8 else 0) + (1 if args.expert_choice else 0)) * K,
+            # experts; + the per-expert selection with expert choice (+ x's quantisation
+            # per token with both)
+            "gpu_launches": (moe.NUM_STAGES + (1 if fp8 else 0) + (1 if args.expert_choice else 0)
+                             + (1 if fp8 and args.expert_choice else 0)) * K,
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)

@@ -117,7 +117,9 @@ typedef struct {
 /* FP8 experts: the expert weights are E4M3 codes with scales (moe_fp8_experts,
  * made by moe_quantize_weights_fp8) and the layer runs through
  * moe_forward_fp8; moe_workspace_size then sizes that call's workspace.
- * Needs dtype == MOE_DT_BF16 (x, y, W_g, b1, b2 stay bf16) and token choice. */
+ * Needs dtype == MOE_DT_BF16 (x, y, W_g, b1, b2 stay bf16).  With
+ * MOE_FLAG_EXPERT_CHOICE x is quantised once per token and the chosen rows
+ * take their token's codes and scale. */
 #define MOE_FLAG_FP8_EXPERTS 4
 
 /* Launch options; pass NULL for defaults. */

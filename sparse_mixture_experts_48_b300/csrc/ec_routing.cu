@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32) ec_gather_kernel(EcGatherAr
   const int64_t r = (int64_t)blockIdx.x * kGatherWarps + threadIdx.x / 32;
   if (r >= a.rows || *(volatile const uint32_t*)a.err != 0u) return;
   const int64_t t = a.perm[r];
+  if (a.xs_perm && lane == 0) a.xs_perm[r] = a.xs_tok[t];
   const int64_t chunks = (int64_t)a.d * a.esz / 16;
   const uint4* src = (const uint4*)((const uint8_t*)a.x + t * chunks * 16);
   uint4* dst = (uint4*)((uint8_t*)a.xperm + r * chunks * 16);

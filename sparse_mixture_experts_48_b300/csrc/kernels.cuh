@@ -130,12 +130,14 @@ struct EcSelectArgs {
 cudaError_t launch_ec_select(const EcSelectArgs& a, cudaStream_t s);
 
 struct EcGatherArgs {
-  const void* x;
+  const void* x;            // [T, d]: x, or with FP8 experts its E4M3 codes
   const int32_t* perm;
   int64_t rows;
   int d, esz;
   void* xperm;
   const uint32_t* err;
+  const float* xs_tok;      // FP8: each token row's decoding scale [T], or null
+  float* xs_perm;           // FP8: copied to each grouped row [rows]
 };
 cudaError_t launch_ec_gather(const EcGatherArgs& a, cudaStream_t s);
 

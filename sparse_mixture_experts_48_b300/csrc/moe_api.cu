@@ -35,8 +35,7 @@ moe_status check_cfg(const moe_config* c) {
   if (c->gating != MOE_GATE_SOFTMAX && c->gating != MOE_GATE_SIGMOID_NORM) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_DT_F32 && c->dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
   if (c->flags & ~(int64_t)(MOE_FLAG_Y_F32 | MOE_FLAG_EXPERT_CHOICE | MOE_FLAG_FP8_EXPERTS)) return MOE_ERR_INVALID_ARG;
-  if ((c->flags & MOE_FLAG_FP8_EXPERTS) && (c->dtype != MOE_DT_BF16 || (c->flags & MOE_FLAG_EXPERT_CHOICE)))
-    return MOE_ERR_UNSUPPORTED;
+  if ((c->flags & MOE_FLAG_FP8_EXPERTS) && c->dtype != MOE_DT_BF16) return MOE_ERR_UNSUPPORTED;
   if (!isfinite(c->capacity_factor) || !isfinite(c->alpha)) return MOE_ERR_INVALID_ARG;
   if (c->E > kMaxE || c->k > kMaxK || c->n_shared > kMaxShared) return MOE_ERR_UNSUPPORTED;
   if (c->dtype == MOE_DT_BF16 && (c->d_model % 64 != 0 || c->d_ff % 64 != 0)) return MOE_ERR_UNSUPPORTED;
@@ -82,7 +81,9 @@ WsLayout layout(const moe_config* c) {
   L.ec_tokrow = take(ec ? (size_t)c->T * c->E * 4 : 0);
   L.ec_wrow = take(ec ? (size_t)L.rows_tk * 4 : 0);
   L.ec_perm = take(ec ? (size_t)L.rows_tk * 4 : 0);
-  const bool sh8 = fp8 && c->n_shared > 0;
+  // FP8: the token-order codes of x serve the shared experts, and with expert
+  // choice also the grouped copy (gathered from them)
+  const bool sh8 = fp8 && (c->n_shared > 0 || ec);
   L.xs_perm = take(fp8 ? (size_t)L.rows_tk * 4 : 0);
   L.xq = take(sh8 ? (size_t)c->T * c->d_model : 0);
   L.xs_tok = take(sh8 ? (size_t)c->T * 4 : 0);
@@ -340,7 +341,15 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   if (ec) {
     EcGatherArgs eg;
     eg.x = x; eg.perm = (const int32_t*)(ws + L.ec_perm); eg.rows = c.T > 0 ? L.rows_tk : 0; eg.d = c.d_model;
-    eg.esz = (int)esz; eg.xperm = ws + L.xperm; eg.err = &hdr->err;
+    eg.esz = (int)esz; eg.xperm = ws + L.xperm; eg.err = &hdr->err; eg.xs_tok = nullptr; eg.xs_perm = nullptr;
+    if (fp8) {
+      // quantise x once per token, then gather the codes and their scales
+      QuantRowsArgs qx;
+      qx.X = x; qx.Q = ws + L.xq; qx.scale = (float*)(ws + L.xs_tok); qx.cols = c.d_model; qx.rows0 = c.T;
+      qx.live0 = nullptr; qx.row1 = c.T; qx.rows1 = 0; qx.err = &hdr->err;
+      if (launch_quantize_rows(qx, s) != cudaSuccess) return MOE_ERR_CUDA;
+      eg.x = ws + L.xq; eg.esz = 1; eg.xs_tok = (const float*)(ws + L.xs_tok); eg.xs_perm = (float*)(ws + L.xs_perm);
+    }
     if (launch_ec_gather(eg, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (perm_token && L.rows_tk > 0 &&
         cudaMemcpyAsync(perm_token, ws + L.ec_perm, (size_t)L.rows_tk * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)

@@ -141,7 +141,10 @@ def test_fp8_config_rules(L):
     assert moe.validate(c8) == 0
     assert moe.workspace_size(c8) > 0 and moe.workspace_size(c8) != moe.workspace_size(_cfg())
     assert moe.validate(_cfg(fp8_experts=True, dtype=moe.F32, d=64, f=64)) == 2
-    assert moe.validate(_cfg(fp8_experts=True, expert_choice=True)) == 2
+    ce8 = _cfg(fp8_experts=True, expert_choice=True)
+    assert moe.validate(ce8) == 0
+    # expert choice keeps x's codes per token as well as per grouped row
+    assert moe.workspace_size(ce8) > moe.workspace_size(_cfg(expert_choice=True))
     # FP8 regions exist only with the flag
     assert moe.workspace_region(c8, moe.REGION_H_CODES)[1] == (4096 * 2) * 3072
     with pytest.raises(moe.MoEError):

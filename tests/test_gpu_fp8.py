@@ -242,3 +242,69 @@ def test_fp8_host_buffers_match_device_call():
     assert moe.check_device_errors(host.workspace) == 0
     for n in ("y", "topk_idx", "topk_w", "expert_counts", "dropped_mask", "f", "P", "L_aux", "route_stats"):
         assert torch.equal(getattr(dev, n).cpu(), getattr(host, n)), n
+
+
+EC_CASES = [
+    ("gpt2_softmax_bias", "gpt2_top2_gelu_bf16", dict(T=300, d=256, f=512)),
+    ("mixtral_swiglu", "mixtral_swiglu_bf16", dict(T=260, d=512, f=1024)),
+    ("deepseek_sigmoid_shared", "deepseek_shared_sigmoid_bf16", dict(T=300, d=512, f=320)),
+    ("skew_cf_unchosen", "skew_capacity_gelu_bf16", dict(T=500, d=256, f=384)),
+]
+
+
+@pytest.mark.parametrize("label,base,over", EC_CASES, ids=[c[0] for c in EC_CASES])
+def test_fp8_expert_choice_layer(label, base, over):
+    """Expert choice with FP8 experts: the choice bit for bit on the GPU's own
+    scores, the chosen rows' codes and scales bit for bit against the oracle's
+    quantisation of x, the hidden codes bit for bit on the kernel's own H, and
+    y against the oracle's FP8 expert-choice layer and the unquantised one."""
+    cfg = si.CONFIGS[base].replace(expert_choice=True, **over)
+    inp = si.layer_inputs(cfg, seed=34)
+    ex, out = run_fp8(cfg, inp)
+    cfg8 = cfg.replace(fp8_experts=True)
+    T, d, f, E, S = cfg.T, cfg.d, cfg.f, cfg.E, cfg.S
+    C = moe.capacity(cfg8)
+    gs = out.router_logits.cpu().numpy().astype(np.float64)
+    wq = oracle.quantize_experts(cfg, inp)
+    check_weights(ex, wq)
+    ref = oracle.fp8_ec_forward(cfg, inp, scores=gs, wq=wq)
+    assert ref["capacity"] == C
+    perm = out.perm_token.cpu().numpy()[:E * C]
+    assert np.array_equal(perm.reshape(E, C), ref["perm"])
+    assert np.all(out.expert_counts.cpu().numpy() == C)
+    rows_tk = E * C
+    ws = out.workspace
+    xp = _region(cfg8, ws, moe.REGION_XPERM, torch.uint8, (rows_tk, d)).cpu().numpy()
+    xs = _region(cfg8, ws, moe.REGION_X_SCALE, torch.float32, (rows_tk,)).cpu().numpy()
+    assert np.array_equal(xp, ref["xq"][perm]) and np.array_equal(xs, ref["xs"][perm])
+    rows_all = rows_tk + S * T
+    H = _np_bf16(_region(cfg8, ws, moe.REGION_H, torch.bfloat16, (rows_all, f)))
+    Hq = _region(cfg8, ws, moe.REGION_H_CODES, torch.uint8, (rows_all, f)).cpu().numpy()
+    Hs = _region(cfg8, ws, moe.REGION_H_SCALE, torch.float32, (rows_all,)).cpu().numpy()
+    q, s = oracle.quantize_rows(H)
+    assert np.array_equal(q, Hq) and np.array_equal(s, Hs)
+    y = to_host_f32(out.y).astype(np.float64)
+    yr = ref["y"]
+    chosen = np.zeros(T, bool)
+    chosen[np.unique(ref["perm"])] = True
+    skipped = ~chosen if S == 0 else np.zeros(T, bool)
+    assert np.all(y[skipped] == 0.0)
+    rel = float(np.linalg.norm(y - yr) / np.linalg.norm(yr))
+    assert rel <= 5e-3, rel
+    y16 = oracle.ec_forward(cfg, inp, scores=gs)["y"]
+    rel16 = float(np.linalg.norm(y - y16) / np.linalg.norm(y16))
+    assert rel16 <= 8e-2, rel16
+    if label == "skew_cf_unchosen":
+        assert skipped.any()
+
+
+def test_fp8_expert_choice_host_buffers_equal_the_device_call():
+    cfg = si.CONFIGS["mixtral_swiglu_bf16"].replace(T=260, d=256, f=512, expert_choice=True)
+    inp = si.layer_inputs(cfg, seed=35)
+    ex, out = run_fp8(cfg, inp)
+    dinp = device_inputs(inp)
+    host = moe.forward_fp8_host(cfg, dinp["x"].cpu().pin_memory(), dinp["W_g"], dinp["b_g"], ex,
+                                dinp["b1"], dinp["b2"])
+    torch.cuda.synchronize()
+    assert torch.equal(host.y.view(torch.int16), out.y.cpu().view(torch.int16))
+    assert torch.equal(host.expert_counts, out.expert_counts.cpu())
