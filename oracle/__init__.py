@@ -68,6 +68,7 @@ def _L() -> ctypes.CDLL:
         lib.oracle_add_noise.argtypes = [i64, i32, vp, vp]
         lib.oracle_route_health.argtypes = [i64, i32, i32, vp, vp]
         lib.oracle_backward.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32, dbl, dbl] + [vp] * 21
+        lib.oracle_ec_backward.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, dbl, dbl, i64] + [vp] * 18
         lib.oracle_ec_capacity.restype = i64
         lib.oracle_ec_capacity.argtypes = [i64, i32, i32, dbl]
         lib.oracle_ec_select.argtypes = [i64, i32, i64, vp, vp]
@@ -331,6 +332,36 @@ def backward(cfg, inp: Dict, dy: np.ndarray, dL_aux: float = 1.0,
                          _p(dyc), _p(out["dx"]), _p(out["dW_g"]), _p(out["db_g"]), _p(out["dW1"]), _p(out["db1"]),
                          _p(out["dW2"]), _p(out["db2"]), _p(out["dW3"]))
     out["routing"] = r
+    return out
+
+
+def ec_backward(cfg, inp: Dict, dy: np.ndarray, dL_aux: float = 1.0,
+                scores: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """Gradients of sum_t <dy_t, y_t> + dL_aux * L_aux with expert-choice
+    routing, fp64.  ``scores``: the experts choose on these gate probabilities
+    [T, E] (as in ec_forward); the gradient is taken at the oracle's own
+    logits either way."""
+    dt = cfg.dtype
+    lg = router_logits(inp["x"], inp["W_g"], inp["b_g"], dt)
+    if inp.get("noise") is not None:
+        lg = add_noise(lg, inp["noise"])
+    probs = gate_probs(lg, cfg.gating)
+    T, d, f, E, S = cfg.T, cfg.d, cfg.f, cfg.E, cfg.S
+    C = ec_capacity(T, E, cfg.k, cfg.capacity_factor)
+    perm = ec_select(probs if scores is None else scores, C)
+    G = E + S
+    out = dict(dx=np.empty((T, d)), dW_g=np.empty((d, E)), db_g=np.empty(E), dW1=np.empty((G, d, f)),
+               db1=np.empty((G, f)), dW2=np.empty((G, f, d)), db2=np.empty((G, d)),
+               dW3=np.empty((G, d, f)) if cfg.act == SWIGLU else None)
+    _L().oracle_ec_backward(T, d, f, E, S, cfg.act, cfg.gating, dt, cfg.alpha, dL_aux, C,
+                            _p(np.ascontiguousarray(perm, np.int32)), _p(_stored(inp["x"], dt)),
+                            _p(_stored(inp["W_g"], dt)), _p(np.ascontiguousarray(lg)),
+                            _p(_stored(inp["W1"], dt)), _p(_stored(inp["b1"], dt)), _p(_stored(inp["W2"], dt)),
+                            _p(_stored(inp["b2"], dt)), _p(_stored(inp["W3"], dt)),
+                            _p(np.ascontiguousarray(dy, np.float64)), _p(out["dx"]), _p(out["dW_g"]),
+                            _p(out["db_g"]), _p(out["dW1"]), _p(out["db1"]), _p(out["dW2"]), _p(out["db2"]),
+                            _p(out["dW3"]))
+    out.update(perm=perm, capacity=C, probs=probs, logits=lg)
     return out
 
 

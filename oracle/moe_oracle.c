@@ -551,6 +551,154 @@ void oracle_backward(int64_t T, int d, int f, int E, int k, int S, int act, int 
   free(xr); free(a); free(u); free(h); free(dh); free(da); free(du); free(o); free(p); free(dl); free(dp); free(dw);
 }
 
+/* ---- backward pass with expert-choice routing --------------------------------------
+ * Gradients of the same scalar L = sum_t <dy_t, y_t> + dL_aux * L_aux when each
+ * expert chooses its C tokens ["MoE架构解析" §2.2]:
+ *   y_t = sum over the experts e that chose t of p_te o_e(x_t) + sum_s o_s(x_t),
+ * p the gate probabilities over all E (softmax, or normalised sigmoid), the
+ * weights of the sum as they are (no renormalisation).  The choice itself is
+ * piecewise constant: no gradient.  By the chain rule:
+ *  - dp_te = <dy_t, o_e(x_t)> where e chose t; do_e = p_te dy_t;
+ *  - the expert FFN as in the token-choice backward above;
+ *  - L_aux = alpha E sum_e f_e P_e with f_e = 1/E (every expert holds C of the
+ *    E C selections): dp_te += dL_aux alpha E f_e / T;
+ *  - through the gating over all E: softmax dl = p (dp - <p, dp>); normalised
+ *    sigmoid p = s / sum s: dl_e = (dp_e - <p, dp>) / sum s * s_e (1 - s_e);
+ *  - l = x W_g + b_g (+ noise): dW_g += x dl^T, db_g += dl, dx += W_g dl.
+ * perm [E*C]: the chosen tokens of each expert; logits [T, E] (noisy) logits.
+ * All outputs fp64, overwritten. */
+
+/* One expert g on one token row xr with output weight wj: adds the expert's
+ * parameter gradients and its part of dx_t (dxr), and returns <dy_t, o_g(x_t)>. */
+static double expert_row_bwd(int d, int f, int act, int dtype, int g, double wj, const double* xr,
+                             const double* dyt, const void* W1, const void* b1, const void* W2, const void* b2,
+                             const void* W3, double* dxr, double* dW1, double* db1, double* dW2, double* db2,
+                             double* dW3) {
+  const int swiglu = act == OACT_SWIGLU;
+  const int64_t w1o = (int64_t)g * d * f, w2o = (int64_t)g * f * d;
+  double* a = (double*)malloc(sizeof(double) * (size_t)f);
+  double* u = (double*)malloc(sizeof(double) * (size_t)f);
+  double* h = (double*)malloc(sizeof(double) * (size_t)f);
+  double* dh = (double*)malloc(sizeof(double) * (size_t)f);
+  double* da = (double*)malloc(sizeof(double) * (size_t)f);
+  double* du = (double*)malloc(sizeof(double) * (size_t)f);
+  double* o = (double*)malloc(sizeof(double) * (size_t)d);
+  /* forward of the expert: a = W1^T x + b1 (u = W3^T x), h = act(a) (silu(a) u) */
+  for (int c = 0; c < f; ++c) { a[c] = (b1 && !swiglu) ? ld(b1, dtype, (int64_t)g * f + c) : 0.0; u[c] = 0.0; }
+  for (int i = 0; i < d; ++i) {
+    for (int c = 0; c < f; ++c) a[c] += xr[i] * ld(W1, dtype, w1o + (int64_t)i * f + c);
+    if (swiglu)
+      for (int c = 0; c < f; ++c) u[c] += xr[i] * ld(W3, dtype, w1o + (int64_t)i * f + c);
+  }
+  for (int c = 0; c < f; ++c) h[c] = swiglu ? oracle_act(OACT_SWIGLU, a[c]) * u[c] : oracle_act(act, a[c]);
+  /* o = W2^T h + b2 and <dy, o> */
+  for (int c = 0; c < d; ++c) o[c] = (b2 && !swiglu) ? ld(b2, dtype, (int64_t)g * d + c) : 0.0;
+  for (int r = 0; r < f; ++r)
+    for (int c = 0; c < d; ++c) o[c] += h[r] * ld(W2, dtype, w2o + (int64_t)r * d + c);
+  double dot = 0.0;
+  for (int c = 0; c < d; ++c) dot += dyt[c] * o[c];
+  /* do = wj dy: dh = W2 do, dW2 += h do^T, db2 += do */
+  for (int r = 0; r < f; ++r) {
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) {
+      const double doc = wj * dyt[c];
+      acc += ld(W2, dtype, w2o + (int64_t)r * d + c) * doc;
+      dW2[w2o + (int64_t)r * d + c] += h[r] * doc;
+    }
+    dh[r] = acc;
+  }
+  if (b2 && !swiglu)
+    for (int c = 0; c < d; ++c) db2[(int64_t)g * d + c] += wj * dyt[c];
+  /* activation: da (, du) */
+  for (int r = 0; r < f; ++r) {
+    if (swiglu) {
+      const double sa = sig(a[r]);
+      da[r] = dh[r] * u[r] * (sa + a[r] * sa * (1.0 - sa));
+      du[r] = dh[r] * a[r] * sa;
+    } else if (act == OACT_RELU) {
+      da[r] = a[r] > 0.0 ? dh[r] : 0.0;
+    } else {
+      da[r] = dh[r] * gelu_grad(a[r]);
+    }
+  }
+  /* dx += W1 da (+ W3 du), dW1 += x da^T, dW3 += x du^T, db1 += da */
+  for (int i = 0; i < d; ++i) {
+    double acc = 0.0;
+    for (int r = 0; r < f; ++r) {
+      acc += ld(W1, dtype, w1o + (int64_t)i * f + r) * da[r];
+      dW1[w1o + (int64_t)i * f + r] += xr[i] * da[r];
+      if (swiglu) {
+        acc += ld(W3, dtype, w1o + (int64_t)i * f + r) * du[r];
+        dW3[w1o + (int64_t)i * f + r] += xr[i] * du[r];
+      }
+    }
+    dxr[i] += acc;
+  }
+  if (b1 && !swiglu)
+    for (int r = 0; r < f; ++r) db1[(int64_t)g * f + r] += da[r];
+  free(a); free(u); free(h); free(dh); free(da); free(du); free(o);
+  return dot;
+}
+
+void oracle_ec_backward(int64_t T, int d, int f, int E, int S, int act, int gating, int dtype, double alpha,
+                        double dL_aux, int64_t C, const int32_t* perm, const void* x, const void* W_g,
+                        const double* logits, const void* W1, const void* b1, const void* W2, const void* b2,
+                        const void* W3, const double* dy, double* dx, double* dWg, double* dbg, double* dW1,
+                        double* db1, double* dW2, double* db2, double* dW3) {
+  const int G = E + S;
+  memset(dx, 0, sizeof(double) * (size_t)(T * d));
+  memset(dWg, 0, sizeof(double) * (size_t)d * E);
+  memset(dbg, 0, sizeof(double) * (size_t)E);
+  memset(dW1, 0, sizeof(double) * (size_t)G * d * f);
+  memset(db1, 0, sizeof(double) * (size_t)G * f);
+  memset(dW2, 0, sizeof(double) * (size_t)G * f * d);
+  memset(db2, 0, sizeof(double) * (size_t)G * d);
+  if (dW3) memset(dW3, 0, sizeof(double) * (size_t)G * d * f);
+  double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+  double* p = (double*)malloc(sizeof(double) * (size_t)E);
+  double* dp = (double*)malloc(sizeof(double) * (size_t)E);
+  for (int64_t t = 0; t < T; ++t) {
+    const double* dyt = dy + t * d;
+    double* dxt = dx + t * d;
+    for (int i = 0; i < d; ++i) xr[i] = ld(x, dtype, t * d + i);
+    const double* l = logits + t * E;
+    oracle_gate_probs(1, E, gating, l, p);
+    for (int e = 0; e < E; ++e) dp[e] = dL_aux * alpha * E * (1.0 / E) / (double)T;
+    /* the experts that chose t, ascending */
+    for (int e = 0; e < E; ++e) {
+      int chose = 0;
+      for (int64_t i = 0; i < C; ++i)
+        if (perm[(int64_t)e * C + i] == t) { chose = 1; break; }
+      if (chose)
+        dp[e] += expert_row_bwd(d, f, act, dtype, e, p[e], xr, dyt, W1, b1, W2, b2, W3, dxt, dW1, db1, dW2, db2,
+                                dW3);
+    }
+    for (int s = 0; s < S; ++s)
+      expert_row_bwd(d, f, act, dtype, E + s, 1.0, xr, dyt, W1, b1, W2, b2, W3, dxt, dW1, db1, dW2, db2, dW3);
+    /* through the gating over all E */
+    double pdp = 0.0;
+    for (int e = 0; e < E; ++e) pdp += p[e] * dp[e];
+    double zs = 0.0;
+    if (gating != OGATE_SOFTMAX)
+      for (int e = 0; e < E; ++e) zs += sig(l[e]);
+    for (int e = 0; e < E; ++e) {
+      double dl;
+      if (gating == OGATE_SOFTMAX) {
+        dl = p[e] * (dp[e] - pdp);
+      } else {
+        const double se = sig(l[e]);
+        dl = (dp[e] - pdp) / zs * se * (1.0 - se);
+      }
+      dbg[e] += dl;
+      for (int i = 0; i < d; ++i) {
+        dWg[(int64_t)i * E + e] += xr[i] * dl;
+        dxt[i] += ld(W_g, dtype, (int64_t)i * E + e) * dl;
+      }
+    }
+  }
+  free(xr); free(p); free(dp);
+}
+
 /* ---- FP8 (E4M3) experts ---------------------------------------------------------
  * ["MoE混合专家模型：Transformer稀疏前馈网络原理与PyTorch实现" §5.2: the expert
  * parameters are quantised from 16-bit to 8-bit floats, which halves their memory
