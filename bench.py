@@ -296,7 +296,8 @@ def run_backward(args, cfg, d, dev, world, rank, local):
             "value": replica_throughput(cfg.T, ms, world), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_desc(cfg), "T": cfg.T},
+            "config": {"workload": workload_desc(cfg), "T": cfg.T,
+                       "routing": "expert choice" if getattr(cfg, "expert_choice", False) else "token choice"},
             "gemm_flop_per_step": flop, "gemm_tflops": round(tf, 1),
             "frac_of_bf16_sustained": round(tf / sust, 4),
             # the call's GEMM work over the whole call's time: a lower bound of

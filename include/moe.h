@@ -217,7 +217,7 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
                             float* L_aux_host, float* route_stats_host, void* workspace, size_t workspace_bytes,
                             moe_stream stream, const moe_launch_opts* opts);
 
-/* Backward pass of the layer (token choice, bf16): gradients of
+/* Backward pass of the layer (bf16; token or expert choice): gradients of
  *   L = sum_t <dy_t, y_t> + dL_aux * L_aux
  * (the load-balance loss joins the main loss before one backward, "MoE混合专家
  * 模型：Transformer稀疏前馈网络原理与PyTorch实现" §4.3) with respect to x, W_g,
@@ -229,8 +229,12 @@ moe_status moe_forward_host(const moe_config* cfg, const void* x_host, const voi
  * Outputs (device, fp32, overwritten): dx [T, d], dW_g [d, E], db_g [E] (iff
  * b_g), dW1 [E+S, d, f], db1 [E+S, f] (iff b1), dW2 [E+S, f, d], db2 [E+S, d]
  * (iff b2), dW3 [E+S, d, f] (iff SwiGLU).
+ * With MOE_FLAG_EXPERT_CHOICE the choice of tokens carries no gradient, the
+ * gate probabilities s[t,e] weighting the chosen experts' outputs carry the
+ * router's, and L_aux (constant alpha there: f_e = 1/E and sum_e P_e = 1)
+ * carries none beyond rounding.
  * workspace: >= moe_backward_workspace_size(cfg) bytes, 256-byte aligned.
- * MOE_ERR_UNSUPPORTED for fp32 layers and for MOE_FLAG_EXPERT_CHOICE.
+ * MOE_ERR_UNSUPPORTED for fp32 layers and for MOE_FLAG_FP8_EXPERTS.
  * Deterministic: bitwise the same gradients for the same inputs. */
 size_t moe_backward_workspace_size(const moe_config* cfg);
 moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, const void* b_g,

@@ -10,6 +10,8 @@
 //               order perm[e*C + i], each row's gate weight, each (token,
 //               expert)'s row, and a per-token bit mask of the choosing experts.
 //   ec_gather   one warp per grouped row: copies its token's row of x.
+// Each expert's rows start Cs >= C apart (Cs = C in the forward; the backward
+// pads them to whole blocks of its weight-gradient GEMMs).
 //   ec_combine  one warp per token: sum over the experts that chose it, in
 //               ascending expert order, of weight x expert output, then the
 //               shared experts.  No atomics: bitwise reproducible.
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(kSelThreads) ec_select_kernel(EcSelectArgs a) 
       const bool take = g || (q && eq_seen + __popc(qb & lt) < my_take_eq);
       const uint32_t tb = __ballot_sync(0xffffffffu, take);
       if (take) {
-        const int64_t row = (int64_t)e * C + pos + __popc(tb & lt);
+        const int64_t row = (int64_t)e * a.Cs + pos + __popc(tb & lt);
         a.perm[row] = (int32_t)t;
         a.w_row[row] = __uint_as_float(k);
         a.tok_row[t * a.E + e] = (int32_t)row;
@@ -205,7 +207,7 @@ constexpr int kGatherWarps = 8;
 __global__ void __launch_bounds__(kGatherWarps * 32) ec_gather_kernel(EcGatherArgs a) {
   const int lane = threadIdx.x % 32;
   const int64_t r = (int64_t)blockIdx.x * kGatherWarps + threadIdx.x / 32;
-  if (r >= a.rows || *(volatile const uint32_t*)a.err != 0u) return;
+  if (r >= a.rows || *(volatile const uint32_t*)a.err != 0u || r % a.Cs >= a.C) return;
   const int64_t t = a.perm[r];
   if (a.xs_perm && lane == 0) a.xs_perm[r] = a.xs_tok[t];
   const int64_t chunks = (int64_t)a.d * a.esz / 16;
@@ -309,6 +311,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) ec_combine_kernel(EcCombin
 
 cudaError_t launch_ec_select(const EcSelectArgs& a, cudaStream_t s) {
   if (a.E <= 0) return cudaSuccess;
+  if (a.Cs < a.C) return cudaErrorInvalidValue;
   const size_t smem = a.T <= kMaxCachedT ? (size_t)(a.T > 0 ? a.T : 1) * 4 : 0;
   cudaError_t e = cudaFuncSetAttribute(ec_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
   if (e != cudaSuccess) return e;
@@ -318,6 +321,7 @@ cudaError_t launch_ec_select(const EcSelectArgs& a, cudaStream_t s) {
 
 cudaError_t launch_ec_gather(const EcGatherArgs& a, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;
+  if (a.C <= 0 || a.Cs < a.C) return cudaErrorInvalidValue;
   ec_gather_kernel<<<(unsigned)((a.rows + kGatherWarps - 1) / kGatherWarps), kGatherWarps * 32, 0, s>>>(a);
   return cudaGetLastError();
 }

@@ -25,6 +25,7 @@ struct RouterArgs {
   uint32_t* err;       // workspace status word
   int64_t timeout_ns;  // limit of every device-side wait
   float* scores_em;    // expert choice: gate probabilities [E, T] (no top-k), else null
+  float* raw_logits;   // [T, E] the (noisy) logits before gating, or null (the backward's copy)
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 
@@ -120,9 +121,10 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 struct EcSelectArgs {
   const float* scores_em;  // [E, T] gate probabilities
   int64_t T, C;
+  int64_t Cs;              // rows reserved per expert in the grouped order (>= C; padding after C)
   int E, EW;               // EW = ceil(E / 32) words of the per-token expert mask
-  int32_t* perm;           // [E * C] chosen tokens, grouped by expert, tokens ascending
-  float* w_row;            // [E * C] gate weight of each grouped row
+  int32_t* perm;           // [E * Cs] chosen tokens, grouped by expert, tokens ascending
+  float* w_row;            // [E * Cs] gate weight of each grouped row
   int32_t* tok_row;        // [T, E] grouped row of (token, expert) where chosen
   uint32_t* bits;          // [T, EW] choosing experts of each token (zeroed by the caller)
   const uint32_t* err;
@@ -132,7 +134,8 @@ cudaError_t launch_ec_select(const EcSelectArgs& a, cudaStream_t s);
 struct EcGatherArgs {
   const void* x;            // [T, d]: x, or with FP8 experts its E4M3 codes
   const int32_t* perm;
-  int64_t rows;
+  int64_t rows;             // E * Cs; the rows c >= C of each expert's Cs are skipped
+  int64_t C, Cs;
   int d, esz;
   void* xperm;
   const uint32_t* err;
@@ -270,8 +273,42 @@ struct DxArgs {
   int64_t rows_routed, shared_stride;
   float* dx;               // [T, d]
   const uint32_t* err;
+  // expert choice (k = 0, slot unused): the chosen rows of token t are
+  // tok_row[t, e] for the experts e set in bits[t]; else null
+  const uint32_t* ec_bits;
+  const int32_t* ec_tok_row;
+  int EW;
 };
 cudaError_t launch_dx(const DxArgs& a, cudaStream_t s);
+
+// Expert-choice backward: grouped rows e * Cs + c (c < C), tok_row / bits as
+// written by ec_select.
+struct EcCombineBwdArgs {
+  const void* dy;          // [T, d] bf16
+  const float* o;          // expert outputs [rows, d] fp32
+  const int32_t* perm;     // [E * Cs]
+  const float* w_row;      // [E * Cs]
+  int64_t rows, C, Cs;     // rows = E * Cs
+  int d;
+  void* dO;                // [rows, d] bf16
+  float* dw_row;           // [E * Cs] <dy_t, o_row>
+  const uint32_t* err;
+};
+cudaError_t launch_ec_combine_bwd(const EcCombineBwdArgs& a, cudaStream_t s);
+
+struct EcRouterBwdArgs {
+  const float* logits;     // [T, E] (noisy) router logits
+  const uint32_t* bits;    // [T, EW] choosing experts of each token
+  const int32_t* tok_row;  // [T, E]
+  const float* dw_row;     // [E * Cs]
+  int64_t T;
+  int E, EW, gating;
+  double alpha;
+  float dL_aux;
+  float* dl;               // [T, E]
+  const uint32_t* err;
+};
+cudaError_t launch_ec_router_bwd(const EcRouterBwdArgs& a, cudaStream_t s);
 
 struct DwgArgs {
   const void* x;           // [T, d] bf16

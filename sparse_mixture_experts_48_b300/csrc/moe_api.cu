@@ -148,8 +148,10 @@ HostStage host_stage(const moe_config* c, size_t base) {
 struct BwdLayout {
   size_t hdr, hist, psum, base, lrank, npre, offsets, seg, slot, idx, w, drop, cnt, f, P, L, logits;
   size_t xperm, pre_a, pre_u, h, o, dO, dA, dU, dxp, dw, dl, part, bpart, total;
+  size_t ec_scores, ec_bits, ec_tokrow, ec_wrow, ec_perm, ec_dw;   // expert choice
   int64_t nblk, Tpad, rows_routed, rows_all, nchunk;
-  int G;
+  int64_t ec_C, ec_Cs;   // expert choice: tokens per expert, rows reserved per expert (C padded)
+  int G, EW;
 };
 
 BwdLayout bwd_layout(const moe_config* c) {
@@ -159,7 +161,12 @@ BwdLayout bwd_layout(const moe_config* c) {
   L.G = c->E + c->n_shared;
   L.nblk = (T + kRouterBM - 1) / kRouterBM;
   L.Tpad = (T + 127) / 128 * 128;
-  L.rows_routed = (T * c->k + 127) / 128 * 128 + 128 * (int64_t)c->E;   // >= sum of padded segments
+  const bool ec = (c->flags & MOE_FLAG_EXPERT_CHOICE) != 0;
+  L.ec_C = ec ? ec_capacity_of(c) : -1;
+  L.ec_Cs = ec ? (L.ec_C + 127) / 128 * 128 : 0;
+  L.EW = (c->E + 31) / 32;
+  L.rows_routed = ec ? (int64_t)c->E * L.ec_Cs
+                     : (T * c->k + 127) / 128 * 128 + 128 * (int64_t)c->E;   // >= sum of padded segments
   L.rows_all = L.rows_routed + (int64_t)c->n_shared * L.Tpad;
   L.nchunk = dwg_chunks(T);
   const size_t d = c->d_model, f = c->d_ff, tk = (size_t)T * c->k, ra = (size_t)L.rows_all;
@@ -199,6 +206,13 @@ BwdLayout bwd_layout(const moe_config* c) {
   L.dl = take((size_t)T * c->E * 4);
   L.part = take((size_t)L.nchunk * d * c->E * 4);
   L.bpart = take((size_t)L.nchunk * c->E * 4);
+  const size_t ecr = ec ? (size_t)L.rows_routed : 0;
+  L.ec_scores = take(ec ? (size_t)c->E * T * 4 : 0);
+  L.ec_bits = take(ec ? (size_t)T * L.EW * 4 : 0);
+  L.ec_tokrow = take(ec ? (size_t)T * c->E * 4 : 0);
+  L.ec_wrow = take(ecr * 4);
+  L.ec_perm = take(ecr * 4);
+  L.ec_dw = take(ecr * 4);
   L.total = off;
   return L;
 }
@@ -206,7 +220,7 @@ BwdLayout bwd_layout(const moe_config* c) {
 moe_status check_bwd_cfg(const moe_config* c) {
   moe_status st = check_cfg(c);
   if (st != MOE_OK) return st;
-  if (c->dtype != MOE_DT_BF16 || (c->flags & (MOE_FLAG_EXPERT_CHOICE | MOE_FLAG_FP8_EXPERTS))) return MOE_ERR_UNSUPPORTED;
+  if (c->dtype != MOE_DT_BF16 || (c->flags & MOE_FLAG_FP8_EXPERTS)) return MOE_ERR_UNSUPPORTED;
   const BwdLayout L = bwd_layout(c);
   if (L.rows_all >= ((int64_t)1 << 31) - 2 * kGemmBM) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -314,7 +328,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   ra.gating = c.gating; ra.dtype = c.dtype; ra.logits_out = router_logits; ra.topk_idx = topk_idx;
   ra.topk_w = topk_w; ra.lrank = ws + L.lrank; ra.hist = (int32_t*)(ws + L.hist); ra.psum = (float*)(ws + L.psum);
   ra.err = &hdr->err; ra.timeout_ns = timeout; ra.nblk = L.nblk;
-  ra.scores_em = ec ? (float*)(ws + L.ec_scores) : nullptr;
+  ra.scores_em = ec ? (float*)(ws + L.ec_scores) : nullptr; ra.raw_logits = nullptr;
   if (launch_router(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 2. scan: ranks, capacity, offsets, statistics, segment table (expert
@@ -322,7 +336,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   if (clk.mark(1) != cudaSuccess) return MOE_ERR_CUDA;
   if (ec) {
     EcSelectArgs ea;
-    ea.scores_em = (const float*)(ws + L.ec_scores); ea.T = c.T; ea.C = L.ec_C; ea.E = c.E; ea.EW = L.EW;
+    ea.scores_em = (const float*)(ws + L.ec_scores); ea.T = c.T; ea.C = L.ec_C; ea.Cs = L.ec_C; ea.E = c.E; ea.EW = L.EW;
     ea.perm = (int32_t*)(ws + L.ec_perm); ea.w_row = (float*)(ws + L.ec_wrow); ea.tok_row = (int32_t*)(ws + L.ec_tokrow);
     ea.bits = (uint32_t*)(ws + L.ec_bits); ea.err = &hdr->err;
     if (c.T > 0 && launch_ec_select(ea, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -342,6 +356,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
     EcGatherArgs eg;
     eg.x = x; eg.perm = (const int32_t*)(ws + L.ec_perm); eg.rows = c.T > 0 ? L.rows_tk : 0; eg.d = c.d_model;
     eg.esz = (int)esz; eg.xperm = ws + L.xperm; eg.err = &hdr->err; eg.xs_tok = nullptr; eg.xs_perm = nullptr;
+    eg.C = L.ec_C; eg.Cs = L.ec_C;
     if (fp8) {
       // quantise x once per token, then gather the codes and their scales
       QuantRowsArgs qx;
@@ -589,6 +604,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
   if (st != MOE_OK) return st;
   const moe_config& c = *cfg;
   const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  const bool ec = (c.flags & MOE_FLAG_EXPERT_CHOICE) != 0;
   const bool empty = c.T == 0;
   if (!W_g || !W1 || !W2 || !dW_g || !dW1 || !dW2) return MOE_ERR_INVALID_ARG;
   if (!empty && (!x || !dy || !dx)) return MOE_ERR_INVALID_ARG;
@@ -630,10 +646,24 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
   ra.topk_idx = (int32_t*)(ws + L.idx); ra.topk_w = (float*)(ws + L.w); ra.lrank = ws + L.lrank;
   ra.hist = (int32_t*)(ws + L.hist); ra.psum = (float*)(ws + L.psum); ra.err = &hdr->err; ra.timeout_ns = timeout;
   ra.nblk = L.nblk;
+  if (ec) {
+    // the experts choose on the gate probabilities; the gating's backward
+    // needs the logits themselves
+    ra.scores_em = (float*)(ws + L.ec_scores); ra.logits_out = nullptr; ra.raw_logits = (float*)(ws + L.logits);
+    if (cudaMemsetAsync(ws + L.ec_bits, 0, (size_t)T * L.EW * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if (launch_router(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ec) {
+    EcSelectArgs ea;
+    ea.scores_em = (const float*)(ws + L.ec_scores); ea.T = T; ea.C = L.ec_C; ea.Cs = L.ec_Cs; ea.E = E;
+    ea.EW = L.EW; ea.perm = (int32_t*)(ws + L.ec_perm); ea.w_row = (float*)(ws + L.ec_wrow);
+    ea.tok_row = (int32_t*)(ws + L.ec_tokrow); ea.bits = (uint32_t*)(ws + L.ec_bits); ea.err = &hdr->err;
+    if (launch_ec_select(ea, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   ScanArgs sa;
   memset(&sa, 0, sizeof(sa));
-  sa.T = T; sa.E = E; sa.k = k; sa.S = S; sa.capacity = C; sa.alpha = c.alpha; sa.nblk = L.nblk; sa.ec_C = -1;
+  sa.T = T; sa.E = E; sa.k = k; sa.S = S; sa.capacity = ec ? -1 : C; sa.alpha = c.alpha; sa.nblk = L.nblk;
+  sa.ec_C = ec ? L.ec_C : -1;
   sa.pad_rows = 128; sa.shared_stride = L.Tpad; sa.hist = ra.hist; sa.psum = ra.psum;
   sa.base = (int32_t*)(ws + L.base); sa.n_pre = (int32_t*)(ws + L.npre); sa.counts = (int32_t*)(ws + L.cnt);
   sa.offsets = (int32_t*)(ws + L.offsets); sa.f = (float*)(ws + L.f); sa.P = (float*)(ws + L.P);
@@ -646,7 +676,14 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
   ga.topk_idx = ra.topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.nblk = L.nblk; ga.offsets = sa.offsets;
   ga.slot = (int32_t*)(ws + L.slot); ga.dropped = ws + L.drop; ga.perm_token = nullptr; ga.xperm = ws + L.xperm;
   ga.err = &hdr->err;
-  if (launch_gather(ga, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ec) {
+    EcGatherArgs eg;
+    eg.x = x; eg.perm = (const int32_t*)(ws + L.ec_perm); eg.rows = L.rows_routed; eg.C = L.ec_C; eg.Cs = L.ec_Cs;
+    eg.d = d; eg.esz = 2; eg.xperm = ws + L.xperm; eg.err = &hdr->err; eg.xs_tok = nullptr; eg.xs_perm = nullptr;
+    if (launch_ec_gather(eg, s) != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (launch_gather(ga, s) != cudaSuccess) {
+    return MOE_ERR_CUDA;
+  }
   PadZeroArgs pz;
   pz.buf = ws + L.xperm; pz.row_bytes = (int64_t)d * 2; pz.G = E; pz.E = E; pz.T = T; pz.counts = sa.counts;
   pz.seg = seg;
@@ -671,14 +708,31 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
   cb.dy = dy; cb.o = (const float*)(ws + L.o); cb.slot = ga.slot; cb.topk_w = ra.topk_w; cb.T = T; cb.d = d;
   cb.k = k; cb.S = S; cb.rows_routed = L.rows_routed; cb.shared_stride = L.Tpad; cb.dO = ws + L.dO;
   cb.dw = (float*)(ws + L.dw); cb.err = &hdr->err;
-  if (launch_combine_bwd(cb, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ec) {
+    EcCombineBwdArgs ecb;
+    ecb.dy = dy; ecb.o = (const float*)(ws + L.o); ecb.perm = (const int32_t*)(ws + L.ec_perm);
+    ecb.w_row = (const float*)(ws + L.ec_wrow); ecb.rows = L.rows_routed; ecb.C = L.ec_C; ecb.Cs = L.ec_Cs;
+    ecb.d = d; ecb.dO = ws + L.dO; ecb.dw_row = (float*)(ws + L.ec_dw); ecb.err = &hdr->err;
+    if (launch_ec_combine_bwd(ecb, s) != cudaSuccess) return MOE_ERR_CUDA;
+    cb.k = 0; cb.slot = nullptr; cb.topk_w = nullptr;   // the shared rows only
+  }
+  if ((!ec || S > 0) && launch_combine_bwd(cb, s) != cudaSuccess) return MOE_ERR_CUDA;
   pz.buf = ws + L.dO; pz.G = G;
   if (launch_pad_zero(pz, s) != cudaSuccess) return MOE_ERR_CUDA;
   RouterBwdArgs rb;
   rb.logits = (const float*)(ws + L.logits); rb.topk_idx = ra.topk_idx; rb.topk_w = ra.topk_w;
   rb.dw = cb.dw; rb.n_pre = sa.n_pre; rb.T = T; rb.E = E; rb.k = k; rb.gating = c.gating; rb.alpha = c.alpha;
   rb.dL_aux = dL_aux; rb.dl = (float*)(ws + L.dl); rb.err = &hdr->err;
-  if (launch_router_bwd(rb, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ec) {
+    EcRouterBwdArgs erb;
+    erb.logits = (const float*)(ws + L.logits); erb.bits = (const uint32_t*)(ws + L.ec_bits);
+    erb.tok_row = (const int32_t*)(ws + L.ec_tokrow); erb.dw_row = (const float*)(ws + L.ec_dw); erb.T = T;
+    erb.E = E; erb.EW = L.EW; erb.gating = c.gating; erb.alpha = c.alpha; erb.dL_aux = dL_aux; erb.dl = rb.dl;
+    erb.err = &hdr->err;
+    if (launch_ec_router_bwd(erb, s) != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (launch_router_bwd(rb, s) != cudaSuccess) {
+    return MOE_ERR_CUDA;
+  }
   // dH = dO W2^T, activation backward -> dA (, dU)
   BwdGemmArgs bg;
   memset(&bg, 0, sizeof(bg));
@@ -725,7 +779,11 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
   DxArgs dxa;
   dxa.dxp = (const float*)(ws + L.dxp); dxa.slot = ga.slot; dxa.dl = rb.dl; dxa.Wg = W_g; dxa.T = T; dxa.d = d;
   dxa.k = k; dxa.E = E; dxa.S = S; dxa.rows_routed = L.rows_routed; dxa.shared_stride = L.Tpad; dxa.dx = dx;
-  dxa.err = &hdr->err;
+  dxa.err = &hdr->err; dxa.ec_bits = nullptr; dxa.ec_tok_row = nullptr; dxa.EW = L.EW;
+  if (ec) {
+    dxa.k = 0; dxa.slot = nullptr;
+    dxa.ec_bits = (const uint32_t*)(ws + L.ec_bits); dxa.ec_tok_row = (const int32_t*)(ws + L.ec_tokrow);
+  }
   if (launch_dx(dxa, s) != cudaSuccess) return MOE_ERR_CUDA;
   DwgArgs dg;
   dg.x = x; dg.dl = rb.dl; dg.T = T; dg.d = d; dg.E = E; dg.nchunk = L.nchunk; dg.part = (float*)(ws + L.part);

@@ -10,8 +10,9 @@
 //                the selected sigmoids) plus the L_aux term through P
 //                (dp_te = dL_aux alpha E f_e / T).
 //   dx           per token: sum of the grouped-row gradients of its kept
-//                assignments and shared experts, plus dl_t W_g^T (8 tokens
-//                per warp share the W_g rows).
+//                assignments (with expert choice: of the experts that chose
+//                it) and shared experts, plus dl_t W_g^T (8 tokens per warp
+//                share the W_g rows).
 //   dWg          x^T dl and sum_t dl, in T-chunks, then the chunks in order.
 //   colsum       bias gradients: column sums of dO / dA over a segment.
 //   pad_zero     the padding rows of a grouped buffer (segments padded to
@@ -134,22 +135,43 @@ __global__ void router_bwd_kernel(RouterBwdArgs a) {
 // dl W_g^T term) serves all of them; a lane owns 4 consecutive columns.
 constexpr int kMaxE = 256;
 
+// Dynamic shared memory: s_dl [kWarps][kDxTok][E] gate-logit gradients, then
+// with expert choice s_row [kWarps][kDxTok][E] the chosen rows of each token
+// (ascending expert), listed once so that the column loop's loads of dxp do
+// not wait on the bit mask and the row table.
 template <int kDxTok>
 __global__ void __launch_bounds__(kWarps * 32) dx_kernel(DxArgs a) {
-  __shared__ float s_dl[kWarps][kDxTok][kMaxE];
+  extern __shared__ float s_dyn[];
   __shared__ int s_slot[kWarps][kDxTok][8];
+  __shared__ int s_nrow[kWarps][kDxTok];
   const int lane = threadIdx.x % 32, wl = threadIdx.x / 32;
   const int64_t t0 = ((int64_t)blockIdx.x * kWarps + wl) * kDxTok;
   if (t0 >= a.T || *(volatile const uint32_t*)a.err != 0u) return;
   const int d = a.d, k = a.k, E = a.E;
+  float* s_dl = s_dyn + (int64_t)wl * kDxTok * E;                          // [kDxTok][E]
+  int* s_row = (int*)(s_dyn + (int64_t)kWarps * kDxTok * E) + (int64_t)wl * kDxTok * E;   // [kDxTok][E]
   const int nt = a.T - t0 < kDxTok ? (int)(a.T - t0) : kDxTok;
   for (int i = lane; i < kDxTok * E; i += 32) {
     const int tt = i / E, e = i % E;
-    s_dl[wl][tt][e] = tt < nt ? a.dl[(t0 + tt) * E + e] : 0.f;
+    s_dl[tt * E + e] = tt < nt ? a.dl[(t0 + tt) * E + e] : 0.f;
   }
   for (int i = lane; i < kDxTok * 8; i += 32) {
     const int tt = i / 8, j = i % 8;
     s_slot[wl][tt][j] = (tt < nt && j < k) ? a.slot[(t0 + tt) * k + j] : -1;
+  }
+  if (a.ec_bits) {
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int tt = 0; tt < nt; ++tt) {
+      const int64_t t = t0 + tt;
+      int n = 0;
+      for (int w = 0; w < a.EW; ++w) {
+        const uint32_t m = a.ec_bits[t * a.EW + w];
+        const int e = 32 * w + lane;
+        if ((m >> lane) & 1u) s_row[tt * E + n + __popc(m & lt)] = a.ec_tok_row[t * E + e];
+        n += __popc(m);
+      }
+      if (lane == 0) s_nrow[wl][tt] = n;
+    }
   }
   __syncwarp();
   const uint16_t* Wg = (const uint16_t*)a.Wg;
@@ -181,7 +203,7 @@ __global__ void __launch_bounds__(kWarps * 32) dx_kernel(DxArgs a) {
         for (int tt = 0; tt < kDxTok; ++tt)
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            if (e0 + j < E) r[tt][q] = fmaf(s_dl[wl][tt][e0 + j], wv[j], r[tt][q]);
+            if (e0 + j < E) r[tt][q] = fmaf(s_dl[tt * E + e0 + j], wv[j], r[tt][q]);
       }
     }
     for (int tt = 0; tt < nt; ++tt) {
@@ -192,6 +214,14 @@ __global__ void __launch_bounds__(kWarps * 32) dx_kernel(DxArgs a) {
         const int sl = s_slot[wl][tt][j];
         if (sl >= 0) {
           const float4 v = *reinterpret_cast<const float4*>(a.dxp + (int64_t)sl * d + c);
+          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+      }
+      if (a.ec_bits) {
+        // expert choice: the rows of the experts that chose t, ascending
+        const int n = s_nrow[wl][tt];
+        for (int j = 0; j < n; ++j) {
+          const float4 v = *reinterpret_cast<const float4*>(a.dxp + (int64_t)s_row[tt * E + j] * d + c);
           acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
         }
       }
@@ -297,11 +327,16 @@ cudaError_t launch_dx(const DxArgs& a, cudaStream_t s) {
   if (a.E > kMaxE || a.k > 8) return cudaErrorInvalidValue;
   // Many experts make the dl W_g^T term heavy: 8 tokens per warp share the
   // W_g rows; with few experts one token per warp keeps more warps busy.
+  const int lists = a.ec_bits ? 2 : 1;   // s_dl, and the chosen rows with expert choice
   if (a.E > 16) {
     const int64_t per_cta = (int64_t)kWarps * 8;
-    dx_kernel<8><<<(unsigned)((a.T + per_cta - 1) / per_cta), kWarps * 32, 0, s>>>(a);
+    const size_t smem = (size_t)lists * kWarps * 8 * a.E * 4;
+    cudaError_t e = cudaFuncSetAttribute(dx_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dx_kernel<8><<<(unsigned)((a.T + per_cta - 1) / per_cta), kWarps * 32, smem, s>>>(a);
   } else {
-    dx_kernel<1><<<(unsigned)((a.T + kWarps - 1) / kWarps), kWarps * 32, 0, s>>>(a);
+    const size_t smem = (size_t)lists * kWarps * 1 * a.E * 4;
+    dx_kernel<1><<<(unsigned)((a.T + kWarps - 1) / kWarps), kWarps * 32, smem, s>>>(a);
   }
   return cudaGetLastError();
 }

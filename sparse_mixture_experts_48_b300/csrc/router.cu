@@ -83,6 +83,7 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
         l[e] += b;
         if (a.noise) l[e] += a.noise[t * E + e];   // noisy scores: everything below uses them
         if (a.logits_out && !a.scores_em) a.logits_out[t * E + e] = l[e];
+        if (a.raw_logits) a.raw_logits[t * E + e] = l[e];
         insert(l[e], e);                           // (expert choice uses only the maximum, val[0])
       }
     }

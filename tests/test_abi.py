@@ -156,6 +156,20 @@ def test_fp8_config_rules(L):
     assert L.moe_backward_workspace_size(ctypes.byref(moe.c_config(c8))) == 0
 
 
+def test_backward_workspace_with_expert_choice(L):
+    ce = _cfg(expert_choice=True)
+    n = L.moe_backward_workspace_size(ctypes.byref(moe.c_config(ce)))
+    assert n > 0
+    # every expert's C rows are padded to whole 128-row blocks: C = 75 and
+    # C = 128 take the same grouped rows, C = 129 one block more
+    sz = [L.moe_backward_workspace_size(ctypes.byref(moe.c_config(_cfg(T=T, expert_choice=True,
+                                                                         capacity_factor=1.0)))) for T in
+          (600, 1024, 1032)]
+    assert 0 < sz[0] <= sz[1] < sz[2]
+    assert sz[2] - sz[1] >= 8 * 128 * 768 * 2
+    assert L.moe_backward_workspace_size(ctypes.byref(moe.c_config(_cfg(expert_choice=True, fp8_experts=True)))) == 0
+
+
 def _call_forward_fp8(L, cfg, w, **over):
     P = ctypes.c_void_p
     args = dict(x=P(0x10000), W_g=P(0x20000), y=P(0x50000000), ws=P(0x100000), ws_bytes=moe.workspace_size(cfg))

@@ -110,3 +110,54 @@ def test_backward_empty_batch_gives_zero_weight_gradients():
     torch.cuda.synchronize()
     for name in ("dW_g", "db_g", "dW1", "db1", "dW2", "db2"):
         assert torch.all(getattr(g, name) == 0), name
+
+
+# ---- expert-choice routing --------------------------------------------------------
+
+EC_CASES = [
+    # C = 75: every expert's rows padded to 128 in the weight-gradient layout;
+    # with cf 1 some tokens are chosen by no expert
+    ("gelu_softmax_bias_unchosen", "gpt2_top2_gelu_bf16", dict(T=300, d=256, f=512, capacity_factor=1.0), 0.0),
+    ("swiglu_mixtral", "mixtral_swiglu_bf16", dict(T=260, d=512, f=1024), 0.0),
+    ("sigmoid_shared_fine", "deepseek_shared_sigmoid_bf16", dict(T=300, d=512, f=320), 0.0),
+    ("many_experts_noise", "deepseek_shared_sigmoid_bf16", dict(T=400, E=40, k=3, S=0, d=256, f=192), 0.5),
+]
+
+
+@pytest.mark.parametrize("label,base,over,noise", EC_CASES, ids=[c[0] for c in EC_CASES])
+def test_expert_choice_backward_matches_oracle(label, base, over, noise):
+    """The experts choose on the GPU's own fp32 probabilities (from a forward
+    call); the oracle takes the gradient at its own fp64 logits."""
+    cfg = si.CONFIGS[base].replace(expert_choice=True, **over)
+    inp = si.layer_inputs(cfg, seed=24)
+    if noise:
+        inp["noise"] = si.router_noise(cfg, seed=24, std=noise)
+    dinp = device_inputs(inp)
+    dy = si.normal(cfg.T * cfg.d, 24, 30, dtype=si.BF16).reshape(cfg.T, cfg.d)
+    fwd = run(cfg, dinp)
+    gs = fwd.router_logits.cpu().numpy().astype(np.float64)          # the probabilities the experts chose on
+    g = moe.backward(cfg, dinp["x"], dinp["W_g"], dinp["b_g"], dinp["W1"], dinp["b1"], dinp["W2"], dinp["b2"],
+                     dinp["W3"], device_inputs({"dy": dy})["dy"], dL_aux=1.0, router_noise=dinp.get("noise"))
+    assert moe.check_device_errors(g.workspace) == 0
+    ref = oracle.ec_backward(cfg, inp, si.as_f32(dy).astype(np.float64), 1.0, scores=gs)
+    assert np.array_equal(fwd.perm_token.cpu().numpy()[:cfg.E * ref["capacity"]].reshape(cfg.E, -1), ref["perm"])
+    for name in ("dx", "dW_g", "db_g", "dW1", "db1", "dW2", "db2", "dW3"):
+        if getattr(g, name) is None:
+            continue
+        _close(name, getattr(g, name), ref[name])
+    if label.endswith("unchosen"):
+        chosen = np.zeros(cfg.T, bool)
+        chosen[np.unique(ref["perm"])] = True
+        assert (~chosen).any()
+
+
+def test_expert_choice_backward_is_deterministic():
+    cfg = si.CONFIGS["mixtral_swiglu_bf16"].replace(T=260, d=256, f=512, expert_choice=True)
+    dinp = device_inputs(si.layer_inputs(cfg, seed=25))
+    dy = device_inputs({"dy": si.normal(cfg.T * cfg.d, 25, 30, dtype=si.BF16).reshape(cfg.T, cfg.d)})["dy"]
+    args = [dinp[n] for n in ("x", "W_g", "b_g", "W1", "b1", "W2", "b2", "W3")]
+    a = moe.backward(cfg, *args, dy)
+    b = moe.backward(cfg, *args, dy)
+    torch.cuda.synchronize()
+    for name in ("dx", "dW_g", "dW1", "dW2", "dW3"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
