@@ -43,7 +43,7 @@ __device__ __forceinline__ int warp_excl_scan(int v, int lane, int* total) {
 
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   __shared__ int s_npre[kMaxE];
-  __shared__ double s_psum[kMaxE];
+  __shared__ float s_psum[kMaxE];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
   const int E = a.E;
   // An earlier stage gave up: its partials are not valid.  Publish empty
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   const bool ec = a.ec_C >= 0;   // expert choice: n_e = C for every expert, no ranks
   for (int e = warp; e < E; e += nwarps) {
     int run = 0;
-    double ps = 0.0;
+    float ps = 0.f;
     for (int64_t b0 = 0; b0 < a.nblk; b0 += 32 * kScanU) {
       int v[kScanU];
       float p[kScanU];
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
         const int ex = warp_excl_scan(v[u], lane, &tot);
         if (b < a.nblk && !ec) a.base[e * a.nblk + b] = run + ex;
         run += tot;
-        ps += (double)p[u];
+        ps += p[u];
       }
     }
     if (ec) run = (int)a.ec_C;
@@ -116,11 +116,11 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       a.counts[e] = c;
       a.offsets[e] = off;
       off += seg_rows(n);
-      const double fe = a.T > 0 ? (double)n / Tk : 0.0;
-      const double Pe = a.T > 0 ? s_psum[e] / (double)a.T : 0.0;
-      a.f[e] = (float)fe;
-      a.P[e] = (float)Pe;
-      L += fe * Pe;
+      const float fe = a.T > 0 ? __fdiv_rn((float)n, (float)Tk) : 0.f;
+      const float Pe = a.T > 0 ? __fdiv_rn(s_psum[e], (float)a.T) : 0.f;
+      a.f[e] = fe;
+      a.P[e] = Pe;
+      L += (double)fe * (double)Pe;
     }
   }
 #pragma unroll
