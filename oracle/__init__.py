@@ -69,6 +69,8 @@ def _L() -> ctypes.CDLL:
         lib.oracle_route_health.argtypes = [i64, i32, i32, vp, vp]
         lib.oracle_backward.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32, dbl, dbl] + [vp] * 21
         lib.oracle_ec_backward.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, dbl, dbl, i64] + [vp] * 18
+        lib.oracle_dx_rows.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32] + [vp] * 13
+        lib.oracle_ec_dx_rows.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32] + [vp] * 10
         lib.oracle_ec_capacity.restype = i64
         lib.oracle_ec_capacity.argtypes = [i64, i32, i32, dbl]
         lib.oracle_ec_select.argtypes = [i64, i32, i64, vp, vp]
@@ -363,6 +365,43 @@ def ec_backward(cfg, inp: Dict, dy: np.ndarray, dL_aux: float = 1.0,
                             _p(out["dW3"]))
     out.update(perm=perm, capacity=C, probs=probs, logits=lg)
     return out
+
+
+def dx_rows(cfg, inp: Dict, rows: Sequence[int], dy_rows: np.ndarray, logits_rows: np.ndarray,
+            idx_rows: np.ndarray, w_rows: np.ndarray, dropped_rows: np.ndarray) -> np.ndarray:
+    """dx of the listed tokens with dL_aux = 0 (token choice), without the
+    parameter gradients: each token's routing row, logits row and dy row are
+    given (from a routing over the whole batch)."""
+    rows = np.asarray(rows, np.int64)
+    n, dt = rows.size, cfg.dtype
+    x = np.ascontiguousarray(inp["x"][rows])
+    dx = np.empty((n, cfg.d))
+    _L().oracle_dx_rows(n, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S, cfg.act, cfg.gating, dt, _p(_stored(x, dt)),
+                        _p(_stored(inp["W_g"], dt)), _p(np.ascontiguousarray(logits_rows, np.float64)),
+                        _p(_stored(inp["W1"], dt)), _p(_stored(inp["b1"], dt)), _p(_stored(inp["W2"], dt)),
+                        _p(_stored(inp["b2"], dt)), _p(_stored(inp["W3"], dt)),
+                        _p(np.ascontiguousarray(idx_rows, np.int32)), _p(np.ascontiguousarray(w_rows, np.float64)),
+                        _p(np.ascontiguousarray(dropped_rows, np.uint8)),
+                        _p(np.ascontiguousarray(dy_rows, np.float64)), _p(dx))
+    return dx
+
+
+def ec_dx_rows(cfg, inp: Dict, rows: Sequence[int], dy_rows: np.ndarray, logits_rows: np.ndarray,
+               chose_rows: np.ndarray) -> np.ndarray:
+    """dx of the listed tokens with dL_aux = 0 (expert choice): chose_rows
+    [n, E] marks the experts that chose each token (from a selection over the
+    whole batch)."""
+    rows = np.asarray(rows, np.int64)
+    n, dt = rows.size, cfg.dtype
+    x = np.ascontiguousarray(inp["x"][rows])
+    dx = np.empty((n, cfg.d))
+    _L().oracle_ec_dx_rows(n, cfg.d, cfg.f, cfg.E, cfg.S, cfg.act, cfg.gating, dt, _p(_stored(x, dt)),
+                           _p(_stored(inp["W_g"], dt)), _p(np.ascontiguousarray(logits_rows, np.float64)),
+                           _p(_stored(inp["W1"], dt)), _p(_stored(inp["b1"], dt)), _p(_stored(inp["W2"], dt)),
+                           _p(_stored(inp["b2"], dt)), _p(_stored(inp["W3"], dt)),
+                           _p(np.ascontiguousarray(chose_rows, np.uint8)),
+                           _p(np.ascontiguousarray(dy_rows, np.float64)), _p(dx))
+    return dx
 
 
 # ---- FP8 (E4M3) experts ----------------------------------------------------------

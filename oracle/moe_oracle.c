@@ -569,7 +569,8 @@ void oracle_backward(int64_t T, int d, int f, int E, int k, int S, int act, int 
  * All outputs fp64, overwritten. */
 
 /* One expert g on one token row xr with output weight wj: adds the expert's
- * parameter gradients and its part of dx_t (dxr), and returns <dy_t, o_g(x_t)>. */
+ * parameter gradients (unless dW1 is NULL) and its part of dx_t (dxr), and
+ * returns <dy_t, o_g(x_t)>. */
 static double expert_row_bwd(int d, int f, int act, int dtype, int g, double wj, const double* xr,
                              const double* dyt, const void* W1, const void* b1, const void* W2, const void* b2,
                              const void* W3, double* dxr, double* dW1, double* db1, double* dW2, double* db2,
@@ -603,11 +604,11 @@ static double expert_row_bwd(int d, int f, int act, int dtype, int g, double wj,
     for (int c = 0; c < d; ++c) {
       const double doc = wj * dyt[c];
       acc += ld(W2, dtype, w2o + (int64_t)r * d + c) * doc;
-      dW2[w2o + (int64_t)r * d + c] += h[r] * doc;
+      if (dW1) dW2[w2o + (int64_t)r * d + c] += h[r] * doc;
     }
     dh[r] = acc;
   }
-  if (b2 && !swiglu)
+  if (dW1 && b2 && !swiglu)
     for (int c = 0; c < d; ++c) db2[(int64_t)g * d + c] += wj * dyt[c];
   /* activation: da (, du) */
   for (int r = 0; r < f; ++r) {
@@ -626,15 +627,15 @@ static double expert_row_bwd(int d, int f, int act, int dtype, int g, double wj,
     double acc = 0.0;
     for (int r = 0; r < f; ++r) {
       acc += ld(W1, dtype, w1o + (int64_t)i * f + r) * da[r];
-      dW1[w1o + (int64_t)i * f + r] += xr[i] * da[r];
+      if (dW1) dW1[w1o + (int64_t)i * f + r] += xr[i] * da[r];
       if (swiglu) {
         acc += ld(W3, dtype, w1o + (int64_t)i * f + r) * du[r];
-        dW3[w1o + (int64_t)i * f + r] += xr[i] * du[r];
+        if (dW1) dW3[w1o + (int64_t)i * f + r] += xr[i] * du[r];
       }
     }
     dxr[i] += acc;
   }
-  if (b1 && !swiglu)
+  if (dW1 && b1 && !swiglu)
     for (int r = 0; r < f; ++r) db1[(int64_t)g * f + r] += da[r];
   free(a); free(u); free(h); free(dh); free(da); free(du); free(o);
   return dot;
@@ -694,6 +695,95 @@ void oracle_ec_backward(int64_t T, int d, int f, int E, int S, int act, int gati
         dWg[(int64_t)i * E + e] += xr[i] * dl;
         dxt[i] += ld(W_g, dtype, (int64_t)i * E + e) * dl;
       }
+    }
+  }
+  free(xr); free(p); free(dp);
+}
+
+/* ---- dx of single tokens, for sampled checks at full size ----------------------------
+ * With dL_aux = 0 the gradient of x_t depends on token t alone (its routing row,
+ * its logits, dy_t): the aux term is what couples the tokens, through n_e and
+ * T.  These two functions give dx for the listed token rows only, without the
+ * parameter gradients, by the same chain rule as the backward passes above
+ * with dL_aux = 0.  Inputs are the rows themselves: x [n, d] (stored dtype),
+ * logits [n, E], dy [n, d]; token choice: idx, w, dropped [n, k]; expert choice:
+ * chose [n, E] (1 where expert e chose the token). */
+void oracle_dx_rows(int64_t n, int d, int f, int E, int k, int S, int act, int gating, int dtype, const void* x,
+                    const void* W_g, const double* logits, const void* W1, const void* b1, const void* W2,
+                    const void* b2, const void* W3, const int32_t* idx, const double* w, const uint8_t* dropped,
+                    const double* dy, double* dx) {
+  double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+  double* p = (double*)malloc(sizeof(double) * (size_t)E);
+  double* dw = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+  for (int64_t t = 0; t < n; ++t) {
+    const double* dyt = dy + t * d;
+    double* dxt = dx + t * d;
+    for (int i = 0; i < d; ++i) { xr[i] = ld(x, dtype, t * d + i); dxt[i] = 0.0; }
+    for (int j = 0; j < k; ++j) {
+      dw[j] = 0.0;
+      if (dropped[t * k + j]) continue;
+      dw[j] = expert_row_bwd(d, f, act, dtype, idx[t * k + j], w[t * k + j], xr, dyt, W1, b1, W2, b2, W3, dxt,
+                             NULL, NULL, NULL, NULL, NULL);
+    }
+    for (int s = 0; s < S; ++s)
+      expert_row_bwd(d, f, act, dtype, E + s, 1.0, xr, dyt, W1, b1, W2, b2, W3, dxt, NULL, NULL, NULL, NULL, NULL);
+    /* the renormalised weights' gradient on the selected logits */
+    const double* l = logits + t * E;
+    oracle_gate_probs(1, E, gating, l, p);
+    double zsel = 0.0, wdw = 0.0;
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[t * k + j];
+      zsel += gating == OGATE_SOFTMAX ? p[e] : sig(l[e]);
+      wdw += w[t * k + j] * dw[j];
+    }
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[t * k + j];
+      double dl;
+      if (gating == OGATE_SOFTMAX) {
+        dl = w[t * k + j] * (dw[j] - wdw);
+      } else {
+        const double se = sig(l[e]);
+        dl = (dw[j] - wdw) / zsel * se * (1.0 - se);
+      }
+      for (int i = 0; i < d; ++i) dxt[i] += ld(W_g, dtype, (int64_t)i * E + e) * dl;
+    }
+  }
+  free(xr); free(p); free(dw);
+}
+
+void oracle_ec_dx_rows(int64_t n, int d, int f, int E, int S, int act, int gating, int dtype, const void* x,
+                       const void* W_g, const double* logits, const void* W1, const void* b1, const void* W2,
+                       const void* b2, const void* W3, const uint8_t* chose, const double* dy, double* dx) {
+  double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+  double* p = (double*)malloc(sizeof(double) * (size_t)E);
+  double* dp = (double*)malloc(sizeof(double) * (size_t)E);
+  for (int64_t t = 0; t < n; ++t) {
+    const double* dyt = dy + t * d;
+    double* dxt = dx + t * d;
+    for (int i = 0; i < d; ++i) { xr[i] = ld(x, dtype, t * d + i); dxt[i] = 0.0; }
+    const double* l = logits + t * E;
+    oracle_gate_probs(1, E, gating, l, p);
+    for (int e = 0; e < E; ++e) {
+      dp[e] = 0.0;
+      if (chose[t * E + e])
+        dp[e] = expert_row_bwd(d, f, act, dtype, e, p[e], xr, dyt, W1, b1, W2, b2, W3, dxt, NULL, NULL, NULL, NULL,
+                               NULL);
+    }
+    for (int s = 0; s < S; ++s)
+      expert_row_bwd(d, f, act, dtype, E + s, 1.0, xr, dyt, W1, b1, W2, b2, W3, dxt, NULL, NULL, NULL, NULL, NULL);
+    double pdp = 0.0, zs = 0.0;
+    for (int e = 0; e < E; ++e) pdp += p[e] * dp[e];
+    if (gating != OGATE_SOFTMAX)
+      for (int e = 0; e < E; ++e) zs += sig(l[e]);
+    for (int e = 0; e < E; ++e) {
+      double dl;
+      if (gating == OGATE_SOFTMAX) {
+        dl = p[e] * (dp[e] - pdp);
+      } else {
+        const double se = sig(l[e]);
+        dl = (dp[e] - pdp) / zs * se * (1.0 - se);
+      }
+      for (int i = 0; i < d; ++i) dxt[i] += ld(W_g, dtype, (int64_t)i * E + e) * dl;
     }
   }
   free(xr); free(p); free(dp);

@@ -161,3 +161,45 @@ def test_expert_choice_backward_is_deterministic():
     torch.cuda.synchronize()
     for name in ("dx", "dW_g", "dW1", "dW2", "dW3"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+# ---- full size, sampled ------------------------------------------------------------
+
+@pytest.mark.parametrize("ec", [False, True], ids=["token_choice", "expert_choice"])
+@pytest.mark.parametrize("name", ["mixtral_swiglu_bf16", "deepseek_shared_sigmoid_bf16"])
+def test_backward_full_size_sampled_dx(name, ec):
+    """The workload shapes at full size, in the bench's launch configuration:
+    dx of sampled tokens against the oracle's per-token dx.  With dL_aux = 0 a
+    token's dx depends on its own routing, logits and dy only, so the oracle
+    computes it one token at a time."""
+    cfg = si.CONFIGS[name].replace(expert_choice=ec)
+    inp = si.layer_inputs(cfg, seed=0)
+    dinp = device_inputs(inp)
+    dy = si.normal(cfg.T * cfg.d, 26, 30, dtype=si.BF16).reshape(cfg.T, cfg.d)
+    fwd = run(cfg, dinp)
+    g = moe.backward(cfg, dinp["x"], dinp["W_g"], dinp["b_g"], dinp["W1"], dinp["b1"], dinp["W2"], dinp["b2"],
+                     dinp["W3"], device_inputs({"dy": dy})["dy"], dL_aux=0.0)
+    assert moe.check_device_errors(g.workspace) == 0
+    T, E = cfg.T, cfg.E
+    rng = np.random.default_rng(26)
+    n = 3 if name == "mixtral_swiglu_bf16" else 6
+    rows = np.array(sorted({0, T - 1} | set(rng.choice(T, size=n - 2, replace=False).tolist())))
+    dyr = si.as_f32(dy)[rows].astype(np.float64)
+    if not ec:
+        gl = fwd.router_logits.cpu().numpy().astype(np.float64)          # the GPU's own logits
+        r = oracle.routing(cfg, gl)
+        ref = oracle.dx_rows(cfg, inp, rows, dyr, gl[rows], r["topk_idx"][rows], r["topk_w"][rows],
+                             r["dropped"][rows])
+    else:
+        C = moe.capacity(cfg)
+        perm = fwd.perm_token.cpu().numpy()[:E * C].reshape(E, C)     # the GPU's choice (bit-exact elsewhere)
+        chose = np.zeros((T, E), np.uint8)
+        for e in range(E):
+            chose[perm[e], e] = 1
+        lg = oracle.router_logits(np.ascontiguousarray(inp["x"][rows]), inp["W_g"], inp["b_g"], cfg.dtype)
+        ref = oracle.ec_dx_rows(cfg, inp, rows, dyr, lg, chose[rows])
+    got = g.dx.cpu().numpy()[rows].astype(np.float64)
+    fro = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    assert fro <= 1e-2, fro
+    assert float(np.abs(got - ref).max()) <= 5e-2 * float(np.sqrt(np.mean(ref ** 2)))
+    assert np.isfinite(g.dW1.cpu().numpy()).all()

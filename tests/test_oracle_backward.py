@@ -164,3 +164,35 @@ def test_ec_aux_loss_is_constant_so_it_carries_no_gradient():
     for key in ("dW1", "dW2", "dW3"):
         assert np.all(g[key] == 0.0)
     assert np.abs(g["dW_g"]).max() <= 1e-15 and np.abs(g["dx"]).max() <= 1e-15
+
+
+# ---- dx of single tokens (the sampled full-size checks use these) ------------------
+
+@pytest.mark.parametrize("over", [dict(capacity_factor=0.9), dict(act=si.SWIGLU, gating=si.SIGMOID_NORM, S=1,
+                                                                  k=3, E=5, ffn_bias=False)])
+def test_dx_rows_equal_the_backward_pass_without_the_aux_term(over):
+    cfg = _cfg(**over)
+    inp = si.layer_inputs(cfg, seed=10)
+    dy = np.random.default_rng(6).standard_normal((cfg.T, cfg.d))
+    g = oracle.backward(cfg, inp, dy, 0.0)
+    r = g["routing"]
+    rows = [0, 3, cfg.T - 1]
+    lg = oracle.router_logits(inp["x"], inp["W_g"], inp["b_g"], cfg.dtype)
+    dx = oracle.dx_rows(cfg, inp, rows, dy[rows], lg[rows], r["topk_idx"][rows], r["topk_w"][rows],
+                        r["dropped"][rows])
+    np.testing.assert_allclose(dx, g["dx"][rows], rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("over", [dict(capacity_factor=0.5, router_bias_std=0.5),
+                                  dict(act=si.SWIGLU, gating=si.SIGMOID_NORM, S=1, E=5, ffn_bias=False)])
+def test_ec_dx_rows_equal_the_expert_choice_backward_without_the_aux_term(over):
+    cfg = _cfg(T=9, expert_choice=True, **over)
+    inp = si.layer_inputs(cfg, seed=11)
+    dy = np.random.default_rng(7).standard_normal((cfg.T, cfg.d))
+    g = oracle.ec_backward(cfg, inp, dy, 0.0)
+    chose = np.zeros((cfg.T, cfg.E), np.uint8)
+    for e in range(cfg.E):
+        chose[g["perm"][e], e] = 1
+    rows = [1, 4, 8]
+    dx = oracle.ec_dx_rows(cfg, inp, rows, dy[rows], g["logits"][rows], chose[rows])
+    np.testing.assert_allclose(dx, g["dx"][rows], rtol=1e-12, atol=1e-14)
