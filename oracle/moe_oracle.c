@@ -13,7 +13,7 @@
  *   [P1] "MoE混合专家模型：Transformer稀疏前馈网络原理与PyTorch实现"
  *        §1.3 (sparse FFN data flow), §2.1 (router: linear + softmax, top-k,
  *        renormalise), §2.3 (Switch load-balance loss), §3.2 (capacity factor),
- *        §4.1 (TopKRouter / ExpertFFN / MoEFFN listing).
+ *        §4.1 (the TopKRouter / ExpertFFN / MoEFFN modules).
  *   [P2] "MoE架构解析" §2.1 (token choice), §三 关键技术① (expert capacity,
  *        overflow tokens skip the layer), §四 技术飞跃② (shared experts,
  *        always active), 技术飞跃③ (normalised sigmoid gating).
@@ -252,7 +252,7 @@ void oracle_layer_rows(int d, int f, int E, int k, int S, int act, int dtype, co
  *   f_i = (selections of i before the capacity cut) / (T * k)
  *   P_i = (1/T) sum_t p[t,i]
  *   L_aux = alpha * E * sum_i f_i * P_i
- * Reading: f divides by T*k as in the kamacoder listing, so sum_i f_i = 1 and
+ * Reading: f divides by T*k as in [P3] §七, so sum_i f_i = 1 and
  * L_aux = alpha exactly when routing is uniform.  T = 0 gives zeros. */
 void oracle_balance(int64_t T, int E, int k, double alpha, const int32_t* n_pre, const double* probs,
                     double* f, double* P, double* L_aux) {

@@ -1,7 +1,7 @@
 """Pins of the fp64 oracle against what the pages and the mathematics fix.
 
 Each test checks the oracle against something other than itself: the worked
-top-k example printed on the kamacoder page, brute force over all subsets,
+top-k example printed in "手撕一个极简 MoE-FFN" §三, brute force over all subsets,
 closed forms (uniform routing gives L_aux = alpha), hand-derived capacity cases,
 and special cases that reduce to library routines (numpy matmul, numpy
 lexsort, scipy erf / expit).  They are chosen so that a dropped term, a wrong
@@ -193,7 +193,7 @@ def test_identical_experts_with_k_equal_E_is_the_dense_ffn(act, dtype):
 ])
 def test_sparse_equals_dense_masked(act, gating, cf, S):
     """Run every expert on every token and mask afterwards (the dense-masked
-    formulation of the yunthe page's MoELayer), with capacity drops and shared
+    formulation of the MoELayer in "Mixture of Experts混合专家模型架构原理与路由策略实现"), with capacity drops and shared
     experts; it must equal the oracle's sparse grouped result."""
     cfg = _cfg(T=23, d=16, f=32, E=6, k=3, S=S, act=act, gating=gating, capacity_factor=cf,
                ffn_bias=(act != si.SWIGLU), dtype=si.BF16)
