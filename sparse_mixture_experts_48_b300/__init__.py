@@ -396,7 +396,8 @@ class MoEGrads:
 def backward(cfg, x, W_g, b_g, W1, b1, W2, b2, W3, dy, dL_aux: float = 1.0, *,
              router_noise: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
              stream: Optional[torch.cuda.Stream] = None) -> MoEGrads:
-    """Gradients of sum <dy, y> + dL_aux * L_aux (moe_backward; fp32 outputs).
+    """Gradients of sum <dy, y> + dL_aux * L_aux (moe_backward; fp32 outputs),
+    with token-choice or expert-choice routing (cfg.expert_choice).
     Recomputes the forward pass inside; asynchronous like forward()."""
     if not torch.cuda.is_available():
         raise RuntimeError("the MoE layer runs on a CUDA device; none is available")

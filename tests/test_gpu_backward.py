@@ -1,7 +1,10 @@
-"""moe_backward on the GPU against the oracle's fp64 backward pass.
+"""moe_backward on the GPU against the oracle's fp64 backward pass, with
+token-choice and expert-choice routing.
 
 Both route on the GPU's own fp32 logits (taken from a forward call, which
-computes the very same logits), so every routing decision agrees.  The GPU
+computes the very same logits), so every routing decision agrees; with expert
+choice both choose on the GPU's own fp32 probabilities.  At the full workload
+sizes the oracle computes dx of sampled tokens one at a time (dL_aux = 0).  The GPU
 keeps several bf16 intermediates (dO, the pre-activations, H, dA, dU) like the
 forward keeps H, so each gradient tensor is checked by its relative Frobenius error
 (<= 1e-2; <= 2e-2 for every expert slab of a weight gradient), and dx and the
