@@ -52,3 +52,26 @@ def test_single_rank_is_unchanged():
     import bench
     assert bench.max_over_ranks(4.0, None, 1) == 4.0
     assert bench.replica_throughput(16384, 8.0, 1) == pytest.approx(16384 / 8e-3)
+
+
+def test_algorithmic_work_matches_the_hand_counts():
+    """The roofline numerators: per-forward work of the Mixtral-shaped layer
+    (T=16384, d=4096, f=14336, E=8, k=2, SwiGLU, bf16, no drops), counted by
+    hand from the shapes."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import seeded_inputs as si
+    cfg = si.CONFIGS["mixtral_swiglu_bf16"]
+    T, d, f, E, k = 16384, 4096, 14336, 8, 2
+    A = T * k
+    w = bench.algorithmic(cfg, A)
+    assert w["gemm1_flop"] == 2 * A * d * f * 2            # x W1 and x W3
+    assert w["gemm2_flop"] == 2 * A * f * d
+    assert abs(w["gemm1_flop"] + w["gemm2_flop"] - 11.54e12) < 0.01e12
+    assert w["router_bytes"] == T * d * 2 + d * E * 2 + T * k * 8
+    assert w["gather_bytes"] == T * d * 2 + A * d * 2      # x read once, one copy per kept slot
+    assert w["combine_bytes"] == A * d * 4 + T * d * 2     # O (fp32) read, y (bf16) written
+    # FP8 experts: one code per element and one scale per grouped row
+    w8 = bench.algorithmic(cfg.replace(fp8_experts=True), A)
+    assert w8["gather_bytes"] == T * d * 2 + A * (d + 4)
+    assert w8["quantize_h_bytes"] == A * (f * 3 + 4)
