@@ -26,6 +26,8 @@ CASES = [
     ("sigmoid_shared_fine", "deepseek_shared_sigmoid_bf16", dict(T=300, d=512, f=320), 0.0),
     ("relu_noise", "gpt2_top2_gelu_bf16", dict(T=200, d=192, f=448, act=si.RELU, E=5, k=3), 0.8),
     ("one_token", "mixtral_swiglu_bf16", dict(T=1, d=256, f=256, S=1), 0.0),
+    # the widest routing: 256 experts (8 mask words, 8 tokens per dx warp), k = 8
+    ("max_E_and_k", "deepseek_shared_sigmoid_bf16", dict(T=150, E=256, k=8, S=1, d=256, f=192), 0.0),
 ]
 
 
@@ -124,6 +126,7 @@ EC_CASES = [
     ("swiglu_mixtral", "mixtral_swiglu_bf16", dict(T=260, d=512, f=1024), 0.0),
     ("sigmoid_shared_fine", "deepseek_shared_sigmoid_bf16", dict(T=300, d=512, f=320), 0.0),
     ("many_experts_noise", "deepseek_shared_sigmoid_bf16", dict(T=400, E=40, k=3, S=0, d=256, f=192), 0.5),
+    ("max_E_shared", "deepseek_shared_sigmoid_bf16", dict(T=300, E=256, k=8, S=2, d=256, f=192), 0.0),
 ]
 
 

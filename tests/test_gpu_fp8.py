@@ -36,6 +36,7 @@ CASES = [
     ("relu_k_tail", "gpt2_top2_gelu_bf16", dict(T=200, d=192, f=320, act=si.RELU, E=5, k=3)),
     ("mixtral_swiglu", "mixtral_swiglu_bf16", dict(T=260, d=512, f=1024)),
     ("deepseek_shared_sigmoid", "deepseek_shared_sigmoid_bf16", dict(T=300, d=512, f=320)),
+    ("max_E_and_k", "deepseek_shared_sigmoid_bf16", dict(T=150, E=256, k=8, S=1, d=256, f=192)),
 ]
 
 
