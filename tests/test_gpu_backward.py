@@ -127,6 +127,8 @@ EC_CASES = [
     ("sigmoid_shared_fine", "deepseek_shared_sigmoid_bf16", dict(T=300, d=512, f=320), 0.0),
     ("many_experts_noise", "deepseek_shared_sigmoid_bf16", dict(T=400, E=40, k=3, S=0, d=256, f=192), 0.5),
     ("max_E_shared", "deepseek_shared_sigmoid_bf16", dict(T=300, E=256, k=8, S=2, d=256, f=192), 0.0),
+    # one token, chosen by every expert: C = 1 row in each 128-row padded segment
+    ("one_token_shared", "mixtral_swiglu_bf16", dict(T=1, d=256, f=256, S=1), 0.0),
 ]
 
 
@@ -150,7 +152,9 @@ def test_expert_choice_backward_matches_oracle(label, base, over, noise):
     for name in ("dx", "dW_g", "db_g", "dW1", "db1", "dW2", "db2", "dW3"):
         if getattr(g, name) is None:
             continue
-        _close(name, getattr(g, name), ref[name])
+        # the logit gradient p (dp - <p, dp>) cancels like the token-choice one
+        loose = name in ("dW_g", "db_g") and cfg.T < FEW_TOKENS
+        _close(name, getattr(g, name), ref[name], *((5e-2, 2.5e-1) if loose else ()))
     if label.endswith("unchosen"):
         chosen = np.zeros(cfg.T, bool)
         chosen[np.unique(ref["perm"])] = True

@@ -23,6 +23,9 @@ CASES = [
     ("skew_cf", "skew_capacity_gelu_bf16", dict(T=500, f=1024, expert_choice=True)),
     ("tiny_f32", "tiny_top1_relu_f32", dict(expert_choice=True, k=2)),
     ("many_experts", "deepseek_shared_sigmoid_bf16", dict(T=700, E=40, k=3, S=0, d=256, f=192, expert_choice=True)),
+    ("max_E_shared", "deepseek_shared_sigmoid_bf16", dict(T=300, E=256, k=8, S=2, d=256, f=192, expert_choice=True)),
+    # one token: every expert chooses it (C = 1)
+    ("one_token", "mixtral_swiglu_bf16", dict(T=1, d=256, f=256, expert_choice=True)),
 ]
 
 

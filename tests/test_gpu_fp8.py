@@ -250,6 +250,8 @@ EC_CASES = [
     ("mixtral_swiglu", "mixtral_swiglu_bf16", dict(T=260, d=512, f=1024)),
     ("deepseek_sigmoid_shared", "deepseek_shared_sigmoid_bf16", dict(T=300, d=512, f=320)),
     ("skew_cf_unchosen", "skew_capacity_gelu_bf16", dict(T=500, d=256, f=384)),
+    ("max_E_shared", "deepseek_shared_sigmoid_bf16", dict(T=300, E=256, k=8, S=2, d=256, f=192)),
+    ("one_token", "mixtral_swiglu_bf16", dict(T=1, d=256, f=256)),
 ]
 
 
