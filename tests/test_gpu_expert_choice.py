@@ -105,3 +105,24 @@ def test_expert_choice_with_router_noise_and_host_buffers():
     torch.cuda.synchronize()
     assert torch.equal(host.y.view(torch.int16), out.y.cpu().view(torch.int16))
     assert torch.equal(host.expert_counts, out.expert_counts.cpu())
+
+
+def test_expert_choice_empty_batch():
+    """T = 0: nothing is chosen; the statistics are zero and nothing is launched
+    that reads a token (also with FP8 experts, and in the backward pass)."""
+    cfg = si.CONFIGS["deepseek_shared_sigmoid_bf16"].replace(T=0, d=256, f=192, expert_choice=True)
+    inp = si.layer_inputs(cfg.replace(T=1), seed=14)
+    dinp = device_inputs(inp)
+    x = dinp["x"][:0]
+    out = moe.forward(cfg, x, dinp["W_g"], dinp["b_g"], dinp["W1"], dinp["b1"], dinp["W2"], dinp["b2"], dinp["W3"])
+    torch.cuda.synchronize()
+    assert moe.check_device_errors(out.workspace) == 0
+    assert np.all(out.expert_counts.cpu().numpy() == 0) and float(out.L_aux.cpu()[0]) == 0.0
+    ex = moe.quantize_experts_fp8(dinp["W1"], dinp["W2"], dinp["W3"])
+    o8 = moe.forward_fp8(cfg, x, dinp["W_g"], dinp["b_g"], ex, dinp["b1"], dinp["b2"])
+    torch.cuda.synchronize()
+    assert moe.check_device_errors(o8.workspace) == 0
+    g = moe.backward(cfg, x, dinp["W_g"], dinp["b_g"], dinp["W1"], dinp["b1"], dinp["W2"], dinp["b2"], dinp["W3"], x)
+    torch.cuda.synchronize()
+    for name in ("dW_g", "dW1", "dW2", "dW3"):
+        assert torch.all(getattr(g, name) == 0), name
