@@ -126,3 +126,41 @@ def test_expert_choice_empty_batch():
     torch.cuda.synchronize()
     for name in ("dW_g", "dW1", "dW2", "dW3"):
         assert torch.all(getattr(g, name) == 0), name
+
+
+@pytest.mark.parametrize("name", ["mixtral_swiglu_bf16", "deepseek_shared_sigmoid_bf16"])
+def test_expert_choice_full_size_sampled(name):
+    """The workload shapes at full size, in the bench's launch configuration:
+    every expert's choice bit for bit (on the GPU's own probabilities), the
+    statistics, and y of sampled tokens against the oracle."""
+    cfg = si.CONFIGS[name].replace(expert_choice=True)
+    inp = si.layer_inputs(cfg, seed=0)
+    out = run(cfg, device_inputs(inp))
+    assert moe.check_device_errors(out.workspace) == 0
+    T, E = cfg.T, cfg.E
+    C = moe.capacity(cfg)
+    gs = out.router_logits.cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(15)
+    perm = out.perm_token.cpu().numpy()[:E * C].reshape(E, C)
+    # sampled tokens: some chosen by several experts, some by none, the ends
+    counts = np.bincount(perm.reshape(-1), minlength=T)
+    rows = {0, T - 1, int(np.argmax(counts))}
+    unchosen = np.flatnonzero(counts == 0)
+    if unchosen.size:
+        rows.add(int(unchosen[0]))
+    while len(rows) < 8:
+        rows.add(int(rng.integers(0, T)))
+    rows = np.array(sorted(rows))
+    ref = oracle.ec_forward(cfg, inp, rows=rows, scores=gs)
+    assert np.array_equal(perm, ref["perm"])
+    np.testing.assert_allclose(gs, ref["probs"], rtol=2e-3, atol=1e-7)
+    np.testing.assert_allclose(out.P.cpu().numpy(), ref["P"], rtol=1e-5, atol=1e-9)
+    assert abs(float(out.L_aux.cpu().numpy()[0]) - ref["L_aux"]) <= 1e-5 * abs(ref["L_aux"])
+    y = to_host_f32(out.y)[rows].astype(np.float64)
+    yr = ref["y"]
+    live = np.ones(rows.size, bool) if cfg.S else counts[rows] > 0
+    assert np.all(y[~live] == 0.0)
+    # RMS over the rows the experts produce, as in the small cases
+    rms = float(np.sqrt(np.mean(yr[live] ** 2)))
+    dy = np.abs(y[live] - yr[live])
+    assert np.all(dy <= Y_TOL[cfg.dtype] * rms + half_ulp_bf16(yr[live])), float(dy.max())
