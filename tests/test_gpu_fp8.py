@@ -311,3 +311,31 @@ def test_fp8_expert_choice_host_buffers_equal_the_device_call():
     torch.cuda.synchronize()
     assert torch.equal(host.y.view(torch.int16), out.y.cpu().view(torch.int16))
     assert torch.equal(host.expert_counts, out.expert_counts.cpu())
+
+
+def test_fp8_expert_choice_full_size_sampled():
+    """Expert choice with FP8 experts on the Mixtral-shaped layer in the
+    launch configuration the bench times: every expert's choice bit for bit,
+    the weight codes bit for bit, the chosen rows' codes and scales, and y of
+    sampled tokens against the oracle's FP8 expert-choice layer."""
+    cfg = si.CONFIGS["mixtral_swiglu_bf16"].replace(expert_choice=True)
+    inp = si.layer_inputs(cfg, seed=0)
+    ex, out = run_fp8(cfg, inp)
+    cfg8 = cfg.replace(fp8_experts=True)
+    T, d, E = cfg.T, cfg.d, cfg.E
+    C = moe.capacity(cfg8)
+    gs = out.router_logits.cpu().numpy().astype(np.float64)
+    wq = oracle.quantize_experts(cfg, inp)
+    check_weights(ex, wq)
+    rows = np.array(sorted(set(np.random.default_rng(16).choice(T, size=6, replace=False).tolist()) | {0, T - 1}))
+    ref = oracle.fp8_ec_forward(cfg, inp, rows=rows, scores=gs, wq=wq)
+    perm = out.perm_token.cpu().numpy()[:E * C]
+    assert np.array_equal(perm.reshape(E, C), ref["perm"])
+    xp = _region(cfg8, out.workspace, moe.REGION_XPERM, torch.uint8, (E * C, d)).cpu().numpy()
+    xs = _region(cfg8, out.workspace, moe.REGION_X_SCALE, torch.float32, (E * C,)).cpu().numpy()
+    sel = np.random.default_rng(17).choice(E * C, size=64, replace=False)
+    assert np.array_equal(xp[sel], ref["xq"][perm[sel]]) and np.array_equal(xs[sel], ref["xs"][perm[sel]])
+    y = to_host_f32(out.y)[rows].astype(np.float64)
+    yr = ref["y"]
+    rel = float(np.linalg.norm(y - yr) / np.linalg.norm(yr))
+    assert rel <= 5e-3, rel
