@@ -162,6 +162,23 @@ PLANTED += [
 ]
 
 
+PLANTED += [
+    ("ec_output_weight_dropped",
+     "const double w = scores[t * E + e];", "const double w = 1.0;",
+     [_c("soft mixture", tp.test_ec_every_token_to_every_expert_is_the_dense_soft_mixture, si.GELU)]),
+    ("P_divided_by_Tk",
+     "P[e] = T > 0 ? s / (double)T : 0.0;", "P[e] = T > 0 ? s / ((double)T * (double)k) : 0.0;",
+     [_c("uniform router", tp.test_laux_is_alpha_under_uniform_router, 2, si.SOFTMAX)]),
+    ("health_variance_unbiased",
+     "  var /= (double)E;", "  var /= (double)(E - 1);",
+     [_c("health closed forms", tp.test_route_health_closed_forms)]),
+    ("dx_rows_router_term_sign",
+     "        dl = w[t * k + j] * (dw[j] - wdw);", "        dl = w[t * k + j] * (wdw - dw[j]);",
+     [_c("dx rows vs backward", tb.test_dx_rows_equal_the_backward_pass_without_the_aux_term,
+         dict(capacity_factor=0.9))]),
+]
+
+
 @pytest.fixture(scope="module")
 def tmp_lib(tmp_path_factory):
     return tmp_path_factory.mktemp("planted")
