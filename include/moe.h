@@ -1,8 +1,10 @@
 /*
- * moe.h -- C ABI of libmoe.so: the forward pass of a token-choice
- * Mixture-of-Experts feed-forward layer on one NVIDIA B300 (sm_103a).
+ * moe.h -- C ABI of libmoe.so: a Mixture-of-Experts feed-forward layer on one
+ * NVIDIA B300 (sm_103a).  The forward pass (token-choice routing below, or
+ * expert choice: MOE_FLAG_EXPERT_CHOICE), with bf16 / fp32 experts or E4M3
+ * experts (moe_forward_fp8), and its backward pass (moe_backward).
  *
- * The layer, per token t of x [T, d]:
+ * The token-choice layer, per token t of x [T, d]:
  *   1. router logits    l[t,e] = b_g[e] + sum_i x[t,i] W_g[i,e]
  *        ("MoE混合专家模型：Transformer稀疏前馈网络原理与PyTorch实现" §2.1;
  *         "Mixture of Experts混合专家模型架构原理与路由策略实现", 门控网络的数学原理:
@@ -77,8 +79,10 @@ enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID_NORM = 1 };
 enum { MOE_ACT_RELU = 0, MOE_ACT_GELU = 1, MOE_ACT_SWIGLU = 2, MOE_ACT_NONE = 3 };
 enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 };
 
-/* Number of kernels moe_forward enqueues (the stages that stage events bracket):
- * router, scan, gather, expert GEMM 1, expert GEMM 2, combine. */
+/* Stages of moe_forward that stage events bracket: router, scan, gather,
+ * expert GEMM 1, expert GEMM 2, combine (one kernel each; with expert choice
+ * the scan stage also holds the per-expert selection, and with FP8 experts the
+ * gather stage the per-token quantisation of x). */
 #define MOE_NUM_STAGES 6
 
 /* The layer.  64 bytes, natural alignment. */
