@@ -201,3 +201,46 @@ def test_quantize_host_checks(L):
     assert L.moe_quantize_rows_fp8(P(0x1000), 4, 40, P(0x2000), P(0x3000), None) == 2              # cols % 16
     assert L.moe_quantize_rows_fp8(P(0x1000), -1, 64, P(0x2000), P(0x3000), None) == 1
     assert L.moe_quantize_rows_fp8(None, 0, 64, None, None, None) == 0
+
+
+def _call_backward(L, cfg, **over):
+    """moe_backward with fake, aligned, never-dereferenced pointers: every case
+    here is rejected by the host checks before any CUDA call."""
+    P = ctypes.c_void_p
+    sw = cfg.act == moe.SWIGLU
+    args = dict(x=P(0x10000), W_g=P(0x20000), b_g=None, noise=None, W1=P(0x30000), b1=None, W2=P(0x40000),
+                b2=None, W3=P(0x50000) if sw else None, dy=P(0x60000), dL_aux=1.0, dx=P(0x70000),
+                dW_g=P(0x80000), db_g=None, dW1=P(0x90000), db1=None, dW2=P(0xA0000), db2=None,
+                dW3=P(0xB0000) if sw else None, ws=P(0x100000),
+                ws_bytes=L.moe_backward_workspace_size(ctypes.byref(moe.c_config(cfg))))
+    args.update(over)
+    c = moe.c_config(cfg)
+    return L.moe_backward(ctypes.byref(c), args["x"], args["W_g"], args["b_g"], args["noise"], args["W1"],
+                          args["b1"], args["W2"], args["b2"], args["W3"], args["dy"], args["dL_aux"], args["dx"],
+                          args["dW_g"], args["db_g"], args["dW1"], args["db1"], args["dW2"], args["db2"], args["dW3"],
+                          args["ws"], args["ws_bytes"], None, None)
+
+
+@pytest.mark.parametrize("ec", [False, True], ids=["token_choice", "expert_choice"])
+def test_backward_host_checks(L, ec):
+    P = ctypes.c_void_p
+    c = _cfg(expert_choice=ec)
+    assert _call_backward(L, c, dy=None) == 1
+    assert _call_backward(L, c, dx=None) == 1
+    assert _call_backward(L, c, dW1=None) == 1
+    assert _call_backward(L, c, b_g=P(0xC0000)) == 1                 # b_g without db_g
+    assert _call_backward(L, c, db1=P(0xD0000)) == 1                 # db1 without b1
+    assert _call_backward(L, c, W3=P(0xE0000)) == 1                  # W3 without SwiGLU
+    assert _call_backward(L, _cfg(act=moe.SWIGLU, expert_choice=ec), dW3=None) == 1
+    assert _call_backward(L, _cfg(act=moe.SWIGLU, expert_choice=ec), b1=P(0xC1000), db1=P(0xC2000)) == 1
+    assert _call_backward(L, c, dL_aux=float("nan")) == 1
+    assert _call_backward(L, c, dy=P(0x60008)) == 1                  # misaligned
+    assert _call_backward(L, c, ws_bytes=L.moe_backward_workspace_size(ctypes.byref(moe.c_config(c))) - 1) == 3
+    assert _call_backward(L, c, ws=P(0x100040)) == 3                 # workspace not 256-byte aligned
+    # fp32 layers and FP8 experts have no backward pass here
+    assert _call_backward(L, _cfg(dtype=moe.F32, d=64, f=64, expert_choice=ec), ws_bytes=1 << 30) == 2
+    assert _call_backward(L, _cfg(fp8_experts=True, expert_choice=ec), ws_bytes=1 << 30) == 2
+    # T == 0: x, dy and dx may be NULL (the host checks pass; without a GPU
+    # the first CUDA call then reports MOE_ERR_CUDA)
+    e = _cfg(T=0, expert_choice=ec)
+    assert _call_backward(L, e, x=None, dy=None, dx=None) in (0, 4)
