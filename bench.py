@@ -2,13 +2,17 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--T TOKENS] [--no-cpu] [--no-e2e]
-                    [--noise-std S] [--expert-choice] [--backward] [--fp8] [--gemm-one-cta]
+                    [--noise-std S] [--expert-choice] [--backward] [--fp8] [--gemm-one-cta] [--graph]
 
 A step is one whole forward pass of the layer (router, scan, gather, expert
 GEMM 1, expert GEMM 2, combine) over one batch of T synthetic tokens.  The
 default workload is the Mixtral-shaped layer (T=16384, d=4096, f=14336, E=8,
 k=2, SwiGLU, bf16) on which the grouped-GEMM bar is stated.  Inputs are larger
 than L2 (x is 134 MB, expert weights 2.8 GB), so no L2 flush is done.
+
+--expert-choice, --fp8 (alone or together) and --backward time those variants
+of the step on the same workload; --graph adds the same forward replayed from
+a CUDA graph.
 
 Prints one JSON line on rank 0.  Under torchrun each rank runs an independent
 replica of the layer on its own GPU (the layer has no cross-GPU step); value is
