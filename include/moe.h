@@ -346,15 +346,19 @@ moe_status moe_grouped_gemm(int32_t dtype, int32_t act, int32_t G, const int32_t
  * inside a framework that owns every allocation, or a loop that must not call
  * cudaMalloc, which can synchronise the device).  The pages have no
  * counterpart: this is a calling convention of this library, not a step of the
- * layer.  Same arguments and results as moe_grouped_gemm minus the workspace.
- * Its scratch (6656 bytes: a status word and the tile table) is a fixed device
- * array inside the library, held by every GPU that loads it until the process
- * exits, so G <= 264 (else MOE_ERR_UNSUPPORTED).  The first call on a device,
- * with that device current, looks up the array's address; make it before any
- * stream capture.  All calls on a device share the array (each clears what it
- * needs first), so calls that may overlap on the GPU race: order them.
- * Device-side failures are not reported; invalid seg_offsets leave C as it was.
- * It calls no cudaMalloc, cudaFree or other allocating routine. */
+ * layer.  Same arguments, options and results as moe_grouped_gemm minus the
+ * workspace.  Its scratch (6656 bytes: a status word and the tile table) is a
+ * fixed device array inside the library, held by every GPU that loads it until
+ * the process exits, so G <= 264 (else MOE_ERR_UNSUPPORTED).  The first call
+ * in a CUDA context, with that context's device current, looks up the array's
+ * address and keeps it for that context; make it before any stream capture.
+ * A context that is destroyed and made again (cudaDeviceReset) gets a new
+ * address, looked up again by its own first call.  All calls on a device share
+ * the array (each clears what it needs first), so calls that may overlap on
+ * the GPU race: order them.  Device-side failures are not reported (use
+ * moe_grouped_gemm with moe_check_device_errors to detect them); invalid
+ * seg_offsets leave C as it was.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine. */
 moe_status moe_grouped_gemm_noalloc(int32_t dtype, int32_t act, int32_t G, const int32_t* seg_offsets, int64_t M,
                                     int32_t K, int32_t N, const void* A, const void* B, const void* B3,
                                     const void* bias, void* C, moe_stream stream, const moe_launch_opts* opts);

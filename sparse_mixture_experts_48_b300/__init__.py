@@ -478,7 +478,8 @@ def grouped_gemm(dtype: int, act: int, seg_offsets: torch.Tensor, A: torch.Tenso
 
 def grouped_gemm_noalloc(dtype: int, act: int, seg_offsets: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
                          B3: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
-                         C: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+                         C: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+                         stage_events=None, timeout_ns: int = 0, single_cta: bool = False):
     """grouped_gemm without a workspace, for callers that cannot allocate at
     call time: the library's own fixed device scratch is used instead (see
     moe.h).  Pass C to avoid any allocation here; if it is omitted, torch (not
@@ -494,9 +495,12 @@ def grouped_gemm_noalloc(dtype: int, act: int, seg_offsets: torch.Tensor, A: tor
     _check(bias, "bias", (G, N), st, required=False)
     if C is None:
         C = torch.zeros((M, N), dtype=A.dtype, device=A.device)
+    opts, keep = _opts(stage_events, timeout_ns, OPT_GEMM_SINGLE_CTA if single_cta else 0)
     with torch.cuda.device(A.device):
         status = lib().moe_grouped_gemm_noalloc(dtype, act, G, _ptr(seg_offsets), M, K, N, _ptr(A), _ptr(B),
-                                                _ptr(B3), _ptr(bias), _ptr(C), _stream_handle(stream), None)
+                                                _ptr(B3), _ptr(bias), _ptr(C), _stream_handle(stream),
+                                                ctypes.byref(opts) if opts is not None else None)
+    del keep
     if status != 0:
         raise MoEError(status, "moe_grouped_gemm_noalloc")
     return C

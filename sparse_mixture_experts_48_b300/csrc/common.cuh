@@ -13,13 +13,24 @@ enum : uint32_t { kErrTimeout = 1u, kErrDevice = 2u };
 
 // Router tile: tokens per router CTA.  A CTA's local ranks fit in uint8.
 constexpr int kRouterBM = 64;
+// The bf16 router with E a multiple of 64 runs its logits on tcgen05 MMAs
+// (M = 128 tokens, N = E) and takes 128 tokens per CTA.
+constexpr int kRouterBMTc = 128;
+__host__ __device__ inline int router_tile_tokens(int dtype, int E) {
+  return (dtype == MOE_DT_BF16 && E % 64 == 0) ? kRouterBMTc : kRouterBM;
+}
 // Expert GEMM tile rows (the M of one tcgen05 MMA with cta_group::1).
 constexpr int kGemmBM = 128;
+// Most groups the standalone grouped GEMM takes.
+constexpr int kGroupedGemmMaxGroups = 264;
+// Limit of every device-side wait unless the caller sets one (2 s).
+constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
 
 struct WsHeader {
-  uint32_t err;        // OR of kErr* bits
-  uint32_t err_where;  // first site that set a bit (diagnostic)
-  uint32_t pad[62];
+  uint32_t err;          // OR of kErr* bits
+  uint32_t err_where;    // first site that set a bit (diagnostic)
+  uint32_t router_done;  // router CTAs finished (the last one runs the dispatch scan)
+  uint32_t pad[61];
 };
 
 // Byte offsets of the regions inside the caller's workspace.
@@ -47,6 +58,7 @@ struct SegTable {
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 __device__ __forceinline__ void record_error(uint32_t* err, uint32_t bit, uint32_t where) {
   if (atomicOr(err, bit) == 0u) atomicExch(err + 1, where);

@@ -21,194 +21,17 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "scan.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kScanThreads = 1024;
-constexpr int kMaxE = 256;
-constexpr int kScanU = 4;   // 32-block chunks loaded per round, per lane
-
-// Exclusive prefix over 32 lanes of per-lane partial sums (lane order).
-__device__ __forceinline__ int warp_excl_scan(int v, int lane, int* total) {
-  int incl = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += n;
-  }
-  *total = __shfl_sync(0xffffffffu, incl, 31);
-  return incl - v;
-}
+constexpr int kScanThreads = 256;
 
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
-  __shared__ int s_npre[kMaxE];
-  __shared__ float s_psum[kMaxE];
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
-  const int E = a.E;
-  // An earlier stage gave up: its partials are not valid.  Publish empty
-  // segments so that nothing later reads or writes through them.
-  const bool failed = *(volatile const uint32_t*)a.err != 0u;
-
-  // Phase 1, one warp per expert: exclusive prefix over the router CTAs of
-  // their selection counts (the rank base of each CTA's tokens), the expert's
-  // total selections n_e, and the sum of its gate probabilities.  Loads of
-  // kScanU chunks are issued before their scans.
-  const bool ec = a.ec_C >= 0;   // expert choice: n_e = C for every expert, no ranks
-  for (int e = warp; e < E; e += nwarps) {
-    int run = 0;
-    float ps = 0.f;
-    for (int64_t b0 = 0; b0 < a.nblk; b0 += 32 * kScanU) {
-      int v[kScanU];
-      float p[kScanU];
-#pragma unroll
-      for (int u = 0; u < kScanU; ++u) {
-        const int64_t b = b0 + 32 * u + lane;
-        v[u] = (b < a.nblk && !ec) ? a.hist[e * a.nblk + b] : 0;
-        p[u] = b < a.nblk ? a.psum[e * a.nblk + b] : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < kScanU; ++u) {
-        const int64_t b = b0 + 32 * u + lane;
-        int tot;
-        const int ex = warp_excl_scan(v[u], lane, &tot);
-        if (b < a.nblk && !ec) a.base[e * a.nblk + b] = run + ex;
-        run += tot;
-        ps += p[u];
-      }
-    }
-    if (ec) run = (int)a.ec_C;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-    if (lane == 0) {
-      s_npre[e] = failed ? 0 : run;
-      s_psum[e] = ps;
-    }
-  }
-  __syncthreads();
-  if (warp != 0) return;
-
-  // Phase 2, one warp: lane l owns experts [l * PE, (l + 1) * PE).
-  const int PE = (E + 31) / 32;
-  const int e0 = lane * PE;
-  // Rows a routed segment occupies: its kept count, padded to a.pad_rows.
-  const int pad = a.pad_rows > 1 ? a.pad_rows : 1;
-  auto seg_rows = [&](int n) {
-    const int c = (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
-    return (c + pad - 1) / pad * pad;
-  };
-  int cnt_local = 0;
-  for (int i = 0; i < PE; ++i) {
-    const int e = e0 + i;
-    if (e < E) cnt_local += seg_rows(s_npre[e]);
-  }
-  int kept_total;
-  int off = warp_excl_scan(cnt_local, lane, &kept_total);
-  // f divides by all selections: T k for token choice, E C for expert choice.
-  const double Tk = ec ? (double)E * (double)a.ec_C : (double)a.T * (double)a.k;
-  double L = 0.0;
-  for (int i = 0; i < PE; ++i) {
-    const int e = e0 + i;
-    if (e < E) {
-      const int n = s_npre[e];
-      const int c = (a.capacity < 0 || n <= a.capacity) ? n : (int)a.capacity;
-      a.n_pre[e] = n;
-      a.counts[e] = c;
-      a.offsets[e] = off;
-      off += seg_rows(n);
-      const float fe = a.T > 0 ? __fdiv_rn((float)n, (float)Tk) : 0.f;
-      const float Pe = a.T > 0 ? __fdiv_rn(s_psum[e], (float)a.T) : 0.f;
-      a.f[e] = fe;
-      a.P[e] = Pe;
-      L += (double)fe * (double)Pe;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);   // fixed tree order
-  if (lane == 0) {
-    a.offsets[E] = kept_total;
-    *a.L_aux = (float)(a.alpha * (double)E * L);
-  }
-  if (a.route_stats) {
-    // Routing health of the pre-capacity shares f_e = n_e / (T k): entropy
-    // -sum f ln f, variance (1/E) sum (f - 1/E)^2, CV = E sqrt(variance).
-    double H = 0.0, V = 0.0;
-    for (int i = 0; i < PE; ++i) {
-      const int e = e0 + i;
-      if (e < E && a.T > 0) {
-        const double fe = (double)s_npre[e] / Tk;
-        if (fe > 0.0) H -= fe * log(fe);
-        V += (fe - 1.0 / E) * (fe - 1.0 / E);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      H += __shfl_xor_sync(0xffffffffu, H, o);
-      V += __shfl_xor_sync(0xffffffffu, V, o);
-    }
-    if (lane == 0) {
-      V /= (double)E;
-      a.route_stats[0] = (float)H;
-      a.route_stats[1] = (float)V;
-      a.route_stats[2] = (float)((double)E * sqrt(V));
-    }
-  }
-  // Segments of the grouped GEMMs: routed experts read the grouped copy of x,
-  // shared experts read x itself and write rows T*k + s*T.  The offsets of
-  // the routed segments are this warp's own (in registers / recomputed), so
-  // nothing is read back from global memory.
-  const int G = E + a.S;
-  const int PG = (G + 31) / 32;
-  const int g0 = lane * PG;
-  int mt_local = 0;
-  for (int i = 0; i < PG; ++i) {
-    const int g = g0 + i;
-    if (g < G) {
-      int rows;
-      if (g < E) {
-        rows = seg_rows(s_npre[g]);
-      } else {
-        rows = failed ? 0 : (int)(pad > 1 ? a.shared_stride : a.T);
-      }
-      mt_local += (rows + kGemmBM - 1) / kGemmBM;
-    }
-  }
-  int mt_total;
-  int mt = warp_excl_scan(mt_local, lane, &mt_total);
-  // Row offsets of routed segments: exclusive prefix of kept counts over g < E.
-  int row_local = 0;
-  for (int i = 0; i < PG; ++i) {
-    const int g = g0 + i;
-    if (g < E) row_local += seg_rows(s_npre[g]);
-  }
-  int row_total;
-  int orow_r = warp_excl_scan(row_local, lane, &row_total);
-  for (int i = 0; i < PG; ++i) {
-    const int g = g0 + i;
-    if (g < G) {
-      int rows, orow, arow, asrc;
-      if (g < E) {
-        rows = seg_rows(s_npre[g]);
-        orow = orow_r;
-        orow_r += rows;
-        arow = orow;
-        asrc = 0;
-      } else {
-        rows = failed ? 0 : (int)(pad > 1 ? a.shared_stride : a.T);
-        orow = (int)(a.rows_tk + (int64_t)(g - E) * a.shared_stride);
-        arow = 0;
-        asrc = 1;
-      }
-      a.seg.rows[g] = rows;
-      a.seg.w[g] = g;
-      a.seg.out_row[g] = orow;
-      a.seg.a_row[g] = arow;
-      a.seg.a_src[g] = asrc;
-      a.seg.mtile_start[g] = mt;
-      mt += (rows + kGemmBM - 1) / kGemmBM;
-    }
-  }
-  if (lane == 0) a.seg.mtile_start[G] = mt_total;
+  __shared__ int s_npre[scan_detail::kMaxE];
+  __shared__ float s_psum[scan_detail::kMaxE];
+  scan_detail::scan_body<4, 8>(a, s_npre, s_psum);
 }
 
 constexpr int kGatherWarps = 8;
@@ -221,7 +44,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(GatherArgs a)
   int my_slot = -1;
   if (lane < k) {
     const int e = a.topk_idx[t * k + lane];
-    const int64_t b = t / kRouterBM;
+    const int64_t b = t / a.bm;
     const int r = a.base[e * a.nblk + b] + (int)a.lrank[t * k + lane];
     const bool kept = a.capacity < 0 || r < a.capacity;
     my_slot = kept ? a.offsets[e] + r : -1;

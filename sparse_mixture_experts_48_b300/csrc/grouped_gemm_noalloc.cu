@@ -11,11 +11,16 @@
 // array below, of a fixed size, which every GPU that loads this library keeps
 // until the process exits.
 //
-// Set-up: the first call on each device, with that device current, looks up the
-// array's device address with cudaGetSymbolAddress and keeps it; make that first
-// call before any stream capture.  Later calls reuse the address.  (In host code
-// the array's name is only a host-side stand-in, never a device address, so
-// kernels are always given the looked-up address.)
+// Set-up: the first call in each CUDA context (normally a device's primary
+// context), with that device current, looks up the array's device address with
+// cudaGetSymbolAddress and keeps it, keyed by the context's ID; make that first
+// call before any stream capture.  Later calls in the same context reuse the
+// address.  If the context is destroyed and made again (cudaDeviceReset, or a
+// context recreated after an error), the library's module is loaded again and
+// the array can move: the new context has a new ID, so the next call looks the
+// address up again and is a first call once more.  (In host code the array's
+// name is only a host-side stand-in, never a device address, so kernels are
+// always given the looked-up address.)
 //
 // Sharing: every call on a device uses the same array, and it keeps the last
 // call's contents.  Each call clears the status word before its kernels run and
@@ -26,7 +31,8 @@
 //
 // Device-side failures (a bounded wait that ran out, offsets outside [0, M])
 // are recorded in the array's status word but are not reported by this entry
-// point: with bad offsets no group gets rows and C is left untouched.
+// point: with bad offsets no group gets rows and C is left untouched.  A caller
+// that needs to detect them uses moe_grouped_gemm and moe_check_device_errors.
 //
 // Nothing here allocates: no cudaMalloc, cudaFree or allocating library call.
 #include <string.h>
@@ -40,33 +46,70 @@ using namespace moe;
 
 namespace {
 
-constexpr int kNoAllocMaxGroups = 264;        // the grouped GEMM's own limit on G
 constexpr size_t kHeaderBytes = 256;           // status word region (sizeof(WsHeader))
-constexpr size_t kTableBytes = (6 * kNoAllocMaxGroups + 1) * 4;
+constexpr size_t kTableBytes = (6 * kGroupedGemmMaxGroups + 1) * 4;
 constexpr size_t kNoAllocScratchBytes = kHeaderBytes + (kTableBytes + 255) / 256 * 256;   // 6656 bytes
 static_assert(sizeof(WsHeader) == kHeaderBytes, "status word region");
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices];             // device address of g_noalloc_scratch, per device
+// The current context's ID, through the driver entry points (this library does
+// not link libcuda).  False if there is no current context or no entry point.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-moe_status scratch_of_current_device(void** out) {
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = (CtxGetCurrentFn)p;
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = (CtxGetIdFn)p;
+  });
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+struct CachedAddress {
+  bool valid;
+  unsigned long long ctx_id;
+  void* addr;                                  // device address of g_noalloc_scratch in that context
+};
+std::mutex g_mu;
+CachedAddress g_cache[kMaxDevices];
+
+moe_status scratch_of_current_context(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  unsigned long long id = 0;
+  bool have_id = current_context_id(&id);
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  CachedAddress& c = g_cache[dev];
+  if (have_id && c.valid && c.ctx_id == id) {
+    *out = c.addr;
+    return MOE_OK;
   }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+  // The lookup makes the device's primary context current if none was.
+  if (!have_id) have_id = current_context_id(&id);
+  c.valid = have_id;                           // without a context ID, look up again on every call
+  c.ctx_id = id;
+  c.addr = p;
+  *out = p;
   return MOE_OK;
 }
-
-bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 }  // namespace
 
@@ -74,45 +117,14 @@ extern "C" moe_status moe_grouped_gemm_noalloc(int32_t dtype, int32_t act, int32
                                                int64_t M, int32_t K, int32_t N, const void* A, const void* B,
                                                const void* B3, const void* bias, void* C, moe_stream stream,
                                                const moe_launch_opts* opts) {
-  if (dtype != MOE_DT_F32 && dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
-  if (act != MOE_ACT_NONE && act != MOE_ACT_RELU && act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU)
-    return MOE_ERR_INVALID_ARG;
-  if (G <= 0 || M < 0 || K <= 0 || N <= 0 || !seg_offsets || !A || !B || !C) return MOE_ERR_INVALID_ARG;
-  if ((act == MOE_ACT_SWIGLU) != (B3 != nullptr)) return MOE_ERR_INVALID_ARG;
-  if (G > kNoAllocMaxGroups) return MOE_ERR_UNSUPPORTED;   // the fixed scratch holds at most this many groups
-  if (dtype == MOE_DT_BF16 && (K % 64 != 0 || N % 64 != 0)) return MOE_ERR_UNSUPPORTED;
-  if (M >= ((int64_t)1 << 31) - 2 * kGemmBM) return MOE_ERR_UNSUPPORTED;
-  const void* all[] = {seg_offsets, A, B, B3, bias, C};
-  for (const void* p : all)
-    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
-
-  void* scratch = nullptr;
-  moe_status st = scratch_of_current_device(&scratch);
+  // The fixed scratch holds the tile table of at most kGroupedGemmMaxGroups
+  // groups; larger G is rejected (MOE_ERR_UNSUPPORTED) by the shared checks.
+  static_assert(kNoAllocScratchBytes >= 256 + (6 * kGroupedGemmMaxGroups + 1) * 4, "scratch holds the table");
+  const moe_status st = check_grouped_gemm_args(dtype, act, G, seg_offsets, M, K, N, A, B, B3, bias, C);
   if (st != MOE_OK) return st;
-  cudaStream_t s = (cudaStream_t)stream;
-  uint8_t* ws = (uint8_t*)scratch;
-  WsHeader* hdr = (WsHeader*)ws;
-  SegTable seg;
-  int* tab = (int*)(ws + kHeaderBytes);
-  seg.rows = tab;
-  seg.w = tab + G;
-  seg.out_row = tab + 2 * G;
-  seg.a_row = tab + 3 * G;
-  seg.a_src = tab + 4 * G;
-  seg.mtile_start = tab + 5 * G;
-  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_segments_from_offsets(seg_offsets, G, M, seg, &hdr->err, s) != cudaSuccess) return MOE_ERR_CUDA;
-  GemmArgs g;
-  memset(&g, 0, sizeof(g));
-  g.dtype = dtype; g.act = act; g.G = G; g.K = K; g.N = N; g.a_from_out_rows = true; g.seg = seg;
-  g.A0 = A; g.rows_A0 = M > 0 ? M : 1; g.A1 = nullptr; g.B = B; g.B3 = B3; g.Gw = G; g.bias = bias; g.C = C;
-  g.max_mtiles = M > 0 ? (M + kGemmBM - 1) / kGemmBM + G : 0;
-  g.err = &hdr->err;
-  g.timeout_ns = (opts && opts->wait_timeout_ns > 0) ? opts->wait_timeout_ns : 2000000000LL;
-  if (opts && opts->stage_events && cudaEventRecord((cudaEvent_t)opts->stage_events[0], s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (launch_grouped_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (opts && opts->stage_events && cudaEventRecord((cudaEvent_t)opts->stage_events[1], s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  void* scratch = nullptr;
+  const moe_status sst = scratch_of_current_context(&scratch);
+  if (sst != MOE_OK) return sst;
+  return launch_grouped_gemm_on_scratch(dtype, act, G, seg_offsets, M, K, N, A, B, B3, bias, C, (uint8_t*)scratch,
+                                        stream, opts);
 }

@@ -8,27 +8,6 @@
 
 namespace moe {
 
-struct RouterArgs {
-  const void* x;    // [T, d]
-  const void* Wg;   // [d, E]
-  const void* bg;   // [E] or null
-  const float* noise;  // [T, E] fp32 added to the logits before gating, or null
-  int64_t T;
-  int d, E, k, gating, dtype;
-  float* logits_out;   // [T, E] or null
-  int32_t* topk_idx;   // [T, k]
-  float* topk_w;       // [T, k]
-  uint8_t* lrank;      // [T, k] rank among the CTA's earlier tokens choosing the same expert
-  int64_t nblk;        // router CTAs (kRouterBM tokens each)
-  int32_t* hist;       // [E, nblk] selections per router CTA (expert-major: the scan reads rows)
-  float* psum;         // [E, nblk] sum of gate probabilities per router CTA
-  uint32_t* err;       // workspace status word
-  int64_t timeout_ns;  // limit of every device-side wait
-  float* scores_em;    // expert choice: gate probabilities [E, T] (no top-k), else null
-  float* raw_logits;   // [T, E] the (noisy) logits before gating, or null (the backward's copy)
-};
-cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
-
 struct ScanArgs {
   int64_t T;
   int E, k, S;
@@ -54,6 +33,35 @@ struct ScanArgs {
 };
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
 
+struct RouterArgs {
+  const void* x;    // [T, d]
+  const void* Wg;   // [d, E]
+  const void* bg;   // [E] or null
+  const float* noise;  // [T, E] fp32 added to the logits before gating, or null
+  int64_t T;
+  int d, E, k, gating, dtype;
+  float* logits_out;   // [T, E] or null
+  int32_t* topk_idx;   // [T, k]
+  float* topk_w;       // [T, k]
+  uint8_t* lrank;      // [T, k] rank among the CTA's earlier tokens choosing the same expert
+  int bm;              // tokens per router CTA: router_tile_tokens(dtype, E)
+  int64_t nblk;        // router CTAs (bm tokens each)
+  int32_t* hist;       // [E, nblk] selections per router CTA (expert-major: the scan reads rows)
+  float* psum;         // [E, nblk] sum of gate probabilities per router CTA
+  uint32_t* err;       // workspace status word
+  int64_t timeout_ns;  // limit of every device-side wait
+  float* scores_em;    // expert choice: gate probabilities [E, T] (no top-k), else null
+  float* raw_logits;   // [T, E] the (noisy) logits before gating, or null (the backward's copy)
+  // When fused_scan is set, the last router CTA to finish runs the dispatch
+  // scan with `scan` (its hist / psum are this launch's partials); `done`
+  // counts finished router CTAs and is zero when the launch starts.
+  bool fused_scan;
+  ScanArgs scan;
+  uint32_t* done;
+};
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+
+
 struct GatherArgs {
   const void* x;
   int64_t T;
@@ -62,6 +70,7 @@ struct GatherArgs {
   const int32_t* topk_idx;
   const uint8_t* lrank;
   const int32_t* base;  // [E, nblk]
+  int bm;               // tokens per router CTA
   int64_t nblk;
   const int32_t* offsets;
   int32_t* slot;        // [T, k]
@@ -332,6 +341,17 @@ struct ColsumArgs {
   float* out;              // [Gw, N]
 };
 cudaError_t launch_colsum(const ColsumArgs& a, cudaStream_t s);
+
+// The standalone grouped GEMM (moe_grouped_gemm and its variant without a
+// workspace): argument checks, and the launches on a scratch area of
+// moe_grouped_gemm_workspace_size(G) bytes (status word, then the tile table).
+moe_status check_grouped_gemm_args(int32_t dtype, int32_t act, int32_t G, const int32_t* seg_offsets, int64_t M,
+                                   int32_t K, int32_t N, const void* A, const void* B, const void* B3,
+                                   const void* bias, const void* C);
+moe_status launch_grouped_gemm_on_scratch(int32_t dtype, int32_t act, int32_t G, const int32_t* seg_offsets,
+                                          int64_t M, int32_t K, int32_t N, const void* A, const void* B,
+                                          const void* B3, const void* bias, void* C, uint8_t* scratch,
+                                          moe_stream stream, const moe_launch_opts* opts);
 
 // Builds a segment table from row offsets (standalone grouped GEMM entry point).
 cudaError_t launch_segments_from_offsets(const int32_t* offsets, int G, int64_t M, SegTable seg, uint32_t* err,

@@ -14,9 +14,7 @@ namespace {
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
 constexpr int kMaxShared = 8;
-constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
 
-bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Expert choice: tokens per expert, min(T, ceil(T cf / E)), or min(T, ceil(T k / E))
 // without a capacity factor (the compute of top-k token choice).
@@ -51,7 +49,8 @@ WsLayout layout(const moe_config* c) {
   WsLayout L;
   const size_t esz = c->dtype == MOE_DT_BF16 ? 2 : 4;
   const bool ec = (c->flags & MOE_FLAG_EXPERT_CHOICE) != 0;
-  L.nblk = (c->T + kRouterBM - 1) / kRouterBM;
+  const int bm = router_tile_tokens(c->dtype, c->E);
+  L.nblk = (c->T + bm - 1) / bm;
   L.ec_C = ec ? ec_capacity_of(c) : -1;
   L.EW = (c->E + 31) / 32;
   L.rows_tk = ec ? (int64_t)c->E * L.ec_C : c->T * (int64_t)c->k;
@@ -159,7 +158,8 @@ BwdLayout bwd_layout(const moe_config* c) {
   const bool swiglu = c->act == MOE_ACT_SWIGLU;
   const int64_t T = c->T;
   L.G = c->E + c->n_shared;
-  L.nblk = (T + kRouterBM - 1) / kRouterBM;
+  const int bm = router_tile_tokens(c->dtype, c->E);
+  L.nblk = (T + bm - 1) / bm;
   L.Tpad = (T + 127) / 128 * 128;
   const bool ec = (c->flags & MOE_FLAG_EXPERT_CHOICE) != 0;
   L.ec_C = ec ? ec_capacity_of(c) : -1;
@@ -236,6 +236,52 @@ struct StageClock {
 };
 
 }  // namespace
+
+namespace moe {
+
+moe_status check_grouped_gemm_args(int32_t dtype, int32_t act, int32_t G, const int32_t* seg_offsets, int64_t M,
+                                   int32_t K, int32_t N, const void* A, const void* B, const void* B3,
+                                   const void* bias, const void* C) {
+  if (dtype != MOE_DT_F32 && dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+  if (act != MOE_ACT_NONE && act != MOE_ACT_RELU && act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU)
+    return MOE_ERR_INVALID_ARG;
+  if (G <= 0 || M < 0 || K <= 0 || N <= 0 || !seg_offsets || !A || !B || !C) return MOE_ERR_INVALID_ARG;
+  if ((act == MOE_ACT_SWIGLU) != (B3 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (G > kGroupedGemmMaxGroups) return MOE_ERR_UNSUPPORTED;
+  if (dtype == MOE_DT_BF16 && (K % 64 != 0 || N % 64 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (M >= ((int64_t)1 << 31) - 2 * kGemmBM) return MOE_ERR_UNSUPPORTED;
+  const void* all[] = {seg_offsets, A, B, B3, bias, C};
+  for (const void* p : all)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status launch_grouped_gemm_on_scratch(int32_t dtype, int32_t act, int32_t G, const int32_t* seg_offsets,
+                                          int64_t M, int32_t K, int32_t N, const void* A, const void* B,
+                                          const void* B3, const void* bias, void* C, uint8_t* scratch,
+                                          moe_stream stream, const moe_launch_opts* opts) {
+  cudaStream_t s = (cudaStream_t)stream;
+  WsHeader* hdr = (WsHeader*)scratch;
+  const SegTable seg = seg_table(scratch, align_up(sizeof(WsHeader), 256), G);
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_segments_from_offsets(seg_offsets, G, M, seg, &hdr->err, s) != cudaSuccess) return MOE_ERR_CUDA;
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.dtype = dtype; g.act = act; g.G = G; g.K = K; g.N = N; g.a_from_out_rows = true; g.seg = seg;
+  g.A0 = A; g.rows_A0 = M > 0 ? M : 1; g.A1 = nullptr; g.B = B; g.B3 = B3; g.Gw = G; g.bias = bias; g.C = C;
+  g.max_mtiles = M > 0 ? (M + kGemmBM - 1) / kGemmBM + G : 0;
+  g.err = &hdr->err;
+  g.timeout_ns = (opts && opts->wait_timeout_ns > 0) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
+  g.single_cta = opts && (opts->flags & MOE_OPT_GEMM_SINGLE_CTA);
+  if (opts && opts->stage_events && cudaEventRecord((cudaEvent_t)opts->stage_events[0], s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_grouped_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (opts && opts->stage_events && cudaEventRecord((cudaEvent_t)opts->stage_events[1], s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace moe
 
 extern "C" {
 
@@ -321,18 +367,33 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   if (ec && c.T > 0 && cudaMemsetAsync(ws + L.ec_bits, 0, (size_t)c.T * L.EW * 4, s) != cudaSuccess)
     return MOE_ERR_CUDA;
 
-  // 1. router
+  // 1. router, and (in its last CTA) the scan: ranks, capacity, offsets,
+  //    statistics, segment table
   if (clk.mark(0) != cudaSuccess) return MOE_ERR_CUDA;
   RouterArgs ra;
+  memset(&ra, 0, sizeof(ra));
   ra.x = x; ra.Wg = W_g; ra.bg = b_g; ra.noise = router_noise; ra.T = c.T; ra.d = c.d_model; ra.E = c.E; ra.k = c.k;
   ra.gating = c.gating; ra.dtype = c.dtype; ra.logits_out = router_logits; ra.topk_idx = topk_idx;
   ra.topk_w = topk_w; ra.lrank = ws + L.lrank; ra.hist = (int32_t*)(ws + L.hist); ra.psum = (float*)(ws + L.psum);
   ra.err = &hdr->err; ra.timeout_ns = timeout; ra.nblk = L.nblk;
+  ra.bm = router_tile_tokens(c.dtype, c.E);
   ra.scores_em = ec ? (float*)(ws + L.ec_scores) : nullptr; ra.raw_logits = nullptr;
+  ScanArgs sa;
+  memset(&sa, 0, sizeof(sa));
+  sa.T = c.T; sa.E = c.E; sa.k = c.k; sa.S = c.n_shared; sa.capacity = ec ? -1 : C; sa.alpha = c.alpha;
+  sa.nblk = L.nblk; sa.ec_C = L.ec_C; sa.pad_rows = 1; sa.shared_stride = c.T;
+  sa.hist = ra.hist; sa.psum = ra.psum; sa.base = (int32_t*)(ws + L.base); sa.n_pre = (int32_t*)(ws + L.npre);
+  sa.counts = expert_counts; sa.offsets = (int32_t*)(ws + L.offsets); sa.f = f; sa.P = P; sa.L_aux = L_aux;
+  sa.route_stats = route_stats;
+  sa.seg = seg; sa.rows_tk = L.rows_tk; sa.err = &hdr->err;
+  ra.fused_scan = L.nblk > 0;
+  ra.scan = sa;
+  ra.done = &hdr->router_done;
   if (launch_router(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // No router CTA (T = 0): the scan on its own writes the empty statistics.
+  if (!ra.fused_scan && launch_scan(sa, s) != cudaSuccess) return MOE_ERR_CUDA;
 
-  // 2. scan: ranks, capacity, offsets, statistics, segment table (expert
-  //    choice: first each expert's choice of tokens)
+  // 2. expert choice: each expert's choice of tokens
   if (clk.mark(1) != cudaSuccess) return MOE_ERR_CUDA;
   if (ec) {
     EcSelectArgs ea;
@@ -341,14 +402,6 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
     ea.bits = (uint32_t*)(ws + L.ec_bits); ea.err = &hdr->err;
     if (c.T > 0 && launch_ec_select(ea, s) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  ScanArgs sa;
-  sa.T = c.T; sa.E = c.E; sa.k = c.k; sa.S = c.n_shared; sa.capacity = ec ? -1 : C; sa.alpha = c.alpha;
-  sa.nblk = L.nblk; sa.ec_C = L.ec_C; sa.pad_rows = 1; sa.shared_stride = c.T;
-  sa.hist = ra.hist; sa.psum = ra.psum; sa.base = (int32_t*)(ws + L.base); sa.n_pre = (int32_t*)(ws + L.npre);
-  sa.counts = expert_counts; sa.offsets = (int32_t*)(ws + L.offsets); sa.f = f; sa.P = P; sa.L_aux = L_aux;
-  sa.route_stats = route_stats;
-  sa.seg = seg; sa.rows_tk = L.rows_tk; sa.err = &hdr->err;
-  if (launch_scan(sa, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 3. gather into the expert-grouped buffer
   if (clk.mark(2) != cudaSuccess) return MOE_ERR_CUDA;
@@ -374,7 +427,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   memset(&ga, 0, sizeof(ga));
   ga.x = x; ga.T = c.T; ga.d = c.d_model; ga.E = c.E; ga.k = c.k; ga.dtype = c.dtype; ga.capacity = C;
   ga.topk_idx = topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.offsets = sa.offsets; ga.slot = slot_buf;
-  ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm; ga.err = &hdr->err; ga.nblk = L.nblk;
+  ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm; ga.err = &hdr->err; ga.nblk = L.nblk; ga.bm = ra.bm;
   const bool sh8 = fp8 && c.n_shared > 0;
   if (fp8) {
     ga.fp8 = true;
@@ -646,6 +699,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
   ra.topk_idx = (int32_t*)(ws + L.idx); ra.topk_w = (float*)(ws + L.w); ra.lrank = ws + L.lrank;
   ra.hist = (int32_t*)(ws + L.hist); ra.psum = (float*)(ws + L.psum); ra.err = &hdr->err; ra.timeout_ns = timeout;
   ra.nblk = L.nblk;
+  ra.bm = router_tile_tokens(c.dtype, c.E);
   if (ec) {
     // the experts choose on the gate probabilities; the gating's backward
     // needs the logits themselves
@@ -673,7 +727,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
   GatherArgs ga;
   memset(&ga, 0, sizeof(ga));
   ga.x = x; ga.T = T; ga.d = d; ga.E = E; ga.k = k; ga.dtype = c.dtype; ga.capacity = C;
-  ga.topk_idx = ra.topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.nblk = L.nblk; ga.offsets = sa.offsets;
+  ga.topk_idx = ra.topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.nblk = L.nblk; ga.bm = ra.bm; ga.offsets = sa.offsets;
   ga.slot = (int32_t*)(ws + L.slot); ga.dropped = ws + L.drop; ga.perm_token = nullptr; ga.xperm = ws + L.xperm;
   ga.err = &hdr->err;
   if (ec) {
@@ -811,39 +865,12 @@ moe_status moe_grouped_gemm(int32_t dtype, int32_t act, int32_t G, const int32_t
                             int32_t N, const void* A, const void* B, const void* B3, const void* bias, void* C,
                             void* workspace, size_t workspace_bytes, moe_stream stream,
                             const moe_launch_opts* opts) {
-  if (dtype != MOE_DT_F32 && dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
-  if (act != MOE_ACT_NONE && act != MOE_ACT_RELU && act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU)
-    return MOE_ERR_INVALID_ARG;
-  if (G <= 0 || M < 0 || K <= 0 || N <= 0 || !seg_offsets || !A || !B || !C) return MOE_ERR_INVALID_ARG;
-  if ((act == MOE_ACT_SWIGLU) != (B3 != nullptr)) return MOE_ERR_INVALID_ARG;
-  if (G > 264) return MOE_ERR_UNSUPPORTED;
-  if (dtype == MOE_DT_BF16 && (K % 64 != 0 || N % 64 != 0)) return MOE_ERR_UNSUPPORTED;
-  if (M >= ((int64_t)1 << 31) - 2 * kGemmBM) return MOE_ERR_UNSUPPORTED;
-  const void* all[] = {seg_offsets, A, B, B3, bias, C};
-  for (const void* p : all)
-    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  const moe_status st = check_grouped_gemm_args(dtype, act, G, seg_offsets, M, K, N, A, B, B3, bias, C);
+  if (st != MOE_OK) return st;
   const size_t need = moe_grouped_gemm_workspace_size(G);
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < need) return MOE_ERR_WORKSPACE;
-  cudaStream_t s = (cudaStream_t)stream;
-  uint8_t* ws = (uint8_t*)workspace;
-  WsHeader* hdr = (WsHeader*)ws;
-  const SegTable seg = seg_table(ws, align_up(sizeof(WsHeader), 256), G);
-  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_segments_from_offsets(seg_offsets, G, M, seg, &hdr->err, s) != cudaSuccess) return MOE_ERR_CUDA;
-  GemmArgs g;
-  memset(&g, 0, sizeof(g));
-  g.dtype = dtype; g.act = act; g.G = G; g.K = K; g.N = N; g.a_from_out_rows = true; g.seg = seg;
-  g.A0 = A; g.rows_A0 = M > 0 ? M : 1; g.A1 = nullptr; g.B = B; g.B3 = B3; g.Gw = G; g.bias = bias; g.C = C;
-  g.max_mtiles = M > 0 ? (M + kGemmBM - 1) / kGemmBM + G : 0;
-  g.err = &hdr->err;
-  g.timeout_ns = (opts && opts->wait_timeout_ns > 0) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
-  g.single_cta = opts && (opts->flags & MOE_OPT_GEMM_SINGLE_CTA);
-  if (opts && opts->stage_events && cudaEventRecord((cudaEvent_t)opts->stage_events[0], s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (launch_grouped_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (opts && opts->stage_events && cudaEventRecord((cudaEvent_t)opts->stage_events[1], s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  return launch_grouped_gemm_on_scratch(dtype, act, G, seg_offsets, M, K, N, A, B, B3, bias, C,
+                                        (uint8_t*)workspace, stream, opts);
 }
 
 }  // extern "C"

@@ -24,6 +24,8 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "scan.cuh"
+#include "tcgen05.cuh"
 
 namespace moe {
 namespace {
@@ -38,23 +40,24 @@ constexpr uint32_t kWhereRouter = 0x300;
 static_assert(kRouterBM == 16 * kRowBlocks, "one m16 row block per MMA warp of a k-group");
 
 // ---- the per-token tail shared by both dtypes ----------------------------------
-// sl: [kRouterBM][ldl] fp32 logits without bias, rows of this CTA's tokens.
-// bits: [E][kRouterBM / 32] scratch words.  The kTPT = 4 threads 4i..4i+3 (one
-// warp) own token i: thread q adds the bias, gates and keeps a sorted top-k of
-// the experts e = q mod 4, then the lists are merged in two butterfly rounds,
-// so all four threads end with the same k experts.  Needs blockDim >=
-// kTPT * kRouterBM.
+// sl: [BM][ldl] fp32 logits without bias, rows of this CTA's BM tokens.
+// bits: [E][BM / 32] scratch words.  The kTPT = 4 threads 4i..4i+3 (one warp)
+// own token i: thread q adds the bias, gates and keeps a sorted top-k of the
+// experts e = q mod 4, then the lists are merged in two butterfly rounds, so
+// all four threads end with the same k experts.  Needs blockDim >= kTPT * BM.
+template <int BM>
 __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const RouterArgs& a, int64_t blk) {
-  constexpr int NW = kRouterBM / 32;
+  static_assert(BM % 32 == 0 && BM <= 256, "local ranks are uint8");
+  constexpr int NW = BM / 32;
   const int tid = threadIdx.x;
   const int E = a.E, k = a.k;
-  const int64_t t0 = blk * kRouterBM;
+  const int64_t t0 = blk * BM;
   for (int i = tid; i < E * NW; i += blockDim.x) bits[i] = 0u;
   __syncthreads();
 
   const int tok = tid / kTPT, q = tid % kTPT;
   const int64_t t = t0 + tok;
-  const bool valid = tid < kTPT * kRouterBM && t < a.T;
+  const bool valid = tid < kTPT * BM && t < a.T;
   float val[8];
   int idx[8];
 #pragma unroll
@@ -73,7 +76,7 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
       }
     }
   };
-  if (tid < kTPT * kRouterBM) {     // whole warps: the shuffles see every thread of each quad
+  if (tid < kTPT * BM) {            // whole warps: the shuffles see every thread of each quad
     float* l = sl + tok * ldl;
     const bool bf = a.dtype == MOE_DT_BF16;
     if (valid) {
@@ -165,7 +168,7 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
   // Per expert: selections (popc of the bit masks) and the sum of gate
   // probabilities over the CTA's tokens, one warp per expert: lane l adds
   // rows l and l + 32, then a fixed xor-tree over the lanes.
-  const int nvalid = (int)(a.T - t0 < kRouterBM ? a.T - t0 : kRouterBM);
+  const int nvalid = (int)(a.T - t0 < BM ? a.T - t0 : BM);
   const int lane = tid % 32, nwarps = blockDim.x / 32;
   for (int e = tid / 32; e < E; e += nwarps) {
     float s = 0.f;
@@ -179,6 +182,26 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
       a.psum[e * a.nblk + blk] = s;
     }
   }
+}
+
+// Every router CTA ends here, also one that stopped early.  With the scan
+// fused, each CTA publishes its partials (fence), takes a ticket, and the CTA
+// that takes the last one runs the dispatch scan over all CTAs' partials; a
+// stopped CTA still takes its ticket, so the scan always runs (and, seeing the
+// status word set, publishes empty segments).  `scratch`: shared memory no
+// longer in use, at least 2 KB.
+__device__ void router_retire(const RouterArgs& a, uint8_t* scratch) {
+  if (!a.fused_scan) return;
+  __shared__ uint32_t s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(a.done, 1u) == (uint32_t)(a.nblk - 1) ? 1u : 0u;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  int* s_npre = reinterpret_cast<int*>(scratch);
+  float* s_psum = reinterpret_cast<float*>(s_npre + scan_detail::kMaxE);
+  scan_detail::scan_body<2, 4>(a.scan, s_npre, s_psum);
 }
 
 // ---- bf16: tensor-core logits ---------------------------------------------------
@@ -392,7 +415,10 @@ __global__ void __launch_bounds__(kThreadsBf16) router_bf16_kernel(const __grid_
     }
   }
   // Every warp is past its last read of the ring before the logits overwrite it.
-  if (__syncthreads_or(stopped)) return;
+  if (__syncthreads_or(stopped)) {
+    router_retire(a, smem);
+    return;
+  }
   float* sl = (float*)smem;
   const int ldl = EP + 1;
   // logits = (even k-tiles) + (odd k-tiles): k-group 1 stores its partial, and
@@ -421,7 +447,8 @@ __global__ void __launch_bounds__(kThreadsBf16) router_bf16_kernel(const __grid_
     }
   }
   __syncthreads();
-  router_finalize(sl, ldl, bits, a, blk);
+  router_finalize<kRouterBM>(sl, ldl, bits, a, blk);
+  router_retire(a, smem);
 }
 
 // ---- fp32: CUDA-core logits ------------------------------------------------------
@@ -459,7 +486,8 @@ __global__ void __launch_bounds__(kThreadsF32) router_f32_kernel(RouterArgs a) {
     }
   }
   __syncthreads();
-  router_finalize(sl, ldl, bits, a, blk);
+  router_finalize<kRouterBM>(sl, ldl, bits, a, blk);
+  router_retire(a, smem);
 }
 
 template <int NT>
@@ -484,11 +512,213 @@ cudaError_t launch_bf16(const RouterArgs& a, int64_t nblk, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+
+// ---- bf16 with E a multiple of 64: tcgen05 logits -------------------------------
+// A CTA owns kRouterBMTc = 128 tokens.  The logit contraction of the tile is
+// one tcgen05 MMA chain, M = 128 tokens x N = E experts x K = d, accumulated
+// in TMEM:
+//   warp 0      TMA producer: per 64-deep k-block the x tile [128 tokens][64 k]
+//               (16 KB, K-major, 128-byte swizzle, rows past T zero-filled) and
+//               the E / 64 W_g boxes [64 k][64 experts] (8 KB each, N-major,
+//               128-byte swizzle) into a ring of about 192 KB;
+//   warp 1      TMEM owner; one lane issues M128 N=E K16 kind::f16 MMAs and
+//               commits ring slots back to the producer;
+//   warps 4-7   read the accumulator (one TMEM lane quadrant each, a token per
+//               lane) into fp32 logits in shared memory, over the drained ring;
+// then all 16 warps run the gating / top-k tail and the per-CTA partials.
+// Against the mma.sync router (64 tokens per CTA, W_g tiles beside every x
+// tile in the ring), a CTA here reads each W_g tile once per 128 tokens and
+// keeps 16 KB of x per stage in flight, and the MMA work is a handful of
+// instructions per k-block.
+namespace rtc {
+constexpr int BM = kRouterBMTc;
+constexpr int XS = BM * kBK * 2;           // 16 KB x tile per k-block
+constexpr int WBOX = kBK * 64 * 2;         // 8 KB per 64-expert W_g box
+constexpr int THREADS = 512;               // 16 warps: the tail runs 4 threads per token
+constexpr int RING = 192 * 1024;
+constexpr int EPI_WARP0 = 4;               // warps 4..7: TMEM lane quadrants 0..3
+constexpr uint32_t kWhere = kWhereRouter + 0x10;
+
+template <int NB>   // E = 64 NB
+struct Shape {
+  static constexpr int E = 64 * NB;
+  static constexpr int STAGE = XS + NB * WBOX;
+  static constexpr int STAGES = RING / STAGE;          // 8, 6, 4, 4
+  static constexpr int TCOLS = NB == 1 ? 64 : NB == 2 ? 128 : 256;   // TMEM columns (a power of 2)
+  static constexpr size_t LOGITS = (size_t)BM * (E + 1) * 4;
+  static constexpr size_t BITS_OFF = (size_t)STAGES * STAGE;
+  static constexpr size_t BITS = (size_t)E * (BM / 32) * 4;
+  static constexpr size_t BAR_OFF = (BITS_OFF + BITS + 7) / 8 * 8;
+  static constexpr size_t SMEM = 1024 + BAR_OFF + (2 * STAGES + 2) * 8 + 16;
+  static_assert(LOGITS <= BITS_OFF, "the logits fit in the drained ring");
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+};
+}  // namespace rtc
+
+template <int NB>
+__global__ void __launch_bounds__(rtc::THREADS, 1) router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                    const __grid_constant__ CUtensorMap tmW,
+                                                                    RouterArgs a) {
+  using L = rtc::Shape<NB>;
+  constexpr int E = L::E, STAGES = L::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t base = smem_u32(smem);
+  uint32_t* bits = (uint32_t*)(smem + L::BITS_OFF);
+  uint64_t* full = (uint64_t*)(smem + L::BAR_OFF);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* done = tfull + 1;
+  uint32_t* tmem_slot = (uint32_t*)(done + 1);
+  uint32_t* abort_flag = tmem_slot + 1;
+  volatile uint32_t* abort = abort_flag;
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int64_t blk = blockIdx.x;
+  const int t0 = (int)(blk * rtc::BM);
+  const int nk = a.d / kBK;
+  const uint64_t limit = (uint64_t)a.timeout_ns;
+  const uint64_t drain_limit = limit > 2000000000ull ? limit : 2000000000ull;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1u);
+      mbar_init(smem_u32(&empty[s]), 1u);
+    }
+    mbar_init(smem_u32(tfull), 1u);
+    mbar_init(smem_u32(done), 1u);
+    *abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(L::TCOLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool stopped = false;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+      const uint64_t x_policy = l2_policy_evict_first();   // x is streamed once
+      int kb = 0;
+      for (; kb < nk; ++kb) {
+        const int st = kb % STAGES;
+        if (kb >= STAGES &&
+            !mbar_wait_i(smem_u32(&empty[st]), (uint32_t)((kb / STAGES) - 1) & 1u, abort, limit, a.err,
+                         rtc::kWhere + 1)) {
+          stopped = true;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[st]);
+        const uint32_t sa = base + (uint32_t)(st * L::STAGE);
+        mbar_expect_tx(fb, (uint32_t)L::STAGE);
+        tma_load_2d_hint(sa, &tmX, kb * kBK, t0, fb, x_policy);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) tma_load_2d(sa + rtc::XS + b * rtc::WBOX, &tmW, 64 * b, kb * kBK, fb);
+      }
+      // Every copy this thread started lands before the CTA goes on: the last
+      // STAGES k-blocks issued, one per slot, may still be in flight.
+      for (int j = kb - STAGES > 0 ? kb - STAGES : 0; j < kb; ++j)
+        mbar_drain(smem_u32(&full[j % STAGES]), (uint32_t)(j / STAGES) & 1u, drain_limit);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int kb = 0;
+      for (; kb < nk; ++kb) {
+        const int st = kb % STAGES;
+        if (!mbar_wait_i(smem_u32(&full[st]), (uint32_t)(kb / STAGES) & 1u, abort, limit, a.err, rtc::kWhere + 2)) {
+          stopped = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = base + (uint32_t)(st * L::STAGE);
+        const uint32_t sb = sa + rtc::XS;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // A (x): K-major, 8-row groups 1024 B apart; a K step of 16 is 32 bytes.
+          const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+          // B (W_g): N-major, 64-expert boxes 8 KB apart (LBO), 8-row k groups
+          // 1024 B apart (SBO); a K step of 16 rows is 2048 bytes.
+          const uint64_t bd = smem_desc(sb + kk * 2048, rtc::WBOX, 1024);
+          mma_bf16_cta1<idesc_bf16(rtc::BM, E)>(tmem, ad, bd, (kb | kk) != 0 ? 1u : 0u);
+        }
+        mma_commit_cta1(smem_u32(&empty[st]));
+      }
+      if (!stopped) mma_commit_cta1(smem_u32(tfull));
+      // Every MMA issued completes before TMEM or the ring is touched again.
+      mma_commit_cta1(smem_u32(done));
+      mbar_drain(smem_u32(done), 0u, drain_limit);
+    }
+  } else if (warp >= rtc::EPI_WARP0 && warp < rtc::EPI_WARP0 + 4) {
+    // ---------------- accumulator -> shared-memory logits ----------------
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_i(smem_u32(tfull), 0u, abort, limit, a.err, rtc::kWhere + 3));
+    if (!ok) {
+      stopped = true;
+    } else {
+      tc_fence_after();
+      const int q = warp & 3;                        // TMEM lanes 32 q .. 32 q + 31
+      const int row = q * 32 + lane;                 // the CTA's token
+      float* sl = (float*)smem;
+#pragma unroll 1
+      for (int c = 0; c < E / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sl[row * (E + 1) + c * 32 + i] = __uint_as_float(v[i]);
+      }
+    }
+    tc_fence_before();
+  }
+  // The ring is drained (every MMA done, every copy landed) and the logits are
+  // in shared memory before the tail reads them; TMEM can go.
+  const bool stop = __syncthreads_or(stopped || *abort != 0u);
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(L::TCOLS) : "memory");
+  }
+  if (!stop) router_finalize<rtc::BM>((float*)smem, E + 1, bits, a, blk);
+  router_retire(a, smem);
+}
+
+template <int NB>
+cudaError_t launch_tc(const RouterArgs& a, int64_t nblk, cudaStream_t s) {
+  using L = rtc::Shape<NB>;
+  CUtensorMap tmX, tmW;
+  if (!tmap_bf16_2d(&tmX, a.x, a.T, a.d, kBK, rtc::BM)) return cudaErrorInvalidValue;
+  if (!tmap_bf16_2d(&tmW, a.Wg, a.d, a.E, 64, kBK)) return cudaErrorInvalidValue;
+  auto kern = router_tc_kernel<NB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)nblk, rtc::THREADS, L::SMEM, s>>>(tmX, tmW, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
-  const int64_t nblk = (a.T + kRouterBM - 1) / kRouterBM;
+  if (a.bm != router_tile_tokens(a.dtype, a.E)) return cudaErrorInvalidValue;
+  const int64_t nblk = (a.T + a.bm - 1) / a.bm;
   if (nblk == 0) return cudaSuccess;
+  if (a.bm == kRouterBMTc) {
+    switch (a.E / 64) {
+      case 1: return launch_tc<1>(a, nblk, s);
+      case 2: return launch_tc<2>(a, nblk, s);
+      case 3: return launch_tc<3>(a, nblk, s);
+      case 4: return launch_tc<4>(a, nblk, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (a.dtype == MOE_DT_F32) {
     size_t bytes = (size_t)kRouterBM * (a.E + 1) * 4 + (size_t)kRouterBM * (kBK32 + 1) * 4 +
                    (size_t)kBK32 * a.E * 4 + (size_t)a.E * (kRouterBM / 32) * 4;
