@@ -6,9 +6,14 @@ computes the very same logits), so every routing decision agrees; with expert
 choice both choose on the GPU's own fp32 probabilities.  At the full workload
 sizes the oracle computes dx of sampled tokens one at a time (dL_aux = 0).  The GPU
 keeps several bf16 intermediates (dO, the pre-activations, H, dA, dU) like the
-forward keeps H, so each gradient tensor is checked by its relative Frobenius error
-(<= 1e-2; <= 2e-2 for every expert slab of a weight gradient), and dx and the
-router gradients also by max-abs error (<= 5e-2 RMS)."""
+forward keeps H.  Checks:
+- the expert-weight gradients (dW1, dW2, dW3, db1, db2) element by element,
+  |error| <= 2 x the first-order error that bf16 storage of those
+  intermediates and fp32 accumulation can put in the entry (see
+  expert_grad_bounds);
+- dx and the router gradients by max-abs error (<= 5e-2 RMS);
+- every gradient tensor also by its relative Frobenius error (<= 1e-2; <= 2e-2
+  for every expert slab of a weight gradient)."""
 import numpy as np
 import pytest
 import torch
@@ -35,6 +40,121 @@ CASES = [
 def _built():
     from sparse_mixture_experts_48_b300 import build
     build.build()
+
+
+# Element-wise bound on the expert-weight gradients: |error| <= 2 x the
+# first-order error that the GPU's storage and arithmetic can put in the entry
+# (expert_grad_bounds); the factor 2 covers second-order terms.
+EW_MARGIN = 2.0
+
+
+def expert_grad_bounds(cfg, inp, dy, groups):
+    """Per expert slab, the first-order worst-case error of each weight-gradient
+    entry, in fp64.  ``groups[g] = (tokens, weights)``: the token rows of slab g
+    and the gate weight of each (1 for shared experts).
+
+    The GPU keeps bf16 copies (relative error r = 2^-8 each) of dO = w dy, of
+    H and of the pre-activations a = x W1 + b1, u = x W3, and of dA and dU; its
+    dot products accumulate in fp32 (error <= n 2^-24 sum|terms| over n terms).
+    Propagated to first order, with S = |dO| |W2|^T and s = silu, g = gelu:
+      e_a = d 2^-24 |x||W1|,  e_u = d 2^-24 |x||W3|        (fp32 a, u)
+      E_a = r|a| + e_a,  E_u = r|u| + e_u                  (stored a, u)
+      E_H = r|H| + |dH/da| e_a + |dH/du| e_u               (stored H)
+      E_dH = (r + d 2^-24) S,  E_dO = r|dO|
+      SwiGLU: E_dA = r|dA| + E_dH|u s'| + |dH s'| E_u + |dH u s''| E_a
+              E_dU = r|dU| + E_dH|s| + |dH s'| E_a
+      GELU:   E_dA = r|dA| + E_dH|g'| + |dH g''| E_a
+      ReLU:   E_dA = r|dA| + E_dH [a > 0]
+    and dW2 = H^T dO, dW1 = X^T dA, dW3 = X^T dU, db1 = sum dA, db2 = sum dO:
+      |dW2 err| <= E_H^T |dO| + |H|^T E_dO,  |dW1 err| <= |X|^T E_dA,
+      |dW3 err| <= |X|^T E_dU,  |db1 err| <= sum E_dA,  |db2 err| <= sum E_dO,
+    each plus the fp32 accumulation over the slab's rows."""
+    import scipy.special as sp
+    r = 2.0 ** -8
+    x = si.as_f32(inp["x"]).astype(np.float64)
+    dyf = np.asarray(dy, np.float64)
+    W1 = si.as_f32(inp["W1"]).astype(np.float64)
+    W2 = si.as_f32(inp["W2"]).astype(np.float64)
+    W3 = si.as_f32(inp["W3"]).astype(np.float64) if inp["W3"] is not None else None
+    b1 = si.as_f32(inp["b1"]).astype(np.float64) if inp["b1"] is not None else None
+    G = len(groups)
+    f, d = cfg.f, cfg.d
+    gd = d * 2.0 ** -24
+    out = {"dW1": np.zeros((G, d, f)), "dW2": np.zeros((G, f, d)), "db1": np.zeros((G, f)), "db2": np.zeros((G, d))}
+    if cfg.act == si.SWIGLU:
+        out["dW3"] = np.zeros((G, d, f))
+    for g, (tt, w) in enumerate(groups):
+        if len(tt) == 0:
+            continue
+        n = len(tt)
+        ga = n * 2.0 ** -24                       # fp32 accumulation over the slab's rows
+        X = x[tt]
+        aX = np.abs(X)
+        dO = np.asarray(w, np.float64)[:, None] * dyf[tt]
+        a = X @ W1[g] + (b1[g] if b1 is not None else 0.0)
+        e_a = gd * (aX @ np.abs(W1[g]))
+        E_a = r * np.abs(a) + e_a
+        dH = dO @ W2[g].T
+        E_dH = (r + gd) * (np.abs(dO) @ np.abs(W2[g]).T)
+        if cfg.act == si.SWIGLU:
+            u = X @ W3[g]
+            e_u = gd * (aX @ np.abs(W3[g]))
+            E_u = r * np.abs(u) + e_u
+            sg = sp.expit(a)
+            s0 = a * sg
+            s1 = sg * (1 + a * (1 - sg))
+            s2 = sg * (1 - sg) * (2 + a * (1 - 2 * sg))
+            H = s0 * u
+            E_H = r * np.abs(H) + np.abs(s1 * u) * e_a + np.abs(s0) * e_u
+            dA, dU = dH * u * s1, dH * s0
+            E_dA = r * np.abs(dA) + E_dH * np.abs(u * s1) + np.abs(dH * s1) * E_u + np.abs(dH * u * s2) * E_a
+            E_dU = r * np.abs(dU) + E_dH * np.abs(s0) + np.abs(dH * s1) * E_a
+            out["dW3"][g] = aX.T @ E_dU + ga * (aX.T @ np.abs(dU))
+        elif cfg.act == si.GELU:
+            phi = np.exp(-0.5 * a * a) / np.sqrt(2 * np.pi)
+            g1 = 0.5 * sp.erfc(-a / np.sqrt(2)) + a * phi
+            g2 = phi * (2 - a * a)
+            H = a * 0.5 * sp.erfc(-a / np.sqrt(2))
+            E_H = r * np.abs(H) + np.abs(g1) * e_a
+            dA = dH * g1
+            E_dA = r * np.abs(dA) + E_dH * np.abs(g1) + np.abs(dH * g2) * E_a
+        else:
+            pos = (a > 0).astype(np.float64)
+            H = np.maximum(a, 0.0)
+            E_H = r * np.abs(H) + pos * e_a
+            dA = dH * pos
+            E_dA = r * np.abs(dA) + E_dH * pos
+        out["dW1"][g] = aX.T @ E_dA + ga * (aX.T @ np.abs(dA))
+        out["db1"][g] = E_dA.sum(axis=0) + ga * np.abs(dA).sum(axis=0)
+        out["dW2"][g] = E_H.T @ np.abs(dO) + r * (np.abs(H).T @ np.abs(dO)) + ga * (np.abs(H).T @ np.abs(dO))
+        out["db2"][g] = (r + ga) * np.abs(dO).sum(axis=0)
+    return out
+
+
+def token_choice_groups(cfg, routing):
+    idx, w, dropped = routing["topk_idx"], routing["topk_w"], routing["dropped"]
+    groups = []
+    for e in range(cfg.E):
+        tt, jj = np.nonzero((idx == e) & (dropped == 0))
+        groups.append((tt, w[tt, jj]))
+    for _ in range(cfg.S):
+        groups.append((np.arange(cfg.T), np.ones(cfg.T)))
+    return groups
+
+
+def check_expert_grads_elementwise(g, ref, bounds):
+    for name, eb in bounds.items():
+        got = getattr(g, name)
+        if got is None:
+            continue
+        got = got.cpu().numpy().astype(np.float64)
+        err = np.abs(got - ref[name])
+        rel = err / np.maximum(eb, 1e-300)
+        ratio = float(rel.max())
+        w = np.unravel_index(int(np.argmax(rel)), rel.shape)
+        print(f"{name}: max |error| / first-order bound = {ratio:.3e} (allowed {EW_MARGIN:.1f}) at "
+              f"{tuple(int(i) for i in w)}: got {got[w]:.6e} ref {ref[name][w]:.6e} bound {eb[w]:.3e}")
+        assert np.all(err <= EW_MARGIN * eb), f"{name}: max |error| / bound = {ratio:.3e} at {tuple(int(i) for i in w)}"
 
 
 def _close(name, got, ref, fro_tol=1e-2, max_tol=5e-2):
@@ -90,6 +210,8 @@ def test_backward_matches_oracle(label, base, over, noise):
             continue
         loose = name in ("dW_g", "db_g") and cfg.T < FEW_TOKENS
         _close(name, getattr(g, name), ref[name], *((5e-2, 2.5e-1) if loose else ()))
+    check_expert_grads_elementwise(g, ref, expert_grad_bounds(cfg, inp, si.as_f32(dy),
+                                                              token_choice_groups(cfg, ref["routing"])))
     if cfg.capacity_factor > 0:
         assert ref["routing"]["dropped"].sum() > 0
 
@@ -155,6 +277,10 @@ def test_expert_choice_backward_matches_oracle(label, base, over, noise):
         # the logit gradient p (dp - <p, dp>) cancels like the token-choice one
         loose = name in ("dW_g", "db_g") and cfg.T < FEW_TOKENS
         _close(name, getattr(g, name), ref[name], *((5e-2, 2.5e-1) if loose else ()))
+    # expert e's rows: its chosen tokens, weighted by the oracle's gate probabilities
+    groups = [(ref["perm"][e], ref["probs"][ref["perm"][e], e]) for e in range(cfg.E)]
+    groups += [(np.arange(cfg.T), np.ones(cfg.T)) for _ in range(cfg.S)]
+    check_expert_grads_elementwise(g, ref, expert_grad_bounds(cfg, inp, si.as_f32(dy), groups))
     if label.endswith("unchosen"):
         chosen = np.zeros(cfg.T, bool)
         chosen[np.unique(ref["perm"])] = True

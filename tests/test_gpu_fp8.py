@@ -15,10 +15,14 @@ the same codes:
 - the expert outputs O, within the fp32 accumulation's bound;
 - y, against the combine of those expert outputs (the bf16 bound).
 
-End to end, y is checked against the oracle's own FP8 layer (relative
-Frobenius error <= 5e-3: only the rare quantisation decisions that the fp32
-and fp64 paths take differently separate them) and against the unquantised
-layer (<= 8%, the bound derived from E4M3's precision)."""
+End to end, y is checked against the oracle's own FP8 layer element by
+element, with the bf16 layer's bound max|dy| <= 2e-2 RMS(y_ref) (with y
+stored in bf16, plus half a bf16 spacing at y_ref for its own rounding); only
+the rare quantisation decisions that the fp32 and fp64 paths take differently
+separate the two (an E4M3 step of one hidden element moves y by about 0.4% of
+RMS(y); measured at most 4.3e-4 with fp32 y).  Beside it: the relative
+Frobenius error <= 5e-3, and the unquantised layer within 8% (the bound
+derived from E4M3's precision)."""
 import numpy as np
 import pytest
 import torch
@@ -84,6 +88,15 @@ def row_expert(ref, cfg, r):
     return cfg.E + s, t
 
 
+def check_y_elementwise(y, yr, y_bf16):
+    """max|y - y_ref| <= 2e-2 RMS(y_ref) (+ half a bf16 spacing at y_ref when y is bf16)."""
+    rms = float(np.sqrt(np.mean(yr ** 2)))
+    bound = Y_TOL[si.BF16] * rms + (half_ulp_bf16(yr) * 1.01 if y_bf16 else 0.0)
+    dy = np.abs(y - yr)
+    print(f"FP8 y {'bf16' if y_bf16 else 'fp32'}: max|dy|/RMS = {dy.max() / rms:.3e}")
+    assert np.all(dy <= bound), f"max|dy|/RMS = {dy.max() / rms:.3e}"
+
+
 def check_layer(cfg, inp, ex, out, rows=None, stages=True):
     cfg8 = cfg.replace(fp8_experts=True)
     ref_route, gl, _ = check_routing(cfg8, inp, out)
@@ -128,6 +141,7 @@ def check_layer(cfg, inp, ex, out, rows=None, stages=True):
     yr = ref["y"]
     skipped = np.asarray(ref["dropped"])[rr].all(axis=1) if S == 0 else np.zeros(len(rr), bool)
     assert np.all(y[skipped] == 0.0)
+    check_y_elementwise(y, yr, out.y.dtype == torch.bfloat16)
     rel = float(np.linalg.norm(y - yr) / np.linalg.norm(yr))
     assert rel <= 5e-3, rel
     y16 = oracle.forward(cfg, inp, rows=rr, logits=gl)["y"]
@@ -136,11 +150,12 @@ def check_layer(cfg, inp, ex, out, rows=None, stages=True):
     return rel, rel16
 
 
+@pytest.mark.parametrize("y_f32", [False, True], ids=["y_bf16", "y_f32"])
 @pytest.mark.parametrize("label,base,over", CASES, ids=[c[0] for c in CASES])
-def test_fp8_layer(label, base, over):
+def test_fp8_layer(label, base, over, y_f32):
     cfg = si.CONFIGS[base].replace(**over)
     inp = si.layer_inputs(cfg, seed=31)
-    ex, out = run_fp8(cfg, inp)
+    ex, out = run_fp8(cfg, inp, y_f32=y_f32)
     check_layer(cfg, inp, ex, out)
     # y against the combine of the kernel's own expert outputs (bf16 bound)
     cfg8 = cfg.replace(fp8_experts=True)
@@ -158,7 +173,7 @@ def test_fp8_layer(label, base, over):
             yc[t] += O[T * k + s * T + t]
     y = to_host_f32(out.y).astype(np.float64)
     rms = float(np.sqrt(np.mean(yc ** 2)))
-    assert np.all(np.abs(y - yc) <= 1e-5 * rms + half_ulp_bf16(yc) * 1.01)
+    assert np.all(np.abs(y - yc) <= 1e-5 * rms + (half_ulp_bf16(yc) * 1.01 if not y_f32 else 0.0))
 
 
 def test_fp8_router_noise():
@@ -292,6 +307,7 @@ def test_fp8_expert_choice_layer(label, base, over):
     chosen[np.unique(ref["perm"])] = True
     skipped = ~chosen if S == 0 else np.zeros(T, bool)
     assert np.all(y[skipped] == 0.0)
+    check_y_elementwise(y, yr, out.y.dtype == torch.bfloat16)
     rel = float(np.linalg.norm(y - yr) / np.linalg.norm(yr))
     assert rel <= 5e-3, rel
     y16 = oracle.ec_forward(cfg, inp, scores=gs)["y"]
@@ -337,5 +353,6 @@ def test_fp8_expert_choice_full_size_sampled():
     assert np.array_equal(xp[sel], ref["xq"][perm[sel]]) and np.array_equal(xs[sel], ref["xs"][perm[sel]])
     y = to_host_f32(out.y)[rows].astype(np.float64)
     yr = ref["y"]
+    check_y_elementwise(y, yr, out.y.dtype == torch.bfloat16)
     rel = float(np.linalg.norm(y - yr) / np.linalg.norm(yr))
     assert rel <= 5e-3, rel
