@@ -1,7 +1,7 @@
 """Bench of the MoE-FFN forward layer on B300: tokens/s and grouped-GEMM TFLOPS.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--T TOKENS] [--no-cpu] [--no-e2e]
+                    [--workload NAME] [--T TOKENS] [--no-cpu] [--no-e2e] [--no-extra]
                     [--noise-std S] [--expert-choice] [--backward] [--fp8] [--gemm-one-cta] [--graph]
 
 A step is one whole forward pass of the layer (router, scan, gather, expert
@@ -9,6 +9,14 @@ GEMM 1, expert GEMM 2, combine) over one batch of T synthetic tokens.  The
 default workload is the Mixtral-shaped layer (T=16384, d=4096, f=14336, E=8,
 k=2, SwiGLU, bf16) on which the grouped-GEMM bar is stated.  Inputs are larger
 than L2 (x is 134 MB, expert weights 2.8 GB), so no L2 flush is done.
+
+The default run also times the four other workloads of the layer (the tiny
+fp32 top-1, GPT-2-width top-2 GELU, skewed top-2 with capacity, and
+DeepSeek-style fine-grained + shared experts) after the headline, one replica
+each, and reports them under other_workloads: tokens/s, per-kernel times and
+fractions, and the CUDA-graph replay.  The headline value, roofline and e2e
+stay on the Mixtral-shaped layer.  The roofline fraction is taken against the
+measured burst bf16 peak: the timed region lasts well under a second.
 
 --expert-choice, --fp8 (alone or together) and --backward time those variants
 of the step on the same workload; --graph adds the same forward replayed from
@@ -144,6 +152,34 @@ def measured_traffic(cfg, kernel: str, one_cta: bool):
     return None
 
 
+def measure_fp8_peak(dev, n: int = 8192, reps: int = 10):
+    """Dense E4M3 tensor throughput of the vendor library on this GPU: an
+    n x n x n cuBLASLt GEMM through torch._scaled_mm (per-tensor scales, bf16
+    output), best of `reps` after warm-up, in TFLOP/s.  None if unavailable."""
+    import torch
+    try:
+        a = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn).t()      # column-major
+        one = torch.ones((), device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best / 1e3) / 1e12
+    except (RuntimeError, AttributeError, TypeError):
+        return None
+
+
 # ---------------------------------------------------------------------------------------------
 # clocks during the timed region
 
@@ -215,7 +251,8 @@ class ClockSampler:
 
 def oracle_sample(cfg, inp, n_ffn_tokens: int, seed: int = 0):
     """Time the oracle on all T tokens' routing plus n tokens' expert FFNs;
-    return (seconds extrapolated to the full batch, description)."""
+    return (seconds extrapolated to the full batch, description, seconds the
+    sample took)."""
     import oracle
     oracle.build()
     t0 = time.perf_counter()
@@ -229,10 +266,17 @@ def oracle_sample(cfg, inp, n_ffn_tokens: int, seed: int = 0):
     total = t_route + t_ffn * cfg.T / n_ffn_tokens
     desc = (f"routing, dispatch and statistics of all {cfg.T} tokens ({t_route:.2f} s) + expert FFNs and "
             f"combine of {n_ffn_tokens} random tokens ({t_ffn:.2f} s), extrapolated linearly to {cfg.T} tokens")
-    return total, desc
+    return total, desc, t_route + t_ffn
 
 
-def ffn_sample_size(cfg, budget_s: float = 12.0) -> int:
+# One oracle sample: the FFNs of as many tokens as take about this long, beside
+# the routing of all T tokens.  The reference arm times K + W such samples and
+# the CPU baseline CPU_SAMPLES of them, so both legs time the same sample.
+SAMPLE_BUDGET_S = 2.0
+CPU_SAMPLES = 5
+
+
+def ffn_sample_size(cfg, budget_s: float = SAMPLE_BUDGET_S) -> int:
     # ~1.5 GMAC/s for the oracle's fp64 loops; per token (k + S) experts of m d f MACs
     per_tok = (cfg.k + cfg.S) * cfg.n_mats * cfg.d * cfg.f / 1.5e9
     return int(max(2, min(cfg.T, budget_s / max(per_tok, 1e-9))))
@@ -243,22 +287,27 @@ def run_reference(args, cfg):
     if rank != 0:
         return
     inp = si.layer_inputs(cfg, seed=0)
-    n = max(2, ffn_sample_size(cfg, budget_s=2.0))
-    times, descs = [], []
+    n = ffn_sample_size(cfg)
+    times, walls, descs = [], [], []
     for i in range(args.warmup + args.steps):
-        s, desc = oracle_sample(cfg, inp, n, seed=i)
+        s, desc, wall = oracle_sample(cfg, inp, n, seed=i)
         if i >= args.warmup:
             times.append(s)
+            walls.append(wall)
             descs.append(desc)
     sec = statistics.median(times)
     value = cfg.T / sec
+    # A step is one bounded sample (its measured wall time is ms_per_step);
+    # value is the full layer's tokens/s extrapolated from it.
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(walls) * 1e3,
+        "extrapolated_ms_per_full_batch": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "T": cfg.T, "parallelism": "single host thread"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": descs[0] + f"; median of {args.steps} samples"},
+                         "sample": descs[0] + f"; a step is this sample, value the median over {args.steps} "
+                                             f"steps extrapolated to the full batch"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -323,6 +372,183 @@ def run_backward(args, cfg, d, dev, world, rank, local):
 # ---------------------------------------------------------------------------------------------
 
 
+# ---------------------------------------------------------------------------------------------
+# one workload on the device: the timed loop, per-kernel times and fractions
+
+
+def measure(cfg, d, args_in, noise, experts8, args, dev, world, peaks, graph=False, barrier=None,
+            clock_ctx=None):
+    """Times args.steps forward steps after args.warmup warm-ups on device
+    buffers, with the library's stage events between its launches (on the
+    launching stream).  Returns the step time (max over ranks), per-kernel
+    times with their algorithmic GB/s or TFLOP/s and roofline fractions, and
+    the graph-replay time when ``graph``."""
+    import contextlib
+    import torch
+    import sparse_mixture_experts_48_b300 as moe
+    fp8 = experts8 is not None
+    out = moe.alloc_outputs(cfg, dev)
+    ws = moe.alloc_workspace(cfg, dev)
+    K, W = args.steps, args.warmup
+    n_ev = moe.NUM_STAGES + (2 if fp8 else 1)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K)]
+    one_cta = getattr(args, "gemm_one_cta", False)
+
+    def step(i=None):
+        if fp8:
+            moe.forward_fp8(cfg, d["x"], d["W_g"], d["b_g"], experts8, d["b1"], d["b2"], router_noise=noise,
+                            out=out, workspace=ws, stage_events=ev[i] if i is not None else None)
+        else:
+            moe.forward(cfg, *args_in, router_noise=noise, out=out, workspace=ws,
+                        stage_events=ev[i] if i is not None else None, gemm_single_cta=one_cta)
+
+    def sync_all():
+        torch.cuda.synchronize()
+        if barrier is not None:
+            barrier()
+
+    for _ in range(W):
+        step()
+    status = moe.check_device_errors(ws)
+    if status != 0:
+        raise SystemExit(f"device error during warm-up: {moe.STATUS.get(status)}")
+    sync_all()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with (clock_ctx if clock_ctx is not None else contextlib.nullcontext()):
+        t_start.record()
+        for i in range(K):
+            step(i)
+        t_end.record()
+        torch.cuda.synchronize()
+    if barrier is not None:
+        barrier()
+    status = moe.check_device_errors(ws)
+    if status != 0:
+        raise SystemExit(f"device error in the timed region: {moe.STATUS.get(status)}")
+    ms_step = max_over_ranks(t_start.elapsed_time(t_end), dev, world) / K
+
+    # per-kernel durations from the stage events; with FP8 experts event
+    # NUM_STAGES + 1 splits GEMM 1 -> GEMM 2 into the H quantisation and GEMM 2
+    names = list(moe.STAGE_NAMES)
+    spans = [(s, s + 1) for s in range(moe.NUM_STAGES)]
+    if fp8:
+        g2 = names.index("expert_gemm2")
+        q = moe.NUM_STAGES + 1
+        spans[g2] = (q, g2 + 1)
+        spans.append((g2, q))
+        names.append("quantize_h")
+    stage_ms = np.array([[ev[i][a].elapsed_time(ev[i][b]) for a, b in spans] for i in range(K)])
+    stage_avg = stage_ms.mean(axis=0)
+    rows_A = int(out.expert_counts.sum().item()) + cfg.S * cfg.T
+    alg = algorithmic(cfg, rows_A)
+    hbm = float(peaks["hbm_gbs"])
+    tc_burst = float(peaks["bf16_tflops"])
+    tc_sust = float(peaks.get("bf16_tflops_sustained", tc_burst))
+    tc_tag = "bf16"
+    if fp8:
+        # E4M3 tensor-core peak: a cuBLASLt E4M3 GEMM measured in this run
+        # (peaks["fp8_tflops"]) when there is one, else the measured bf16
+        # figures times the nominal dense ratio 4.5 / 2.25 PFLOP/s
+        if peaks.get("fp8_tflops"):
+            tc_burst = float(peaks["fp8_tflops"])
+            tc_sust = tc_burst * (tc_sust / float(peaks["bf16_tflops"]))
+        else:
+            tc_burst, tc_sust = 2.0 * tc_burst, 2.0 * tc_sust
+        tc_tag = "fp8"
+    kernels = {name: {"ms": round(float(stage_avg[s]), 5)} for s, name in enumerate(names)}
+    hbm_kernels = [("router", "router_bytes"), ("gather", "gather_bytes"), ("combine", "combine_bytes")]
+    if fp8:
+        hbm_kernels.append(("quantize_h", "quantize_h_bytes"))
+    for name, key in hbm_kernels:
+        gbs = alg[key] / (stage_avg[names.index(name)] / 1e3) / 1e9
+        kernels[name].update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4), "bytes": alg[key]})
+    if "scan" in names:
+        # dispatch as a whole: from the router's end to the gather's end
+        disp_ms = stage_avg[names.index("scan")] + stage_avg[names.index("gather")]
+        gbs = alg["gather_bytes"] / (disp_ms / 1e3) / 1e9
+        kernels["dispatch"] = {"ms": round(float(disp_ms), 5), "GB/s": round(gbs, 1),
+                               "frac_hbm": round(gbs / hbm, 4), "bytes": alg["gather_bytes"],
+                               "spans": "scan + gather"}
+    bf16_path = cfg.dtype == si.BF16
+    for name, key in (("expert_gemm1", "gemm1_flop"), ("expert_gemm2", "gemm2_flop")):
+        tf = alg[key] / (stage_avg[names.index(name)] / 1e3) / 1e12
+        kernels[name].update({"TFLOP/s": round(tf, 1), "flop": alg[key]})
+        if bf16_path:
+            kernels[name].update({f"frac_{tc_tag}_burst": round(tf / tc_burst, 4),
+                                  f"frac_{tc_tag}_sustained": round(tf / tc_sust, 4)})
+    gemm_ms = stage_avg[names.index("expert_gemm1")] + stage_avg[names.index("expert_gemm2")]
+    if fp8:
+        gemm_ms += stage_avg[names.index("quantize_h")]
+    gemm_tf = (alg["gemm1_flop"] + alg["gemm2_flop"]) / (gemm_ms / 1e3) / 1e12
+    grouped = {"tflops": round(gemm_tf, 1), "ms": round(float(gemm_ms), 4)}
+    if bf16_path:
+        grouped.update({f"frac_of_{tc_tag}_burst": round(gemm_tf / tc_burst, 4),
+                        f"frac_of_{tc_tag}_sustained": round(gemm_tf / tc_sust, 4)})
+
+    # The same step captured once in a CUDA graph and replayed: no host-side
+    # launch work per step (what bounds small layers).
+    gres = None
+    if graph:
+        if fp8:
+            fg = moe.ForwardGraph(cfg, d["x"], d["W_g"], d["b_g"], experts=experts8, router_noise=noise)
+        else:
+            fg = moe.ForwardGraph(cfg, *args_in, router_noise=noise, gemm_single_cta=one_cta)
+        for _ in range(W):
+            fg.replay()
+        sync_all()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(K):
+            fg.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        st = moe.check_device_errors(fg.out.workspace)
+        if st != 0:
+            raise SystemExit(f"device error in the graph loop: {moe.STATUS.get(st)}")
+        g_ms = max_over_ranks(g0.elapsed_time(g1) / K, dev, world)
+        gres = {"value": replica_throughput(cfg.T, g_ms, world), "unit": "tokens/s", "ms_per_step": g_ms}
+        del fg
+    return {"out": out, "ws": ws, "ms_step": ms_step, "kernels": kernels, "grouped_gemm": grouped,
+            "graph": gres, "tc_burst": tc_burst, "tc_sust": tc_sust, "rows_A": rows_A,
+            "launches_per_step": moe.NUM_STAGES + (1 if fp8 else 0) + (1 if getattr(cfg, "expert_choice", False)
+                                                                        else 0)
+            + (1 if fp8 and getattr(cfg, "expert_choice", False) else 0)}
+
+
+def other_configs(args, dev, peaks):
+    """The other workloads of the layer in the same run (one replica): per
+    workload tokens/s, per-kernel times and fractions, and the CUDA-graph
+    replay (what bounds the small, launch-bound layers)."""
+    import torch
+    res = {}
+    for name in si.CONFIG_ORDER:
+        if name == DEFAULT_WORKLOAD:
+            continue
+        cfg = si.CONFIGS[name]
+        inp = si.layer_inputs(cfg, seed=0)
+
+        def to_dev(a):
+            if a is None:
+                return None
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+            return torch.from_numpy(a).to(dev)
+
+        d = {k: to_dev(v) for k, v in inp.items()}
+        args_in = [d[n] for n in ("x", "W_g", "b_g", "W1", "b1", "W2", "b2", "W3")]
+        r = measure(cfg, d, args_in, None, None, args, dev, 1, peaks, graph=True)
+        res[name] = {"workload": workload_desc(cfg), "value": cfg.T / (r["ms_step"] / 1e3), "unit": "tokens/s",
+                     "ms_per_step": r["ms_step"], "graph": r["graph"], "grouped_gemm": r["grouped_gemm"],
+                     "kernels": r["kernels"], "rows_A": r["rows_A"],
+                     "l2": "x %.1f MB, expert weights %.1f MB" % (
+                         inp["x"].nbytes / 1e6, sum(inp[n].nbytes for n in ("W1", "W2", "W3")
+                                                    if inp[n] is not None) / 1e6)}
+        del d, args_in, r
+        torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -333,6 +559,8 @@ def main():
     ap.add_argument("--T", type=int, default=0, help="override the token count (profiling runs)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads (reported under other_workloads by the default run)")
     ap.add_argument("--noise-std", type=float, default=0.0,
                     help="add seeded Gaussian router noise of this std before gating and top-k (0: none)")
     ap.add_argument("--expert-choice", action="store_true",
@@ -395,129 +623,53 @@ def main():
     noise = to_dev(si.router_noise(cfg, seed=rank, std=args.noise_std)) if args.noise_std > 0 else None
     if args.backward:
         return run_backward(args, cfg, d, dev, world, rank, local)
-    out = moe.alloc_outputs(cfg, dev)
-    ws = moe.alloc_workspace(cfg, dev)
-    stream = torch.cuda.current_stream()
-    K, W = args.steps, args.warmup
-    fp8 = args.fp8
-    n_ev = moe.NUM_STAGES + (2 if fp8 else 1)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K)]
-    experts8 = moe.quantize_experts_fp8(d["W1"], d["W2"], d["W3"]) if fp8 else None
-    if fp8:
+    experts8 = moe.quantize_experts_fp8(d["W1"], d["W2"], d["W3"]) if args.fp8 else None
+    if args.fp8:
         # the layer keeps only the E4M3 codes and scales of the expert weights
         torch.cuda.synchronize()
         for n in ("W1", "W2", "W3"):
             d[n] = None
         args_in = None
         torch.cuda.empty_cache()
-
-    def step(i=None):
-        if fp8:
-            moe.forward_fp8(cfg, d["x"], d["W_g"], d["b_g"], experts8, d["b1"], d["b2"], router_noise=noise,
-                            out=out, workspace=ws, stage_events=ev[i] if i is not None else None)
-        else:
-            moe.forward(cfg, *args_in, router_noise=noise, out=out, workspace=ws,
-                        stage_events=ev[i] if i is not None else None, gemm_single_cta=args.gemm_one_cta)
-
-    for _ in range(W):
-        step()
-    status = moe.check_device_errors(ws)
-    if status != 0:
-        raise SystemExit(f"device error during warm-up: {moe.STATUS.get(status)}")
+    peaks, peak_kind = load_peaks()
+    if args.fp8:
+        fp8_peak = measure_fp8_peak(dev)
+        if fp8_peak:
+            peaks = dict(peaks, fp8_tflops=fp8_peak)
+    K, W = args.steps, args.warmup
 
     def barrier():
         if world > 1:
             dist.barrier()
 
-    torch.cuda.synchronize()
-    barrier()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        t_start.record()
-        for i in range(K):
-            step(i)
-        t_end.record()
-        torch.cuda.synchronize()
-    barrier()
-    status = moe.check_device_errors(ws)
-    if status != 0:
-        raise SystemExit(f"device error in the timed region: {moe.STATUS.get(status)}")
-    ms_total = t_start.elapsed_time(t_end)
-    ms_total = max_over_ranks(ms_total, dev, world)
-    ms_step = ms_total / K
+    clocks = ClockSampler(local)
+    res = measure(cfg, d, args_in, noise, experts8, args, dev, world, peaks, graph=args.graph,
+                  barrier=(dist.barrier if world > 1 else None), clock_ctx=clocks)
+    out = res["out"]
+    ms_step = res["ms_step"]
     value = replica_throughput(cfg.T, ms_step, world)
-
-    # per-kernel durations from the stage events (on the launching stream);
-    # with FP8 experts event 7 splits [4, 5) into the H quantisation and GEMM 2
-    if fp8:
-        spans = [(0, 1), (1, 2), (2, 3), (3, 4), (7, 5), (5, 6), (4, 7)]
-        names = list(moe.STAGE_NAMES) + ["quantize_h"]
-    else:
-        spans = [(s, s + 1) for s in range(moe.NUM_STAGES)]
-        names = list(moe.STAGE_NAMES)
-    stage_ms = np.array([[ev[i][a].elapsed_time(ev[i][b]) for a, b in spans] for i in range(K)])
-    stage_avg = stage_ms.mean(axis=0)
-    rows_A = int(out.expert_counts.sum().item()) + cfg.S * cfg.T
-    alg = algorithmic(cfg, rows_A)
-    peaks, peak_kind = load_peaks()
-    hbm = float(peaks["hbm_gbs"])
-    tc_burst = float(peaks["bf16_tflops"])
-    tc_sust = float(peaks.get("bf16_tflops_sustained", tc_burst))
-    tc_tag = "bf16"
-    if fp8:
-        # E4M3 tensor-core peak: the measured bf16 figures times the nominal
-        # dense ratio 4.5 / 2.25 PFLOP/s
-        tc_burst, tc_sust, tc_tag = 2.0 * tc_burst, 2.0 * tc_sust, "fp8"
-    kernels = {}
-    for s, name in enumerate(names):
-        kernels[name] = {"ms": round(float(stage_avg[s]), 5)}
-    hbm_kernels = [("router", "router_bytes"), ("gather", "gather_bytes"), ("combine", "combine_bytes")]
-    if fp8:
-        hbm_kernels.append(("quantize_h", "quantize_h_bytes"))
-    for name, key in hbm_kernels:
-        gbs = alg[key] / (stage_avg[names.index(name)] / 1e3) / 1e9
-        kernels[name].update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4), "bytes": alg[key]})
-    for name, key in (("expert_gemm1", "gemm1_flop"), ("expert_gemm2", "gemm2_flop")):
-        tf = alg[key] / (stage_avg[names.index(name)] / 1e3) / 1e12
-        kernels[name].update({"TFLOP/s": round(tf, 1), f"frac_{tc_tag}_sustained": round(tf / tc_sust, 4),
-                              f"frac_{tc_tag}_burst": round(tf / tc_burst, 4), "flop": alg[key]})
-    gemm_ms = stage_avg[3] + stage_avg[4]
-    gemm_tf = (alg["gemm1_flop"] + alg["gemm2_flop"]) / (gemm_ms / 1e3) / 1e12
+    kernels = res["kernels"]
+    fp8 = args.fp8
     dom = "expert_gemm1"
+    tc_tag = "fp8" if fp8 else "bf16"
     dom_tf = kernels[dom]["TFLOP/s"]
+    tc_burst, tc_sust = res["tc_burst"], res["tc_sust"]
     traffic = measured_traffic(cfg, dom + ("_fp8" if fp8 else ""), args.gemm_one_cta)
-    src = ("measured bf16_tflops_sustained x 2 (nominal E4M3 / bf16 dense ratio)" if fp8 else
-           "measured bf16_tflops_sustained (cuBLAS bf16, back to back)")
+    if fp8 and peaks.get("fp8_tflops"):
+        src = ("cuBLASLt E4M3 GEMM 8192^3 (torch._scaled_mm, per-tensor scales, bf16 out) measured in this run: "
+               "best of 10, burst")
+    elif fp8:
+        src = "measured bf16_tflops x 2 (burst; nominal E4M3 / bf16 dense ratio)"
+    else:
+        src = "measured bf16_tflops (cuBLAS bf16 burst: the timed region is well under a second)"
     if peak_kind != "measured":
         src = src.replace("measured", "fallback")
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": tc_sust, "unit": "TFLOP/s",
-                "frac": round(dom_tf / tc_sust, 4), "traffic": traffic, "peak_source": src,
-                "frac_of_burst_peak": round(dom_tf / tc_burst, 4)}
-
-    # The same step captured once in a CUDA graph and replayed: no host-side
-    # launch work per step (what bounds small layers).
-    graph = None
-    if args.graph:
-        if fp8:
-            fg = moe.ForwardGraph(cfg, d["x"], d["W_g"], d["b_g"], experts=experts8, router_noise=noise)
-        else:
-            fg = moe.ForwardGraph(cfg, *args_in, router_noise=noise, gemm_single_cta=args.gemm_one_cta)
-        for _ in range(W):
-            fg.replay()
-        torch.cuda.synchronize()
-        barrier()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record()
-        for _ in range(K):
-            fg.replay()
-        g1.record()
-        torch.cuda.synchronize()
-        st = moe.check_device_errors(fg.out.workspace)
-        if st != 0:
-            raise SystemExit(f"device error in the graph loop: {moe.STATUS.get(st)}")
-        g_ms = max_over_ranks(g0.elapsed_time(g1) / K, dev, world)
-        graph = {"value": replica_throughput(cfg.T, g_ms, world), "unit": "tokens/s", "ms_per_step": g_ms}
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": tc_burst, "unit": "TFLOP/s",
+                "frac": round(dom_tf / tc_burst, 4), "traffic": traffic, "peak_source": src,
+                "frac_of_sustained_peak": round(dom_tf / tc_sust, 4),
+                "timed_region_s": round(ms_step * args.steps / 1e3, 3)}
+    graph = res["graph"]
+    grouped = res["grouped_gemm"]
 
     # End to end through the public API with host buffers (moe_forward_host):
     # every step copies its x from page-locked host memory in and all outputs
@@ -576,9 +728,19 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu:
         n = ffn_sample_size(cfg)
-        sec, desc = oracle_sample(cfg, inp, n)
+        runs = [oracle_sample(cfg, inp, n, seed=i) for i in range(CPU_SAMPLES)]
+        sec = statistics.median(r[0] for r in runs)
         cpu = {"value": cfg.T / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": desc + f"; single thread of {os.cpu_count()} host cores"}
+               "sample": runs[0][1] + f"; median of {CPU_SAMPLES} such samples "
+                                      f"({sum(r[2] for r in runs):.1f} s of CPU work); single thread of "
+                                      f"{os.cpu_count()} host cores"}
+
+    # The other workloads, on rank 0, after the headline's timed region: the
+    # default run reports every workload of the layer.
+    others = None
+    if (rank == 0 and not args.no_extra and args.workload == DEFAULT_WORKLOAD and not args.T and not fp8
+            and not args.expert_choice and not args.gemm_one_cta and args.noise_std == 0):
+        others = other_configs(args, dev, peaks)
 
     if rank == 0:
         line = {
@@ -596,18 +758,17 @@ def main():
                        "l2": "no flush: inputs larger than L2 (x %.0f MB, expert weights %.2f GB)" % (
                            inp["x"].nbytes / 1e6, sum(inp[n].nbytes for n in ("W1", "W2", "W3")
                                                       if inp[n] is not None) / (2e9 if fp8 else 1e9))},
-            "grouped_gemm": {"tflops": round(gemm_tf, 1), f"frac_of_{tc_tag}_sustained": round(gemm_tf / tc_sust, 4),
-                             f"frac_of_{tc_tag}_burst": round(gemm_tf / tc_burst, 4), "ms": round(float(gemm_ms), 4)},
+            "grouped_gemm": grouped,
             "roofline": roofline,
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "graph": graph,
-            # router, scan, gather, GEMM 1, GEMM 2, combine; + the H quantisation with FP8
+            "other_workloads": others,
+            # one launch per stage (STAGE_NAMES); + the H quantisation with FP8
             # experts; + the per-expert selection with expert choice (+ x's quantisation
             # per token with both)
-            "gpu_launches": (moe.NUM_STAGES + (1 if fp8 else 0) + (1 if args.expert_choice else 0)
-                             + (1 if fp8 and args.expert_choice else 0)) * K,
+            "gpu_launches": res["launches_per_step"] * K,
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)
