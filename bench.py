@@ -463,13 +463,13 @@ def measure(cfg, d, args_in, noise, experts8, args, dev, world, peaks, graph=Fal
     for name, key in hbm_kernels:
         gbs = alg[key] / (stage_avg[names.index(name)] / 1e3) / 1e9
         kernels[name].update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4), "bytes": alg[key]})
-    if "scan" in names:
-        # dispatch as a whole: from the router's end to the gather's end
-        disp_ms = stage_avg[names.index("scan")] + stage_avg[names.index("gather")]
-        gbs = alg["gather_bytes"] / (disp_ms / 1e3) / 1e9
-        kernels["dispatch"] = {"ms": round(float(disp_ms), 5), "GB/s": round(gbs, 1),
-                               "frac_hbm": round(gbs / hbm, 4), "bytes": alg["gather_bytes"],
-                               "spans": "scan + gather"}
+    # dispatch as a whole: from the router's end (its last CTA has run the
+    # scan) to the gather's end
+    disp_ms = stage_avg[names.index("select")] + stage_avg[names.index("gather")]
+    gbs = alg["gather_bytes"] / (disp_ms / 1e3) / 1e9
+    kernels["dispatch"] = {"ms": round(float(disp_ms), 5), "GB/s": round(gbs, 1),
+                           "frac_hbm": round(gbs / hbm, 4), "bytes": alg["gather_bytes"],
+                           "spans": "router end to gather end (select + gather stages)"}
     bf16_path = cfg.dtype == si.BF16
     for name, key in (("expert_gemm1", "gemm1_flop"), ("expert_gemm2", "gemm2_flop")):
         tf = alg[key] / (stage_avg[names.index(name)] / 1e3) / 1e12
@@ -511,8 +511,11 @@ def measure(cfg, d, args_in, noise, experts8, args, dev, world, peaks, graph=Fal
         del fg
     return {"out": out, "ws": ws, "ms_step": ms_step, "kernels": kernels, "grouped_gemm": grouped,
             "graph": gres, "tc_burst": tc_burst, "tc_sust": tc_sust, "rows_A": rows_A,
-            "launches_per_step": moe.NUM_STAGES + (1 if fp8 else 0) + (1 if getattr(cfg, "expert_choice", False)
-                                                                        else 0)
+            # router (with the dispatch scan in its last CTA), gather, GEMM 1,
+            # GEMM 2, combine; + the H quantisation with FP8 experts; + the
+            # per-expert selection with expert choice (+ x's quantisation per
+            # token with both)
+            "launches_per_step": 5 + (1 if fp8 else 0) + (1 if getattr(cfg, "expert_choice", False) else 0)
             + (1 if fp8 and getattr(cfg, "expert_choice", False) else 0)}
 
 
@@ -765,9 +768,6 @@ def main():
             "e2e": e2e,
             "graph": graph,
             "other_workloads": others,
-            # one launch per stage (STAGE_NAMES); + the H quantisation with FP8
-            # experts; + the per-expert selection with expert choice (+ x's quantisation
-            # per token with both)
             "gpu_launches": res["launches_per_step"] * K,
             "clocks": clocks.summary(),
         }

@@ -79,10 +79,12 @@ enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID_NORM = 1 };
 enum { MOE_ACT_RELU = 0, MOE_ACT_GELU = 1, MOE_ACT_SWIGLU = 2, MOE_ACT_NONE = 3 };
 enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 };
 
-/* Stages of moe_forward that stage events bracket: router, scan, gather,
- * expert GEMM 1, expert GEMM 2, combine (one kernel each; with expert choice
- * the scan stage also holds the per-expert selection, and with FP8 experts the
- * gather stage the per-token quantisation of x). */
+/* Stages of moe_forward that stage events bracket: router, select, gather,
+ * expert GEMM 1, expert GEMM 2, combine.  The router stage includes the
+ * dispatch scan (ranks, capacity, offsets, statistics), which its last CTA
+ * runs; the select stage holds the per-expert selection with expert choice
+ * and is empty otherwise; with FP8 experts the gather stage also holds the
+ * per-token quantisation of x. */
 #define MOE_NUM_STAGES 6
 
 /* The layer.  64 bytes, natural alignment. */

@@ -34,7 +34,7 @@ REGION_XPERM, REGION_X_SCALE, REGION_H, REGION_H_CODES, REGION_H_SCALE, REGION_O
 SOFTMAX, SIGMOID_NORM = 0, 1
 F32, BF16 = 0, 1
 NUM_STAGES = 6
-STAGE_NAMES = ("router", "scan", "gather", "expert_gemm1", "expert_gemm2", "combine")
+STAGE_NAMES = ("router", "select", "gather", "expert_gemm1", "expert_gemm2", "combine")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE"}

@@ -42,9 +42,11 @@ static_assert(kRouterBM == 16 * kRowBlocks, "one m16 row block per MMA warp of a
 // ---- the per-token tail shared by both dtypes ----------------------------------
 // sl: [BM][ldl] fp32 logits without bias, rows of this CTA's BM tokens.
 // bits: [E][BM / 32] scratch words.  The kTPT = 4 threads 4i..4i+3 (one warp)
-// own token i: thread q adds the bias, gates and keeps a sorted top-k of the
-// experts e = q mod 4, then the lists are merged in two butterfly rounds, so
-// all four threads end with the same k experts.  Needs blockDim >= kTPT * BM.
+// own token i; thread q holds the experts e = q mod 4.  Top-k is k rounds of a
+// quad argmax: each thread's largest not-yet-taken logit (lower index on a
+// tie), merged over the quad with two shuffle rounds, so all four threads pick
+// the same expert in the same round (k (E/4 + 4) steps per thread instead of
+// an insertion of every expert into a sorted list).  Needs blockDim >= kTPT * BM.
 template <int BM>
 __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const RouterArgs& a, int64_t blk) {
   static_assert(BM % 32 == 0 && BM <= 256, "local ranks are uint8");
@@ -62,20 +64,6 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
   int idx[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) { val[j] = 0.f; idx[j] = -1; }
-  // Keeps (val, idx) sorted: larger logit first, equal logits by lower index.
-  auto insert = [&](float cv, int ci) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < k) {
-        const bool better = idx[j] < 0 || cv > val[j] || (cv == val[j] && ci < idx[j]);
-        if (better) {
-          const float tv = val[j]; const int ti = idx[j];
-          val[j] = cv; idx[j] = ci;
-          cv = tv; ci = ti;
-        }
-      }
-    }
-  };
   if (tid < kTPT * BM) {            // whole warps: the shuffles see every thread of each quad
     float* l = sl + tok * ldl;
     const bool bf = a.dtype == MOE_DT_BF16;
@@ -87,23 +75,32 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
         if (a.noise) l[e] += a.noise[t * E + e];   // noisy scores: everything below uses them
         if (a.logits_out && !a.scores_em) a.logits_out[t * E + e] = l[e];
         if (a.raw_logits) a.raw_logits[t * E + e] = l[e];
-        insert(l[e], e);                           // (expert choice uses only the maximum, val[0])
       }
     }
-    // Butterfly merge: take the partner's whole list, then insert it
-    // (inserting while exchanging would read a half-merged list).
-#pragma unroll
-    for (int m = 1; m < kTPT; m <<= 1) {
-      float pv[8];
-      int pi[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        pv[j] = __shfl_xor_sync(0xffffffffu, val[j], m);
-        pi[j] = __shfl_xor_sync(0xffffffffu, idx[j], m);
+    // k rounds of the quad argmax (expert choice uses only the maximum, val[0]).
+    uint64_t taken = 0;             // bit i: expert q + 4 i already chosen (E <= 256)
+    const int kr = a.scores_em ? 1 : k;
+#pragma unroll 1
+    for (int j = 0; j < kr; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      if (valid) {
+        for (int e = q, i = 0; e < E; e += kTPT, ++i) {
+          const float v = l[e];
+          // experts ascend within the thread: a strict > keeps the lower index
+          if (!((taken >> i) & 1ull) && (v > bv || bi == 0x7fffffff)) { bv = v; bi = e; }
+        }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < k && pi[j] >= 0) insert(pv[j], pi[j]);
+      for (int m = 1; m < kTPT; m <<= 1) {
+        const float pv = __shfl_xor_sync(0xffffffffu, bv, m);
+        const int pi = __shfl_xor_sync(0xffffffffu, bi, m);
+        if (pv > bv || (pv == bv && pi < bi)) { bv = pv; bi = pi; }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        if (jj == j) { val[jj] = bv; idx[jj] = bi; }
+      if (valid && (bi % kTPT) == q) taken |= 1ull << (bi / kTPT);
     }
     // Gating over all E (these p feed P), and the renormalised top-k weights.
     float z = 0.f;
