@@ -86,28 +86,43 @@ struct Ctl {
 
 // fp32 outputs (expert GEMM 2) stage each epilogue warp's 32 x 32 tile in
 // shared memory for a TMA store: 4 KB per warp, paid for with one ring stage.
+// bf16 outputs (expert GEMM 1: H) stage their 32 x 32 tile the same way (2 KB
+// per warp, which still fits beside the six ring stages): per-thread 16-byte
+// stores put 32 rows in one store instruction and stall the epilogue on the
+// LSU queue, which costs time whenever the main loop of a tile is short.
 // SAVE_PRE (the backward's recomputed GEMM 1) stages its three bf16 32 x 32
-// tiles (H, pre_a, pre_u: 2 KB each) the same way.
+// tiles (H, pre_a, pre_u: 2 KB each).
+#ifndef MOE_STAGE_BF16_OUT
+#define MOE_STAGE_BF16_OUT 1
+#endif
+constexpr bool kStageBf16Out = MOE_STAGE_BF16_OUT != 0;
 constexpr int kStageTileBytes = 32 * 32 * 4;
 constexpr int kStageBf16Bytes = 32 * 32 * 2;
-// The FP8 GEMM 1 (bf16 H out) stages its H tile too: its main loop per tile is
-// half the bf16 one's, so per-thread stores would weigh twice as much.
 template <bool OUT_F32, bool SAVE_PRE, bool FP8>
 constexpr int warp_stage_bytes() {
-  return OUT_F32 ? kStageTileBytes : SAVE_PRE ? 3 * kStageBf16Bytes : FP8 ? kStageBf16Bytes : 0;
+  return OUT_F32 ? kStageTileBytes
+                 : SAVE_PRE ? 3 * kStageBf16Bytes : (FP8 || kStageBf16Out) ? kStageBf16Bytes : 0;
 }
 template <bool OUT_F32, bool SAVE_PRE, bool FP8>
-constexpr int ring_stages() { return warp_stage_bytes<OUT_F32, SAVE_PRE, FP8>() ? STAGES - 1 : STAGES; }
-template <bool OUT_F32, bool SAVE_PRE, bool FP8>
-constexpr size_t smem_bytes() {
-  return 1024 + (size_t)ring_stages<OUT_F32, SAVE_PRE, FP8>() * STAGE_BYTES + sizeof(Ctl) +
+constexpr size_t smem_for(int stages) {
+  return 1024 + (size_t)stages * STAGE_BYTES + sizeof(Ctl) +
          (warp_stage_bytes<OUT_F32, SAVE_PRE, FP8>()
               ? 1024 + (size_t)EPI_WARPS * warp_stage_bytes<OUT_F32, SAVE_PRE, FP8>()
               : 0);
 }
+// As many ring stages (up to STAGES) as fit beside the staging tiles.
+template <bool OUT_F32, bool SAVE_PRE, bool FP8>
+constexpr int ring_stages() {
+  return smem_for<OUT_F32, SAVE_PRE, FP8>(STAGES) <= 227 * 1024 ? STAGES : STAGES - 1;
+}
+template <bool OUT_F32, bool SAVE_PRE, bool FP8>
+constexpr size_t smem_bytes() {
+  return smem_for<OUT_F32, SAVE_PRE, FP8>(ring_stages<OUT_F32, SAVE_PRE, FP8>());
+}
 static_assert(smem_bytes<false, false, false>() <= 227 * 1024 && smem_bytes<true, false, false>() <= 227 * 1024 &&
                   smem_bytes<false, true, false>() <= 227 * 1024 && smem_bytes<false, false, true>() <= 227 * 1024,
               "shared memory per CTA");
+static_assert(!kStageBf16Out || ring_stages<false, false, false>() == STAGES, "bf16 staging keeps six stages");
 
 // 16 packed bf16 pairs (one thread's 32 columns) into row `lane` of a 32 x 32
 // bf16 staging tile laid out with the 64-byte swizzle: 16-byte chunk j at
@@ -173,7 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                      const __grid_constant__ CUtensorMap tmU, GemmArgs a) {
   constexpr int BN_OUT = SWIGLU ? 128 : 256;   // output columns per pair tile
   constexpr int NST = ring_stages<OUT_F32, SAVE_PRE, FP8>();
-  constexpr bool STAGE_H = !OUT_F32 && (SAVE_PRE || FP8);   // bf16 H leaves by TMA store
+  constexpr bool STAGE_H = !OUT_F32 && (SAVE_PRE || FP8 || kStageBf16Out);   // bf16 H leaves by TMA store
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;            // 1 KB aligned ring for the 128-byte swizzle
@@ -568,7 +583,7 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtenso
     ok_maps = ok_maps && tmap_bf16_2d_swizzle(&mC, a.C, a.rows_C, a.N, 32, 32, 64) &&
               tmap_bf16_2d_swizzle(&mP, a.pre_a, a.rows_C, a.N, 32, 32, 64) &&
               (!SWIGLU || tmap_bf16_2d_swizzle(&mU, a.pre_u, a.rows_C, a.N, 32, 32, 64));
-  } else if (FP8) {
+  } else if (FP8 || kStageBf16Out) {
     ok_maps = ok_maps && tmap_bf16_2d_swizzle(&mC, a.C, a.rows_C, a.N, 32, 32, 64);
   } else {
     ok_maps = false;

@@ -270,6 +270,7 @@ moe_status launch_grouped_gemm_on_scratch(int32_t dtype, int32_t act, int32_t G,
   g.dtype = dtype; g.act = act; g.G = G; g.K = K; g.N = N; g.a_from_out_rows = true; g.seg = seg;
   g.A0 = A; g.rows_A0 = M > 0 ? M : 1; g.A1 = nullptr; g.B = B; g.B3 = B3; g.Gw = G; g.bias = bias; g.C = C;
   g.max_mtiles = M > 0 ? (M + kGemmBM - 1) / kGemmBM + G : 0;
+  g.rows_C = M;               // whole 32-row warp tiles inside a group leave by TMA store
   g.err = &hdr->err;
   g.timeout_ns = (opts && opts->wait_timeout_ns > 0) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
   g.single_cta = opts && (opts->flags & MOE_OPT_GEMM_SINGLE_CTA);
@@ -448,12 +449,12 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   g1.B = W1; g1.B3 = W3; g1.Gw = L.G; g1.bias = b1; g1.C = ws + L.h; g1.max_mtiles = c.T > 0 ? max_mtiles : 0;
   g1.err = &hdr->err; g1.timeout_ns = timeout;
   g1.single_cta = opts && (opts->flags & MOE_OPT_GEMM_SINGLE_CTA);
+  g1.rows_C = L.rows_all;     // H leaves by TMA store (whole 32-row warp tiles)
   if (fp8) {
     g1.fp8 = true;
     g1.A1 = sh8 ? ws + L.xq : nullptr;
     g1.a_scale0 = (const float*)(ws + L.xs_perm); g1.a_scale1 = sh8 ? (const float*)(ws + L.xs_tok) : nullptr;
     g1.B = q8->W1; g1.B3 = q8->W3; g1.b_scale = q8->s1; g1.b3_scale = q8->s3;
-    g1.rows_C = L.rows_all;
   }
   if (clk.mark(3) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_grouped_gemm(g1, s) != cudaSuccess) return MOE_ERR_CUDA;
