@@ -58,8 +58,16 @@ constexpr int B_BOX_BYTES = 64 * BK * 2;        // 8 KB: 64 columns x 64 k
 constexpr int B_BYTES = 2 * B_BOX_BYTES;        // 16 KB: this CTA's 128 columns
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
 constexpr uint32_t kPairStageTx = 2u * STAGE_BYTES;
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 8;                   // epilogue warps (16 for wide-epilogue bf16 outputs)
 constexpr int THREADS = 64 + EPI_WARPS * 32;
+// bf16-output GEMMs with K up to this take 16 epilogue warps (5 ring stages):
+// a short main loop per tile leaves the epilogue (bias, activation, store of
+// 256 columns) as the longer half of the overlap, and twice the warps hide
+// its latencies.  Longer K keep 8 epilogue warps and 6 stages.
+#ifndef MOE_WIDE_EPI_MAX_K
+#define MOE_WIDE_EPI_MAX_K 1024
+#endif
+constexpr int kWideEpiMaxK = MOE_WIDE_EPI_MAX_K;
 constexpr int TMEM_COLS = 512;                  // two 256-column accumulators
 constexpr int MAX_G = 264;
 constexpr uint32_t kWhere = 0x400;
@@ -103,26 +111,27 @@ constexpr int warp_stage_bytes() {
   return OUT_F32 ? kStageTileBytes
                  : SAVE_PRE ? 3 * kStageBf16Bytes : (FP8 || kStageBf16Out) ? kStageBf16Bytes : 0;
 }
-template <bool OUT_F32, bool SAVE_PRE, bool FP8>
+template <bool OUT_F32, bool SAVE_PRE, bool FP8, int EPI = EPI_WARPS>
 constexpr size_t smem_for(int stages) {
   return 1024 + (size_t)stages * STAGE_BYTES + sizeof(Ctl) +
          (warp_stage_bytes<OUT_F32, SAVE_PRE, FP8>()
-              ? 1024 + (size_t)EPI_WARPS * warp_stage_bytes<OUT_F32, SAVE_PRE, FP8>()
+              ? 1024 + (size_t)EPI * warp_stage_bytes<OUT_F32, SAVE_PRE, FP8>()
               : 0);
 }
 // As many ring stages (up to STAGES) as fit beside the staging tiles.
-template <bool OUT_F32, bool SAVE_PRE, bool FP8>
+template <bool OUT_F32, bool SAVE_PRE, bool FP8, int EPI = EPI_WARPS>
 constexpr int ring_stages() {
-  return smem_for<OUT_F32, SAVE_PRE, FP8>(STAGES) <= 227 * 1024 ? STAGES : STAGES - 1;
+  return smem_for<OUT_F32, SAVE_PRE, FP8, EPI>(STAGES) <= 227 * 1024 ? STAGES : STAGES - 1;
 }
-template <bool OUT_F32, bool SAVE_PRE, bool FP8>
+template <bool OUT_F32, bool SAVE_PRE, bool FP8, int EPI = EPI_WARPS>
 constexpr size_t smem_bytes() {
-  return smem_for<OUT_F32, SAVE_PRE, FP8>(ring_stages<OUT_F32, SAVE_PRE, FP8>());
+  return smem_for<OUT_F32, SAVE_PRE, FP8, EPI>(ring_stages<OUT_F32, SAVE_PRE, FP8, EPI>());
 }
 static_assert(smem_bytes<false, false, false>() <= 227 * 1024 && smem_bytes<true, false, false>() <= 227 * 1024 &&
                   smem_bytes<false, true, false>() <= 227 * 1024 && smem_bytes<false, false, true>() <= 227 * 1024,
               "shared memory per CTA");
 static_assert(!kStageBf16Out || ring_stages<false, false, false>() == STAGES, "bf16 staging keeps six stages");
+static_assert(smem_bytes<false, false, false, 16>() <= 227 * 1024, "shared memory per CTA, 16 epilogue warps");
 
 // 16 packed bf16 pairs (one thread's 32 columns) into row `lane` of a 32 x 32
 // bf16 staging tile laid out with the 64-byte swizzle: 16-byte chunk j at
@@ -180,14 +189,14 @@ __device__ __forceinline__ void scale_acc32(uint32_t (&v)[32], float ra, const f
 // SAVE_PRE (expert GEMM 1 of the backward pass's forward recomputation): the
 // pre-activations a = x W1 + b1 (and u = x W3 for SwiGLU) are also stored, in
 // bf16, at the output's rows and columns (a.pre_a, a.pre_u).
-template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE, bool FP8 = false>
-__global__ void __launch_bounds__(THREADS, 1)
+template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE, bool FP8 = false, int EPI = EPI_WARPS>
+__global__ void __launch_bounds__(64 + EPI * 32, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3,
                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
                      const __grid_constant__ CUtensorMap tmU, GemmArgs a) {
   constexpr int BN_OUT = SWIGLU ? 128 : 256;   // output columns per pair tile
-  constexpr int NST = ring_stages<OUT_F32, SAVE_PRE, FP8>();
+  constexpr int NST = ring_stages<OUT_F32, SAVE_PRE, FP8, EPI>();
   constexpr bool STAGE_H = !OUT_F32 && (SAVE_PRE || FP8 || kStageBf16Out);   // bf16 H leaves by TMA store
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -247,7 +256,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&c.tfull[s]), 1);
-      mbar_init(smem_u32(&c.tempty[s]), 2 * EPI_WARPS);
+      mbar_init(smem_u32(&c.tempty[s]), 2 * EPI);
     }
     mbar_init(smem_u32(&c.done), 1);
     c.abort = 0u;
@@ -380,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ---------------- epilogue (both CTAs) ----------------
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;       // which half of the tile's columns
+    const int part = (warp - 2) >> 2;       // which share of the tile's columns (EPI / 4 shares)
     const int row = q * 32 + lane;
     const uint32_t tempty_leader = mapa_shared(smem_u32(&c.tempty[0]), 0);
     int it = 0;
@@ -410,7 +419,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool tma_st = (OUT_F32 || STAGE_H) && a.rows_C > 0 && wrow0 + 31 < c.rows[g];
       const uint32_t wbuf = stg + (uint32_t)((warp - 2) * warp_stage_bytes<OUT_F32, SAVE_PRE, FP8>());
       constexpr int CHUNKS = BN_OUT / 32;   // 32-column chunks per tile
-      for (int ch = half * (CHUNKS / 2); ch < (half + 1) * (CHUNKS / 2); ++ch) {
+      constexpr int PER = CHUNKS / (EPI / 4);
+      for (int ch = part * PER; ch < (part + 1) * PER; ++ch) {
         const int col0 = n0 + ch * 32;
         uint32_t v[32];
         tmem_ld32(tbase + (uint32_t)(ch * 32), v);
@@ -567,11 +577,11 @@ bool map_weights(CUtensorMap* m, const void* ptr, int G, int K, int N) {
   return tmap_bf16_3d(m, ptr, G, K, N, 64, BK);
 }
 
-template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE = false, bool FP8 = false>
+template <bool SWIGLU, bool OUT_F32, bool SAVE_PRE = false, bool FP8 = false, int EPI = EPI_WARPS>
 cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtensorMap& mA1, const CUtensorMap& mB,
                         const CUtensorMap& mB3, int64_t max_pair_tiles, cudaStream_t s) {
-  auto kernel = gemm_pair_kernel<SWIGLU, OUT_F32, SAVE_PRE, FP8>;
-  constexpr size_t kSmemBytes = smem_bytes<OUT_F32, SAVE_PRE, FP8>();
+  auto kernel = gemm_pair_kernel<SWIGLU, OUT_F32, SAVE_PRE, FP8, EPI>;
+  constexpr size_t kSmemBytes = smem_bytes<OUT_F32, SAVE_PRE, FP8, EPI>();
   // C (fp32), or H and the pre-activations (bf16, 64-byte rows), as tensor maps
   // for the TMA-store epilogue (else unused copies of A's)
   CUtensorMap mC = mA0, mP = mA0, mU = mA0;
@@ -596,7 +606,7 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtenso
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.blockDim = dim3(64 + EPI * 32, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -678,10 +688,14 @@ cudaError_t launch_grouped_gemm_pair(const GemmArgs& a, cudaStream_t s) {
     e = launch_pair<true, false, true>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
   else if (a.pre_a)
     e = launch_pair<false, false, true>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
+  else if (swiglu && a.K <= kWideEpiMaxK)
+    e = launch_pair<true, false, false, false, 16>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
   else if (swiglu)
     e = launch_pair<true, false>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
   else if (a.out_f32)
     e = launch_pair<false, true>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
+  else if (a.K <= kWideEpiMaxK)
+    e = launch_pair<false, false, false, false, 16>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
   else
     e = launch_pair<false, false>(a, mA0, mA1, mB, mB3, max_pair_tiles, s);
   if (e != cudaSuccess) return e;

@@ -22,6 +22,7 @@ constexpr int BM = kGemmBM;   // 128 rows: the tile grid of the segment table
 constexpr int BN = 64;
 constexpr int BK = 16;
 constexpr int kThreads = 256; // 16 x 16 threads, each 8 rows x 4 columns
+static_assert(BM * BK % kThreads == 0 && BK * BN % kThreads == 0, "whole slices per thread");
 
 __device__ __forceinline__ float act_f32(int act, float v) {
   if (act == MOE_ACT_RELU) return v > 0.f ? v : 0.f;
@@ -66,19 +67,44 @@ __global__ void __launch_bounds__(kThreads) gemm_f32_kernel(GemmArgs a) {
       if (SWIGLU) acc3[i][j] = 0.f;
     }
 
-  for (int k0 = 0; k0 < K; k0 += BK) {
-    for (int i = threadIdx.x; i < BM * BK; i += kThreads) {
+  // Software pipelined over k: the next k-slice's A and B elements are
+  // loaded into registers while the current slice in shared memory is
+  // multiplied, so a k-step costs its FMAs rather than a load round trip.
+  constexpr int AE = BM * BK / kThreads;   // A elements per thread per slice (8)
+  constexpr int BE = BK * BN / kThreads;   // B elements per thread per slice (4)
+  float ra[AE], rb[BE], rb3[SWIGLU ? BE : 1];
+  auto load_slice = [&](int k0) {
+#pragma unroll
+    for (int u = 0; u < AE; ++u) {
+      const int i = threadIdx.x + u * kThreads;
       const int r = i / BK, c = i % BK;
       const bool ok = m0 + r < rows && k0 + c < K;
-      As[c][r] = ok ? A[(int64_t)(arow + m0 + r) * K + k0 + c] : 0.f;
+      ra[u] = ok ? A[(int64_t)(arow + m0 + r) * K + k0 + c] : 0.f;
     }
-    for (int i = threadIdx.x; i < BK * BN; i += kThreads) {
+#pragma unroll
+    for (int u = 0; u < BE; ++u) {
+      const int i = threadIdx.x + u * kThreads;
       const int r = i / BN, c = i % BN;
       const bool ok = k0 + r < K && n0 + c < N;
-      Bs[r][c] = ok ? B[(int64_t)(k0 + r) * N + n0 + c] : 0.f;
-      if (SWIGLU) B3s[r][c] = ok ? B3[(int64_t)(k0 + r) * N + n0 + c] : 0.f;
+      rb[u] = ok ? B[(int64_t)(k0 + r) * N + n0 + c] : 0.f;
+      if (SWIGLU) rb3[u] = ok ? B3[(int64_t)(k0 + r) * N + n0 + c] : 0.f;
+    }
+  };
+  load_slice(0);
+  for (int k0 = 0; k0 < K; k0 += BK) {
+#pragma unroll
+    for (int u = 0; u < AE; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      As[i % BK][i / BK] = ra[u];
+    }
+#pragma unroll
+    for (int u = 0; u < BE; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      Bs[i / BN][i % BN] = rb[u];
+      if (SWIGLU) B3s[i / BN][i % BN] = rb3[u];
     }
     __syncthreads();
+    if (k0 + BK < K) load_slice(k0 + BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float av[8], bv[4], b3v[4];
