@@ -428,7 +428,8 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   memset(&ga, 0, sizeof(ga));
   ga.x = x; ga.T = c.T; ga.d = c.d_model; ga.E = c.E; ga.k = c.k; ga.dtype = c.dtype; ga.capacity = C;
   ga.topk_idx = topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.offsets = sa.offsets; ga.slot = slot_buf;
-  ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm; ga.err = &hdr->err; ga.nblk = L.nblk; ga.bm = ra.bm;
+  ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm; ga.err = &hdr->err;
+  ga.nblk = L.nblk; ga.bm = ra.bm;
   const bool sh8 = fp8 && c.n_shared > 0;
   if (fp8) {
     ga.fp8 = true;
@@ -707,14 +708,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
     ra.scores_em = (float*)(ws + L.ec_scores); ra.logits_out = nullptr; ra.raw_logits = (float*)(ws + L.logits);
     if (cudaMemsetAsync(ws + L.ec_bits, 0, (size_t)T * L.EW * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  if (launch_router(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (ec) {
-    EcSelectArgs ea;
-    ea.scores_em = (const float*)(ws + L.ec_scores); ea.T = T; ea.C = L.ec_C; ea.Cs = L.ec_Cs; ea.E = E;
-    ea.EW = L.EW; ea.perm = (int32_t*)(ws + L.ec_perm); ea.w_row = (float*)(ws + L.ec_wrow);
-    ea.tok_row = (int32_t*)(ws + L.ec_tokrow); ea.bits = (uint32_t*)(ws + L.ec_bits); ea.err = &hdr->err;
-    if (launch_ec_select(ea, s) != cudaSuccess) return MOE_ERR_CUDA;
-  }
+  // The scan (padded segments) runs in the router's last CTA.
   ScanArgs sa;
   memset(&sa, 0, sizeof(sa));
   sa.T = T; sa.E = E; sa.k = k; sa.S = S; sa.capacity = ec ? -1 : C; sa.alpha = c.alpha; sa.nblk = L.nblk;
@@ -724,11 +718,22 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const void* W_g, c
   sa.offsets = (int32_t*)(ws + L.offsets); sa.f = (float*)(ws + L.f); sa.P = (float*)(ws + L.P);
   sa.L_aux = (float*)(ws + L.L); sa.route_stats = nullptr; sa.seg = seg; sa.rows_tk = L.rows_routed;
   sa.err = &hdr->err;
-  if (launch_scan(sa, s) != cudaSuccess) return MOE_ERR_CUDA;
+  ra.fused_scan = true;
+  ra.scan = sa;
+  ra.done = &hdr->router_done;
+  if (launch_router(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ec) {
+    EcSelectArgs ea;
+    ea.scores_em = (const float*)(ws + L.ec_scores); ea.T = T; ea.C = L.ec_C; ea.Cs = L.ec_Cs; ea.E = E;
+    ea.EW = L.EW; ea.perm = (int32_t*)(ws + L.ec_perm); ea.w_row = (float*)(ws + L.ec_wrow);
+    ea.tok_row = (int32_t*)(ws + L.ec_tokrow); ea.bits = (uint32_t*)(ws + L.ec_bits); ea.err = &hdr->err;
+    if (launch_ec_select(ea, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   GatherArgs ga;
   memset(&ga, 0, sizeof(ga));
   ga.x = x; ga.T = T; ga.d = d; ga.E = E; ga.k = k; ga.dtype = c.dtype; ga.capacity = C;
-  ga.topk_idx = ra.topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.nblk = L.nblk; ga.bm = ra.bm; ga.offsets = sa.offsets;
+  ga.topk_idx = ra.topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.nblk = L.nblk; ga.bm = ra.bm;
+  ga.offsets = sa.offsets;
   ga.slot = (int32_t*)(ws + L.slot); ga.dropped = ws + L.drop; ga.perm_token = nullptr; ga.xperm = ws + L.xperm;
   ga.err = &hdr->err;
   if (ec) {
