@@ -57,6 +57,9 @@ EDGE = [
     ("k_equals_E", "gpt2_top2_gelu_bf16", dict(T=130, E=4, k=4, d=256, f=512)),
     ("E_not_multiple_of_8", "gpt2_top2_gelu_bf16", dict(T=200, E=5, k=3, d=256, f=256)),
     ("max_E_and_k", "deepseek_shared_sigmoid_bf16", dict(T=150, E=256, k=8, S=1, d=256, f=192)),
+    # the tcgen05 router's other widths: N = 128 and N = 192 experts per MMA
+    ("E_128_tcgen05_router", "deepseek_shared_sigmoid_bf16", dict(T=300, E=128, k=4, S=0, d=256, f=128)),
+    ("E_192_softmax_tcgen05_router", "gpt2_top2_gelu_bf16", dict(T=270, E=192, k=8, d=320, f=128)),
     ("capacity_one", "skew_capacity_gelu_bf16", dict(T=100, E=16, k=2, d=256, f=256, capacity_factor=0.1)),
     ("sigmoid_top1_capacity", "deepseek_shared_sigmoid_bf16",
      dict(T=333, E=8, k=1, S=1, d=256, f=128, capacity_factor=1.0, router_bias=True, router_bias_std=1.0)),
