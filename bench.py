@@ -427,13 +427,43 @@ def measure(cfg, d, args_in, noise, experts8, args, dev, world, peaks, graph=Fal
         torch.cuda.synchronize()
     if barrier is not None:
         barrier()
+    status = moe.check_device_errors(ws)
+    if status != 0:
+        raise SystemExit(f"device error in the timed region: {moe.STATUS.get(status)}")
+    ms_step = max_over_ranks(t_start.elapsed_time(t_end), dev, world) / K
+
+    # The same step captured once in a CUDA graph and replayed: no host-side
+    # launch work per step (what bounds small layers).
+    gres = None
+    if graph:
+        if fp8:
+            fg = moe.ForwardGraph(cfg, d["x"], d["W_g"], d["b_g"], experts=experts8, router_noise=noise)
+        else:
+            fg = moe.ForwardGraph(cfg, *args_in, router_noise=noise, gemm_single_cta=one_cta)
+        for _ in range(W):
+            fg.replay()
+        sync_all()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(K):
+            fg.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        st = moe.check_device_errors(fg.out.workspace)
+        if st != 0:
+            raise SystemExit(f"device error in the graph loop: {moe.STATUS.get(st)}")
+        g_ms = max_over_ranks(g0.elapsed_time(g1) / K, dev, world)
+        gres = {"value": replica_throughput(cfg.T, g_ms, world), "unit": "tokens/s", "ms_per_step": g_ms}
+        del fg
+    # The per-kernel breakdown: K more calls that record the stage events
+    # (after the plain calls and the graph replays, so that neither carries
+    # the events' cost).
     for i in range(K):
         step(i)
     torch.cuda.synchronize()
     status = moe.check_device_errors(ws)
     if status != 0:
-        raise SystemExit(f"device error in the timed region: {moe.STATUS.get(status)}")
-    ms_step = max_over_ranks(t_start.elapsed_time(t_end), dev, world) / K
+        raise SystemExit(f"device error in the stage-event calls: {moe.STATUS.get(status)}")
 
     # per-kernel durations from the stage events; with FP8 experts event
     # NUM_STAGES + 1 splits GEMM 1 -> GEMM 2 into the H quantisation and GEMM 2
@@ -493,29 +523,6 @@ def measure(cfg, d, args_in, noise, experts8, args, dev, world, peaks, graph=Fal
         grouped.update({f"frac_of_{tc_tag}_burst": round(gemm_tf / tc_burst, 4),
                         f"frac_of_{tc_tag}_sustained": round(gemm_tf / tc_sust, 4)})
 
-    # The same step captured once in a CUDA graph and replayed: no host-side
-    # launch work per step (what bounds small layers).
-    gres = None
-    if graph:
-        if fp8:
-            fg = moe.ForwardGraph(cfg, d["x"], d["W_g"], d["b_g"], experts=experts8, router_noise=noise)
-        else:
-            fg = moe.ForwardGraph(cfg, *args_in, router_noise=noise, gemm_single_cta=one_cta)
-        for _ in range(W):
-            fg.replay()
-        sync_all()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record()
-        for _ in range(K):
-            fg.replay()
-        g1.record()
-        torch.cuda.synchronize()
-        st = moe.check_device_errors(fg.out.workspace)
-        if st != 0:
-            raise SystemExit(f"device error in the graph loop: {moe.STATUS.get(st)}")
-        g_ms = max_over_ranks(g0.elapsed_time(g1) / K, dev, world)
-        gres = {"value": replica_throughput(cfg.T, g_ms, world), "unit": "tokens/s", "ms_per_step": g_ms}
-        del fg
     return {"out": out, "ws": ws, "ms_step": ms_step, "kernels": kernels, "grouped_gemm": grouped,
             "graph": gres, "tc_burst": tc_burst, "tc_sust": tc_sust, "rows_A": rows_A,
             # router (with the dispatch scan in its last CTA), gather, GEMM 1,
