@@ -31,7 +31,7 @@ constexpr int kScanThreads = 256;
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   __shared__ int s_npre[scan_detail::kMaxE];
   __shared__ float s_psum[scan_detail::kMaxE];
-  scan_detail::scan_body<4, 8>(a, s_npre, s_psum);
+  scan_detail::scan_body<4, 8>(a, s_npre, s_psum, threadIdx.x / 32, blockDim.x / 32, false);
 }
 
 constexpr int kGatherWarps = 8;

@@ -32,70 +32,106 @@ namespace {
 
 constexpr int kRowBlocks = 4;                         // m16 row blocks of a CTA's 64 tokens
 constexpr int kMmaWarps = 2 * kRowBlocks;             // x 2 k-groups (even / odd k-tiles)
-constexpr int kThreadsBf16 = (kMmaWarps + 1) * 32;    // + the producer warp
+constexpr int kWarmTailWarp = kMmaWarps + 1;          // after the producer warp: dry tail pass
+constexpr int kWarmScanWarp = kMmaWarps + 2;          // dry scan pass
+constexpr int kThreadsBf16 = (kMmaWarps + 3) * 32;    // MMA warps, producer, two warm-up warps
+constexpr int kTailThreadsBf16 = kThreadsBf16 - 32;   // all but the scan warm-up warp (the last)
+constexpr int kDryTokens = 8;                         // tokens of a dry tail pass (one warp)
 constexpr int kThreadsF32 = 256;
 constexpr int kTPT = 4;                               // threads per token in the tail
 constexpr int kBK = 64;                               // bf16 k-tile (128 bytes per x row)
 constexpr uint32_t kWhereRouter = 0x300;
 static_assert(kRouterBM == 16 * kRowBlocks, "one m16 row block per MMA warp of a k-group");
 
+// Named barrier 1 over the `count` threads running the tail (a multiple of 32;
+// the whole CTA except, in the mma.sync router, its scan warm-up warp).
+__device__ __forceinline__ void tail_sync(int count) { asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory"); }
+__device__ __forceinline__ bool tail_sync_or(int count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(count)
+      : "memory");
+  return r != 0u;
+}
+
 // ---- the per-token tail shared by both dtypes ----------------------------------
 // sl: [BM][ldl] fp32 logits without bias, rows of this CTA's BM tokens.
-// bits: [E][BM / 32] scratch words.  The kTPT = 4 threads 4i..4i+3 (one warp)
-// own token i; thread q holds the experts e = q mod 4.  Top-k is k rounds of a
-// quad argmax: each thread's largest not-yet-taken logit (lower index on a
-// tie), merged over the quad with two shuffle rounds, so all four threads pick
-// the same expert in the same round (k (E/4 + 4) steps per thread instead of
-// an insertion of every expert into a sorted list).  Needs blockDim >= kTPT * BM.
-template <int BM>
-__device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const RouterArgs& a, int64_t blk) {
+// bits: [E][BM / 32] scratch words.  Threads with virtual ids 4i..4i+3 (one
+// warp) own token i; thread q holds the experts e = q + 4 j, j < EPT, in
+// registers.  Top-k is k rounds of a quad argmax: each thread's largest
+// not-yet-taken logit (lower index on a tie), merged over the quad with two
+// shuffle rounds, so all four threads pick the same expert in the same round.
+//
+// vt / nvt: this thread's id among the nvt threads running the tail (threads
+// 0 .. nvt - 1 of the CTA, nvt >= 4 BM, synchronised by tail_sync).  dry: one warp (vt = lane, nvt = 32) runs the same
+// code on the first 8 tokens while the CTA still streams x, writing only its
+// own scratch (sl, bits) and nothing in global memory.  The tail runs once per
+// CTA, so on a cold instruction cache its time is the fetch of its code (the
+// expert GEMMs' weights have pushed it out of L2 since the previous call);
+// the dry pass fetches it in the shadow of the stream.  Each kernel calls it
+// from one place only, inside a two-pass loop (dry, then real), so that both
+// passes run the same instructions.
+template <int BM, int EPT>
+__device__ __forceinline__ void router_finalize(float* sl, int ldl, uint32_t* bits, const RouterArgs& a,
+                                             int64_t blk, int vt, int nvt, bool dry) {
   static_assert(BM % 32 == 0 && BM <= 256, "local ranks are uint8");
+  static_assert(EPT >= 1 && EPT <= 64, "taken bits are one uint64_t");
   constexpr int NW = BM / 32;
-  const int tid = threadIdx.x;
   const int E = a.E, k = a.k;
   const int64_t t0 = blk * BM;
-  for (int i = tid; i < E * NW; i += blockDim.x) bits[i] = 0u;
-  __syncthreads();
+  for (int i = vt; i < E * NW; i += nvt) bits[i] = 0u;
+  if (dry) __syncwarp(); else tail_sync(nvt);
 
-  const int tok = tid / kTPT, q = tid % kTPT;
+  const int tok = vt / kTPT, q = vt % kTPT;
   const int64_t t = t0 + tok;
-  const bool valid = tid < kTPT * BM && t < a.T;
+  const bool valid = vt < kTPT * BM && t < a.T && (!dry || tok < 8);
+  const bool wr = valid && !dry;   // global writes
   float val[8];
   int idx[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) { val[j] = 0.f; idx[j] = -1; }
-  if (tid < kTPT * BM) {            // whole warps: the shuffles see every thread of each quad
+  if (vt < kTPT * BM) {            // whole warps: the shuffles see every thread of each quad
     float* l = sl + tok * ldl;
     const bool bf = a.dtype == MOE_DT_BF16;
-    if (valid) {
-      for (int e = q; e < E; e += kTPT) {
-        float b = 0.f;
-        if (a.bg) b = bf ? bf16_bits_to_f32(((const uint16_t*)a.bg)[e]) : ((const float*)a.bg)[e];
-        l[e] += b;
-        if (a.noise) l[e] += a.noise[t * E + e];   // noisy scores: everything below uses them
-        if (a.logits_out && !a.scores_em) a.logits_out[t * E + e] = l[e];
-        if (a.raw_logits) a.raw_logits[t * E + e] = l[e];
+    float v[EPT];
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) {
+      const int e = q + kTPT * i;
+      v[i] = 0.f;
+      if (valid && e < E) {
+        float x = l[e];
+        if (dry) x = 0.f;   // the dry pass's scratch rows hold no logits
+        if (a.bg) x += bf ? bf16_bits_to_f32(((const uint16_t*)a.bg)[e]) : ((const float*)a.bg)[e];
+        if (a.noise) x += a.noise[t * E + e];   // noisy scores: everything below uses them
+        v[i] = x;
+        if (wr && a.logits_out && !a.scores_em) a.logits_out[t * E + e] = x;
+        if (wr && a.raw_logits) a.raw_logits[t * E + e] = x;
       }
     }
     // k rounds of the quad argmax (expert choice uses only the maximum, val[0]).
-    uint64_t taken = 0;             // bit i: expert q + 4 i already chosen (E <= 256)
+    uint64_t taken = 0;             // bit i: expert q + 4 i already chosen
     const int kr = a.scores_em ? 1 : k;
 #pragma unroll 1
     for (int j = 0; j < kr; ++j) {
       float bv = -INFINITY;
       int bi = 0x7fffffff;
       if (valid) {
-        for (int e = q, i = 0; e < E; e += kTPT, ++i) {
-          const float v = l[e];
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+          const int e = q + kTPT * i;
           // experts ascend within the thread: a strict > keeps the lower index
-          if (!((taken >> i) & 1ull) && (v > bv || bi == 0x7fffffff)) { bv = v; bi = e; }
+          if (e < E && !((taken >> i) & 1ull) && (v[i] > bv || bi == 0x7fffffff)) { bv = v[i]; bi = e; }
         }
       }
 #pragma unroll
       for (int m = 1; m < kTPT; m <<= 1) {
         const float pv = __shfl_xor_sync(0xffffffffu, bv, m);
         const int pi = __shfl_xor_sync(0xffffffffu, bi, m);
-        if (pv > bv || (pv == bv && pi < bi)) { bv = pv; bi = pi; }
+        // A thread with no candidate left (bi unset) takes its partner's; a
+        // NaN logit never replaces a candidate nor leaves an index unset.
+        if (bi == 0x7fffffff || (pi != 0x7fffffff && (pv > bv || (pv == bv && pi < bi)))) { bv = pv; bi = pi; }
       }
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj)
@@ -105,11 +141,15 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
     // Gating over all E (these p feed P), and the renormalised top-k weights.
     float z = 0.f;
     if (valid) {
-      if (a.gating == MOE_GATE_SOFTMAX) {
-        const float mx = val[0];
-        for (int e = q; e < E; e += kTPT) { const float v = expf(l[e] - mx); l[e] = v; z += v; }
-      } else {
-        for (int e = q; e < E; e += kTPT) { const float v = 1.f / (1.f + expf(-l[e])); l[e] = v; z += v; }
+      const bool sm = a.gating == MOE_GATE_SOFTMAX;
+      const float mx = val[0];
+#pragma unroll
+      for (int i = 0; i < EPT; ++i) {
+        if (q + kTPT * i < E) {
+          const float p = sm ? expf(v[i] - mx) : 1.f / (1.f + expf(-v[i]));
+          v[i] = p;
+          z += p;
+        }
       }
     }
     // The same total on every thread of the quad: (z0 + z1) + (z2 + z3), each
@@ -121,14 +161,20 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
     }
     if (valid) {
       const float rz = 1.f / z;
-      for (int e = q; e < E; e += kTPT) l[e] *= rz;
-      if (a.scores_em) {
-        // Expert choice: the experts choose on these gate probabilities.
-        for (int e = q; e < E; e += kTPT) {
-          a.scores_em[(int64_t)e * a.T + t] = l[e];
-          if (a.logits_out) a.logits_out[t * E + e] = l[e];
+#pragma unroll
+      for (int i = 0; i < EPT; ++i) {
+        const int e = q + kTPT * i;
+        if (e < E) {
+          const float p = v[i] * rz;
+          l[e] = p;
+          if (wr && a.scores_em) {
+            // Expert choice: the experts choose on these gate probabilities.
+            a.scores_em[(int64_t)e * a.T + t] = p;
+            if (a.logits_out) a.logits_out[t * E + e] = p;
+          }
         }
-      } else if (q == 0) {
+      }
+      if (!a.scores_em && q == 0) {
         float g[8], zsel = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -140,16 +186,18 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (j < k) {
-            a.topk_idx[t * k + j] = idx[j];
-            a.topk_w[t * k + j] = g[j] / zsel;
+            if (wr) {
+              a.topk_idx[t * k + j] = idx[j];
+              a.topk_w[t * k + j] = g[j] / zsel;
+            }
             atomicOr(&bits[idx[j] * NW + tok / 32], 1u << (tok % 32));
           }
         }
       }
     }
   }
-  __syncthreads();
-  if (valid && q == 0) {
+  if (dry) __syncwarp(); else tail_sync(nvt);
+  if (valid && q == 0 && !a.scores_em) {
     const int w = tok / 32;
     const uint32_t below = (1u << (tok % 32)) - 1u;
 #pragma unroll
@@ -158,21 +206,21 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
         const uint32_t* be = bits + idx[j] * NW;
         int r = __popc(be[w] & below);
         for (int qq = 0; qq < w; ++qq) r += __popc(be[qq]);
-        a.lrank[t * k + j] = (uint8_t)r;
+        if (wr) a.lrank[t * k + j] = (uint8_t)r;
       }
     }
   }
   // Per expert: selections (popc of the bit masks) and the sum of gate
   // probabilities over the CTA's tokens, one warp per expert: lane l adds
-  // rows l and l + 32, then a fixed xor-tree over the lanes.
-  const int nvalid = (int)(a.T - t0 < BM ? a.T - t0 : BM);
-  const int lane = tid % 32, nwarps = blockDim.x / 32;
-  for (int e = tid / 32; e < E; e += nwarps) {
+  // rows l, l + 32, ..., then a fixed xor-tree over the lanes.
+  const int nvalid = dry ? 8 : (int)(a.T - t0 < BM ? a.T - t0 : BM);
+  const int lane = vt % 32, nwarps = nvt / 32;
+  for (int e = vt / 32; e < (dry ? 1 : E); e += nwarps) {
     float s = 0.f;
     for (int r = lane; r < nvalid; r += 32) s += sl[r * ldl + e];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) {
+    if (lane == 0 && !dry) {
       int h = 0;
       for (int qq = 0; qq < NW; ++qq) h += __popc(bits[e * NW + qq]);
       a.hist[e * a.nblk + blk] = h;
@@ -187,18 +235,27 @@ __device__ void router_finalize(float* sl, int ldl, uint32_t* bits, const Router
 // stopped CTA still takes its ticket, so the scan always runs (and, seeing the
 // status word set, publishes empty segments).  `scratch`: shared memory no
 // longer in use, at least 2 KB.
-__device__ void router_retire(const RouterArgs& a, uint8_t* scratch) {
+// dry: one warp runs the scan's dry pass instead (no ticket, no global
+// writes; `scratch` its own 2 KB), fetching the scan's code while x streams:
+// any CTA may be the last to finish.  Each kernel calls this from one place.
+// warp / nwarps: this warp's part of the scan (the real pass: every warp of
+// the CTA; a dry pass: its warm-up warps).
+template <int kScanE, int kScanU>
+__device__ __forceinline__ void router_retire(const RouterArgs& a, uint8_t* scratch, bool dry, int warp,
+                                              int nwarps) {
   if (!a.fused_scan) return;
   __shared__ uint32_t s_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(a.done, 1u) == (uint32_t)(a.nblk - 1) ? 1u : 0u;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  if (!dry) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(a.done, 1u) == (uint32_t)(a.nblk - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+  }
   int* s_npre = reinterpret_cast<int*>(scratch);
   float* s_psum = reinterpret_cast<float*>(s_npre + scan_detail::kMaxE);
-  scan_detail::scan_body<2, 4>(a.scan, s_npre, s_psum);
+  scan_detail::scan_body<kScanE, kScanU>(a.scan, s_npre, s_psum, warp, nwarps, dry);
 }
 
 // ---- bf16: tensor-core logits ---------------------------------------------------
@@ -223,7 +280,13 @@ struct RouterBf16 {
   static constexpr size_t LOGITS = (size_t)kRouterBM * (EP + 1) * 4;
   static constexpr size_t BITS_OFF = RING > LOGITS ? RING : LOGITS;
   static constexpr size_t BITS = (size_t)EP * (kRouterBM / 32) * 4;
-  static constexpr size_t BAR_OFF = (BITS_OFF + BITS + 7) / 8 * 8;
+  // Scratch of the warm-up warps: the dry tail's logit rows and bit masks, the
+  // dry scan's totals.
+  static constexpr size_t DRY_OFF = (BITS_OFF + BITS + 15) / 16 * 16;
+  static constexpr size_t DRY_SL = (size_t)kDryTokens * (EP + 1) * 4;
+  static constexpr size_t DRY_BITS = BITS;
+  static constexpr size_t DRY_SCAN = 2 * scan_detail::kMaxE * 4;
+  static constexpr size_t BAR_OFF = (DRY_OFF + DRY_SL + DRY_BITS + DRY_SCAN + 7) / 8 * 8;
   static constexpr size_t SMEM = 1024 + BAR_OFF + 2 * STAGES * 8 + 16;   // + 1 KB to align the ring
 
   // Byte offset in a W k-tile of 16-byte chunk c (experts 8c..8c+7) of k-row r:
@@ -250,8 +313,10 @@ template <> struct RouterShape<16> { static constexpr int KSUB = 2, STAGES = 2; 
 template <> struct RouterShape<32> { static constexpr int KSUB = 1, STAGES = 2; };
 
 // NT n-tiles of 8 experts; EP = 8 NT >= E.  Warps 0-7 compute (row block w %
-// 4: tokens 16 (w % 4) .. + 15; k-tiles of parity w / 4); warp 8 is the producer.  tma_w: W_g tiles come by TMA (E == EP);
-// otherwise the producer warp copies them with plain loads.
+// 4: tokens 16 (w % 4) .. + 15; k-tiles of parity w / 4); warp 8 is the
+// producer; warps 9 and 10 make the dry passes of the tail and of the scan
+// while x streams.  tma_w: W_g tiles come by TMA (E == EP); otherwise the
+// producer warp copies them with plain loads.
 template <int NT, int KSUB, int STAGES_>
 __global__ void __launch_bounds__(kThreadsBf16) router_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                    const __grid_constant__ CUtensorMap tmW,
@@ -351,7 +416,7 @@ __global__ void __launch_bounds__(kThreadsBf16) router_bf16_kernel(const __grid_
       for (int j = kt - STAGES > 0 ? kt - STAGES : 0; j < kt; ++j)
         mbar_drain(smem_u32(&full[j % STAGES]), (uint32_t)(j / STAGES) & 1u, drain_limit);
     }
-  } else {
+  } else if (warp < kMmaWarps) {
     // ---------------- MMA warps ----------------
     // Warp w: row block w % 4, k-group w / 4 (k-tiles of that parity).  Every
     // warp waits on and releases every stage, so the empty barrier's phases
@@ -411,45 +476,66 @@ __global__ void __launch_bounds__(kThreadsBf16) router_bf16_kernel(const __grid_
       if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
     }
   }
-  // Every warp is past its last read of the ring before the logits overwrite it.
-  if (__syncthreads_or(stopped)) {
-    router_retire(a, smem);
-    return;
-  }
-  float* sl = (float*)smem;
+  // The tail, in two passes through one copy of its code.  Pass 0 (dry) runs
+  // only on the two warm-up warps, while the other warps still stream: the
+  // tail on 8 tokens of scratch, and the scan.  Pass 1 runs the tail on every
+  // warp but the scan warm-up warp (which may still be in its dry pass; the
+  // tail's barriers leave it out), then the retirement on all.
   const int ldl = EP + 1;
-  // logits = (even k-tiles) + (odd k-tiles): k-group 1 stores its partial, and
-  // the k-group 0 warp of the same row block (same lane -> same elements) adds
-  // its own in front.
-  const int r0 = (warp % kRowBlocks) * 16 + (lane >> 2);
-  if (warp >= kRowBlocks && warp < kMmaWarps) {
+  uint8_t* dry_area = smem + L::DRY_OFF;
+#pragma unroll 1
+  for (int pass = warp >= kWarmTailWarp ? 0 : 1; pass < 2; ++pass) {
+    const bool dry = pass == 0;
+    if (dry ? warp == kWarmTailWarp : warp != kWarmScanWarp) {
+      bool stop = false;
+      if (!dry) {
+        // Every warp is past its last read of the ring before the logits overwrite it.
+        stop = tail_sync_or(kTailThreadsBf16, stopped);
+        if (!stop) {
+          float* sl = (float*)smem;
+          // logits = (even k-tiles) + (odd k-tiles): k-group 1 stores its partial, and
+          // the k-group 0 warp of the same row block (same lane -> same elements) adds
+          // its own in front.
+          const int r0 = (warp % kRowBlocks) * 16 + (lane >> 2);
+          if (warp >= kRowBlocks && warp < kMmaWarps) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const int c = n * 8 + 2 * (lane & 3);
-      sl[r0 * ldl + c] = acc[n][0];
-      sl[r0 * ldl + c + 1] = acc[n][1];
-      sl[(r0 + 8) * ldl + c] = acc[n][2];
-      sl[(r0 + 8) * ldl + c + 1] = acc[n][3];
-    }
-  }
-  __syncthreads();
-  if (warp < kRowBlocks) {
+            for (int n = 0; n < NT; ++n) {
+              const int c = n * 8 + 2 * (lane & 3);
+              sl[r0 * ldl + c] = acc[n][0];
+              sl[r0 * ldl + c + 1] = acc[n][1];
+              sl[(r0 + 8) * ldl + c] = acc[n][2];
+              sl[(r0 + 8) * ldl + c + 1] = acc[n][3];
+            }
+          }
+          tail_sync(kTailThreadsBf16);
+          if (warp < kRowBlocks) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const int c = n * 8 + 2 * (lane & 3);
-      sl[r0 * ldl + c] = acc[n][0] + sl[r0 * ldl + c];
-      sl[r0 * ldl + c + 1] = acc[n][1] + sl[r0 * ldl + c + 1];
-      sl[(r0 + 8) * ldl + c] = acc[n][2] + sl[(r0 + 8) * ldl + c];
-      sl[(r0 + 8) * ldl + c + 1] = acc[n][3] + sl[(r0 + 8) * ldl + c + 1];
+            for (int n = 0; n < NT; ++n) {
+              const int c = n * 8 + 2 * (lane & 3);
+              sl[r0 * ldl + c] = acc[n][0] + sl[r0 * ldl + c];
+              sl[r0 * ldl + c + 1] = acc[n][1] + sl[r0 * ldl + c + 1];
+              sl[(r0 + 8) * ldl + c] = acc[n][2] + sl[(r0 + 8) * ldl + c];
+              sl[(r0 + 8) * ldl + c + 1] = acc[n][3] + sl[(r0 + 8) * ldl + c + 1];
+            }
+          }
+          tail_sync(kTailThreadsBf16);
+        }
+      }
+      if (!stop)
+        router_finalize<kRouterBM, EP / kTPT>(dry ? (float*)dry_area : (float*)smem, ldl,
+                                              dry ? (uint32_t*)(dry_area + L::DRY_SL) : bits, a, blk,
+                                              dry ? lane : tid, dry ? 32 : kTailThreadsBf16, dry);
     }
+    if (!dry || warp == kWarmScanWarp)
+      router_retire<2, 4>(a, dry ? dry_area + L::DRY_SL + L::DRY_BITS : smem, dry, dry ? 0 : warp,
+                          dry ? 1 : kThreadsBf16 / 32);
   }
-  __syncthreads();
-  router_finalize<kRouterBM>(sl, ldl, bits, a, blk);
-  router_retire(a, smem);
 }
 
 // ---- fp32: CUDA-core logits ------------------------------------------------------
 constexpr int kBK32 = 32;
+// EPT: experts per tail thread, E <= 4 EPT.
+template <int EPT>
 __global__ void __launch_bounds__(kThreadsF32) router_f32_kernel(RouterArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int E = a.E, d = a.d;
@@ -483,8 +569,8 @@ __global__ void __launch_bounds__(kThreadsF32) router_f32_kernel(RouterArgs a) {
     }
   }
   __syncthreads();
-  router_finalize<kRouterBM>(sl, ldl, bits, a, blk);
-  router_retire(a, smem);
+  router_finalize<kRouterBM, EPT>(sl, ldl, bits, a, blk, tid, kThreadsF32, false);
+  router_retire<2, 4>(a, smem, false, tid / 32, kThreadsF32 / 32);
 }
 
 template <int NT>
@@ -522,6 +608,7 @@ cudaError_t launch_bf16(const RouterArgs& a, int64_t nblk, cudaStream_t s) {
 //               commits ring slots back to the producer;
 //   warps 4-7   read the accumulator (one TMEM lane quadrant each, a token per
 //               lane) into fp32 logits in shared memory, over the drained ring;
+//   warps 8-12 dry passes of the tail and of the scan (instruction warm-up);
 // then all 16 warps run the gating / top-k tail and the per-CTA partials.
 // Against the mma.sync router (64 tokens per CTA, W_g tiles beside every x
 // tile in the ring), a CTA here reads each W_g tile once per 128 tokens and
@@ -534,6 +621,8 @@ constexpr int WBOX = kBK * 64 * 2;         // 8 KB per 64-expert W_g box
 constexpr int THREADS = 512;               // 16 warps: the tail runs 4 threads per token
 constexpr int RING = 192 * 1024;
 constexpr int EPI_WARP0 = 4;               // warps 4..7: TMEM lane quadrants 0..3
+constexpr int WARM_TAIL_WARP = 8;          // idle until the tail: its dry pass
+constexpr int WARM_SCAN_WARP0 = 9;         // warps 9..12: the scan's dry pass, a role each
 constexpr uint32_t kWhere = kWhereRouter + 0x10;
 
 template <int NB>   // E = 64 NB
@@ -545,7 +634,12 @@ struct Shape {
   static constexpr size_t LOGITS = (size_t)BM * (E + 1) * 4;
   static constexpr size_t BITS_OFF = (size_t)STAGES * STAGE;
   static constexpr size_t BITS = (size_t)E * (BM / 32) * 4;
-  static constexpr size_t BAR_OFF = (BITS_OFF + BITS + 7) / 8 * 8;
+  // Scratch of the warm-up warps (dry tail rows and masks, dry scan totals).
+  static constexpr size_t DRY_OFF = (BITS_OFF + BITS + 15) / 16 * 16;
+  static constexpr size_t DRY_SL = (size_t)kDryTokens * (E + 1) * 4;
+  static constexpr size_t DRY_BITS = BITS;
+  static constexpr size_t DRY_SCAN = 2 * scan_detail::kMaxE * 4;
+  static constexpr size_t BAR_OFF = (DRY_OFF + DRY_SL + DRY_BITS + DRY_SCAN + 7) / 8 * 8;
   static constexpr size_t SMEM = 1024 + BAR_OFF + (2 * STAGES + 2) * 8 + 16;
   static_assert(LOGITS <= BITS_OFF, "the logits fit in the drained ring");
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
@@ -677,15 +771,33 @@ __global__ void __launch_bounds__(rtc::THREADS, 1) router_tc_kernel(const __grid
     }
     tc_fence_before();
   }
-  // The ring is drained (every MMA done, every copy landed) and the logits are
-  // in shared memory before the tail reads them; TMEM can go.
-  const bool stop = __syncthreads_or(stopped || *abort != 0u);
-  if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(L::TCOLS) : "memory");
+  // The tail in two passes through one copy of its code: pass 0 (dry) on the
+  // warm-up warps while the stream runs (warp 8 the tail, warps 9-12 the scan's
+  // four roles side by side), pass 1 on every warp (the tail needs all 512
+  // threads, four per token).
+  uint8_t* dry_area = smem + L::DRY_OFF;
+  const bool warm_scan = warp >= rtc::WARM_SCAN_WARP0 && warp < rtc::WARM_SCAN_WARP0 + 4;
+#pragma unroll 1
+  for (int pass = (warp == rtc::WARM_TAIL_WARP || warm_scan) ? 0 : 1; pass < 2; ++pass) {
+    const bool dry = pass == 0;
+    bool stop = false;
+    if (!dry) {
+      // The ring is drained (every MMA done, every copy landed) and the logits are
+      // in shared memory before the tail reads them; TMEM can go.
+      stop = __syncthreads_or(stopped || *abort != 0u);
+      if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(L::TCOLS) : "memory");
+      }
+    }
+    if (!stop && (!dry || warp == rtc::WARM_TAIL_WARP))
+      router_finalize<rtc::BM, E / kTPT>(dry ? (float*)dry_area : (float*)smem, E + 1,
+                                         dry ? (uint32_t*)(dry_area + L::DRY_SL) : bits, a, blk, dry ? lane : tid,
+                                         dry ? 32 : rtc::THREADS, dry);
+    if (!dry || warm_scan)
+      router_retire<2, 4>(a, dry ? dry_area + L::DRY_SL + L::DRY_BITS : smem, dry,
+                          dry ? warp - rtc::WARM_SCAN_WARP0 : warp, dry ? 4 : rtc::THREADS / 32);
   }
-  if (!stop) router_finalize<rtc::BM>((float*)smem, E + 1, bits, a, blk);
-  router_retire(a, smem);
 }
 
 template <int NB>
@@ -719,10 +831,10 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t s) {
   if (a.dtype == MOE_DT_F32) {
     size_t bytes = (size_t)kRouterBM * (a.E + 1) * 4 + (size_t)kRouterBM * (kBK32 + 1) * 4 +
                    (size_t)kBK32 * a.E * 4 + (size_t)a.E * (kRouterBM / 32) * 4;
-    cudaError_t e = cudaFuncSetAttribute(router_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)bytes);
+    auto kern = a.E <= 8 ? router_f32_kernel<2> : a.E <= 32 ? router_f32_kernel<8> : router_f32_kernel<64>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
-    router_f32_kernel<<<(unsigned)nblk, kThreadsF32, bytes, s>>>(a);
+    kern<<<(unsigned)nblk, kThreadsF32, bytes, s>>>(a);
     return cudaGetLastError();
   }
   const int ep = (a.E + 7) / 8;

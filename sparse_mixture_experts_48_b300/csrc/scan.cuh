@@ -33,18 +33,26 @@ __device__ __forceinline__ int warp_excl_scan(int v, int lane, int* total) {
   return incl - v;
 }
 
-// Needs every thread of the CTA (one barrier inside), at least four warps;
-// s_npre and s_psum are
+// Run by every thread of the CTA (warp = threadIdx.x / 32, nwarps = blockDim.x
+// / 32, at least four warps; one barrier inside); s_npre and s_psum are
 // shared arrays of kMaxE entries.  The router CTAs' partials are read with
 // L1-bypassing loads: in the fused form they were written by other SMs during
 // this same launch.
 // kScanE experts per warp per round, kScanU 32-block chunks of each loaded per
 // round: the standalone scan kernel takes <4, 8>, the router's last CTA a
 // lighter <2, 4> so that its kernel keeps the registers of its own main loop.
+// dry: the same code over one round of phase 1 and the roles of phase 2,
+// writing only s_npre / s_psum (no barrier: one warp alone takes all four
+// roles, or four warps one each): it brings the code into the instruction
+// cache before the real pass, which runs once per launch and is otherwise
+// bound by fetching its code (the caller runs both passes through one call
+// site).
 template <int kScanE, int kScanU>
-__device__ inline void scan_body(const ScanArgs& a, int* s_npre, float* s_psum) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
-  const int E = a.E;
+__device__ __forceinline__ void scan_body(const ScanArgs& a, int* s_npre, float* s_psum, int warp, int nwarps,
+                                       bool dry) {
+  const int lane = threadIdx.x % 32;
+  const int E = dry ? (a.E < 1 ? a.E : 1) : a.E;
+  const int64_t nblk = dry ? (a.nblk < 32 * kScanU ? a.nblk : 32 * kScanU) : a.nblk;
   // An earlier stage gave up: its partials are not valid.  Publish empty
   // segments so that nothing later reads or writes through them.
   const bool failed = *(volatile const uint32_t*)a.err != 0u;
@@ -61,7 +69,7 @@ __device__ inline void scan_body(const ScanArgs& a, int* s_npre, float* s_psum) 
     float ps[kScanE];
 #pragma unroll
     for (int j = 0; j < kScanE; ++j) { run[j] = 0; ps[j] = 0.f; }
-    for (int64_t b0 = 0; b0 < a.nblk; b0 += 32 * kScanU) {
+    for (int64_t b0 = 0; b0 < nblk; b0 += 32 * kScanU) {
       int v[kScanE][kScanU];
       float p[kScanE][kScanU];
 #pragma unroll
@@ -70,7 +78,7 @@ __device__ inline void scan_body(const ScanArgs& a, int* s_npre, float* s_psum) 
 #pragma unroll
         for (int u = 0; u < kScanU; ++u) {
           const int64_t b = b0 + 32 * u + lane;
-          const bool in = e < E && b < a.nblk;
+          const bool in = e < E && b < nblk;
           v[j][u] = (in && !ec) ? __ldcg(a.hist + e * a.nblk + b) : 0;
           p[j][u] = in ? __ldcg(a.psum + e * a.nblk + b) : 0.f;
         }
@@ -83,7 +91,7 @@ __device__ inline void scan_body(const ScanArgs& a, int* s_npre, float* s_psum) 
           const int64_t b = b0 + 32 * u + lane;
           int tot;
           const int ex = warp_excl_scan(v[j][u], lane, &tot);
-          if (e < E && b < a.nblk && !ec) a.base[e * a.nblk + b] = run[j] + ex;
+          if (e < E && b < nblk && !ec && !dry) a.base[e * a.nblk + b] = run[j] + ex;
           run[j] += tot;
           ps[j] += p[j][u];
         }
@@ -101,7 +109,7 @@ __device__ inline void scan_body(const ScanArgs& a, int* s_npre, float* s_psum) 
       }
     }
   }
-  __syncthreads();
+  if (dry) __syncwarp(); else __syncthreads();
 
   // Phase 2: four warps at once, each from the shared totals, so the single-
   // warp chains run side by side: warp 0 counts and offsets (what the gather
@@ -118,7 +126,12 @@ __device__ inline void scan_body(const ScanArgs& a, int* s_npre, float* s_psum) 
   // Selections in all: T k for token choice, E C for expert choice.
   const int64_t Tk = ec ? (int64_t)E * a.ec_C : a.T * (int64_t)a.k;
 
-  if (warp == 0) {
+  // Warp w < 4 takes role w; a dry pass on one warp takes all four.
+  const bool all_roles = dry && nwarps == 1;
+  const int role_end = all_roles ? 4 : (warp < 4 ? warp + 1 : 0);
+#pragma unroll 1
+  for (int role = all_roles ? 0 : warp; role < role_end; ++role) {
+  if (role == 0) {
     int cnt_local = 0;
     for (int i = 0; i < PE; ++i) {
       const int e = e0 + i;
@@ -130,14 +143,16 @@ __device__ inline void scan_body(const ScanArgs& a, int* s_npre, float* s_psum) 
       const int e = e0 + i;
       if (e < E) {
         const int n = s_npre[e];
-        a.n_pre[e] = n;
-        a.counts[e] = kept(n);
-        a.offsets[e] = off;
+        if (!dry) {
+          a.n_pre[e] = n;
+          a.counts[e] = kept(n);
+          a.offsets[e] = off;
+        }
         off += seg_rows(n);
       }
     }
-    if (lane == 0) a.offsets[E] = kept_total;
-  } else if (warp == 1) {
+    if (lane == 0 && !dry) a.offsets[E] = kept_total;
+  } else if (role == 1) {
     // f = n / (T k) and P = (sum of p) / T, each one correctly rounded fp32
     // division; L_aux = alpha E sum f P (positive terms, fixed tree).
     float L = 0.f;
@@ -146,15 +161,17 @@ __device__ inline void scan_body(const ScanArgs& a, int* s_npre, float* s_psum) 
       if (e < E) {
         const float fe = a.T > 0 ? __fdiv_rn((float)s_npre[e], (float)Tk) : 0.f;
         const float Pe = a.T > 0 ? __fdiv_rn(s_psum[e], (float)a.T) : 0.f;
-        a.f[e] = fe;
-        a.P[e] = Pe;
+        if (!dry) {
+          a.f[e] = fe;
+          a.P[e] = Pe;
+        }
         L = __fmaf_rn(fe, Pe, L);
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);   // fixed tree order
-    if (lane == 0) *a.L_aux = (float)a.alpha * (float)E * L;
-  } else if (warp == 2) {
+    if (lane == 0 && !dry) *a.L_aux = (float)a.alpha * (float)E * L;
+  } else if (role == 2) {
     if (a.route_stats) {
       // Routing health of the pre-capacity shares f_e = n_e / (T k): entropy
       // -sum f ln f, variance (1/E) sum (f - 1/E)^2 with f - 1/E = (n E - T k) /
@@ -175,14 +192,14 @@ __device__ inline void scan_body(const ScanArgs& a, int* s_npre, float* s_psum) 
         H += __shfl_xor_sync(0xffffffffu, H, o);
         V += __shfl_xor_sync(0xffffffffu, V, o);
       }
-      if (lane == 0) {
+      if (lane == 0 && !dry) {
         V = __fdiv_rn(V, (float)E);
         a.route_stats[0] = H;
         a.route_stats[1] = V;
         a.route_stats[2] = (float)E * sqrtf(V);
       }
     }
-  } else if (warp == 3) {
+  } else if (role == 3) {
     // Segments of the grouped GEMMs: routed experts read the grouped copy of
     // x, shared experts read x itself and write rows T*k + s*T.
     const int G = E + a.S;
@@ -221,17 +238,20 @@ __device__ inline void scan_body(const ScanArgs& a, int* s_npre, float* s_psum) 
           arow = 0;
           asrc = 1;
         }
-        a.seg.rows[g] = rows;
-        a.seg.w[g] = g;
-        a.seg.out_row[g] = orow;
-        a.seg.a_row[g] = arow;
-        a.seg.a_src[g] = asrc;
-        a.seg.mtile_start[g] = mt;
+        if (!dry) {
+          a.seg.rows[g] = rows;
+          a.seg.w[g] = g;
+          a.seg.out_row[g] = orow;
+          a.seg.a_row[g] = arow;
+          a.seg.a_src[g] = asrc;
+          a.seg.mtile_start[g] = mt;
+        }
         mt += (rows + kGemmBM - 1) / kGemmBM;
       }
     }
-    if (lane == 0) a.seg.mtile_start[G] = mt_total;
+    if (lane == 0 && !dry) a.seg.mtile_start[G] = mt_total;
   }
+  }   // roles
 }
 
 }  // namespace scan_detail
