@@ -68,6 +68,7 @@ constexpr int THREADS = 64 + EPI_WARPS * 32;
 #define MOE_WIDE_EPI_MAX_K 1024
 #endif
 constexpr int kWideEpiMaxK = MOE_WIDE_EPI_MAX_K;
+
 constexpr int TMEM_COLS = 512;                  // two 256-column accumulators
 constexpr int MAX_G = 264;
 constexpr uint32_t kWhere = 0x400;
@@ -121,7 +122,9 @@ constexpr size_t smem_for(int stages) {
 // As many ring stages (up to STAGES) as fit beside the staging tiles.
 template <bool OUT_F32, bool SAVE_PRE, bool FP8, int EPI = EPI_WARPS>
 constexpr int ring_stages() {
-  return smem_for<OUT_F32, SAVE_PRE, FP8, EPI>(STAGES) <= 227 * 1024 ? STAGES : STAGES - 1;
+  int s = STAGES;
+  while (s > 2 && smem_for<OUT_F32, SAVE_PRE, FP8, EPI>(s) > 227 * 1024) --s;
+  return s;
 }
 template <bool OUT_F32, bool SAVE_PRE, bool FP8, int EPI = EPI_WARPS>
 constexpr size_t smem_bytes() {
@@ -132,6 +135,7 @@ static_assert(smem_bytes<false, false, false>() <= 227 * 1024 && smem_bytes<true
               "shared memory per CTA");
 static_assert(!kStageBf16Out || ring_stages<false, false, false>() == STAGES, "bf16 staging keeps six stages");
 static_assert(smem_bytes<false, false, false, 16>() <= 227 * 1024, "shared memory per CTA, 16 epilogue warps");
+
 
 // 16 packed bf16 pairs (one thread's 32 columns) into row `lane` of a 32 x 32
 // bf16 staging tile laid out with the 64-byte swizzle: 16-byte chunk j at

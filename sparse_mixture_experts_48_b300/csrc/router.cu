@@ -527,7 +527,9 @@ __global__ void __launch_bounds__(kThreadsBf16) router_bf16_kernel(const __grid_
                                               dry ? lane : tid, dry ? 32 : kTailThreadsBf16, dry);
     }
     if (!dry || warp == kWarmScanWarp)
-      router_retire<2, 4>(a, dry ? dry_area + L::DRY_SL + L::DRY_BITS : smem, dry, dry ? 0 : warp,
+      // E <= 32: one expert per warp and round, 256 router CTAs per load
+      // round (T = 16384 in one round); more experts: two per warp.
+      router_retire<(NT <= 4 ? 1 : 2), (NT <= 4 ? 8 : 4)>(a, dry ? dry_area + L::DRY_SL + L::DRY_BITS : smem, dry, dry ? 0 : warp,
                           dry ? 1 : kThreadsBf16 / 32);
   }
 }
