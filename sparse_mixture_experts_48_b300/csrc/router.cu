@@ -65,9 +65,10 @@ __device__ __forceinline__ bool tail_sync_or(int count, bool v) {
 // shuffle rounds, so all four threads pick the same expert in the same round.
 //
 // vt / nvt: this thread's id among the nvt threads running the tail (threads
-// 0 .. nvt - 1 of the CTA, nvt >= 4 BM, synchronised by tail_sync).  dry: one warp (vt = lane, nvt = 32) runs the same
-// code on the first 8 tokens while the CTA still streams x, writing only its
-// own scratch (sl, bits) and nothing in global memory.  The tail runs once per
+// 0 .. nvt - 1 of the CTA, nvt >= 4 BM, synchronised by tail_sync).
+// dry: one warp (vt = lane, nvt = 32) runs the same code on the first 8
+// tokens while the CTA still streams x, writing only its own scratch (sl,
+// bits) and nothing in global memory.  The tail runs once per
 // CTA, so on a cold instruction cache its time is the fetch of its code (the
 // expert GEMMs' weights have pushed it out of L2 since the previous call);
 // the dry pass fetches it in the shadow of the stream.  Each kernel calls it
