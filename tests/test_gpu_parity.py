@@ -60,6 +60,12 @@ EDGE = [
     # the tcgen05 router's other widths: N = 128 and N = 192 experts per MMA
     ("E_128_tcgen05_router", "deepseek_shared_sigmoid_bf16", dict(T=300, E=128, k=4, S=0, d=256, f=128)),
     ("E_192_softmax_tcgen05_router", "gpt2_top2_gelu_bf16", dict(T=270, E=192, k=8, d=320, f=128)),
+    # the mma.sync router's wider instantiations (8 NT >= E experts, W_g by plain
+    # copies when E < 8 NT): NT = 4, 16 and 32, each thread's E / 4 logits in registers
+    ("E_24_mma_router", "gpt2_top2_gelu_bf16", dict(T=300, E=24, k=3, d=256, f=128)),
+    ("E_96_mma_router", "deepseek_shared_sigmoid_bf16", dict(T=200, E=96, k=6, S=0, d=256, f=128)),
+    ("E_160_mma_router", "gpt2_top2_gelu_bf16", dict(T=150, E=160, k=8, d=256, f=128)),
+    ("f32_E_40", "tiny_top1_relu_f32", dict(T=100, E=40, k=4)),
     ("capacity_one", "skew_capacity_gelu_bf16", dict(T=100, E=16, k=2, d=256, f=256, capacity_factor=0.1)),
     ("sigmoid_top1_capacity", "deepseek_shared_sigmoid_bf16",
      dict(T=333, E=8, k=1, S=1, d=256, f=128, capacity_factor=1.0, router_bias=True, router_bias_std=1.0)),
