@@ -1,7 +1,7 @@
 """Bench of the MoE-FFN forward layer on B300: tokens/s and grouped-GEMM TFLOPS.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--T TOKENS] [--no-cpu] [--no-e2e] [--no-extra]
+                    [--workload NAME] [--T TOKENS] [--no-cpu] [--no-e2e] [--e2e-depth D] [--no-extra]
                     [--noise-std S] [--expert-choice] [--backward] [--fp8] [--gemm-one-cta] [--graph]
 
 A step is one whole forward pass of the layer (router with the dispatch scan
@@ -19,6 +19,10 @@ each, and reports them under other_workloads: tokens/s, per-kernel times and
 fractions, and the CUDA-graph replay.  The headline value, roofline and e2e
 stay on the Mixtral-shaped layer.  The roofline fraction is taken against the
 measured burst bf16 peak: the timed region lasts well under a second.
+
+The end-to-end figure (e2e) calls moe_forward_host on pinned host buffers,
+the steps rotating over D streams and workspaces (--e2e-depth, default 3) so
+that each step's copies overlap other steps' kernels.
 
 --expert-choice, --fp8 (alone or together) and --backward time those variants
 of the step on the same workload; --graph adds the same forward replayed from
@@ -576,6 +580,9 @@ def main():
     ap.add_argument("--T", type=int, default=0, help="override the token count (profiling runs)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop")
+    ap.add_argument("--e2e-depth", type=int, default=3,
+                    help="streams (and workspaces) the end-to-end loop rotates over (>= 2; 3 measured best: "
+                         "a stream's copies out and in then have two other steps' kernels to hide behind)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads (reported under other_workloads by the default run)")
     ap.add_argument("--noise-std", type=float, default=0.0,
@@ -690,26 +697,28 @@ def main():
 
     # End to end through the public API with host buffers (moe_forward_host):
     # every step copies its x from page-locked host memory in and all outputs
-    # back out.  Steps alternate two streams and two workspaces, so one step's
-    # copies overlap the other's kernels; the timed region spans all K steps.
+    # back out.  Steps rotate over D streams and D workspaces (D =
+    # --e2e-depth), so a step's copies overlap the other steps' kernels; the
+    # timed region spans all K steps.
     e2e = None
     if not args.no_e2e:
         x_host = torch.empty(d["x"].shape, dtype=d["x"].dtype, pin_memory=True)
         x_host.copy_(d["x"].cpu())
         noise_host = noise.cpu().pin_memory() if noise is not None else None
         weights = args_in[1:] if args_in is not None else None
-        streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
-        hws = [torch.empty((moe.host_workspace_size(cfg),), dtype=torch.uint8, device=dev) for _ in range(2)]
-        houts = [moe.alloc_host_outputs(cfg) for _ in range(2)]
+        D = max(2, args.e2e_depth)
+        streams = [torch.cuda.Stream(device=dev) for _ in range(D)]
+        hws = [torch.empty((moe.host_workspace_size(cfg),), dtype=torch.uint8, device=dev) for _ in range(D)]
+        houts = [moe.alloc_host_outputs(cfg) for _ in range(D)]
 
         def e2e_step(i):
             if fp8:
                 moe.forward_fp8_host(cfg, x_host, d["W_g"], d["b_g"], experts8, d["b1"], d["b2"],
-                                     router_noise_host=noise_host, out=houts[i % 2], workspace=hws[i % 2],
-                                     stream=streams[i % 2])
+                                     router_noise_host=noise_host, out=houts[i % D], workspace=hws[i % D],
+                                     stream=streams[i % D])
             else:
-                moe.forward_host(cfg, x_host, *weights, router_noise_host=noise_host, out=houts[i % 2],
-                                 workspace=hws[i % 2], stream=streams[i % 2], gemm_single_cta=args.gemm_one_cta)
+                moe.forward_host(cfg, x_host, *weights, router_noise_host=noise_host, out=houts[i % D],
+                                 workspace=hws[i % D], stream=streams[i % D], gemm_single_cta=args.gemm_one_cta)
 
         for i in range(W):
             e2e_step(i)
@@ -718,12 +727,14 @@ def main():
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(streams[0])
-        streams[1].wait_event(e0)
+        for st_ in streams[1:]:
+            st_.wait_event(e0)
         for i in range(K):
             e2e_step(i)
-        last = torch.cuda.Event()
-        last.record(streams[1])
-        streams[0].wait_event(last)
+        for st_ in streams[1:]:
+            last = torch.cuda.Event()
+            last.record(st_)
+            streams[0].wait_event(last)
         e1.record(streams[0])
         torch.cuda.synchronize()
         barrier()
@@ -740,7 +751,7 @@ def main():
         e2e = {"value": replica_throughput(cfg.T, e_ms, world), "unit": "tokens/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "how": ("moe_forward_fp8_host" if fp8 else "moe_forward_host") +
-                      ", pinned host x in / all outputs out every step, 2 streams x 2 workspaces"}
+                      f", pinned host x in / all outputs out every step, {D} streams x {D} workspaces"}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
