@@ -236,9 +236,10 @@ __device__ __forceinline__ void router_finalize(float* sl, int ldl, uint32_t* bi
 // stopped CTA still takes its ticket, so the scan always runs (and, seeing the
 // status word set, publishes empty segments).  `scratch`: shared memory no
 // longer in use, at least 2 KB.
-// dry: one warp runs the scan's dry pass instead (no ticket, no global
-// writes; `scratch` its own 2 KB), fetching the scan's code while x streams:
-// any CTA may be the last to finish.  Each kernel calls this from one place.
+// dry: the warm-up warps run the scan's dry pass instead (no ticket, no
+// global writes; `scratch` their own 2 KB), fetching the scan's code while x
+// streams: any CTA may be the last to finish.  Each kernel calls this from
+// one place.
 // warp / nwarps: this warp's part of the scan (the real pass: every warp of
 // the CTA; a dry pass: its warm-up warps).
 template <int kScanE, int kScanU>
