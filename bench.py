@@ -436,8 +436,18 @@ def measure(cfg, d, args_in, noise, experts8, args, dev, world, peaks, graph=Fal
         raise SystemExit(f"device error in the timed region: {moe.STATUS.get(status)}")
     ms_step = max_over_ranks(t_start.elapsed_time(t_end), dev, world) / K
 
-    # The same step captured once in a CUDA graph and replayed: no host-side
-    # launch work per step (what bounds small layers).
+    # The per-kernel breakdown: K more calls that record the stage events,
+    # right after the plain calls (so that the plain calls carry none of the
+    # events' cost, and the kernels run in the same state of the power cap).
+    for i in range(K):
+        step(i)
+    torch.cuda.synchronize()
+    status = moe.check_device_errors(ws)
+    if status != 0:
+        raise SystemExit(f"device error in the stage-event calls: {moe.STATUS.get(status)}")
+
+    # Last, the same step captured once in a CUDA graph and replayed: no
+    # host-side launch work per step (what bounds small layers).
     gres = None
     if graph:
         if fp8:
@@ -459,16 +469,6 @@ def measure(cfg, d, args_in, noise, experts8, args, dev, world, peaks, graph=Fal
         g_ms = max_over_ranks(g0.elapsed_time(g1) / K, dev, world)
         gres = {"value": replica_throughput(cfg.T, g_ms, world), "unit": "tokens/s", "ms_per_step": g_ms}
         del fg
-    # The per-kernel breakdown: K more calls that record the stage events
-    # (after the plain calls and the graph replays, so that neither carries
-    # the events' cost).
-    for i in range(K):
-        step(i)
-    torch.cuda.synchronize()
-    status = moe.check_device_errors(ws)
-    if status != 0:
-        raise SystemExit(f"device error in the stage-event calls: {moe.STATUS.get(status)}")
-
     # per-kernel durations from the stage events; with FP8 experts event
     # NUM_STAGES + 1 splits GEMM 1 -> GEMM 2 into the H quantisation and GEMM 2
     names = list(moe.STAGE_NAMES)
