@@ -36,6 +36,7 @@ __device__ __forceinline__ float4 ld_stream(const float4* p, uint64_t policy) {
 // whatever the storage dtype, so y is rounded once, at the store.
 template <int NJ, bool Y_F32>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineArgs a) {
+  pdl_wait();
   constexpr int U = NJ >= 8 ? 1 : 8 / NJ;
   const int lane = threadIdx.x % 32;
   const int64_t t = (int64_t)blockIdx.x * kWarps + threadIdx.x / 32;
@@ -98,11 +99,8 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineArgs a) {
 
 template <int NJ>
 cudaError_t launch_nj(const CombineArgs& a, int64_t blocks, cudaStream_t s) {
-  if (a.y_f32)
-    combine_kernel<NJ, true><<<(unsigned)blocks, kWarps * 32, 0, s>>>(a);
-  else
-    combine_kernel<NJ, false><<<(unsigned)blocks, kWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.y_f32) return launch_maybe_pdl(a.pdl, combine_kernel<NJ, true>, dim3((unsigned)blocks), dim3(kWarps * 32), 0, s, a);
+  return launch_maybe_pdl(a.pdl, combine_kernel<NJ, false>, dim3((unsigned)blocks), dim3(kWarps * 32), 0, s, a);
 }
 
 }  // namespace

@@ -64,6 +64,12 @@ __device__ __forceinline__ void record_error(uint32_t* err, uint32_t bit, uint32
   if (atomicOr(err, bit) == 0u) atomicExch(err + 1, where);
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor has finished; it waits here,
+// before its first read of the predecessor's results, until that grid has
+// completed and its writes are visible.  Without the launch attribute this
+// returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

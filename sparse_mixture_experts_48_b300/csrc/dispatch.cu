@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
 constexpr int kGatherWarps = 8;
 
 __global__ void __launch_bounds__(kGatherWarps * 32) gather_kernel(GatherArgs a) {
+  pdl_wait();
   const int lane = threadIdx.x % 32;
   const int64_t t = (int64_t)blockIdx.x * kGatherWarps + threadIdx.x / 32;
   if (t >= a.T || *(volatile const uint32_t*)a.err != 0u) return;
@@ -152,8 +153,7 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s) {
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
   const int64_t blocks = (a.T + kGatherWarps - 1) / kGatherWarps;
-  gather_kernel<<<(unsigned)blocks, kGatherWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_maybe_pdl(a.pdl, gather_kernel, dim3((unsigned)blocks), dim3(kGatherWarps * 32), 0, s, a);
 }
 
 }  // namespace moe

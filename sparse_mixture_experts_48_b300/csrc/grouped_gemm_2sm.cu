@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(64 + EPI * 32, 1)
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3,
                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
                      const __grid_constant__ CUtensorMap tmU, GemmArgs a) {
+  pdl_wait();   // launched after the previous kernel may start early: its results come first
   constexpr int BN_OUT = SWIGLU ? 128 : 256;   // output columns per pair tile
   constexpr int NST = ring_stages<OUT_F32, SAVE_PRE, FP8, EPI>();
   constexpr bool STAGE_H = !OUT_F32 && (SAVE_PRE || FP8 || kStageBf16Out);   // bf16 H leaves by TMA store
@@ -605,7 +606,7 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtenso
   if (!ok_maps) args.rows_C = 0;
   static int max_clusters = -1;   // per kernel instantiation, per process (one device type)
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
@@ -627,6 +628,11 @@ cudaError_t launch_pair(const GemmArgs& a, const CUtensorMap& mA0, const CUtenso
   }
   const int64_t pairs = max_pair_tiles < max_clusters ? max_pair_tiles : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  if (a.pdl) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, kernel, mA0, mA1, mB, mB3, mC, mP, mU, args);
 }
 

@@ -32,6 +32,7 @@ __device__ __forceinline__ float act_f32(int act, float v) {
 
 template <bool SWIGLU>
 __global__ void __launch_bounds__(kThreads) gemm_f32_kernel(GemmArgs a) {
+  pdl_wait();
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN];
   __shared__ float B3s[SWIGLU ? BK : 1][BN];
@@ -154,11 +155,8 @@ __global__ void __launch_bounds__(kThreads) gemm_f32_kernel(GemmArgs a) {
 cudaError_t launch_grouped_gemm_f32(const GemmArgs& a, cudaStream_t s) {
   if (a.max_mtiles <= 0) return cudaSuccess;
   dim3 grid((unsigned)((a.N + BN - 1) / BN), (unsigned)(a.max_mtiles < 65535 ? a.max_mtiles : 65535));
-  if (a.act == MOE_ACT_SWIGLU)
-    gemm_f32_kernel<true><<<grid, kThreads, 0, s>>>(a);
-  else
-    gemm_f32_kernel<false><<<grid, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.act == MOE_ACT_SWIGLU) return launch_maybe_pdl(a.pdl, gemm_f32_kernel<true>, grid, dim3(kThreads), 0, s, a);
+  return launch_maybe_pdl(a.pdl, gemm_f32_kernel<false>, grid, dim3(kThreads), 0, s, a);
 }
 
 }  // namespace moe

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace moe {
@@ -85,8 +87,28 @@ struct GatherArgs {
   float* xs_perm;
   uint8_t* xq;
   float* xs_tok;
+  bool pdl;             // launch with programmatic serialization after the previous kernel
 };
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
+
+// Launch `kern` on `s`, with programmatic stream serialization when `pdl`: the
+// kernel may then be scheduled while the stream's previous kernel finishes,
+// and it calls pdl_wait() before reading that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_maybe_pdl(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Per-row E4M3 quantisation of bf16 rows (fp8.cu): row r of X -> codes Q[r]
 // and decoding scale scale[r].  Rows [0, rows0) are live only below *live0
@@ -123,6 +145,7 @@ struct CombineArgs {
   const float* topk_w;
   void* y;              // [T, d]
   const uint32_t* err;  // non-zero: skip (an earlier stage failed)
+  bool pdl;             // launch with programmatic serialization after the previous kernel
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 
@@ -203,6 +226,7 @@ struct GemmArgs {
   const float* a_scale1;
   const float* b_scale;
   const float* b3_scale;
+  bool pdl;             // launch with programmatic serialization after the previous kernel
 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_grouped_gemm_pair(const GemmArgs& a, cudaStream_t s);

@@ -430,6 +430,12 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   ga.topk_idx = topk_idx; ga.lrank = ra.lrank; ga.base = sa.base; ga.offsets = sa.offsets; ga.slot = slot_buf;
   ga.dropped = dropped_mask; ga.perm_token = perm_token; ga.xperm = ws + L.xperm; ga.err = &hdr->err;
   ga.nblk = L.nblk; ga.bm = ra.bm;
+  // Without stage events between them, the gather, the GEMMs and the combine
+  // of a token-choice bf16 / fp32 forward launch with programmatic stream
+  // serialization: each may be scheduled while its predecessor finishes, and
+  // waits in the kernel for that predecessor's results.
+  const bool pdl = !ec && !fp8 && !(opts && opts->stage_events);
+  ga.pdl = pdl;
   const bool sh8 = fp8 && c.n_shared > 0;
   if (fp8) {
     ga.fp8 = true;
@@ -451,6 +457,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   g1.err = &hdr->err; g1.timeout_ns = timeout;
   g1.single_cta = opts && (opts->flags & MOE_OPT_GEMM_SINGLE_CTA);
   g1.rows_C = L.rows_all;     // H leaves by TMA store (whole 32-row warp tiles)
+  g1.pdl = pdl;
   if (fp8) {
     g1.fp8 = true;
     g1.A1 = sh8 ? ws + L.xq : nullptr;
@@ -485,6 +492,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x, const void*
   CombineArgs ca;
   ca.o = (const float*)(ws + L.o); ca.T = c.T; ca.d = c.d_model; ca.k = c.k; ca.S = c.n_shared; ca.y_f32 = y_f32;
   ca.rows_tk = L.rows_tk; ca.slot = slot_buf; ca.topk_w = topk_w; ca.y = y; ca.err = &hdr->err;
+  ca.pdl = pdl;
   if (ec) {
     EcCombineArgs ek;
     ek.o = (const float*)(ws + L.o); ek.bits = (const uint32_t*)(ws + L.ec_bits);
