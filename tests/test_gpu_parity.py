@@ -169,6 +169,29 @@ def test_deterministic(name):
                            tb.view(torch.uint8) if tb.dtype == torch.bfloat16 else tb), field
 
 
+@pytest.mark.parametrize("name", ["tiny_top1_relu_f32", "gpt2_top2_gelu_bf16", "deepseek_shared_sigmoid_bf16"])
+def test_dependent_launch_changes_nothing(name):
+    """Without stage events the gather, GEMMs and combine launch with
+    programmatic stream serialization (each waits in the kernel for its
+    predecessor); stage events between the launches turn that off.  Both,
+    repeated (the second calls reuse the encoded tensor maps), give the same
+    bits."""
+    cfg = si.CONFIGS[name].replace(**SMALL[name])
+    dinp = device_inputs(si.layer_inputs(cfg, seed=6))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)]
+    outs = [run(cfg, dinp), run(cfg, dinp, stage_events=ev), run(cfg, dinp), run(cfg, dinp, stage_events=ev)]
+    torch.cuda.synchronize()
+    for o in outs:
+        assert moe.check_device_errors(o.workspace) == 0
+    for field in ("y", "topk_idx", "topk_w", "expert_counts", "dropped_mask", "f", "P", "L_aux", "perm_token",
+                  "slot"):
+        ref = getattr(outs[0], field)
+        for o in outs[1:]:
+            t = getattr(o, field)
+            assert torch.equal(ref.view(torch.uint8) if ref.dtype == torch.bfloat16 else ref,
+                               t.view(torch.uint8) if t.dtype == torch.bfloat16 else t), field
+
+
 def _sample_rows(T, out, n=12, seed=0):
     rng = np.random.default_rng(seed)
     rows = {0, T - 1, T // 2}
