@@ -97,47 +97,141 @@ __device__ __forceinline__ void router_finalize(float* sl, int ldl, uint32_t* bi
     float* l = sl + tok * ldl;
     const bool bf = a.dtype == MOE_DT_BF16;
     float v[EPT];
+    if constexpr (EPT <= 32) {
+      // Loads first, stores after: with a store between two loads the compiler
+      // has to keep them in order (the pointers may alias), and every load then
+      // waits out the previous one.
 #pragma unroll
-    for (int i = 0; i < EPT; ++i) {
-      const int e = q + kTPT * i;
-      v[i] = 0.f;
-      if (valid && e < E) {
-        float x = l[e];
-        if (dry) x = 0.f;   // the dry pass's scratch rows hold no logits
-        if (a.bg) x += bf ? bf16_bits_to_f32(((const uint16_t*)a.bg)[e]) : ((const float*)a.bg)[e];
-        if (a.noise) x += a.noise[t * E + e];   // noisy scores: everything below uses them
-        v[i] = x;
-        if (wr && a.logits_out && !a.scores_em) a.logits_out[t * E + e] = x;
-        if (wr && a.raw_logits) a.raw_logits[t * E + e] = x;
+      for (int i = 0; i < EPT; ++i) {
+        const int e = q + kTPT * i;
+        v[i] = 0.f;
+        if (valid && e < E) {
+          v[i] = l[e];
+          if (dry) v[i] = 0.f;   // the dry pass's scratch rows hold no logits
+        }
       }
-    }
-    // k rounds of the quad argmax (expert choice uses only the maximum, val[0]).
-    uint64_t taken = 0;             // bit i: expert q + 4 i already chosen
-    const int kr = a.scores_em ? 1 : k;
-#pragma unroll 1
-    for (int j = 0; j < kr; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      if (valid) {
+      if (a.bg) {
 #pragma unroll
         for (int i = 0; i < EPT; ++i) {
           const int e = q + kTPT * i;
-          // experts ascend within the thread: a strict > keeps the lower index
-          if (e < E && !((taken >> i) & 1ull) && (v[i] > bv || bi == 0x7fffffff)) { bv = v[i]; bi = e; }
+          if (valid && e < E) v[i] += bf ? bf16_bits_to_f32(((const uint16_t*)a.bg)[e]) : ((const float*)a.bg)[e];
         }
       }
+      if (a.noise) {   // noisy scores: everything below uses them
 #pragma unroll
-      for (int m = 1; m < kTPT; m <<= 1) {
-        const float pv = __shfl_xor_sync(0xffffffffu, bv, m);
-        const int pi = __shfl_xor_sync(0xffffffffu, bi, m);
-        // A thread with no candidate left (bi unset) takes its partner's; a
-        // NaN logit never replaces a candidate nor leaves an index unset.
-        if (bi == 0x7fffffff || (pi != 0x7fffffff && (pv > bv || (pv == bv && pi < bi)))) { bv = pv; bi = pi; }
+        for (int i = 0; i < EPT; ++i) {
+          const int e = q + kTPT * i;
+          if (valid && e < E) v[i] += a.noise[t * E + e];
+        }
       }
+      if (wr && (a.raw_logits || (a.logits_out && !a.scores_em))) {
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj)
-        if (jj == j) { val[jj] = bv; idx[jj] = bi; }
-      if (valid && (bi % kTPT) == q) taken |= 1ull << (bi / kTPT);
+        for (int i = 0; i < EPT; ++i) {
+          const int e = q + kTPT * i;
+          if (e < E) {
+            if (a.logits_out && !a.scores_em) a.logits_out[t * E + e] = v[i];
+            if (a.raw_logits) a.raw_logits[t * E + e] = v[i];
+          }
+        }
+      }
+    } else {   // 64 logits a thread: one pass, so that they fit in registers
+#pragma unroll
+      for (int i = 0; i < EPT; ++i) {
+        const int e = q + kTPT * i;
+        v[i] = 0.f;
+        if (valid && e < E) {
+          float x = l[e];
+          if (dry) x = 0.f;
+          if (a.bg) x += bf ? bf16_bits_to_f32(((const uint16_t*)a.bg)[e]) : ((const float*)a.bg)[e];
+          if (a.noise) x += a.noise[t * E + e];
+          v[i] = x;
+          if (wr && a.logits_out && !a.scores_em) a.logits_out[t * E + e] = x;
+          if (wr && a.raw_logits) a.raw_logits[t * E + e] = x;
+        }
+      }
+    }
+    // k rounds of the quad argmax (expert choice uses only the maximum, val[0]).
+    const int kr = a.scores_em ? 1 : k;
+    if constexpr (EPT <= 32) {
+      // Each thread's logits as order-preserving unsigned keys: the IEEE bits
+      // with the sign folded, -0 read as +0 (so that it ties with +0), 1 for
+      // NaN (below every number), 0 for an expert past E.  A round takes the
+      // thread's largest key not yet chosen by a pairwise tree (depth log2 EPT
+      // instead of a chain of EPT compares), whose left operand always holds
+      // the lower experts, so that a tie keeps the lower index.
+      uint32_t key[EPT];
+#pragma unroll
+      for (int i = 0; i < EPT; ++i) {
+        uint32_t b = __float_as_uint(v[i]);
+        b = b == 0x80000000u ? 0u : b;
+        const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+        key[i] = (!valid || q + kTPT * i >= E) ? 0u : ((b & 0x7fffffffu) > 0x7f800000u ? 1u : ord);
+      }
+      uint32_t taken = 0;           // bit i: expert q + 4 i already chosen
+#pragma unroll 1
+      for (int j = 0; j < kr; ++j) {
+        uint32_t kk[EPT];
+        int ss[EPT];
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+          kk[i] = ((taken >> i) & 1u) ? 0u : key[i];
+          ss[i] = i;
+        }
+#pragma unroll
+        for (int st = 1; st < EPT; st <<= 1) {
+#pragma unroll
+          for (int i = 0; i + st < EPT; i += 2 * st) {
+            const bool r = kk[i + st] > kk[i];
+            kk[i] = r ? kk[i + st] : kk[i];
+            ss[i] = r ? ss[i + st] : ss[i];
+          }
+        }
+        uint32_t bk = kk[0];
+        int bi = bk != 0u ? q + kTPT * ss[0] : 0x7fffffff;
+#pragma unroll
+        for (int m = 1; m < kTPT; m <<= 1) {
+          const uint32_t pk = __shfl_xor_sync(0xffffffffu, bk, m);
+          const int pi = __shfl_xor_sync(0xffffffffu, bi, m);
+          // The larger key, the lower index on equal keys; key 0 (no candidate
+          // left) loses to every candidate.
+          if (pk > bk || (pk == bk && pi < bi)) { bk = pk; bi = pi; }
+        }
+        const float bv = bk >= 0x80000000u ? __uint_as_float(bk & 0x7fffffffu)
+                         : bk > 1u         ? __uint_as_float(~bk)
+                         : bk == 1u        ? __uint_as_float(0x7fc00000u)
+                                           : -INFINITY;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+          if (jj == j) { val[jj] = bv; idx[jj] = bi; }
+        if (bk != 0u && (bi % kTPT) == q) taken |= 1u << (bi / kTPT);
+      }
+    } else {
+      uint64_t taken = 0;           // bit i: expert q + 4 i already chosen
+#pragma unroll 1
+      for (int j = 0; j < kr; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < EPT; ++i) {
+            const int e = q + kTPT * i;
+            // experts ascend within the thread: a strict > keeps the lower index
+            if (e < E && !((taken >> i) & 1ull) && (v[i] > bv || bi == 0x7fffffff)) { bv = v[i]; bi = e; }
+          }
+        }
+#pragma unroll
+        for (int m = 1; m < kTPT; m <<= 1) {
+          const float pv = __shfl_xor_sync(0xffffffffu, bv, m);
+          const int pi = __shfl_xor_sync(0xffffffffu, bi, m);
+          // A thread with no candidate left (bi unset) takes its partner's; a
+          // NaN logit never replaces a candidate nor leaves an index unset.
+          if (bi == 0x7fffffff || (pi != 0x7fffffff && (pv > bv || (pv == bv && pi < bi)))) { bv = pv; bi = pi; }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+          if (jj == j) { val[jj] = bv; idx[jj] = bi; }
+        if (valid && (bi % kTPT) == q) taken |= 1ull << (bi / kTPT);
+      }
     }
     // Gating over all E (these p feed P), and the renormalised top-k weights.
     float z = 0.f;
@@ -185,15 +279,20 @@ __device__ __forceinline__ void router_finalize(float* sl, int ldl, uint32_t* bi
           }
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (j < k) {
-            if (wr) {
+        for (int j = 0; j < 8; ++j)
+          if (j < k) g[j] = g[j] / zsel;
+        if (wr) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (j < k) {
               a.topk_idx[t * k + j] = idx[j];
-              a.topk_w[t * k + j] = g[j] / zsel;
+              a.topk_w[t * k + j] = g[j];
             }
-            atomicOr(&bits[idx[j] * NW + tok / 32], 1u << (tok % 32));
           }
         }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j < k) atomicOr(&bits[idx[j] * NW + tok / 32], 1u << (tok % 32));
       }
     }
   }
@@ -201,31 +300,66 @@ __device__ __forceinline__ void router_finalize(float* sl, int ldl, uint32_t* bi
   if (valid && q == 0 && !a.scores_em) {
     const int w = tok / 32;
     const uint32_t below = (1u << (tok % 32)) - 1u;
+    int rk[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
+      rk[j] = 0;
       if (j < k) {
         const uint32_t* be = bits + idx[j] * NW;
-        int r = __popc(be[w] & below);
-        for (int qq = 0; qq < w; ++qq) r += __popc(be[qq]);
-        if (wr) a.lrank[t * k + j] = (uint8_t)r;
+        rk[j] = __popc(be[w] & below);
+#pragma unroll
+        for (int qq = 0; qq < NW - 1; ++qq)
+          if (qq < w) rk[j] += __popc(be[qq]);
       }
+    }
+    if (wr) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < k) a.lrank[t * k + j] = (uint8_t)rk[j];
     }
   }
   // Per expert: selections (popc of the bit masks) and the sum of gate
   // probabilities over the CTA's tokens, one warp per expert: lane l adds
-  // rows l, l + 32, ..., then a fixed xor-tree over the lanes.
+  // rows l, l + 32, ..., then a fixed xor-tree over the lanes.  With many
+  // experts a warp takes four of its experts at a time, so that their chains
+  // overlap.
   const int nvalid = dry ? 8 : (int)(a.T - t0 < BM ? a.T - t0 : BM);
   const int lane = vt % 32, nwarps = nvt / 32;
-  for (int e = vt / 32; e < (dry ? 1 : E); e += nwarps) {
-    float s = 0.f;
-    for (int r = lane; r < nvalid; r += 32) s += sl[r * ldl + e];
+  const int Ep = dry ? 1 : E;
+  constexpr int EU = EPT >= 8 ? 4 : 1;
+  for (int e0 = vt / 32; e0 < Ep; e0 += EU * nwarps) {
+    float s[EU];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    for (int u = 0; u < EU; ++u) s[u] = 0.f;
+    for (int r = lane; r < nvalid; r += 32) {
+#pragma unroll
+      for (int u = 0; u < EU; ++u)
+        if (e0 + u * nwarps < Ep) s[u] += sl[r * ldl + e0 + u * nwarps];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+      for (int u = 0; u < EU; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], off);
+    }
     if (lane == 0 && !dry) {
-      int h = 0;
-      for (int qq = 0; qq < NW; ++qq) h += __popc(bits[e * NW + qq]);
-      a.hist[e * a.nblk + blk] = h;
-      a.psum[e * a.nblk + blk] = s;
+      int h[EU];
+#pragma unroll
+      for (int u = 0; u < EU; ++u) {
+        const int e = e0 + u * nwarps;
+        h[u] = 0;
+        if (e < E) {
+#pragma unroll
+          for (int qq = 0; qq < NW; ++qq) h[u] += __popc(bits[e * NW + qq]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < EU; ++u) {
+        const int e = e0 + u * nwarps;
+        if (e < E) {
+          a.hist[e * a.nblk + blk] = h[u];
+          a.psum[e * a.nblk + blk] = s[u];
+        }
+      }
     }
   }
 }
@@ -635,12 +769,17 @@ struct Shape {
   static constexpr int STAGE = XS + NB * WBOX;
   static constexpr int STAGES = RING / STAGE;          // 8, 6, 4, 4
   static constexpr int TCOLS = NB == 1 ? 64 : NB == 2 ? 128 : 256;   // TMEM columns (a power of 2)
-  static constexpr size_t LOGITS = (size_t)BM * (E + 1) * 4;
+  // Logit rows E + 4 floats apart: E + 4 is 4 mod 32 words, so the tail's
+  // reads (8 tokens x 4 threads of a warp, experts q + 4 i) fall in 32
+  // different banks, and a row starts on a 16-byte boundary for the vector
+  // stores out of TMEM.
+  static constexpr int LDL = E + 4;
+  static constexpr size_t LOGITS = (size_t)BM * LDL * 4;
   static constexpr size_t BITS_OFF = (size_t)STAGES * STAGE;
   static constexpr size_t BITS = (size_t)E * (BM / 32) * 4;
   // Scratch of the warm-up warps (dry tail rows and masks, dry scan totals).
   static constexpr size_t DRY_OFF = (BITS_OFF + BITS + 15) / 16 * 16;
-  static constexpr size_t DRY_SL = (size_t)kDryTokens * (E + 1) * 4;
+  static constexpr size_t DRY_SL = (size_t)kDryTokens * LDL * 4;
   static constexpr size_t DRY_BITS = BITS;
   static constexpr size_t DRY_SCAN = 2 * scan_detail::kMaxE * 4;
   static constexpr size_t BAR_OFF = (DRY_OFF + DRY_SL + DRY_BITS + DRY_SCAN + 7) / 8 * 8;
@@ -770,7 +909,10 @@ __global__ void __launch_bounds__(rtc::THREADS, 1) router_tc_kernel(const __grid
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sl[row * (E + 1) + c * 32 + i] = __uint_as_float(v[i]);
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(sl + row * L::LDL + c * 32 + i) =
+              make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
+                          __uint_as_float(v[i + 3]));
       }
     }
     tc_fence_before();
@@ -795,7 +937,7 @@ __global__ void __launch_bounds__(rtc::THREADS, 1) router_tc_kernel(const __grid
       }
     }
     if (!stop && (!dry || warp == rtc::WARM_TAIL_WARP))
-      router_finalize<rtc::BM, E / kTPT>(dry ? (float*)dry_area : (float*)smem, E + 1,
+      router_finalize<rtc::BM, E / kTPT>(dry ? (float*)dry_area : (float*)smem, L::LDL,
                                          dry ? (uint32_t*)(dry_area + L::DRY_SL) : bits, a, blk, dry ? lane : tid,
                                          dry ? 32 : rtc::THREADS, dry);
     if (!dry || warm_scan)
