@@ -152,7 +152,7 @@ __device__ __forceinline__ void router_finalize(float* sl, int ldl, uint32_t* bi
     }
     // k rounds of the quad argmax (expert choice uses only the maximum, val[0]).
     const int kr = a.scores_em ? 1 : k;
-    if constexpr (EPT <= 32) {
+    if constexpr (EPT >= 8 && EPT <= 32) {
       // Each thread's logits as order-preserving unsigned keys: the IEEE bits
       // with the sign folded, -0 read as +0 (so that it ties with +0), 1 for
       // NaN (below every number), 0 for an expert past E.  A round takes the
@@ -205,7 +205,7 @@ __device__ __forceinline__ void router_finalize(float* sl, int ldl, uint32_t* bi
           if (jj == j) { val[jj] = bv; idx[jj] = bi; }
         if (bk != 0u && (bi % kTPT) == q) taken |= 1u << (bi / kTPT);
       }
-    } else {
+    } else {   // a few logits a thread (a short chain), or 64 (registers)
       uint64_t taken = 0;           // bit i: expert q + 4 i already chosen
 #pragma unroll 1
       for (int j = 0; j < kr; ++j) {
@@ -941,7 +941,7 @@ __global__ void __launch_bounds__(rtc::THREADS, 1) router_tc_kernel(const __grid
                                          dry ? (uint32_t*)(dry_area + L::DRY_SL) : bits, a, blk, dry ? lane : tid,
                                          dry ? 32 : rtc::THREADS, dry);
     if (!dry || warm_scan)
-      router_retire<2, 4>(a, dry ? dry_area + L::DRY_SL + L::DRY_BITS : smem, dry,
+      router_retire<4, 4>(a, dry ? dry_area + L::DRY_SL + L::DRY_BITS : smem, dry,
                           dry ? warp - rtc::WARM_SCAN_WARP0 : warp, dry ? 4 : rtc::THREADS / 32);
   }
 }

@@ -39,8 +39,10 @@ __device__ __forceinline__ int warp_excl_scan(int v, int lane, int* total) {
 // L1-bypassing loads: in the fused form they were written by other SMs during
 // this same launch.
 // kScanE experts per warp per round, kScanU 32-block chunks of each loaded per
-// round: the standalone scan kernel takes <4, 8>, the router's last CTA a
-// lighter <2, 4> so that its kernel keeps the registers of its own main loop.
+// round: the standalone scan kernel takes <4, 8>, the last CTA of the
+// mma.sync and fp32 routers a lighter <2, 4> (or <1, 8>) so that their kernels
+// keep the registers of their own main loops, and that of the 512-thread
+// tcgen05 router <4, 4> (64 experts over its 16 warps in one round).
 // dry: the same code over one round of phase 1 and the roles of phase 2,
 // writing only s_npre / s_psum (no barrier: one warp alone takes all four
 // roles, or four warps one each): it brings the code into the instruction
