@@ -87,6 +87,52 @@ def test_layer_edge_cases(label, base, over):
     check_y(cfg, inp, out, gl, np.arange(cfg.T))
 
 
+# Exact ties in every top-k path of the routers: the chain over 2 logits a
+# thread (E = 8), the keyed tree over 8, 16 and 32 (mma.sync E = 24 and 96,
+# tcgen05 E = 64, fp32 E = 20), and the chain over 64 (E = 160).
+TIE_CASES = [
+    ("E_8_chain", "gpt2_top2_gelu_bf16", dict(T=200, E=8, k=2, d=256, f=128, router_bias=False)),
+    ("E_24_tree", "gpt2_top2_gelu_bf16", dict(T=200, E=24, k=3, d=256, f=128, router_bias=False)),
+    ("E_64_tcgen05_tree", "deepseek_shared_sigmoid_bf16", dict(T=300, E=64, k=6, S=0, d=256, f=128)),
+    ("E_96_tree", "deepseek_shared_sigmoid_bf16", dict(T=200, E=96, k=6, S=0, d=256, f=128)),
+    ("E_160_chain", "gpt2_top2_gelu_bf16", dict(T=150, E=160, k=8, d=256, f=128, router_bias=False)),
+    ("f32_E_20_tree", "tiny_top1_relu_f32", dict(T=150, E=20, k=4, router_bias=False)),
+]
+
+
+@pytest.mark.parametrize("label,base,over", TIE_CASES, ids=[c[0] for c in TIE_CASES])
+def test_router_ties_go_to_the_lower_expert(label, base, over):
+    """Experts with equal logits are taken lower index first ("手撕一个极简
+    MoE-FFN" §三: top-k of the scores).  Column e of W_g repeats column e mod 3,
+    and base columns 1 and 2 are +0 and -0, so every token's logits take at
+    most two values (its column-0 logit and zero), each shared by a third of
+    the experts or more, spread over the four threads of a token; -0 and +0
+    are equal.  Rows 0-9 of x are zero, so all their logits tie at 0 and they
+    choose experts 0 .. k-1."""
+    cfg = si.CONFIGS[base].replace(**over)
+    inp = si.layer_inputs(cfg, seed=11)
+    W = inp["W_g"].copy()
+    pos0, neg0 = (np.uint16(0x0000), np.uint16(0x8000)) if W.dtype == np.uint16 else (np.float32(0.0), np.float32(-0.0))
+    W[:, 1] = pos0
+    W[:, 2] = neg0
+    for e in range(3, cfg.E):
+        W[:, e] = W[:, e % 3]
+    x = inp["x"].copy()
+    x[:10] = 0
+    inp = dict(inp, W_g=W, x=x)
+    out = run(cfg, device_inputs(inp))
+    assert moe.check_device_errors(out.workspace) == 0
+    ref, gl, _ = check_routing(cfg, inp, out)
+    idx = out.topk_idx.cpu().numpy()
+    assert np.array_equal(idx[:10], np.tile(np.arange(cfg.k), (10, 1)))
+    # the oracle's stable sort on the GPU's own logits, written out: the lowest
+    # experts of the largest value first
+    for t in range(10, cfg.T):
+        order = sorted(range(cfg.E), key=lambda e: (-gl[t, e], e))
+        assert list(idx[t]) == order[:cfg.k], t
+    check_y(cfg, inp, out, gl, np.arange(cfg.T))
+
+
 @pytest.mark.parametrize("name", ["mixtral_swiglu_bf16", "deepseek_shared_sigmoid_bf16", "gpt2_top2_gelu_bf16"])
 def test_layer_small_one_cta_gemm(name):
     """The layer with its bf16 expert GEMMs on the one-CTA tile kernel."""
